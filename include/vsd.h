@@ -1,0 +1,241 @@
+/*
+ * vsd.h -- C ABI of the GB300 greedy block-verify library.
+ *
+ * One call, vsd_verify_step, runs the target-model verification step of
+ * block speculative decoding on the GPU: for every request, the pending token
+ * and a block of 16 drafted tokens pass through the decoder-only target in
+ * one forward over the request's KV cache (causal inside the block); the
+ * greedy token of every row is compared with the drafts; the longest
+ * matching prefix plus one target token is accepted; only the accepted rows'
+ * K and V are committed to the cache.
+ *
+ * Where the method is defined:
+ *   - one target pass verifies a whole drafted block: "The Inference Stack
+ *     Behind OCRia", section "Generate more tokens per target pass:
+ *     speculative decoding"; HunyuanOCR-1.5 summary, section one, inference
+ *     steps 2-3 (block size B = 16);
+ *   - accept the longest valid prefix, cutting at the first mismatch from the
+ *     left, then append the target's own token (correction or bonus):
+ *     HunyuanOCR-1.5 summary, section one, inference step 4; the accept /
+ *     correct / bonus branch of the speculative decoder in "LLM inference
+ *     acceleration", section 3.2;
+ *   - the output equals the target's own greedy output: OCRia post,
+ *     speculative-decoding section ("100% lossless");
+ *   - BF16 / FP8 / NVFP4 weights: OCRia post, section "Reducing the data
+ *     moved: workload-aware quantization";
+ *   - KV cache (no recomputation of earlier tokens), GQA, paged KV:
+ *     OCRia post, speculative-decoding section; "LLM inference
+ *     acceleration", section two;
+ *   - per-step batch metadata (sequence lengths, cache locations) kept where
+ *     the kernels read it, no host round trip per step: OCRia post, section
+ *     "Fixing CPU-side preparation".
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are CUDA device pointers; *_host are host memory.
+ *     The caller owns every pointer it passes; the library owns what it
+ *     allocates inside vsd_model / vsd_kv and frees it in *_destroy.
+ *   - Work is enqueued on the given stream and is asynchronous unless the
+ *     comment says the call synchronises.  vsd_verify_step never synchronises
+ *     and never copies to the host, so it can be captured in a CUDA graph.
+ *   - Errors the host can see (null pointers, sizes out of range, a missing
+ *     CUDA device) return a nonzero vsd_status before anything is enqueued;
+ *     vsd_last_error() then describes it (per thread).  Errors only the
+ *     device can see (a token id >= vocab, a sequence length beyond the
+ *     cache, a page id outside the pool, a bounded wait that ran out) set a
+ *     bit in the cache's device status word (vsd_get_device_status); an
+ *     affected request is left unchanged (no commit, accepted = -1).
+ *   - Token ids, lengths and counts are int32.  BF16 is raw 16-bit storage
+ *     (uint16_t bit patterns); FP8 is E4M3 ("fn": max 448, no infinities);
+ *     FP4 is E2M1, two per byte with the even element in the low nibble.
+ */
+#ifndef VSD_H
+#define VSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* vsd_stream; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  VSD_OK = 0,
+  VSD_ERR_ARG = 1,        /* bad pointer / size / enum */
+  VSD_ERR_CUDA = 2,       /* a CUDA runtime call failed */
+  VSD_ERR_OOM = 3,        /* device allocation failed */
+  VSD_ERR_CAPACITY = 4,   /* request does not fit the cache that was created */
+  VSD_ERR_DEVICE = 5,     /* the device status word has bits set */
+  VSD_ERR_UNSUPPORTED = 6 /* shape the kernels do not cover */
+} vsd_status;
+
+/* Bits of the device status word. */
+#define VSD_DEV_BAD_TOKEN   0x1  /* token id outside [0, vocab) */
+#define VSD_DEV_BAD_SEQLEN  0x2  /* seq_len < 0 or seq_len + 17 > max_tokens_per_req */
+#define VSD_DEV_BAD_PAGE    0x4  /* page-table entry outside [0, num_pages) */
+#define VSD_DEV_TIMEOUT     0x8  /* a bounded device-side wait ran out */
+
+typedef enum { VSD_FMT_BF16 = 0, VSD_FMT_FP8 = 1, VSD_FMT_NVFP4 = 2 } vsd_weight_format;
+
+/* Decoder-only target: pre-norm layers, RMSNorm (weight 1), rotate-half
+ * RoPE, GQA attention (query head h reads KV head h / (n_q / n_kv)), SwiGLU
+ * MLP, final RMSNorm, lm_head (tied to the embedding or separate). */
+typedef struct {
+  int32_t layers, hidden, n_q, n_kv, head_dim, ffn, vocab;
+  float rope_theta;
+  float eps;
+  int32_t tied;          /* 1: lm_head is the embedding matrix */
+  int32_t attn_fmt;      /* vsd_weight_format of wq, wk, wv, wo */
+  int32_t mlp_fmt;       /* vsd_weight_format of wg, wu, wd */
+  int32_t max_positions; /* length of the RoPE table; positions must stay below it */
+} vsd_model_config;
+
+/* One weight matrix W [N, K] (y = x W^T) in canonical form, device memory:
+ *   BF16 : data = uint16 [N, K] row-major; scale unused
+ *   FP8  : data = e4m3 [N, K] row-major; scale = float [N], w = e4m3 * scale[n]
+ *   NVFP4: data = packed e2m1 [N, K/2]; scale = e4m3 [N, K/16] (one per 16
+ *          consecutive k of a row); tensor_scale = float [1];
+ *          w = e2m1 * e4m3(scale) * tensor_scale
+ * (the quantised forms are what vsd_quantize_* write). */
+typedef struct {
+  int32_t fmt;
+  const void* data_dev;
+  const void* scale_dev;
+  const float* tensor_scale_dev;
+} vsd_weight;
+
+/* All weights.  layers points to layers*7 entries, per layer in the order
+ * wq [n_q*hd, H], wk [n_kv*hd, H], wv [n_kv*hd, H], wo [H, n_q*hd],
+ * wg [F, H], wu [F, H], wd [H, F]. */
+typedef struct {
+  const uint16_t* embed_dev;   /* BF16 [vocab, hidden] */
+  const uint16_t* lm_head_dev; /* BF16 [vocab, hidden], or NULL when tied */
+  const vsd_weight* layers;    /* host array of layers*7 entries */
+} vsd_weights;
+
+typedef struct vsd_model vsd_model;
+typedef struct vsd_kv vsd_kv;
+
+/* Library build string, e.g. "vsd 0.1 sm_103a". */
+const char* vsd_version(void);
+/* Description of the last error returned on this thread ("" if none). */
+const char* vsd_last_error(void);
+
+/* ---------------------------------------------------------------- quantisers
+ * Round-to-nearest (ties to even, saturating) quantisation of a BF16 matrix,
+ * the weight recipe of "The Inference Stack Behind OCRia", section "Reducing
+ * the data moved" (BF16 master -> FP8 / NVFP4; the pages' calibration set is
+ * replaced by plain rounding).  Scale arithmetic is float32, one rounding per
+ * operation:
+ *   FP8  : s[n] = amax_row / 448;  q = e4m3(w / s[n]);  s == 0 -> q = 0
+ *   NVFP4: S = amax / 2688;  s_blk = e4m3(amax_blk / (6 S));
+ *          q = e2m1(w / (e4m3(s_blk) * S));  a zero scale -> q = 0
+ * w_dev BF16 [N, K] row-major; outputs as in vsd_weight.  NVFP4 needs
+ * K % 16 == 0.  Asynchronous on the stream; no allocation. */
+vsd_status vsd_quantize_fp8_rowwise(const uint16_t* w_dev, int32_t n, int32_t k,
+                                    uint8_t* q_dev, float* scale_dev, vsd_stream stream);
+vsd_status vsd_quantize_nvfp4(const uint16_t* w_dev, int32_t n, int32_t k,
+                              uint8_t* q_dev, uint8_t* block_scale_dev,
+                              float* tensor_scale_dev, vsd_stream stream);
+
+/* ---------------------------------------------------------------- model
+ * Repacks the caller's canonical weights into the kernels' tile layout
+ * (library-owned copies) and builds the RoPE table.  Synchronises the stream
+ * before returning; the caller's buffers may be freed afterwards. */
+vsd_status vsd_model_create(const vsd_model_config* cfg, const vsd_weights* w,
+                            vsd_stream stream, vsd_model** out);
+void vsd_model_destroy(vsd_model* m);
+
+/* ---------------------------------------------------------------- KV cache
+ * Paged BF16 KV cache for up to max_batch requests (request slot b = row b
+ * of every per-request array), each holding up to max_tokens_per_req tokens
+ * including the 17 rows of an in-flight block.  page_size must be 16.
+ * num_pages = 0 gives max_batch * ceil(max_tokens_per_req / 16) pages.  The
+ * page table starts as the identity (slot b, page i -> b * pages_per_req + i).
+ * Also owns the step's device workspace.  Synchronises. */
+vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_tokens_per_req,
+                         int32_t page_size, int32_t num_pages, vsd_kv** out);
+void vsd_kv_destroy(vsd_kv* kv);
+int32_t vsd_kv_pages_per_req(const vsd_kv* kv);
+int32_t vsd_kv_num_pages(const vsd_kv* kv);
+
+/* Replaces the page table: table_dev int32 [max_batch, pages_per_req], every
+ * entry in [0, num_pages) (checked on the device; a bad entry sets
+ * VSD_DEV_BAD_PAGE).  Pages of one request must be distinct and not shared. */
+vsd_status vsd_kv_set_page_table(vsd_kv* kv, const int32_t* table_dev, vsd_stream stream);
+
+/* Writes (read) cache rows [start, start+count) of request slot req, all
+ * layers: k_dev / v_dev BF16 [layers, count, n_kv, head_dim].  Asynchronous. */
+vsd_status vsd_kv_write(vsd_kv* kv, int32_t req, int32_t start, int32_t count,
+                        const uint16_t* k_dev, const uint16_t* v_dev, vsd_stream stream);
+vsd_status vsd_kv_read(const vsd_kv* kv, int32_t req, int32_t start, int32_t count,
+                       uint16_t* k_dev, uint16_t* v_dev, vsd_stream stream);
+
+/* Reads and clears the device status word (VSD_DEV_* bits).  Synchronises
+ * the stream. */
+vsd_status vsd_get_device_status(vsd_kv* kv, vsd_stream stream, int32_t* status_host);
+
+/* ---------------------------------------------------------------- the step
+ * Greedy block verification of B requests (slots 0..B-1), 1 <= B <= max_batch.
+ *   seq_lens_dev   int32 [B] in/out: committed length L_b; += accepted+1
+ *   pending_dev    int32 [B] in/out: last emitted token (its K/V not yet
+ *                  cached); becomes the target's token after the accepted
+ *                  prefix (correction or bonus)
+ *   drafts_dev     int32 [B, 16]: drafted tokens
+ *   accepted_dev   int32 [B] out: a_b in 0..16 = index of the first draft
+ *                  that differs from the target's greedy token (16 if none)
+ *   out_tokens_dev int32 [B, 17] out: the target's greedy tokens g_0..g_a,
+ *                  -1 beyond (g_i = d_i for i < a)
+ * Rows [pending, d_0..d_15] run at positions L_b..L_b+16.  Rows 0..a_b (the
+ * pending token and the accepted drafts) have their K (after RoPE) and V
+ * committed at positions L_b..L_b+a_b; no other cache row changes.  argmax
+ * ties go to the lowest token id.  Needs L_b + 17 <= max_tokens_per_req. */
+vsd_status vsd_verify_step(const vsd_model* m, vsd_kv* kv, int32_t batch,
+                           int32_t* seq_lens_dev, int32_t* pending_dev,
+                           const int32_t* drafts_dev, int32_t* accepted_dev,
+                           int32_t* out_tokens_dev, vsd_stream stream);
+
+/* The same step, also writing float32 logits [B*17, vocab] and the residual
+ * stream hidden [layers+1, B*17, hidden] (entry 0 = embeddings, entry l+1 =
+ * after layer l); either pointer may be NULL.  Row index = b*17 + j. */
+vsd_status vsd_verify_step_debug(const vsd_model* m, vsd_kv* kv, int32_t batch,
+                                 int32_t* seq_lens_dev, int32_t* pending_dev,
+                                 const int32_t* drafts_dev, int32_t* accepted_dev,
+                                 int32_t* out_tokens_dev, float* logits_dev,
+                                 float* hidden_dev, vsd_stream stream);
+
+/* ---------------------------------------------------------------- components
+ * Single kernels of the step, exposed so that each can be checked alone.  */
+
+/* y = x W^T for one weight in any format (the step's GEMM kernel with a
+ * plain float32 store): x_dev f16 [m, K] row-major, y_dev float32 [m, N].
+ * W as in vsd_weight, repacked inside the call (allocates; test use). */
+vsd_status vsd_linear(const vsd_weight* w, int32_t n, int32_t k, const uint16_t* x_f16_dev,
+                      int32_t m, float* y_dev, vsd_stream stream);
+
+/* Block attention of one layer for B requests: q_dev BF16 [B, 17, n_q, hd]
+ * (RoPE already applied), k_new_dev / v_new_dev BF16 [B, 17, n_kv, hd] (the
+ * block's own rows), cache rows [0, seq_lens[b]) of the layer; row j sees the
+ * cached rows and block rows 0..j.  out_dev f16 [B*17, n_q*hd].  The block
+ * rows go to the step's scratch, not to the cache. */
+vsd_status vsd_block_attention(const vsd_model* m, vsd_kv* kv, int32_t layer, int32_t batch,
+                               const int32_t* seq_lens_dev, const uint16_t* q_dev,
+                               const uint16_t* k_new_dev, const uint16_t* v_new_dev,
+                               uint16_t* out_dev, vsd_stream stream);
+
+/* The accept-and-commit tail of the step driven by given float32 logits
+ * [B*17, vocab] and block K/V rows k_new_dev / v_new_dev BF16
+ * [layers, B, 17, n_kv, hd]: per-row argmax, prefix accept, outputs, KV
+ * commit, seq_lens / pending update -- exactly as in vsd_verify_step. */
+vsd_status vsd_accept_commit(const vsd_model* m, vsd_kv* kv, int32_t batch,
+                             const float* logits_dev, const uint16_t* k_new_dev,
+                             const uint16_t* v_new_dev, int32_t* seq_lens_dev,
+                             int32_t* pending_dev, const int32_t* drafts_dev,
+                             int32_t* accepted_dev, int32_t* out_tokens_dev,
+                             vsd_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VSD_H */

@@ -1,0 +1,266 @@
+"""ctypes binding of libvsd.so (include/vsd.h): the same names, torch tensors in.
+
+Argument marshalling only -- every step of the verify path runs in the
+library's CUDA kernels.  Tensors must be CUDA, contiguous, of the dtype the
+header states; BF16 data may be passed as torch.bfloat16 or int16/uint16
+bit patterns.  The stream is torch's current stream unless one is given.
+Loading fails loudly if the shared library is missing: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvsd.so")
+
+VSD_OK, VSD_ERR_ARG, VSD_ERR_CUDA, VSD_ERR_OOM, VSD_ERR_CAPACITY, VSD_ERR_DEVICE, VSD_ERR_UNSUPPORTED = range(7)
+VSD_DEV_BAD_TOKEN, VSD_DEV_BAD_SEQLEN, VSD_DEV_BAD_PAGE, VSD_DEV_TIMEOUT = 1, 2, 4, 8
+FMT = {"bf16": 0, "fp8": 1, "nvfp4": 2}
+
+EXPORTS = [
+    "vsd_version", "vsd_last_error", "vsd_quantize_fp8_rowwise", "vsd_quantize_nvfp4",
+    "vsd_model_create", "vsd_model_destroy", "vsd_kv_create", "vsd_kv_destroy",
+    "vsd_kv_pages_per_req", "vsd_kv_num_pages", "vsd_kv_set_page_table", "vsd_kv_write",
+    "vsd_kv_read", "vsd_get_device_status", "vsd_verify_step", "vsd_verify_step_debug",
+    "vsd_linear", "vsd_block_attention", "vsd_accept_commit",
+]
+
+
+class VsdError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"vsd status {status}: {msg}")
+        self.status = status
+
+
+class ModelConfig(ctypes.Structure):
+    _fields_ = [("layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_q", ctypes.c_int32),
+                ("n_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("eps", ctypes.c_float),
+                ("tied", ctypes.c_int32), ("attn_fmt", ctypes.c_int32), ("mlp_fmt", ctypes.c_int32),
+                ("max_positions", ctypes.c_int32)]
+
+
+class Weight(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("data_dev", ctypes.c_void_p), ("scale_dev", ctypes.c_void_p),
+                ("tensor_scale_dev", ctypes.c_void_p)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed_dev", ctypes.c_void_p), ("lm_head_dev", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(Weight))]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m speculative_decoding_block_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        c_int, p = ctypes.c_int32, ctypes.c_void_p
+        sig = {
+            "vsd_version": ([], ctypes.c_char_p),
+            "vsd_last_error": ([], ctypes.c_char_p),
+            "vsd_quantize_fp8_rowwise": ([p, c_int, c_int, p, p, p], c_int),
+            "vsd_quantize_nvfp4": ([p, c_int, c_int, p, p, p, p], c_int),
+            "vsd_model_create": ([ctypes.POINTER(ModelConfig), ctypes.POINTER(Weights), p,
+                                  ctypes.POINTER(p)], c_int),
+            "vsd_model_destroy": ([p], None),
+            "vsd_kv_create": ([p, c_int, c_int, c_int, c_int, ctypes.POINTER(p)], c_int),
+            "vsd_kv_destroy": ([p], None),
+            "vsd_kv_pages_per_req": ([p], c_int),
+            "vsd_kv_num_pages": ([p], c_int),
+            "vsd_kv_set_page_table": ([p, p, p], c_int),
+            "vsd_kv_write": ([p, c_int, c_int, c_int, p, p, p], c_int),
+            "vsd_kv_read": ([p, c_int, c_int, c_int, p, p, p], c_int),
+            "vsd_get_device_status": ([p, p, ctypes.POINTER(c_int)], c_int),
+            "vsd_verify_step": ([p, p, c_int, p, p, p, p, p, p], c_int),
+            "vsd_verify_step_debug": ([p, p, c_int, p, p, p, p, p, p, p, p], c_int),
+            "vsd_linear": ([ctypes.POINTER(Weight), c_int, c_int, p, c_int, p, p], c_int),
+            "vsd_block_attention": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
+            "vsd_accept_commit": ([p, p, c_int, p, p, p, p, p, p, p, p, p], c_int),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != VSD_OK:
+        raise VsdError(status, lib().vsd_last_error().decode())
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor | None, dtypes, name: str, numel: int | None = None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+B16 = (torch.bfloat16, torch.int16, torch.uint16, torch.float16)
+U8 = (torch.uint8,)
+I32 = (torch.int32,)
+F32 = (torch.float32,)
+
+
+def vsd_version() -> str:
+    return lib().vsd_version().decode()
+
+
+def vsd_quantize_fp8_rowwise(w, q, scale, stream=None) -> None:
+    n, k = w.shape
+    _check(lib().vsd_quantize_fp8_rowwise(_dev(w, B16, "w"), n, k, _dev(q, U8, "q", n * k),
+                                          _dev(scale, F32, "scale", n), _stream(stream)))
+
+
+def vsd_quantize_nvfp4(w, q, block_scale, tensor_scale, stream=None) -> None:
+    n, k = w.shape
+    _check(lib().vsd_quantize_nvfp4(_dev(w, B16, "w"), n, k, _dev(q, U8, "q", n * k // 2),
+                                    _dev(block_scale, U8, "block_scale", n * k // 16),
+                                    _dev(tensor_scale, F32, "tensor_scale", 1), _stream(stream)))
+
+
+class Model:
+    """Owns a vsd_model handle."""
+
+    def __init__(self, handle: ctypes.c_void_p, cfg: ModelConfig):
+        self.handle, self.cfg = handle, cfg
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.vsd_model_destroy(self.handle)
+            self.handle = None
+
+
+class KV:
+    """Owns a vsd_kv handle (paged cache + step workspace)."""
+
+    def __init__(self, handle, model: Model, max_batch: int, max_tokens: int):
+        self.handle, self.model = handle, model
+        self.max_batch, self.max_tokens = max_batch, max_tokens
+
+    @property
+    def pages_per_req(self) -> int:
+        return lib().vsd_kv_pages_per_req(self.handle)
+
+    @property
+    def num_pages(self) -> int:
+        return lib().vsd_kv_num_pages(self.handle)
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.vsd_kv_destroy(self.handle)
+            self.handle = None
+
+
+def weight_entry(fmt: str, data, scale=None, tensor_scale=None) -> Weight:
+    f = FMT[fmt]
+    dd = {0: B16, 1: U8, 2: U8}[f]
+    sd = {0: None, 1: F32, 2: U8}[f]
+    return Weight(f, _dev(data, dd, "data"), _dev(scale, sd, "scale") if sd else None,
+                  _dev(tensor_scale, F32, "tensor_scale") if f == 2 else None)
+
+
+def vsd_model_create(cfg: ModelConfig, embed, layer_weights: list, lm_head=None, stream=None) -> Model:
+    """layer_weights: layers*7 Weight entries (wq, wk, wv, wo, wg, wu, wd per layer)."""
+    arr = (Weight * len(layer_weights))(*layer_weights)
+    w = Weights(_dev(embed, B16, "embed"), _dev(lm_head, B16, "lm_head"), arr)
+    h = ctypes.c_void_p()
+    _check(lib().vsd_model_create(ctypes.byref(cfg), ctypes.byref(w), _stream(stream), ctypes.byref(h)))
+    return Model(h, cfg)
+
+
+def vsd_kv_create(model: Model, max_batch: int, max_tokens_per_req: int, page_size: int = 16,
+                  num_pages: int = 0) -> KV:
+    h = ctypes.c_void_p()
+    _check(lib().vsd_kv_create(model.handle, max_batch, max_tokens_per_req, page_size, num_pages,
+                               ctypes.byref(h)))
+    return KV(h, model, max_batch, max_tokens_per_req)
+
+
+def vsd_kv_set_page_table(kv: KV, table, stream=None) -> None:
+    _check(lib().vsd_kv_set_page_table(kv.handle, _dev(table, I32, "table", kv.max_batch * kv.pages_per_req),
+                                       _stream(stream)))
+
+
+def vsd_kv_write(kv: KV, req: int, start: int, k, v, stream=None) -> None:
+    count = k.shape[1]
+    _check(lib().vsd_kv_write(kv.handle, req, start, count, _dev(k, B16, "k"), _dev(v, B16, "v"),
+                              _stream(stream)))
+
+
+def vsd_kv_read(kv: KV, req: int, start: int, k, v, stream=None) -> None:
+    count = k.shape[1]
+    _check(lib().vsd_kv_read(kv.handle, req, start, count, _dev(k, B16, "k"), _dev(v, B16, "v"),
+                             _stream(stream)))
+
+
+def vsd_get_device_status(kv: KV, stream=None) -> int:
+    out = ctypes.c_int32()
+    _check(lib().vsd_get_device_status(kv.handle, _stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def vsd_verify_step(model: Model, kv: KV, batch: int, seq_lens, pending, drafts, accepted, out_tokens,
+                    stream=None) -> None:
+    _check(lib().vsd_verify_step(model.handle, kv.handle, batch, _dev(seq_lens, I32, "seq_lens", batch),
+                                 _dev(pending, I32, "pending", batch), _dev(drafts, I32, "drafts", batch * 16),
+                                 _dev(accepted, I32, "accepted", batch),
+                                 _dev(out_tokens, I32, "out_tokens", batch * 17), _stream(stream)))
+
+
+def vsd_verify_step_debug(model: Model, kv: KV, batch: int, seq_lens, pending, drafts, accepted,
+                          out_tokens, logits=None, hidden=None, stream=None) -> None:
+    _check(lib().vsd_verify_step_debug(model.handle, kv.handle, batch,
+                                       _dev(seq_lens, I32, "seq_lens", batch),
+                                       _dev(pending, I32, "pending", batch),
+                                       _dev(drafts, I32, "drafts", batch * 16),
+                                       _dev(accepted, I32, "accepted", batch),
+                                       _dev(out_tokens, I32, "out_tokens", batch * 17),
+                                       _dev(logits, F32, "logits"), _dev(hidden, F32, "hidden"),
+                                       _stream(stream)))
+
+
+def vsd_linear(weight: Weight, n: int, k: int, x, y, stream=None) -> None:
+    m = x.shape[0]
+    _check(lib().vsd_linear(ctypes.byref(weight), n, k, _dev(x, (torch.float16,), "x", m * k), m,
+                            _dev(y, F32, "y", m * n), _stream(stream)))
+
+
+def vsd_block_attention(model: Model, kv: KV, layer: int, batch: int, seq_lens, q, k_new, v_new, out,
+                        stream=None) -> None:
+    _check(lib().vsd_block_attention(model.handle, kv.handle, layer, batch,
+                                     _dev(seq_lens, I32, "seq_lens", batch), _dev(q, B16, "q"),
+                                     _dev(k_new, B16, "k_new"), _dev(v_new, B16, "v_new"),
+                                     _dev(out, (torch.float16,), "out"), _stream(stream)))
+
+
+def vsd_accept_commit(model: Model, kv: KV, batch: int, logits, k_new, v_new, seq_lens, pending, drafts,
+                      accepted, out_tokens, stream=None) -> None:
+    _check(lib().vsd_accept_commit(model.handle, kv.handle, batch, _dev(logits, F32, "logits"),
+                                   _dev(k_new, B16, "k_new"), _dev(v_new, B16, "v_new"),
+                                   _dev(seq_lens, I32, "seq_lens", batch), _dev(pending, I32, "pending", batch),
+                                   _dev(drafts, I32, "drafts", batch * 16), _dev(accepted, I32, "accepted", batch),
+                                   _dev(out_tokens, I32, "out_tokens", batch * 17), _stream(stream)))

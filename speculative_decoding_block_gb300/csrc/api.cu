@@ -1,0 +1,826 @@
+// api.cu -- the C ABI of include/vsd.h: model and cache objects, weight
+// repacking, tensor maps, argument checks, and the kernel sequence of the
+// greedy block-verify step.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "launch.h"
+#include "quant_kernels.cuh"
+#include "step_kernels.cuh"
+
+using namespace vsd;
+
+namespace {
+
+thread_local std::string g_err;
+
+vsd_status fail(vsd_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+#define CK(call)                                                                                     \
+  do {                                                                                               \
+    cudaError_t e_ = (call);                                                                         \
+    if (e_ != cudaSuccess)                                                                           \
+      return fail(e_ == cudaErrorMemoryAllocation ? VSD_ERR_OOM : VSD_ERR_CUDA, "%s: %s (%s:%d)", #call, \
+                  cudaGetErrorString(e_), __FILE__, __LINE__);                                       \
+  } while (0)
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D tiled tensor map over a row-major [outer, inner] matrix of 2-byte elements.
+vsd_status tmap_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer,
+                   uint32_t box_inner, uint32_t box_outer) {
+  if (!get_encoder()) return fail(VSD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(VSD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box %u x %u", (int)r,
+                (unsigned long long)outer, (unsigned long long)inner, box_outer, box_inner);
+  return VSD_OK;
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+int ceil_div(int x, int m) { return (x + m - 1) / m; }
+
+template <typename T>
+vsd_status dalloc(T** p, size_t count, bool zero = true) {
+  *p = nullptr;
+  if (count == 0) count = 1;
+  CK(cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T)));
+  if (zero) CK(cudaMemset(*p, 0, count * sizeof(T)));
+  return VSD_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+// One packed weight matrix of the GEMM kernel.
+struct Linear {
+  int fmt = 0;
+  int n_rows = 0;   // packed rows with data (tile rows beyond are zero)
+  int k = 0;
+  int n_tiles = 0, k_tiles = 0;
+  void* data = nullptr;        // BF16 [n_rows][k] | FP8 / NVFP4 tiles
+  float* row_scale = nullptr;  // FP8 / NVFP4
+  bool owns = true;
+  CUtensorMap tm{};            // BF16 only
+};
+
+void free_linear(Linear& l) {
+  if (l.owns && l.data) cudaFree(l.data);
+  if (l.row_scale) cudaFree(l.row_scale);
+  l.data = nullptr;
+  l.row_scale = nullptr;
+}
+
+}  // namespace
+
+struct vsd_model {
+  vsd_model_config cfg{};
+  uint16_t* embed = nullptr;
+  Linear lm;
+  std::vector<Linear> qkv, o, gu, down;
+  float2* rope = nullptr;
+  float* gamma = nullptr;
+  int sms = 1;
+};
+
+struct vsd_kv {
+  const vsd_model* m = nullptr;
+  int max_batch = 0, max_tokens = 0, num_pages = 0, ppr = 0, m_alloc = 0;
+  __nv_bfloat16 *k_pool = nullptr, *v_pool = nullptr;
+  int* page_table = nullptr;
+  float* x = nullptr;
+  __half *u = nullptr, *act_o = nullptr, *act_a = nullptr;
+  __nv_bfloat16 *q_tile = nullptr, *k_new = nullptr, *v_new = nullptr;
+  unsigned long long* keys = nullptr;
+  int* ctx_len = nullptr;
+  float* partials = nullptr;
+  size_t partials_cap = 0;
+  int* counters = nullptr;
+  int counters_cap = 0;
+  float *attn_o = nullptr, *attn_ml = nullptr;
+  int* attn_counters = nullptr;
+  size_t attn_items_cap = 0;
+  int* status = nullptr;
+  CUtensorMap tm_u{}, tm_o{}, tm_a{}, tm_q{}, tm_kc{}, tm_vc{}, tm_kn{}, tm_vn{};
+};
+
+namespace {
+
+// ------------------------------------------------------------------ weight packing
+// Builds a Linear from canonical matrices stacked in order (all the same
+// format and K); perm[p] = stacked source row of packed row p (-1 = zero row).
+vsd_status build_linear(const vsd_weight* const* parts, const int* part_rows, int n_parts, int K,
+                        const std::vector<int>& perm, cudaStream_t st, Linear* out) {
+  const int fmt = parts[0]->fmt;
+  int rows = 0;
+  for (int i = 0; i < n_parts; ++i) {
+    if (parts[i]->fmt != fmt) return fail(VSD_ERR_ARG, "stacked matrices must share one format");
+    if (!parts[i]->data_dev) return fail(VSD_ERR_ARG, "weight data pointer is NULL");
+    if (fmt != VSD_FMT_BF16 && !parts[i]->scale_dev) return fail(VSD_ERR_ARG, "weight scale pointer is NULL");
+    if (fmt == VSD_FMT_NVFP4 && !parts[i]->tensor_scale_dev) return fail(VSD_ERR_ARG, "NVFP4 tensor scale is NULL");
+    rows += part_rows[i];
+  }
+  if (fmt == VSD_FMT_NVFP4 && K % 16) return fail(VSD_ERR_ARG, "NVFP4 needs K %% 16 == 0 (K = %d)", K);
+  const int np = static_cast<int>(perm.size());
+  Linear L;
+  L.fmt = fmt;
+  L.n_rows = np;
+  L.k = K;
+  L.n_tiles = ceil_div(np, kTileN);
+  L.k_tiles = ceil_div(K, kTileK);
+  int* perm_d = nullptr;
+  vsd_status s = dalloc(&perm_d, np, false);
+  if (s) return s;
+  CK(cudaMemcpyAsync(perm_d, perm.data(), np * sizeof(int), cudaMemcpyHostToDevice, st));
+  if (fmt == VSD_FMT_BF16) {
+    uint16_t* stacked = nullptr;
+    if ((s = dalloc(&stacked, static_cast<size_t>(rows) * K, false))) return s;
+    size_t off = 0;
+    for (int i = 0; i < n_parts; ++i) {
+      CK(cudaMemcpyAsync(stacked + off, parts[i]->data_dev, static_cast<size_t>(part_rows[i]) * K * 2,
+                         cudaMemcpyDeviceToDevice, st));
+      off += static_cast<size_t>(part_rows[i]) * K;
+    }
+    uint16_t* packed = nullptr;
+    if ((s = dalloc(&packed, static_cast<size_t>(np) * K, false))) return s;
+    pack_bf16_kernel<<<1024, 256, 0, st>>>(stacked, perm_d, np, K, packed);
+    CK(cudaGetLastError());
+    CK(cudaStreamSynchronize(st));
+    cudaFree(stacked);
+    L.data = packed;
+    if ((s = tmap_2d(&L.tm, packed, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, np, 64, 128))) return s;
+  } else {
+    const size_t vbytes_row = fmt == VSD_FMT_FP8 ? K : K / 2;
+    uint8_t* stacked = nullptr;
+    uint8_t* stacked_sb = nullptr;
+    float* src_scale = nullptr;
+    if ((s = dalloc(&stacked, static_cast<size_t>(rows) * vbytes_row, false))) return s;
+    if ((s = dalloc(&src_scale, rows, false))) return s;
+    if (fmt == VSD_FMT_NVFP4 && (s = dalloc(&stacked_sb, static_cast<size_t>(rows) * (K / 16), false))) return s;
+    size_t off = 0;
+    for (int i = 0; i < n_parts; ++i) {
+      const size_t r = part_rows[i];
+      CK(cudaMemcpyAsync(stacked + off * vbytes_row, parts[i]->data_dev, r * vbytes_row, cudaMemcpyDeviceToDevice, st));
+      if (fmt == VSD_FMT_FP8) {
+        CK(cudaMemcpyAsync(src_scale + off, parts[i]->scale_dev, r * 4, cudaMemcpyDeviceToDevice, st));
+      } else {
+        CK(cudaMemcpyAsync(stacked_sb + off * (K / 16), parts[i]->scale_dev, r * (K / 16), cudaMemcpyDeviceToDevice, st));
+        float S = 0.0f;  // every row of this matrix gets its tensor scale
+        CK(cudaMemcpyAsync(&S, parts[i]->tensor_scale_dev, 4, cudaMemcpyDeviceToHost, st));
+        CK(cudaStreamSynchronize(st));
+        std::vector<float> rep(r, S);
+        CK(cudaMemcpyAsync(src_scale + off, rep.data(), r * 4, cudaMemcpyHostToDevice, st));
+        CK(cudaStreamSynchronize(st));
+      }
+      off += r;
+    }
+    const uint32_t tile_bytes = fmt == VSD_FMT_FP8 ? kFp8TileBytes : kFp4TileBytes;
+    uint8_t* tiles = nullptr;
+    if ((s = dalloc(&tiles, static_cast<size_t>(L.n_tiles) * L.k_tiles * tile_bytes, false))) return s;
+    if ((s = dalloc(&L.row_scale, static_cast<size_t>(L.n_tiles) * kTileN))) return s;
+    dim3 grid(L.k_tiles, L.n_tiles);
+    if (fmt == VSD_FMT_FP8) {
+      pack_fp8_kernel<<<grid, 256, 0, st>>>(stacked, src_scale, perm_d, np, K, L.k_tiles, tiles, L.row_scale);
+    } else {
+      pack_fp4_kernel<<<grid, 256, 0, st>>>(stacked, stacked_sb, perm_d, np, K, L.k_tiles, tiles);
+      pack_row_scale_kernel<<<ceil_div(np, 256), 256, 0, st>>>(src_scale, perm_d, np, L.row_scale);
+    }
+    CK(cudaGetLastError());
+    CK(cudaStreamSynchronize(st));
+    cudaFree(stacked);
+    cudaFree(src_scale);
+    if (stacked_sb) cudaFree(stacked_sb);
+    L.data = tiles;
+  }
+  cudaFree(perm_d);
+  *out = L;
+  return VSD_OK;
+}
+
+// Packed QKV rows: within every head, row pairs (i, i + hd/2) become
+// neighbours (2i, 2i+1) so that the RoPE partner sits in the adjacent lane.
+std::vector<int> rope_pair_perm(int rows, int hd) {
+  std::vector<int> p(rows);
+  for (int r = 0; r < rows; ++r) {
+    const int head = r / hd, w = r % hd;
+    p[r] = head * hd + ((w & 1) ? (w >> 1) + hd / 2 : (w >> 1));
+  }
+  return p;
+}
+
+// Packed gate/up rows: tile t holds 64 features, gate row of feature f at
+// 2(f - 64t), up row right after it.  Stacked source: [wg; wu].
+std::vector<int> gate_up_perm(int ffn) {
+  const int fp = round_up(ffn, 64);
+  std::vector<int> p(2 * fp);
+  for (int r = 0; r < 2 * fp; ++r) {
+    const int t = r / 128, w = r % 128, f = t * 64 + (w >> 1);
+    p[r] = f < ffn ? ((w & 1) ? ffn + f : f) : -1;
+  }
+  return p;
+}
+
+std::vector<int> identity_perm(int n) {
+  std::vector<int> p(n);
+  for (int i = 0; i < n; ++i) p[i] = i;
+  return p;
+}
+
+// ------------------------------------------------------------------ GEMM planning
+struct Plan {
+  int n_tok, tok_tiles, splits, kps, stages, grid;
+};
+
+Plan plan_gemm(const Linear& w, int M, bool no_split, int sms) {
+  Plan p;
+  p.tok_tiles = ceil_div(M, 256);
+  p.n_tok = std::max(16, round_up(ceil_div(M, p.tok_tiles), 16));
+  const int T = w.n_tiles * p.tok_tiles;
+  int splits = no_split ? 1 : std::max(1, std::min(w.k_tiles, sms / std::max(T, 1)));
+  p.kps = ceil_div(w.k_tiles, splits);
+  p.splits = ceil_div(w.k_tiles, p.kps);
+  const int wf = w.fmt;
+  const GemmSmem L = gemm_smem_layout(wf, p.n_tok, 1);
+  const int budget = 232448 - 1024 - static_cast<int>(gemm_ctrl_bytes());
+  p.stages = std::max(2, std::min(8, budget / static_cast<int>(L.stage_bytes)));
+  const int total = T * p.splits;
+  p.grid = std::min(total, sms);
+  return p;
+}
+
+// Programmatic dependent launch is used on explicit streams only (the
+// legacy default stream keeps plain stream ordering).
+bool use_pdl(cudaStream_t st) { return st != nullptr; }
+
+vsd_status run_gemm(const vsd_kv* kv, const Linear& w, int epi, const CUtensorMap& tm_act, int M, GemmArgs a,
+                    cudaStream_t st) {
+  const Plan p = plan_gemm(w, M, epi == EPI_ARGMAX, kv->m->sms);
+  a.w_tiles = static_cast<const uint8_t*>(w.data);
+  a.row_scale = w.row_scale;
+  a.n_rows = w.n_rows;
+  a.n_tiles = w.n_tiles;
+  a.k_tiles = w.k_tiles;
+  a.tok_tiles = p.tok_tiles;
+  a.n_tok = p.n_tok;
+  a.splits = p.splits;
+  a.kt_per_split = p.kps;
+  a.m_tokens = M;
+  a.stages = p.stages;
+  a.partials = kv->partials;
+  a.counters = kv->counters;
+  a.status = kv->status;
+  if (p.splits > 1) {
+    const size_t need = static_cast<size_t>(w.n_tiles) * p.tok_tiles * p.splits * 128 * p.n_tok;
+    if (need > kv->partials_cap || w.n_tiles * p.tok_tiles > kv->counters_cap)
+      return fail(VSD_ERR_UNSUPPORTED, "split-K workspace too small (%zu > %zu)", need, kv->partials_cap);
+  }
+  const cudaError_t e = launch_gemm(w.fmt, epi, tm_act, w.tm, a, p.grid, st, use_pdl(st));
+  if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
+  return VSD_OK;
+}
+
+vsd_status run_attention(vsd_kv* kv, int layer, int B, cudaStream_t st) {
+  const vsd_model* m = kv->m;
+  const vsd_model_config& c = m->cfg;
+  const int max_chunks = ceil_div(kv->max_tokens, 128) + 1;
+  int cps = std::max(1, ceil_div(B * c.n_kv * max_chunks, 2 * m->sms));
+  const int max_splits = ceil_div(max_chunks, cps);
+  if (static_cast<size_t>(B) * c.n_kv * max_splits > kv->attn_items_cap)
+    return fail(VSD_ERR_UNSUPPORTED, "attention workspace too small");
+  AttnArgs a{};
+  a.batch_cap = kv->max_batch;
+  a.n_q = c.n_q;
+  a.n_kv = c.n_kv;
+  a.hd = c.head_dim;
+  a.group = c.n_q / c.n_kv;
+  a.rows_valid = kRows * a.group;
+  a.chunks_per_split = cps;
+  a.max_splits = max_splits;
+  a.layer = layer;
+  a.num_pages = kv->num_pages;
+  a.pages_per_req = kv->ppr;
+  a.ctx_len = kv->ctx_len;
+  a.page_table = kv->page_table;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
+  a.part_o = kv->attn_o;
+  a.part_ml = kv->attn_ml;
+  a.counters = kv->attn_counters;
+  a.out = kv->act_o;
+  a.status = kv->status;
+  const cudaError_t e = launch_attn(c.head_dim, kv->tm_q, kv->tm_kc, kv->tm_vc, kv->tm_kn, kv->tm_vn, a,
+                                    dim3(max_splits, c.n_kv, B), st, use_pdl(st));
+  if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  return VSD_OK;
+}
+
+vsd_status check_model_config(const vsd_model_config* c) {
+  if (!c) return fail(VSD_ERR_ARG, "config is NULL");
+  if (c->layers < 1 || c->hidden < 64 || c->n_q < 1 || c->n_kv < 1 || c->ffn < 16 || c->vocab < 2 ||
+      c->max_positions < vsd::kRows)
+    return fail(VSD_ERR_ARG, "config has a non-positive or too small dimension");
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(VSD_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c->n_q % c->n_kv) return fail(VSD_ERR_ARG, "n_q must be a multiple of n_kv");
+  if (kRows * (c->n_q / c->n_kv) > 128)
+    return fail(VSD_ERR_UNSUPPORTED, "17 * (n_q / n_kv) must fit a 128-row attention tile");
+  if (c->hidden % 8 || c->ffn % 8 || (c->n_q * c->head_dim) % 8)
+    return fail(VSD_ERR_UNSUPPORTED, "hidden, ffn and n_q*head_dim must be multiples of 8");
+  if (c->hidden > 16384) return fail(VSD_ERR_UNSUPPORTED, "hidden above 16384");
+  for (int f : {c->attn_fmt, c->mlp_fmt})
+    if (f < VSD_FMT_BF16 || f > VSD_FMT_NVFP4) return fail(VSD_ERR_ARG, "unknown weight format %d", f);
+  if (!(c->eps > 0.0f) || !(c->rope_theta > 0.0f)) return fail(VSD_ERR_ARG, "eps and rope_theta must be > 0");
+  return VSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vsd_version(void) { return "vsd 0.1 sm_103a"; }
+const char* vsd_last_error(void) { return g_err.c_str(); }
+
+// ------------------------------------------------------------------ quantisers
+vsd_status vsd_quantize_fp8_rowwise(const uint16_t* w, int32_t n, int32_t k, uint8_t* q, float* scale,
+                                    vsd_stream stream) {
+  if (!w || !q || !scale) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (n < 1 || k < 2 || (k & 1)) return fail(VSD_ERR_ARG, "need n >= 1 and an even k >= 2");
+  quant_fp8_rowwise_kernel<<<n, 256, 0, stream>>>(w, k, q, scale);
+  CK(cudaGetLastError());
+  return VSD_OK;
+}
+
+vsd_status vsd_quantize_nvfp4(const uint16_t* w, int32_t n, int32_t k, uint8_t* q, uint8_t* sb, float* S,
+                              vsd_stream stream) {
+  if (!w || !q || !sb || !S) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (n < 1 || k < 16 || (k % 16)) return fail(VSD_ERR_ARG, "need n >= 1 and k a positive multiple of 16");
+  const size_t total = static_cast<size_t>(n) * k;
+  CK(cudaMemsetAsync(S, 0, 4, stream));
+  amax_kernel<<<std::min<size_t>(1024, (total + 255) / 256), 256, 0, stream>>>(w, total,
+                                                                               reinterpret_cast<unsigned int*>(S));
+  const size_t nb = total / 16;
+  quant_nvfp4_kernel<<<(nb + 255) / 256, 256, 0, stream>>>(w, nb, S, q, sb);
+  nvfp4_tensor_scale_kernel<<<1, 1, 0, stream>>>(S);
+  CK(cudaGetLastError());
+  return VSD_OK;
+}
+
+// ------------------------------------------------------------------ model
+vsd_status vsd_model_create(const vsd_model_config* cfg, const vsd_weights* w, vsd_stream stream, vsd_model** out) {
+  if (!out) return fail(VSD_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  vsd_status s = check_model_config(cfg);
+  if (s) return s;
+  if (!w || !w->embed_dev || !w->layers) return fail(VSD_ERR_ARG, "weights are NULL");
+  if (!cfg->tied && !w->lm_head_dev) return fail(VSD_ERR_ARG, "untied model needs lm_head");
+  int dev_count = 0;
+  if (cudaGetDeviceCount(&dev_count) != cudaSuccess || dev_count < 1) return fail(VSD_ERR_CUDA, "no CUDA device");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const vsd_model_config& c = *cfg;
+  vsd_model* m = new vsd_model();
+  m->cfg = c;
+  m->sms = sm_count();
+  auto cleanup = [&](vsd_status e) {
+    vsd_model_destroy(m);
+    return e;
+  };
+  const int H = c.hidden, hd = c.head_dim, F = c.ffn;
+  if ((s = dalloc(&m->embed, static_cast<size_t>(c.vocab) * H, false))) return cleanup(s);
+  if (cudaMemcpyAsync(m->embed, w->embed_dev, static_cast<size_t>(c.vocab) * H * 2, cudaMemcpyDeviceToDevice, st))
+    return cleanup(fail(VSD_ERR_CUDA, "embedding copy failed"));
+  // lm_head: BF16 rows of the vocabulary
+  vsd_weight lmw{VSD_FMT_BF16, c.tied ? m->embed : w->lm_head_dev, nullptr, nullptr};
+  const vsd_weight* lmp = &lmw;
+  int vrows = c.vocab;
+  if ((s = build_linear(&lmp, &vrows, 1, H, identity_perm(c.vocab), st, &m->lm))) return cleanup(s);
+  const int nq = c.n_q * hd, nk = c.n_kv * hd;
+  for (int l = 0; l < c.layers; ++l) {
+    const vsd_weight* L = w->layers + static_cast<size_t>(l) * 7;
+    for (int i = 0; i < 7; ++i) {
+      const int want = i < 4 ? c.attn_fmt : c.mlp_fmt;
+      if (L[i].fmt != want) return cleanup(fail(VSD_ERR_ARG, "layer %d matrix %d has format %d, config says %d", l, i, L[i].fmt, want));
+    }
+    Linear lin;
+    const vsd_weight* qkv[3] = {&L[0], &L[1], &L[2]};
+    int qkv_rows[3] = {nq, nk, nk};
+    if ((s = build_linear(qkv, qkv_rows, 3, H, rope_pair_perm(nq + 2 * nk, hd), st, &lin))) return cleanup(s);
+    m->qkv.push_back(lin);
+    const vsd_weight* op = &L[3];
+    int orows = H;
+    if ((s = build_linear(&op, &orows, 1, nq, identity_perm(H), st, &lin))) return cleanup(s);
+    m->o.push_back(lin);
+    const vsd_weight* gu[2] = {&L[4], &L[5]};
+    int gu_rows[2] = {F, F};
+    if ((s = build_linear(gu, gu_rows, 2, H, gate_up_perm(F), st, &lin))) return cleanup(s);
+    m->gu.push_back(lin);
+    const vsd_weight* dp = &L[6];
+    if ((s = build_linear(&dp, &orows, 1, F, identity_perm(H), st, &lin))) return cleanup(s);
+    m->down.push_back(lin);
+  }
+  // RoPE table: angle = pos * theta^(-2i/hd), evaluated in double, stored as fp32 (cos, sin)
+  {
+    const int half = hd / 2;
+    std::vector<float2> tab(static_cast<size_t>(c.max_positions) * half);
+    for (int p = 0; p < c.max_positions; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double ang = p * std::pow(static_cast<double>(c.rope_theta), -2.0 * i / hd);
+        tab[static_cast<size_t>(p) * half + i] = make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
+      }
+    if ((s = dalloc(&m->rope, tab.size(), false))) return cleanup(s);
+    if (cudaMemcpy(m->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice))
+      return cleanup(fail(VSD_ERR_CUDA, "RoPE table copy failed"));
+  }
+  {
+    std::vector<float> ones(std::max(H, 1), 1.0f);
+    if ((s = dalloc(&m->gamma, ones.size(), false))) return cleanup(s);
+    if (cudaMemcpy(m->gamma, ones.data(), ones.size() * 4, cudaMemcpyHostToDevice))
+      return cleanup(fail(VSD_ERR_CUDA, "norm weight copy failed"));
+  }
+  if (cudaStreamSynchronize(st) != cudaSuccess) return cleanup(fail(VSD_ERR_CUDA, "model creation failed"));
+  *out = m;
+  return VSD_OK;
+}
+
+void vsd_model_destroy(vsd_model* m) {
+  if (!m) return;
+  free_linear(m->lm);
+  for (auto* v : {&m->qkv, &m->o, &m->gu, &m->down})
+    for (auto& l : *v) free_linear(l);
+  if (m->embed) cudaFree(m->embed);
+  if (m->rope) cudaFree(m->rope);
+  if (m->gamma) cudaFree(m->gamma);
+  delete m;
+}
+
+// ------------------------------------------------------------------ KV cache + workspace
+vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_tokens, int32_t page_size,
+                         int32_t num_pages, vsd_kv** out) {
+  if (!m || !out) return fail(VSD_ERR_ARG, "NULL pointer");
+  *out = nullptr;
+  if (page_size != kPage) return fail(VSD_ERR_UNSUPPORTED, "page_size must be 16");
+  if (max_batch < 1 || max_batch > 4096) return fail(VSD_ERR_ARG, "max_batch out of range");
+  if (max_tokens < kRows || max_tokens > m->cfg.max_positions)
+    return fail(VSD_ERR_ARG, "max_tokens_per_req must lie in [17, max_positions]");
+  const vsd_model_config& c = m->cfg;
+  vsd_kv* kv = new vsd_kv();
+  auto cleanup = [&](vsd_status e) {
+    vsd_kv_destroy(kv);
+    return e;
+  };
+  kv->m = m;
+  kv->max_batch = max_batch;
+  kv->max_tokens = max_tokens;
+  kv->ppr = ceil_div(max_tokens, kPage);
+  kv->num_pages = num_pages > 0 ? num_pages : max_batch * kv->ppr;
+  const int hd = c.head_dim, H = c.hidden, F = c.ffn, nqd = c.n_q * hd;
+  const size_t pool = static_cast<size_t>(c.layers) * kv->num_pages * c.n_kv * kPage * hd;
+  vsd_status s;
+  if ((s = dalloc(&kv->k_pool, pool)) || (s = dalloc(&kv->v_pool, pool))) return cleanup(s);
+  {
+    std::vector<int> ident(static_cast<size_t>(max_batch) * kv->ppr);
+    for (size_t i = 0; i < ident.size(); ++i) ident[i] = static_cast<int>(i % kv->num_pages);
+    if ((s = dalloc(&kv->page_table, ident.size(), false))) return cleanup(s);
+    if (cudaMemcpy(kv->page_table, ident.data(), ident.size() * 4, cudaMemcpyHostToDevice))
+      return cleanup(fail(VSD_ERR_CUDA, "page table copy failed"));
+  }
+  const int M = kRows * max_batch;
+  kv->m_alloc = round_up(M, 16);
+  if ((s = dalloc(&kv->x, static_cast<size_t>(kv->m_alloc) * H)) || (s = dalloc(&kv->u, static_cast<size_t>(kv->m_alloc) * H)) ||
+      (s = dalloc(&kv->act_o, static_cast<size_t>(kv->m_alloc) * nqd)) ||
+      (s = dalloc(&kv->act_a, static_cast<size_t>(kv->m_alloc) * F)) ||
+      (s = dalloc(&kv->q_tile, static_cast<size_t>(max_batch) * c.n_kv * 128 * hd)) ||
+      (s = dalloc(&kv->k_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
+      (s = dalloc(&kv->v_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
+      (s = dalloc(&kv->keys, M)) || (s = dalloc(&kv->ctx_len, max_batch)) || (s = dalloc(&kv->status, 1)))
+    return cleanup(s);
+  kv->partials_cap = static_cast<size_t>(m->sms) * 128 * 256;
+  kv->counters_cap = m->sms;
+  if ((s = dalloc(&kv->partials, kv->partials_cap, false)) || (s = dalloc(&kv->counters, kv->counters_cap)))
+    return cleanup(s);
+  kv->attn_items_cap = static_cast<size_t>(4) * m->sms + static_cast<size_t>(2) * max_batch * c.n_kv;
+  if ((s = dalloc(&kv->attn_o, kv->attn_items_cap * 128 * hd, false)) ||
+      (s = dalloc(&kv->attn_ml, kv->attn_items_cap * 128 * 2, false)) ||
+      (s = dalloc(&kv->attn_counters, static_cast<size_t>(max_batch) * c.n_kv)))
+    return cleanup(s);
+  const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16, BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((s = tmap_2d(&kv->tm_u, kv->u, F16, H, kv->m_alloc, 64, 16)) ||
+      (s = tmap_2d(&kv->tm_o, kv->act_o, F16, nqd, kv->m_alloc, 64, 16)) ||
+      (s = tmap_2d(&kv->tm_a, kv->act_a, F16, F, kv->m_alloc, 64, 16)) ||
+      (s = tmap_2d(&kv->tm_q, kv->q_tile, BF16, hd, static_cast<uint64_t>(max_batch) * c.n_kv * 128, 64, 128)) ||
+      (s = tmap_2d(&kv->tm_kc, kv->k_pool, BF16, hd, pool / hd, 64, 16)) ||
+      (s = tmap_2d(&kv->tm_vc, kv->v_pool, BF16, hd, pool / hd, 64, 16)) ||
+      (s = tmap_2d(&kv->tm_kn, kv->k_new, BF16, hd, static_cast<uint64_t>(c.layers) * max_batch * c.n_kv * 32, 64, 32)) ||
+      (s = tmap_2d(&kv->tm_vn, kv->v_new, BF16, hd, static_cast<uint64_t>(c.layers) * max_batch * c.n_kv * 32, 64, 32)))
+    return cleanup(s);
+  if (cudaDeviceSynchronize() != cudaSuccess) return cleanup(fail(VSD_ERR_CUDA, "cache creation failed"));
+  *out = kv;
+  return VSD_OK;
+}
+
+void vsd_kv_destroy(vsd_kv* kv) {
+  if (!kv) return;
+  void* ptrs[] = {kv->k_pool, kv->v_pool, kv->page_table, kv->x, kv->u, kv->act_o, kv->act_a, kv->q_tile,
+                  kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->partials, kv->counters, kv->attn_o,
+                  kv->attn_ml, kv->attn_counters, kv->status};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  delete kv;
+}
+
+int32_t vsd_kv_pages_per_req(const vsd_kv* kv) { return kv ? kv->ppr : -1; }
+int32_t vsd_kv_num_pages(const vsd_kv* kv) { return kv ? kv->num_pages : -1; }
+
+vsd_status vsd_kv_set_page_table(vsd_kv* kv, const int32_t* table, vsd_stream stream) {
+  if (!kv || !table) return fail(VSD_ERR_ARG, "NULL pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t n = static_cast<size_t>(kv->max_batch) * kv->ppr;
+  CK(cudaMemcpyAsync(kv->page_table, table, n * 4, cudaMemcpyDeviceToDevice, st));
+  check_pages_kernel<<<64, 256, 0, st>>>(kv->page_table, n, kv->num_pages, kv->status);
+  CK(cudaGetLastError());
+  return VSD_OK;
+}
+
+static vsd_status kv_rows(const vsd_kv* kv, int req, int start, int count, uint16_t* k, uint16_t* v, int write,
+                          cudaStream_t st) {
+  if (!kv || !k || !v) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (req < 0 || req >= kv->max_batch) return fail(VSD_ERR_ARG, "request slot out of range");
+  if (start < 0 || count < 0 || start + count > kv->max_tokens) return fail(VSD_ERR_CAPACITY, "rows outside the cache");
+  if (count == 0) return VSD_OK;
+  const vsd_model_config& c = kv->m->cfg;
+  const size_t n = static_cast<size_t>(c.layers) * count * c.n_kv * c.head_dim;
+  const int grid = static_cast<int>(std::min<size_t>(4096, (n + 255) / 256));
+  for (int pass = 0; pass < 2; ++pass)
+    kv_rows_kernel<<<grid, 256, 0, st>>>(pass ? kv->v_pool : kv->k_pool, kv->page_table, kv->ppr, kv->num_pages,
+                                         c.layers, c.n_kv, c.head_dim, req, start, count,
+                                         reinterpret_cast<__nv_bfloat16*>(pass ? v : k), write, kv->status);
+  CK(cudaGetLastError());
+  return VSD_OK;
+}
+
+vsd_status vsd_kv_write(vsd_kv* kv, int32_t req, int32_t start, int32_t count, const uint16_t* k, const uint16_t* v,
+                        vsd_stream stream) {
+  return kv_rows(kv, req, start, count, const_cast<uint16_t*>(k), const_cast<uint16_t*>(v), 1,
+                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+vsd_status vsd_kv_read(const vsd_kv* kv, int32_t req, int32_t start, int32_t count, uint16_t* k, uint16_t* v,
+                       vsd_stream stream) {
+  return kv_rows(kv, req, start, count, k, v, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+vsd_status vsd_get_device_status(vsd_kv* kv, vsd_stream stream, int32_t* out) {
+  if (!kv || !out) return fail(VSD_ERR_ARG, "NULL pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  CK(cudaMemcpyAsync(&v, kv->status, 4, cudaMemcpyDeviceToHost, st));
+  CK(cudaMemsetAsync(kv->status, 0, 4, st));
+  CK(cudaStreamSynchronize(st));
+  *out = v;
+  return VSD_OK;
+}
+
+// ------------------------------------------------------------------ the step
+static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_lens, int* pending, const int* drafts,
+                              int* accepted, int* out_tokens, float* logits, float* hidden, cudaStream_t st) {
+  if (!m || !kv || !seq_lens || !pending || !drafts || !accepted || !out_tokens)
+    return fail(VSD_ERR_ARG, "NULL pointer");
+  if (kv->m != m) return fail(VSD_ERR_ARG, "the cache was created for another model");
+  if (B < 1 || B > kv->max_batch) return fail(VSD_ERR_ARG, "batch %d outside [1, %d]", B, kv->max_batch);
+  const vsd_model_config& c = m->cfg;
+  const int M = kRows * B, H = c.hidden;
+  vsd_status s;
+  {
+    EmbedArgs e{};
+    e.embed = m->embed;
+    e.vocab = c.vocab;
+    e.hidden = H;
+    e.seq_lens = seq_lens;
+    e.pending = pending;
+    e.drafts = drafts;
+    e.max_tokens = kv->max_tokens;
+    e.eps = c.eps;
+    e.gamma = m->gamma;
+    e.x = kv->x;
+    e.u = kv->u;
+    e.ctx_len = kv->ctx_len;
+    e.hidden0 = hidden;
+    e.status = kv->status;
+    CK(launch_ex(embed_norm_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), e));
+  }
+  const size_t layer_scratch = static_cast<size_t>(kv->max_batch) * c.n_kv * 32 * c.head_dim;
+  for (int l = 0; l < c.layers; ++l) {
+    GemmArgs a{};
+    a.q_tile = kv->q_tile;
+    a.k_new = kv->k_new + l * layer_scratch;
+    a.v_new = kv->v_new + l * layer_scratch;
+    a.ctx_len = kv->ctx_len;
+    a.rope = m->rope;
+    a.n_q = c.n_q;
+    a.n_kv = c.n_kv;
+    a.head_dim = c.head_dim;
+    if ((s = run_gemm(kv, m->qkv[l], EPI_QKV, kv->tm_u, M, a, st))) return s;
+    if ((s = run_attention(kv, l, B, st))) return s;
+    GemmArgs r{};
+    r.out_f32 = kv->x;
+    r.ld_out = H;
+    if ((s = run_gemm(kv, m->o[l], EPI_RESID, kv->tm_o, M, r, st))) return s;
+    CK(launch_ex(rmsnorm_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), (const float*)kv->x, H, c.eps,
+                 (const float*)m->gamma, kv->u, (float*)nullptr));
+    GemmArgs g{};
+    g.act_out = kv->act_a;
+    g.ffn = c.ffn;
+    if ((s = run_gemm(kv, m->gu[l], EPI_SILU, kv->tm_u, M, g, st))) return s;
+    if ((s = run_gemm(kv, m->down[l], EPI_RESID, kv->tm_a, M, r, st))) return s;
+    float* copy = hidden ? hidden + static_cast<size_t>(l + 1) * M * H : nullptr;
+    CK(launch_ex(rmsnorm_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), (const float*)kv->x, H, c.eps,
+                 (const float*)m->gamma, kv->u, copy));
+  }
+  {
+    GemmArgs a{};
+    a.keys = kv->keys;
+    a.logits = logits;
+    if ((s = run_gemm(kv, m->lm, EPI_ARGMAX, kv->tm_u, M, a, st))) return s;
+  }
+  CommitArgs ca{};
+  ca.vocab = c.vocab;
+  ca.layers = c.layers;
+  ca.n_kv = c.n_kv;
+  ca.hd = c.head_dim;
+  ca.batch_cap = kv->max_batch;
+  ca.num_pages = kv->num_pages;
+  ca.pages_per_req = kv->ppr;
+  ca.max_tokens = kv->max_tokens;
+  ca.keys = kv->keys;
+  ca.drafts = drafts;
+  ca.seq_lens = seq_lens;
+  ca.pending = pending;
+  ca.accepted = accepted;
+  ca.out_tokens = out_tokens;
+  ca.page_table = kv->page_table;
+  ca.k_new = kv->k_new;
+  ca.v_new = kv->v_new;
+  ca.k_pool = kv->k_pool;
+  ca.v_pool = kv->v_pool;
+  ca.status = kv->status;
+  CK(launch_ex(accept_commit_kernel, dim3(B), dim3(256), 0, st, use_pdl(st), ca));
+  return VSD_OK;
+}
+
+vsd_status vsd_verify_step(const vsd_model* m, vsd_kv* kv, int32_t batch, int32_t* seq_lens, int32_t* pending,
+                           const int32_t* drafts, int32_t* accepted, int32_t* out_tokens, vsd_stream stream) {
+  return verify_impl(m, kv, batch, seq_lens, pending, drafts, accepted, out_tokens, nullptr, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+vsd_status vsd_verify_step_debug(const vsd_model* m, vsd_kv* kv, int32_t batch, int32_t* seq_lens, int32_t* pending,
+                                 const int32_t* drafts, int32_t* accepted, int32_t* out_tokens, float* logits,
+                                 float* hidden, vsd_stream stream) {
+  return verify_impl(m, kv, batch, seq_lens, pending, drafts, accepted, out_tokens, logits, hidden,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ components
+vsd_status vsd_linear(const vsd_weight* w, int32_t n, int32_t k, const uint16_t* x, int32_t mtok, float* y,
+                      vsd_stream stream) {
+  if (!w || !x || !y) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (n < 1 || k < 8 || mtok < 1 || (k % 8)) return fail(VSD_ERR_ARG, "need n >= 1, m >= 1 and k a multiple of 8");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Linear L;
+  vsd_status s = build_linear(&w, &n, 1, k, identity_perm(n), st, &L);
+  if (s) return s;
+  CUtensorMap tm{};
+  if ((s = tmap_2d(&tm, x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k, mtok, 64, 16))) {
+    free_linear(L);
+    return s;
+  }
+  // a throw-away workspace sized like a cache's
+  vsd_kv kv;
+  vsd_model mm;
+  mm.sms = sm_count();
+  kv.m = &mm;
+  kv.partials_cap = static_cast<size_t>(mm.sms) * 128 * 256;
+  kv.counters_cap = mm.sms;
+  if ((s = dalloc(&kv.partials, kv.partials_cap, false)) || (s = dalloc(&kv.counters, kv.counters_cap)) ||
+      (s = dalloc(&kv.status, 1))) {
+    free_linear(L);
+    return s;
+  }
+  GemmArgs a{};
+  a.out_f32 = y;
+  a.ld_out = n;
+  s = run_gemm(&kv, L, EPI_STORE, tm, mtok, a, st);
+  cudaStreamSynchronize(st);
+  cudaFree(kv.partials);
+  cudaFree(kv.counters);
+  cudaFree(kv.status);
+  kv.partials = nullptr;
+  kv.counters = nullptr;
+  kv.status = nullptr;
+  free_linear(L);
+  mm.lm.data = nullptr;
+  return s;
+}
+
+vsd_status vsd_block_attention(const vsd_model* m, vsd_kv* kv, int32_t layer, int32_t B, const int32_t* seq_lens,
+                               const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new, uint16_t* out,
+                               vsd_stream stream) {
+  if (!m || !kv || !seq_lens || !q || !k_new || !v_new || !out) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (kv->m != m) return fail(VSD_ERR_ARG, "the cache was created for another model");
+  const vsd_model_config& c = m->cfg;
+  if (B < 1 || B > kv->max_batch || layer < 0 || layer >= c.layers) return fail(VSD_ERR_ARG, "batch or layer out of range");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t nq = static_cast<size_t>(B) * kRows * c.n_q * c.head_dim;
+  scatter_q_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), B, c.n_q, c.n_kv, c.head_dim,
+                                        kv->q_tile);
+  scatter_block_rows_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k_new), 1, B, c.n_kv,
+                                                 c.head_dim, kv->max_batch, layer, kv->k_new);
+  scatter_block_rows_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(v_new), 1, B, c.n_kv,
+                                                 c.head_dim, kv->max_batch, layer, kv->v_new);
+  clamp_ctx_kernel<<<ceil_div(B, 128), 128, 0, st>>>(seq_lens, B, kv->max_tokens, kv->ctx_len, kv->status);
+  CK(cudaGetLastError());
+  (void)nq;
+  vsd_status s = run_attention(kv, layer, B, st);
+  if (s) return s;
+  CK(cudaMemcpyAsync(out, kv->act_o, static_cast<size_t>(B) * kRows * c.n_q * c.head_dim * 2,
+                     cudaMemcpyDeviceToDevice, st));
+  return VSD_OK;
+}
+
+vsd_status vsd_accept_commit(const vsd_model* m, vsd_kv* kv, int32_t B, const float* logits, const uint16_t* k_new,
+                             const uint16_t* v_new, int32_t* seq_lens, int32_t* pending, const int32_t* drafts,
+                             int32_t* accepted, int32_t* out_tokens, vsd_stream stream) {
+  if (!m || !kv || !logits || !k_new || !v_new || !seq_lens || !pending || !drafts || !accepted || !out_tokens)
+    return fail(VSD_ERR_ARG, "NULL pointer");
+  if (kv->m != m) return fail(VSD_ERR_ARG, "the cache was created for another model");
+  const vsd_model_config& c = m->cfg;
+  if (B < 1 || B > kv->max_batch) return fail(VSD_ERR_ARG, "batch out of range");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  scatter_block_rows_kernel<<<512, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k_new), c.layers, B, c.n_kv,
+                                                 c.head_dim, kv->max_batch, 0, kv->k_new);
+  scatter_block_rows_kernel<<<512, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(v_new), c.layers, B, c.n_kv,
+                                                 c.head_dim, kv->max_batch, 0, kv->v_new);
+  logits_argmax_kernel<<<B * kRows, 256, 0, st>>>(logits, c.vocab, kv->keys);
+  CK(cudaGetLastError());
+  CommitArgs ca{};
+  ca.vocab = c.vocab;
+  ca.layers = c.layers;
+  ca.n_kv = c.n_kv;
+  ca.hd = c.head_dim;
+  ca.batch_cap = kv->max_batch;
+  ca.num_pages = kv->num_pages;
+  ca.pages_per_req = kv->ppr;
+  ca.max_tokens = kv->max_tokens;
+  ca.keys = kv->keys;
+  ca.drafts = drafts;
+  ca.seq_lens = seq_lens;
+  ca.pending = pending;
+  ca.accepted = accepted;
+  ca.out_tokens = out_tokens;
+  ca.page_table = kv->page_table;
+  ca.k_new = kv->k_new;
+  ca.v_new = kv->v_new;
+  ca.k_pool = kv->k_pool;
+  ca.v_pool = kv->v_pool;
+  ca.status = kv->status;
+  CK(launch_ex(accept_commit_kernel, dim3(B), dim3(256), 0, st, false, ca));
+  return VSD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,30 @@
+// attention.cu -- instantiations and launcher of the verify attention.
+#include <utility>
+
+#include "launch.h"
+
+namespace vsd {
+
+template <int HD>
+static cudaError_t launch_hd(const CUtensorMap& tm_q, const CUtensorMap& tm_kc, const CUtensorMap& tm_vc,
+                             const CUtensorMap& tm_kn, const CUtensorMap& tm_vn, const AttnArgs& a, dim3 grid,
+                             cudaStream_t st, bool pdl) {
+  static bool configured = false;
+  const uint32_t smem = attn_smem_bytes(HD);
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return launch_ex(attn_kernel<HD>, grid, dim3(kAttnThreads), smem, st, pdl, tm_q, tm_kc, tm_vc, tm_kn, tm_vn, a);
+}
+
+cudaError_t launch_attn(int hd, const CUtensorMap& tm_q, const CUtensorMap& tm_kc, const CUtensorMap& tm_vc,
+                        const CUtensorMap& tm_kn, const CUtensorMap& tm_vn, const AttnArgs& a, dim3 grid,
+                        cudaStream_t st, bool pdl) {
+  if (hd == 64) return launch_hd<64>(tm_q, tm_kc, tm_vc, tm_kn, tm_vn, a, grid, st, pdl);
+  if (hd == 128) return launch_hd<128>(tm_q, tm_kc, tm_vc, tm_kn, tm_vn, a, grid, st, pdl);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace vsd

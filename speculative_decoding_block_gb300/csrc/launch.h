@@ -1,0 +1,34 @@
+// launch.h -- host-side launchers of the templated kernels (one translation
+// unit per kernel family keeps the build parallel).
+#pragma once
+
+#include "attention.cuh"
+#include "gemm.cuh"
+
+namespace vsd {
+
+// Launches gemm_kernel<wf, epi> on `grid` persistent CTAs; programmatic
+// dependent launch when pdl is set.
+cudaError_t launch_gemm(int wf, int epi, const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
+                        int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_attn(int hd, const CUtensorMap& tm_q, const CUtensorMap& tm_kc, const CUtensorMap& tm_vc,
+                        const CUtensorMap& tm_kn, const CUtensorMap& tm_vn, const AttnArgs& a, dim3 grid,
+                        cudaStream_t st, bool pdl);
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
+
+}  // namespace vsd
