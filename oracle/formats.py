@@ -92,11 +92,21 @@ def _encode_rne(x, finite_mags: np.ndarray, sign_bit: int, nan_code: int | None)
     return code
 
 
+def _encode_chunked(x, finite_mags, sign_bit, nan_code, chunk=1 << 16):
+    """_encode_rne over slices of a flattened array (keeps temporaries small)."""
+    x = np.asarray(x, dtype=np.float64)
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, np.uint8)
+    for i in range(0, flat.size, chunk):
+        out[i:i + chunk] = _encode_rne(flat[i:i + chunk], finite_mags, sign_bit, nan_code)
+    return out.reshape(x.shape)
+
+
 def f64_to_e4m3(x) -> np.ndarray:
     """Round to nearest E4M3 code (ties to even), saturating at +-448."""
-    return _encode_rne(x, E4M3_MAG[:0x7F], 0x80, 0x7F)
+    return _encode_chunked(x, E4M3_MAG[:0x7F], 0x80, 0x7F)
 
 
 def f64_to_e2m1(x) -> np.ndarray:
     """Round to nearest E2M1 code (ties to even), saturating at +-6 (low nibble)."""
-    return _encode_rne(x, E2M1_MAG, 0x8, None)
+    return _encode_chunked(x, E2M1_MAG, 0x8, None)
