@@ -1,0 +1,536 @@
+"""Throughput of the greedy block-verify step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one vsd_verify_step over the whole batch of the workload (every
+request: pending token + 16 drafts through the target, argmax, prefix accept,
+KV commit).  The step is replayed from a CUDA graph with seq_lens / pending
+restored before each replay (the step is deterministic, so the re-committed
+rows get identical values); L2 is flushed between timed steps.  value =
+verified tokens (sum of accepted+1) per second over all ranks.
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun): the
+verify step has no cross-request exchange, so there is no collective on the
+data path; the barrier and the max over ranks are for timing only.
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workload import ROWS, WORKLOADS, gen, linear_shapes  # noqa: E402
+
+DEFAULT_WORKLOAD = "0.5b_mixed_b8_ctx512-4096"
+METRIC = "verified tokens/sec per GB300, 0.5B target, block 16; verify-step HBM % peak"
+
+
+# ------------------------------------------------------------------ byte accounting
+def weight_bytes(shape, name: str) -> int:
+    n, k, fmt = linear_shapes(shape)[name]
+    if fmt == "bf16":
+        return 2 * n * k
+    if fmt == "fp8":
+        return n * k + 4 * n
+    return n * k // 2 + n * k // 16 + 4
+
+
+def kernel_bytes(shape, lens, accepted):
+    """Algorithmic HBM bytes per launch of each kernel kind (weights / KV that must be read,
+    results that must be written; intermediates that can stay on chip are not counted)."""
+    B = len(lens)
+    M = ROWS * B
+    H = shape.hidden
+    kv_row = 2 * shape.n_kv * shape.head_dim * 2            # K + V of one token, one layer
+    act = lambda k: M * k * 2
+    return {
+        "embed": M * H * 2 + M * H * 6 + M * 4,
+        "qkv_gemm": sum(weight_bytes(shape, n) for n in ("wq", "wk", "wv")) + act(H),
+        "attention": int(np.sum(lens)) * kv_row + M * shape.n_q * shape.head_dim * 2 * 2,
+        "o_proj_gemm": weight_bytes(shape, "wo") + act(shape.n_q * shape.head_dim) + 2 * M * H * 4 + act(H),
+        "gate_up_gemm": weight_bytes(shape, "wg") + weight_bytes(shape, "wu") + act(H) + act(shape.ffn),
+        "down_gemm": weight_bytes(shape, "wd") + act(shape.ffn) + 2 * M * H * 4 + act(H),
+        "lm_head_gemm": shape.vocab * H * 2 + act(H),
+        "accept_commit": int(np.sum(np.asarray(accepted) + 1)) * kv_row * shape.layers + B * 4 * 60,
+    }
+
+
+def step_bytes(shape, lens, accepted) -> int:
+    """Algorithmic bytes of one whole step: every weight once (incl. scales), the lm_head,
+    17*B embedding rows, the KV context, the committed rows, ids and outputs."""
+    B = len(lens)
+    w = sum(weight_bytes(shape, n) for n in linear_shapes(shape)) * shape.layers
+    w += shape.vocab * shape.hidden * 2
+    emb = ROWS * B * shape.hidden * 2
+    kv_row = 2 * shape.n_kv * shape.head_dim * 2 * shape.layers
+    kv = int(np.sum(lens)) * kv_row
+    commit = int(np.sum(np.asarray(accepted) + 1)) * kv_row
+    io = B * (16 * 4 + 8) + B * (4 + 17 * 4 + 8)
+    return w + emb + kv + commit + io
+
+
+def step_flops(shape, lens) -> float:
+    B = len(lens)
+    M = ROWS * B
+    params = sum(n * k for n, k, _ in linear_shapes(shape).values()) * shape.layers + shape.vocab * shape.hidden
+    attn = 4 * ROWS * shape.n_q * shape.head_dim * (float(np.sum(lens)) + 9) * shape.layers
+    return 2.0 * M * params + attn
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "speculative_decoding_block_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_source_sha()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == kind and parts[1] == workload \
+                and parts[3] == sha:
+            return int(parts[2])
+    return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) sample
+def _oracle_worker(name: str, n_requests: int, budget_s: float, go, q):
+    """Runs in a spawned process: oracle set-up, then (after `go`) a timed sample."""
+    try:
+        import torch  # noqa: F401  (CPU only)
+        from oracle import model as OM
+        from tests.oracle_helpers import oracle_model, oracle_state_from_kv
+        w = WORKLOADS[name]
+        shape = w.shape
+        master = gen.master_weights(shape, w.seed)
+        om = oracle_model(shape, master)
+        del master
+        lens = gen.context_lengths(w)
+        pend = gen.pending_tokens(w)
+        ks = gen.prefix_lengths(w)
+        reqs = []
+        for b in range(min(n_requests, w.batch)):
+            kk, vv = gen.synthetic_kv(shape, int(lens[b]), w.seed, b)
+            st = oracle_state_from_kv(shape, kk, vv, int(pend[b]))
+            g = OM.ar_greedy(om, st.copy(), min(int(ks[b]) + 1, 16))
+            reqs.append((st, gen.plant_drafts(g, int(ks[b]), shape.vocab, "bench", w.seed, b)))
+        q.put(("ready", None))
+        go.wait()
+        tokens, steps, t0 = 0, 0, time.perf_counter()
+        while True:
+            st, d = reqs[steps % len(reqs)]
+            r = OM.verify_step(om, st.copy(), d)
+            tokens += r["accepted"] + 1
+            steps += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        q.put(("done", {"tokens": tokens, "steps": steps, "seconds": dt,
+                        "cores": len(os.sched_getaffinity(0))}))
+    except Exception as e:  # report, never hang the parent
+        q.put(("error", repr(e)))
+
+
+def start_oracle(name: str, n_requests: int, budget_s: float):
+    ctx = mp.get_context("spawn")
+    go, q = ctx.Event(), ctx.Queue()
+    p = ctx.Process(target=_oracle_worker, args=(name, n_requests, budget_s, go, q), daemon=True)
+    p.start()
+    return p, go, q
+
+
+def finish_oracle(handle, timeout=900):
+    p, go, q = handle
+    go.set()
+    res = None
+    t_end = time.time() + timeout
+    while time.time() < t_end:
+        try:
+            kind, val = q.get(timeout=5)
+        except Exception:
+            if not p.is_alive():
+                break
+            continue
+        if kind == "done":
+            res = val
+            break
+        if kind == "error":
+            res = {"error": val}
+            break
+    p.join(timeout=10)
+    if p.is_alive():
+        p.kill()
+    return res
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, rank: int, world: int):
+    import torch
+    from speculative_decoding_block_gb300 import binding as B
+    from speculative_decoding_block_gb300.build import build
+    from speculative_decoding_block_gb300.target import build_target
+
+    w = WORKLOADS[args.workload]
+    shape = w.shape
+    oracle_handle = None
+    if rank == 0 and not args.no_cpu_baseline:
+        oracle_handle = start_oracle(args.workload, n_requests=2, budget_s=args.cpu_budget)
+
+    build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = "cuda"
+    max_tok = w.max_tokens_per_req()
+    master = gen.master_weights(shape, w.seed)
+    model, _ = build_target(shape, master, max_positions=max_tok)
+    del master
+    Bn = w.batch
+    kv = B.vsd_kv_create(model, Bn, max_tok)
+    if w.paged:
+        pt = gen.page_table(w, kv.pages_per_req)
+        B.vsd_kv_set_page_table(kv, torch.tensor(pt, device=dev).contiguous())
+    lens = gen.context_lengths(w)
+    pend = gen.pending_tokens(w)
+    for b in range(Bn):
+        kk, vv = gen.synthetic_kv(shape, int(lens[b]), w.seed, b)
+        B.vsd_kv_write(kv, b, 0, kk.to(dev).contiguous(), vv.to(dev).contiguous())
+        del kk, vv
+    torch.cuda.synchronize()
+
+    seq0 = torch.tensor(lens, dtype=torch.int32, device=dev)
+    pend0 = torch.tensor(pend, dtype=torch.int32, device=dev)
+    seq = seq0.clone()
+    pen = pend0.clone()
+    acc = torch.empty(Bn, dtype=torch.int32, device=dev)
+    out = torch.empty((Bn, ROWS), dtype=torch.int32, device=dev)
+    drafts = torch.zeros((Bn, 16), dtype=torch.int32, device=dev)
+
+    # greedy trace of every request from the library itself (verify steps with
+    # arbitrary drafts advance the greedy continuation by a+1 >= 1 tokens)
+    trace = [[] for _ in range(Bn)]
+    rnd = np.random.default_rng(12345)
+    while min(len(t) for t in trace) < ROWS:
+        drafts.copy_(torch.tensor(rnd.integers(0, shape.vocab, (Bn, 16)), dtype=torch.int32))
+        B.vsd_verify_step(model, kv, Bn, seq, pen, drafts, acc, out)
+        o = out.cpu().numpy()
+        for b in range(Bn):
+            trace[b].extend(int(x) for x in o[b] if x >= 0)
+    ks = gen.prefix_lengths(w)
+    planted = np.stack([gen.plant_drafts(np.array(trace[b]), int(ks[b]), shape.vocab, "bench", w.seed, b)
+                        for b in range(Bn)])
+    drafts.copy_(torch.tensor(planted, dtype=torch.int32))
+    seq.copy_(seq0)
+    pen.copy_(pend0)
+    B.vsd_verify_step(model, kv, Bn, seq, pen, drafts, acc, out)
+    torch.cuda.synchronize()
+    assert B.vsd_get_device_status(kv) == 0
+    accepted = acc.cpu().numpy()
+    tokens_per_step = int(np.sum(accepted + 1))
+
+    # CUDA graph of one step on a side stream
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    seq.copy_(seq0)
+    pen.copy_(pend0)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        B.vsd_verify_step(model, kv, Bn, seq, pen, drafts, acc, out, stream=stream)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def one_step(timed_events=None):
+        with torch.cuda.stream(stream):
+            seq.copy_(seq0)
+            pen.copy_(pend0)
+            flush.fill_(1.0)
+            if timed_events:
+                timed_events[0].record(stream)
+            g.replay()
+            if timed_events:
+                timed_events[1].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    if not np.array_equal(acc.cpu().numpy(), accepted):
+        raise RuntimeError("graph replay gave different accepted lengths than the direct call")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(args.steps):
+            one_step(evs[i])
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+
+    # per-kernel times of the same step (events around every launch)
+    prof = []
+    for _ in range(3):
+        seq.copy_(seq0)
+        pen.copy_(pend0)
+        flush.fill_(1.0)
+        prof = B.vsd_verify_step_profiled(model, kv, Bn, seq, pen, drafts, acc, out, stream=stream)
+    per_kind = {}
+    for kind, ms in prof:
+        per_kind.setdefault(kind, []).append(ms)
+    kb = kernel_bytes(shape, lens, accepted)
+    kernels = {}
+    for kind, v in per_kind.items():
+        avg = sum(v) / len(v)
+        kernels[kind] = {"launches": len(v), "ms_total": round(sum(v), 4), "us_avg": round(avg * 1e3, 2),
+                         "bytes_per_launch": kb[kind], "gbs": round(kb[kind] / (avg * 1e-3) / 1e9, 1)}
+    tot_prof = sum(k["ms_total"] for k in kernels.values())
+    for k in kernels.values():
+        k["share"] = round(k["ms_total"] / tot_prof, 4)
+    dominant = max(kernels, key=lambda k: kernels[k]["ms_total"])
+
+    # end to end through the public call: pinned host inputs -> device, step, outputs -> host
+    h_seq = torch.tensor(lens, dtype=torch.int32).pin_memory()
+    h_pen = torch.tensor(pend, dtype=torch.int32).pin_memory()
+    h_dr = torch.tensor(planted, dtype=torch.int32).pin_memory()
+    h_acc = torch.empty(Bn, dtype=torch.int32).pin_memory()
+    h_out = torch.empty((Bn, ROWS), dtype=torch.int32).pin_memory()
+    h_seq_out = torch.empty(Bn, dtype=torch.int32).pin_memory()
+    h_pen_out = torch.empty(Bn, dtype=torch.int32).pin_memory()
+    e2e_times = []
+    e2e_tokens = 0
+    for i in range(args.warmup + args.steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            seq.copy_(h_seq, non_blocking=True)
+            pen.copy_(h_pen, non_blocking=True)
+            drafts.copy_(h_dr, non_blocking=True)
+            B.vsd_verify_step(model, kv, Bn, seq, pen, drafts, acc, out, stream=stream)
+            h_acc.copy_(acc, non_blocking=True)
+            h_out.copy_(out, non_blocking=True)
+            h_seq_out.copy_(seq, non_blocking=True)
+            h_pen_out.copy_(pen, non_blocking=True)
+        stream.synchronize()
+        if i >= args.warmup:
+            e2e_times.append(time.perf_counter() - t0)
+            e2e_tokens += int(np.sum(h_acc.numpy() + 1))
+    h2d = 4 * Bn + 4 * Bn + 4 * Bn * 16
+    d2h = 4 * Bn + 4 * Bn * ROWS + 8 * Bn
+    e2e_value = e2e_tokens * world / sum(e2e_times)
+
+    hbm, tf_burst, tf_sust, peak_src = peaks()
+    sb = step_bytes(shape, lens, accepted)
+    ms_per_step = total_s * 1e3 / args.steps
+    value = tokens_per_step * args.steps * world / total_s
+    dk = kernels[dominant]
+    achieved = dk["bytes_per_launch"] / (dk["us_avg"] * 1e-6) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded random-init weights, random KV context, planted draft prefixes)",
+        "config": {
+            "workload": w.name, "model": shape.name, "layers": shape.layers, "hidden": shape.hidden,
+            "heads": f"{shape.n_q}q/{shape.n_kv}kv/{shape.head_dim}", "ffn": shape.ffn, "vocab": shape.vocab,
+            "weights": f"attn {shape.attn_fmt}, mlp {shape.mlp_fmt}, embed/lm_head bf16",
+            "batch": Bn, "rows_per_request": ROWS, "ctx_lens": [int(x) for x in lens],
+            "paged": w.paged, "accepted": [int(a) for a in accepted],
+            "tokens_per_step": tokens_per_step, "mean_accepted_plus_1": round(tokens_per_step / Bn, 3),
+            "parallelism": f"replicas x{world}", "l2": "flushed between steps (256 MiB write)",
+            "graph": "one CUDA graph per step", "step_bytes": sb, "step_gflop": round(step_flops(shape, lens) / 1e9, 2),
+        },
+        "verify_steps_per_s": round(args.steps * world / total_s, 2),
+        "step_hbm_frac": round(sb / (ms_per_step * 1e-3) / 1e9 / hbm, 4),
+        "step_hbm_frac_nominal_8tbs": round(sb / (ms_per_step * 1e-3) / 1e9 / 8000.0, 4),
+        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": recorded_traffic(dominant, w.name),
+                     "bytes_per_launch": dk["bytes_per_launch"], "us_avg": dk["us_avg"]},
+        "kernels": kernels,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * statistics.mean(e2e_times), 4),
+                "call": "vsd_verify_step (direct launches, no graph)"},
+        "gpu_launches": len(prof),
+        "clocks": clk.summary(),
+    }
+    if oracle_handle is not None:
+        r = finish_oracle(oracle_handle)
+        if r and "tokens" in r:
+            result["cpu_baseline"] = {
+                "value": round(r["tokens"] / r["seconds"], 3), "unit": "tokens/s", "cores": r["cores"],
+                "kind": "oracle",
+                "sample": f"{r['steps']} float64 verify steps of requests 0-1 of this workload "
+                          f"(one request per step) in {r['seconds']:.1f} s"}
+        else:
+            result["cpu_baseline"] = {"value": None, "unit": "tokens/s", "kind": "oracle",
+                                      "error": (r or {}).get("error", "no result")}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The float64 oracle on the host cores: each step = one request's verify step."""
+    import torch  # noqa: F401
+    from oracle import model as OM
+    from tests.oracle_helpers import oracle_model, oracle_state_from_kv
+    w = WORKLOADS[args.workload]
+    shape = w.shape
+    master = gen.master_weights(shape, w.seed)
+    om = oracle_model(shape, master)
+    del master
+    lens, pend, ks = gen.context_lengths(w), gen.pending_tokens(w), gen.prefix_lengths(w)
+    reqs = []
+    for b in range(min(2, w.batch)):
+        kk, vv = gen.synthetic_kv(shape, int(lens[b]), w.seed, b)
+        st = oracle_state_from_kv(shape, kk, vv, int(pend[b]))
+        g = OM.ar_greedy(om, st.copy(), min(int(ks[b]) + 1, 16))
+        reqs.append((st, gen.plant_drafts(g, int(ks[b]), shape.vocab, "bench", w.seed, b)))
+    for i in range(args.warmup):
+        st, d = reqs[i % len(reqs)]
+        OM.verify_step(om, st.copy(), d)
+    tokens, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        st, d = reqs[i % len(reqs)]
+        tokens += OM.verify_step(om, st.copy(), d)["accepted"] + 1
+    dt = time.perf_counter() - t0
+    value = tokens / dt
+    cores = len(os.sched_getaffinity(0))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded random-init weights, random KV context, planted draft prefixes)",
+        "config": {"workload": w.name, "model": shape.name, "batch_sample": "one request per step, requests 0-1",
+                   "parallelism": "none (host cores)"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} float64 verify steps (one request each), {dt:.1f} s"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of timed oracle work")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_gpu(args, rank, world)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -172,6 +172,19 @@ vsd_status vsd_kv_write(vsd_kv* kv, int32_t req, int32_t start, int32_t count,
 vsd_status vsd_kv_read(const vsd_kv* kv, int32_t req, int32_t start, int32_t count,
                        uint16_t* k_dev, uint16_t* v_dev, vsd_stream stream);
 
+/* Phase tracing for profiling.  With max_launches > 0, the kernels of later
+ * steps store globaltimer (ns) at their phase boundaries into a library-owned
+ * table [launch][CTA < 1024][tag < 64] (0 = not reached); 0 turns tracing
+ * off.  Launch ids count kernel launches in order from 0 after each read.
+ * vsd_trace_read copies the table rows of up to max_launches launches to
+ * slots_host (max_launches * 1024 * 64 words), clears the table, restarts the
+ * launch ids and returns the number of table rows copied; it synchronises
+ * the stream.  A step captured in a CUDA graph keeps the launch ids it was
+ * captured with. */
+vsd_status vsd_trace_enable(vsd_kv* kv, int32_t max_launches);
+vsd_status vsd_trace_read(vsd_kv* kv, uint64_t* slots_host, int32_t max_launches, int32_t* n_launches,
+                          vsd_stream stream);
+
 /* Reads and clears the device status word (VSD_DEV_* bits).  Synchronises
  * the stream. */
 vsd_status vsd_get_device_status(vsd_kv* kv, vsd_stream stream, int32_t* status_host);
@@ -204,6 +217,28 @@ vsd_status vsd_verify_step_debug(const vsd_model* m, vsd_kv* kv, int32_t batch,
                                  const int32_t* drafts_dev, int32_t* accepted_dev,
                                  int32_t* out_tokens_dev, float* logits_dev,
                                  float* hidden_dev, vsd_stream stream);
+
+/* Kernel kinds reported by vsd_verify_step_profiled. */
+#define VSD_K_EMBED      0  /* embedding gather (+ f16 copy, sums of squares) */
+#define VSD_K_QKV        1  /* QKV GEMM + RMSNorm scale + RoPE + block K/V to scratch */
+#define VSD_K_ATTENTION  2  /* verify attention */
+#define VSD_K_O_PROJ     3  /* O GEMM + residual */
+#define VSD_K_GATE_UP    4  /* gate/up GEMM + RMSNorm scale + SiLU * up */
+#define VSD_K_DOWN       5  /* down GEMM + residual */
+#define VSD_K_LM_HEAD    6  /* lm_head GEMM + RMSNorm scale + argmax */
+#define VSD_K_COMMIT     7  /* accept + KV commit */
+
+/* The same step with a CUDA event recorded before and after every kernel
+ * launch (which keeps each launch from overlapping its neighbours).  Writes,
+ * for each launch i < *n_launches_host (at most max_launches), its kind
+ * (VSD_K_*) to kinds_host[i] and its duration in milliseconds to
+ * ms_host[i].  Synchronises the stream; for measurement, not for serving. */
+vsd_status vsd_verify_step_profiled(const vsd_model* m, vsd_kv* kv, int32_t batch,
+                                    int32_t* seq_lens_dev, int32_t* pending_dev,
+                                    const int32_t* drafts_dev, int32_t* accepted_dev,
+                                    int32_t* out_tokens_dev, int32_t max_launches,
+                                    int32_t* kinds_host, float* ms_host,
+                                    int32_t* n_launches_host, vsd_stream stream);
 
 /* ---------------------------------------------------------------- components
  * Single kernels of the step, exposed so that each can be checked alone.  */

@@ -25,8 +25,11 @@ EXPORTS = [
     "vsd_model_create", "vsd_model_destroy", "vsd_kv_create", "vsd_kv_destroy",
     "vsd_kv_pages_per_req", "vsd_kv_num_pages", "vsd_kv_set_page_table", "vsd_kv_write",
     "vsd_kv_read", "vsd_get_device_status", "vsd_verify_step", "vsd_verify_step_debug",
-    "vsd_linear", "vsd_block_attention", "vsd_accept_commit",
+    "vsd_linear", "vsd_block_attention", "vsd_accept_commit", "vsd_verify_step_profiled",
+    "vsd_trace_enable", "vsd_trace_read",
 ]
+KERNEL_KINDS = ["embed", "qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm",
+                "lm_head_gemm", "accept_commit"]
 
 
 class VsdError(RuntimeError):
@@ -83,7 +86,11 @@ def lib() -> ctypes.CDLL:
             "vsd_get_device_status": ([p, p, ctypes.POINTER(c_int)], c_int),
             "vsd_verify_step": ([p, p, c_int, p, p, p, p, p, p], c_int),
             "vsd_verify_step_debug": ([p, p, c_int, p, p, p, p, p, p, p, p], c_int),
+            "vsd_verify_step_profiled": ([p, p, c_int, p, p, p, p, p, c_int, p, p, ctypes.POINTER(c_int)],
+                                         c_int),
             "vsd_linear": ([ctypes.POINTER(Weight), c_int, c_int, p, c_int, p, p], c_int),
+            "vsd_trace_enable": ([p, c_int], c_int),
+            "vsd_trace_read": ([p, p, c_int, ctypes.POINTER(c_int), p], c_int),
             "vsd_block_attention": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
             "vsd_accept_commit": ([p, p, c_int, p, p, p, p, p, p, p, p, p], c_int),
         }
@@ -217,6 +224,23 @@ def vsd_kv_read(kv: KV, req: int, start: int, k, v, stream=None) -> None:
                              _stream(stream)))
 
 
+def vsd_trace_enable(kv: KV, max_launches: int) -> None:
+    _check(lib().vsd_trace_enable(kv.handle, max_launches))
+
+
+TRACE_CTAS, TRACE_TAGS = 1024, 64
+
+
+def vsd_trace_read(kv: KV, max_launches: int = 256, stream=None):
+    """Timestamp table as a numpy array [launches, 1024 CTAs, 64 tags] of uint64 ns (0 = not reached)."""
+    import numpy as np
+    buf = np.zeros((max_launches, TRACE_CTAS, TRACE_TAGS), dtype=np.uint64)
+    n = ctypes.c_int32()
+    _check(lib().vsd_trace_read(kv.handle, ctypes.c_void_p(buf.ctypes.data), max_launches, ctypes.byref(n),
+                                _stream(stream)))
+    return buf[: n.value]
+
+
 def vsd_get_device_status(kv: KV, stream=None) -> int:
     out = ctypes.c_int32()
     _check(lib().vsd_get_device_status(kv.handle, _stream(stream), ctypes.byref(out)))
@@ -241,6 +265,23 @@ def vsd_verify_step_debug(model: Model, kv: KV, batch: int, seq_lens, pending, d
                                        _dev(out_tokens, I32, "out_tokens", batch * 17),
                                        _dev(logits, F32, "logits"), _dev(hidden, F32, "hidden"),
                                        _stream(stream)))
+
+
+def vsd_verify_step_profiled(model: Model, kv: KV, batch: int, seq_lens, pending, drafts, accepted,
+                             out_tokens, max_launches: int = 4096, stream=None):
+    """Runs one step with per-launch events; returns [(kind name, ms)] in launch order."""
+    kinds = (ctypes.c_int32 * max_launches)()
+    ms = (ctypes.c_float * max_launches)()
+    n = ctypes.c_int32()
+    _check(lib().vsd_verify_step_profiled(model.handle, kv.handle, batch,
+                                          _dev(seq_lens, I32, "seq_lens", batch),
+                                          _dev(pending, I32, "pending", batch),
+                                          _dev(drafts, I32, "drafts", batch * 16),
+                                          _dev(accepted, I32, "accepted", batch),
+                                          _dev(out_tokens, I32, "out_tokens", batch * 17), max_launches,
+                                          ctypes.cast(kinds, ctypes.c_void_p), ctypes.cast(ms, ctypes.c_void_p),
+                                          ctypes.byref(n), _stream(stream)))
+    return [(KERNEL_KINDS[kinds[i]], float(ms[i])) for i in range(min(n.value, max_launches))]
 
 
 def vsd_linear(weight: Weight, n: int, k: int, x, y, stream=None) -> None:

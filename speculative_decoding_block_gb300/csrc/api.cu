@@ -118,7 +118,6 @@ struct vsd_model {
   Linear lm;
   std::vector<Linear> qkv, o, gu, down;
   float2* rope = nullptr;
-  float* gamma = nullptr;
   int sms = 1;
 };
 
@@ -132,18 +131,31 @@ struct vsd_kv {
   __nv_bfloat16 *q_tile = nullptr, *k_new = nullptr, *v_new = nullptr;
   unsigned long long* keys = nullptr;
   int* ctx_len = nullptr;
-  float* partials = nullptr;
-  size_t partials_cap = 0;
-  int* counters = nullptr;
-  int counters_cap = 0;
+  int* req_ok = nullptr;
+  float* ssq = nullptr;  // [ceil(H/128)][m_alloc] sums of squares of the residual rows
   float *attn_o = nullptr, *attn_ml = nullptr;
   int* attn_counters = nullptr;
   size_t attn_items_cap = 0;
   int* status = nullptr;
-  CUtensorMap tm_u{}, tm_o{}, tm_a{}, tm_q{}, tm_kc{}, tm_vc{}, tm_kn{}, tm_vn{};
+  unsigned long long* trace = nullptr;  // optional phase timestamps [launch][CTA][tag]
+  int trace_launches = 0;
+  int trace_seq = 0;
+  // GEMM activation maps, one per token-tile height 16, 32, ..., 256 rows
+  CUtensorMap tm_u[kActBoxes]{}, tm_o[kActBoxes]{}, tm_a[kActBoxes]{};
+  CUtensorMap tm_q{}, tm_kc{}, tm_vc{}, tm_kn{}, tm_vn{};
 };
 
 namespace {
+
+Trace next_trace(vsd_kv* kv) {
+  Trace t{};
+  if (kv && kv->trace) {
+    t.buf = kv->trace;
+    t.max_launches = kv->trace_launches;
+    t.id = kv->trace_seq++;
+  }
+  return t;
+}
 
 // ------------------------------------------------------------------ weight packing
 // Builds a Linear from canonical matrices stacked in order (all the same
@@ -187,7 +199,7 @@ vsd_status build_linear(const vsd_weight* const* parts, const int* part_rows, in
     CK(cudaStreamSynchronize(st));
     cudaFree(stacked);
     L.data = packed;
-    if ((s = tmap_2d(&L.tm, packed, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, np, 64, 128))) return s;
+    if ((s = tmap_2d(&L.tm, packed, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, np, 64, 128))) return s;
   } else {
     const size_t vbytes_row = fmt == VSD_FMT_FP8 ? K : K / 2;
     uint8_t* stacked = nullptr;
@@ -266,34 +278,83 @@ std::vector<int> identity_perm(int n) {
 }
 
 // ------------------------------------------------------------------ GEMM planning
-struct Plan {
-  int n_tok, tok_tiles, splits, kps, stages, grid;
-};
-
-Plan plan_gemm(const Linear& w, int M, bool no_split, int sms) {
-  Plan p;
-  p.tok_tiles = ceil_div(M, 256);
-  p.n_tok = std::max(16, round_up(ceil_div(M, p.tok_tiles), 16));
-  const int T = w.n_tiles * p.tok_tiles;
-  int splits = no_split ? 1 : std::max(1, std::min(w.k_tiles, sms / std::max(T, 1)));
-  p.kps = ceil_div(w.k_tiles, splits);
-  p.splits = ceil_div(w.k_tiles, p.kps);
-  const int wf = w.fmt;
-  const GemmSmem L = gemm_smem_layout(wf, p.n_tok, 1);
-  const int budget = 232448 - 1024 - static_cast<int>(gemm_ctrl_bytes());
-  p.stages = std::max(2, std::min(8, budget / static_cast<int>(L.stage_bytes)));
-  const int total = T * p.splits;
-  p.grid = std::min(total, sms);
-  return p;
-}
-
 // Programmatic dependent launch is used on explicit streams only (the
 // legacy default stream keeps plain stream ordering).
 bool use_pdl(cudaStream_t st) { return st != nullptr; }
 
-vsd_status run_gemm(const vsd_kv* kv, const Linear& w, int epi, const CUtensorMap& tm_act, int M, GemmArgs a,
-                    cudaStream_t st) {
-  const Plan p = plan_gemm(w, M, epi == EPI_ARGMAX, kv->m->sms);
+struct Plan {
+  int n_tok, tok_tiles, cs, kps, rd, da, db, grid;
+};
+
+// Chooses token tiles (MMA N <= 256) and the k split (cluster of 1..8 CTAs)
+// with a small latency model: every CTA pays a fixed start-up and drain
+// cost, streams its weight k tiles plus the matching activation tiles, and
+// a split pays for the cluster reduction.  Token tiles re-read the same
+// weight tile (from L2), which costs far less than a reduction.
+Plan plan_gemm(const Linear& w, int M, bool no_split, int sms) {
+  const double wbytes = w.fmt == VSD_FMT_BF16 ? 16384.0 : (w.fmt == VSD_FMT_FP8 ? 8192.0 : 4608.0);
+  const double fixed_us = 3.0, bytes_per_us = 120e3, reduce_us = 1.5, reduce_per_cta_us = 0.3;
+  Plan best{};
+  double best_cost = 1e30;
+  const int max_t = std::max(1, ceil_div(M, 16));
+  for (int t = ceil_div(M, 256); t <= max_t; ++t) {
+    const int n_tok = std::max(16, round_up(ceil_div(M, t), 16));
+    if (n_tok > 256 || (t > 1 && round_up(ceil_div(M, t - 1), 16) == n_tok)) continue;
+    for (int want : {1, 2, 4, 8}) {
+      if (no_split && want > 1) break;
+      if (want > w.k_tiles) break;
+      const int kps = ceil_div(w.k_tiles, want);
+      const int cs = ceil_div(w.k_tiles, kps);  // every rank gets at least one k tile
+      const int items = w.n_tiles * t;
+      const int ctas = items * cs;
+      const int waves = ceil_div(ctas, sms);
+      const double per_cta = kps * (wbytes + n_tok * 128.0);
+      double cost = fixed_us + waves * per_cta / bytes_per_us;
+      if (cs > 1) cost += reduce_us + reduce_per_cta_us * cs;
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best.tok_tiles = t;
+        best.n_tok = n_tok;
+        best.kps = kps;
+        best.cs = cs;
+      }
+    }
+  }
+  const int items = w.n_tiles * best.tok_tiles;
+  const int clusters = std::max(1, std::min(items, sms / best.cs));
+  best.grid = clusters * best.cs;
+  // ring depths: the weight ring holds the CTA's whole weight stream when it fits
+  const int ki = ceil_div(items, clusters) * best.kps;  // k iterations of one CTA
+  const int wslot = static_cast<int>(weight_slot_bytes(w.fmt)), bslot = best.n_tok * 128;
+  const int r_bytes = best.cs > 1 ? round_up(best.n_tok * 132 * 4, 1024) : 0;
+  const int budget = 232448 - 1024 - static_cast<int>(gemm_ctrl_bytes()) - r_bytes - 1024;
+  if (w.fmt == VSD_FMT_BF16) {
+    best.da = 1;
+    const int d = std::max(2, std::min({8, ki, budget / (wslot + bslot)}));
+    best.rd = best.db = d;
+  } else {
+    // expanded tiles: deep enough that expansion runs ahead of the MMAs
+    best.da = std::max(2, std::min(kMaxDa, ki));
+    const int rest = budget - best.da * 16384;
+    best.db = std::max(2, std::min({kMaxDb, ki, std::max(2, (rest - std::min(ki, kMaxRd) * wslot) / bslot)}));
+    best.rd = std::max(2, std::min({kMaxRd, ki, (rest - best.db * bslot) / wslot}));
+  }
+  return best;
+}
+
+// Per-token RMSNorm scale of the GEMM input (rows held unnormalised).
+void set_norm_input(GemmArgs& a, const vsd_kv* kv) {
+  const vsd_model_config& c = kv->m->cfg;
+  a.ssq_in = kv->ssq;
+  a.n_ssq = ceil_div(c.hidden, kTileN);
+  a.ssq_ld = kv->m_alloc;
+  a.inv_hidden = 1.0f / static_cast<float>(c.hidden);
+  a.eps = c.eps;
+}
+
+vsd_status run_gemm(const vsd_model* m, const Linear& w, int epi, const CUtensorMap* tm_acts, int M, GemmArgs a,
+                    int* status, cudaStream_t st, Trace trace = Trace{}) {
+  const Plan p = plan_gemm(w, M, epi == EPI_ARGMAX, m->sms);
   a.w_tiles = static_cast<const uint8_t*>(w.data);
   a.row_scale = w.row_scale;
   a.n_rows = w.n_rows;
@@ -301,32 +362,34 @@ vsd_status run_gemm(const vsd_kv* kv, const Linear& w, int epi, const CUtensorMa
   a.k_tiles = w.k_tiles;
   a.tok_tiles = p.tok_tiles;
   a.n_tok = p.n_tok;
-  a.splits = p.splits;
-  a.kt_per_split = p.kps;
+  a.cs = p.cs;
+  a.kps = p.kps;
   a.m_tokens = M;
-  a.stages = p.stages;
-  a.partials = kv->partials;
-  a.counters = kv->counters;
-  a.status = kv->status;
-  if (p.splits > 1) {
-    const size_t need = static_cast<size_t>(w.n_tiles) * p.tok_tiles * p.splits * 128 * p.n_tok;
-    if (need > kv->partials_cap || w.n_tiles * p.tok_tiles > kv->counters_cap)
-      return fail(VSD_ERR_UNSUPPORTED, "split-K workspace too small (%zu > %zu)", need, kv->partials_cap);
-  }
-  const cudaError_t e = launch_gemm(w.fmt, epi, tm_act, w.tm, a, p.grid, st, use_pdl(st));
+  a.rd = p.rd;
+  a.da = p.da;
+  a.db = p.db;
+  a.status = status;
+  a.trace = trace;
+  if (gemm_smem_bytes(w.fmt, p.n_tok, p.rd, p.da, p.db, p.cs) > 232448)
+    return fail(VSD_ERR_UNSUPPORTED, "GEMM tile does not fit in shared memory");
+  const cudaError_t e = launch_gemm(w.fmt, epi, tm_acts[p.n_tok / 16 - 1], w.tm, a, p.grid, st, use_pdl(st));
   if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
   return VSD_OK;
 }
 
-vsd_status run_attention(vsd_kv* kv, int layer, int B, cudaStream_t st) {
+vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cudaStream_t st) {
   const vsd_model* m = kv->m;
   const vsd_model_config& c = m->cfg;
+  if (B > kMaxReqs) return fail(VSD_ERR_UNSUPPORTED, "at most %d requests per step", kMaxReqs);
   const int max_chunks = ceil_div(kv->max_tokens, 128) + 1;
+  // about two work items per SM at the longest contexts
   int cps = std::max(1, ceil_div(B * c.n_kv * max_chunks, 2 * m->sms));
   const int max_splits = ceil_div(max_chunks, cps);
   if (static_cast<size_t>(B) * c.n_kv * max_splits > kv->attn_items_cap)
     return fail(VSD_ERR_UNSUPPORTED, "attention workspace too small");
+  const int grid = std::min(B * c.n_kv * max_splits, m->sms);
   AttnArgs a{};
+  a.batch = B;
   a.batch_cap = kv->max_batch;
   a.n_q = c.n_q;
   a.n_kv = c.n_kv;
@@ -338,7 +401,8 @@ vsd_status run_attention(vsd_kv* kv, int layer, int B, cudaStream_t st) {
   a.layer = layer;
   a.num_pages = kv->num_pages;
   a.pages_per_req = kv->ppr;
-  a.ctx_len = kv->ctx_len;
+  a.max_tokens = kv->max_tokens;
+  a.seq_lens = seq_lens;
   a.page_table = kv->page_table;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
   a.part_o = kv->attn_o;
@@ -346,10 +410,39 @@ vsd_status run_attention(vsd_kv* kv, int layer, int B, cudaStream_t st) {
   a.counters = kv->attn_counters;
   a.out = kv->act_o;
   a.status = kv->status;
+  a.trace = next_trace(kv);
   const cudaError_t e = launch_attn(c.head_dim, kv->tm_q, kv->tm_kc, kv->tm_vc, kv->tm_kn, kv->tm_vn, a,
-                                    dim3(max_splits, c.n_kv, B), st, use_pdl(st));
+                                    dim3(grid), st, use_pdl(st));
   if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
   return VSD_OK;
+}
+
+CommitArgs commit_args(const vsd_kv* kv, const int* drafts, int* seq_lens, int* pending, int* accepted,
+                       int* out_tokens) {
+  const vsd_model_config& c = kv->m->cfg;
+  CommitArgs ca{};
+  ca.vocab = c.vocab;
+  ca.layers = c.layers;
+  ca.n_kv = c.n_kv;
+  ca.hd = c.head_dim;
+  ca.batch_cap = kv->max_batch;
+  ca.num_pages = kv->num_pages;
+  ca.pages_per_req = kv->ppr;
+  ca.keys = kv->keys;
+  ca.drafts = drafts;
+  ca.ctx_len = kv->ctx_len;
+  ca.req_ok = kv->req_ok;
+  ca.seq_lens = seq_lens;
+  ca.pending = pending;
+  ca.accepted = accepted;
+  ca.out_tokens = out_tokens;
+  ca.page_table = kv->page_table;
+  ca.k_new = kv->k_new;
+  ca.v_new = kv->v_new;
+  ca.k_pool = kv->k_pool;
+  ca.v_pool = kv->v_pool;
+  ca.status = kv->status;
+  return ca;
 }
 
 vsd_status check_model_config(const vsd_model_config* c) {
@@ -467,12 +560,6 @@ vsd_status vsd_model_create(const vsd_model_config* cfg, const vsd_weights* w, v
     if (cudaMemcpy(m->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice))
       return cleanup(fail(VSD_ERR_CUDA, "RoPE table copy failed"));
   }
-  {
-    std::vector<float> ones(std::max(H, 1), 1.0f);
-    if ((s = dalloc(&m->gamma, ones.size(), false))) return cleanup(s);
-    if (cudaMemcpy(m->gamma, ones.data(), ones.size() * 4, cudaMemcpyHostToDevice))
-      return cleanup(fail(VSD_ERR_CUDA, "norm weight copy failed"));
-  }
   if (cudaStreamSynchronize(st) != cudaSuccess) return cleanup(fail(VSD_ERR_CUDA, "model creation failed"));
   *out = m;
   return VSD_OK;
@@ -485,7 +572,6 @@ void vsd_model_destroy(vsd_model* m) {
     for (auto& l : *v) free_linear(l);
   if (m->embed) cudaFree(m->embed);
   if (m->rope) cudaFree(m->rope);
-  if (m->gamma) cudaFree(m->gamma);
   delete m;
 }
 
@@ -528,22 +614,24 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
       (s = dalloc(&kv->q_tile, static_cast<size_t>(max_batch) * c.n_kv * 128 * hd)) ||
       (s = dalloc(&kv->k_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
       (s = dalloc(&kv->v_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
-      (s = dalloc(&kv->keys, M)) || (s = dalloc(&kv->ctx_len, max_batch)) || (s = dalloc(&kv->status, 1)))
+      (s = dalloc(&kv->keys, M)) || (s = dalloc(&kv->ctx_len, max_batch)) || (s = dalloc(&kv->req_ok, max_batch)) ||
+      (s = dalloc(&kv->status, 1)))
     return cleanup(s);
-  kv->partials_cap = static_cast<size_t>(m->sms) * 128 * 256;
-  kv->counters_cap = m->sms;
-  if ((s = dalloc(&kv->partials, kv->partials_cap, false)) || (s = dalloc(&kv->counters, kv->counters_cap)))
-    return cleanup(s);
+  if ((s = dalloc(&kv->ssq, static_cast<size_t>(ceil_div(H, kTileN)) * kv->m_alloc))) return cleanup(s);
   kv->attn_items_cap = static_cast<size_t>(4) * m->sms + static_cast<size_t>(2) * max_batch * c.n_kv;
   if ((s = dalloc(&kv->attn_o, kv->attn_items_cap * 128 * hd, false)) ||
       (s = dalloc(&kv->attn_ml, kv->attn_items_cap * 128 * 2, false)) ||
       (s = dalloc(&kv->attn_counters, static_cast<size_t>(max_batch) * c.n_kv)))
     return cleanup(s);
   const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16, BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if ((s = tmap_2d(&kv->tm_u, kv->u, F16, H, kv->m_alloc, 64, 16)) ||
-      (s = tmap_2d(&kv->tm_o, kv->act_o, F16, nqd, kv->m_alloc, 64, 16)) ||
-      (s = tmap_2d(&kv->tm_a, kv->act_a, F16, F, kv->m_alloc, 64, 16)) ||
-      (s = tmap_2d(&kv->tm_q, kv->q_tile, BF16, hd, static_cast<uint64_t>(max_batch) * c.n_kv * 128, 64, 128)) ||
+  for (int j = 0; j < kActBoxes; ++j) {
+    const uint32_t rows = 16u * (j + 1);
+    if ((s = tmap_2d(&kv->tm_u[j], kv->u, F16, H, kv->m_alloc, 64, rows)) ||
+        (s = tmap_2d(&kv->tm_o[j], kv->act_o, F16, nqd, kv->m_alloc, 64, rows)) ||
+        (s = tmap_2d(&kv->tm_a[j], kv->act_a, F16, F, kv->m_alloc, 64, rows)))
+      return cleanup(s);
+  }
+  if ((s = tmap_2d(&kv->tm_q, kv->q_tile, BF16, hd, static_cast<uint64_t>(max_batch) * c.n_kv * 128, 64, 128)) ||
       (s = tmap_2d(&kv->tm_kc, kv->k_pool, BF16, hd, pool / hd, 64, 16)) ||
       (s = tmap_2d(&kv->tm_vc, kv->v_pool, BF16, hd, pool / hd, 64, 16)) ||
       (s = tmap_2d(&kv->tm_kn, kv->k_new, BF16, hd, static_cast<uint64_t>(c.layers) * max_batch * c.n_kv * 32, 64, 32)) ||
@@ -557,8 +645,8 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
 void vsd_kv_destroy(vsd_kv* kv) {
   if (!kv) return;
   void* ptrs[] = {kv->k_pool, kv->v_pool, kv->page_table, kv->x, kv->u, kv->act_o, kv->act_a, kv->q_tile,
-                  kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->partials, kv->counters, kv->attn_o,
-                  kv->attn_ml, kv->attn_counters, kv->status};
+                  kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->req_ok, kv->ssq, kv->attn_o,
+                  kv->attn_ml, kv->attn_counters, kv->status, kv->trace};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete kv;
@@ -605,6 +693,37 @@ vsd_status vsd_kv_read(const vsd_kv* kv, int32_t req, int32_t start, int32_t cou
   return kv_rows(kv, req, start, count, k, v, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
+vsd_status vsd_trace_enable(vsd_kv* kv, int32_t max_launches) {
+  if (!kv || max_launches < 0) return fail(VSD_ERR_ARG, "bad arguments");
+  if (kv->trace) cudaFree(kv->trace);
+  kv->trace = nullptr;
+  kv->trace_launches = 0;
+  kv->trace_seq = 0;
+  if (max_launches == 0) return VSD_OK;
+  vsd_status s;
+  if ((s = dalloc(&kv->trace, static_cast<size_t>(max_launches) * kTraceCtas * kTraceTags))) return s;
+  kv->trace_launches = max_launches;
+  return VSD_OK;
+}
+
+vsd_status vsd_trace_read(vsd_kv* kv, uint64_t* slots_host, int32_t max_launches, int32_t* n_launches,
+                          vsd_stream stream) {
+  if (!kv || !slots_host || !n_launches || max_launches < 0) return fail(VSD_ERR_ARG, "bad arguments");
+  if (!kv->trace) {
+    *n_launches = 0;
+    return VSD_OK;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int n = std::min(kv->trace_launches, max_launches);  // graph replays keep their capture-time ids
+  const size_t bytes = static_cast<size_t>(n) * kTraceCtas * kTraceTags * 8;
+  CK(cudaStreamSynchronize(st));
+  if (n > 0) CK(cudaMemcpy(slots_host, kv->trace, bytes, cudaMemcpyDeviceToHost));
+  CK(cudaMemset(kv->trace, 0, static_cast<size_t>(kv->trace_launches) * kTraceCtas * kTraceTags * 8));
+  kv->trace_seq = 0;
+  *n_launches = n;
+  return VSD_OK;
+}
+
 vsd_status vsd_get_device_status(vsd_kv* kv, vsd_stream stream, int32_t* out) {
   if (!kv || !out) return fail(VSD_ERR_ARG, "NULL pointer");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -617,8 +736,35 @@ vsd_status vsd_get_device_status(vsd_kv* kv, vsd_stream stream, int32_t* out) {
 }
 
 // ------------------------------------------------------------------ the step
+// Optional per-launch event timing of one step.
+struct LaunchTimer {
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> kinds;
+  cudaStream_t st = nullptr;
+  void before(int kind) {
+    cudaEvent_t a, b;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    ev.push_back(a);
+    ev.push_back(b);
+    kinds.push_back(kind);
+    cudaEventRecord(a, st);
+  }
+  void after() { cudaEventRecord(ev.back(), st); }
+  ~LaunchTimer() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+};
+
 static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_lens, int* pending, const int* drafts,
-                              int* accepted, int* out_tokens, float* logits, float* hidden, cudaStream_t st) {
+                              int* accepted, int* out_tokens, float* logits, float* hidden, cudaStream_t st,
+                              LaunchTimer* timer = nullptr) {
+#define TIMED(kind, ...)          \
+  do {                            \
+    if (timer) timer->before(kind); \
+    __VA_ARGS__;                  \
+    if (timer) timer->after();    \
+  } while (0)
   if (!m || !kv || !seq_lens || !pending || !drafts || !accepted || !out_tokens)
     return fail(VSD_ERR_ARG, "NULL pointer");
   if (kv->m != m) return fail(VSD_ERR_ARG, "the cache was created for another model");
@@ -635,18 +781,22 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     e.pending = pending;
     e.drafts = drafts;
     e.max_tokens = kv->max_tokens;
-    e.eps = c.eps;
-    e.gamma = m->gamma;
     e.x = kv->x;
-    e.u = kv->u;
+    e.x16 = kv->u;
+    e.ssq = kv->ssq;
+    e.ssq_ld = kv->m_alloc;
     e.ctx_len = kv->ctx_len;
+    e.req_ok = kv->req_ok;
+    e.keys = kv->keys;
     e.hidden0 = hidden;
     e.status = kv->status;
-    CK(launch_ex(embed_norm_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), e));
+    e.trace = next_trace(kv);
+    TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), e)));
   }
   const size_t layer_scratch = static_cast<size_t>(kv->max_batch) * c.n_kv * 32 * c.head_dim;
   for (int l = 0; l < c.layers; ++l) {
     GemmArgs a{};
+    set_norm_input(a, kv);
     a.q_tile = kv->q_tile;
     a.k_new = kv->k_new + l * layer_scratch;
     a.v_new = kv->v_new + l * layer_scratch;
@@ -655,51 +805,54 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     a.n_q = c.n_q;
     a.n_kv = c.n_kv;
     a.head_dim = c.head_dim;
-    if ((s = run_gemm(kv, m->qkv[l], EPI_QKV, kv->tm_u, M, a, st))) return s;
-    if ((s = run_attention(kv, l, B, st))) return s;
+    TIMED(VSD_K_QKV, if ((s = run_gemm(m, m->qkv[l], EPI_QKV, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
+    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, seq_lens, st))) return s);
     GemmArgs r{};
     r.out_f32 = kv->x;
     r.ld_out = H;
-    if ((s = run_gemm(kv, m->o[l], EPI_RESID, kv->tm_o, M, r, st))) return s;
-    CK(launch_ex(rmsnorm_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), (const float*)kv->x, H, c.eps,
-                 (const float*)m->gamma, kv->u, (float*)nullptr));
+    r.x16_out = kv->u;
+    r.ssq_out = kv->ssq;
+    r.ssq_ld = kv->m_alloc;
+    TIMED(VSD_K_O_PROJ, if ((s = run_gemm(m, m->o[l], EPI_RESID, kv->tm_o, M, r, kv->status, st, next_trace(kv)))) return s);
     GemmArgs g{};
+    set_norm_input(g, kv);
     g.act_out = kv->act_a;
     g.ffn = c.ffn;
-    if ((s = run_gemm(kv, m->gu[l], EPI_SILU, kv->tm_u, M, g, st))) return s;
-    if ((s = run_gemm(kv, m->down[l], EPI_RESID, kv->tm_a, M, r, st))) return s;
-    float* copy = hidden ? hidden + static_cast<size_t>(l + 1) * M * H : nullptr;
-    CK(launch_ex(rmsnorm_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), (const float*)kv->x, H, c.eps,
-                 (const float*)m->gamma, kv->u, copy));
+    TIMED(VSD_K_GATE_UP, if ((s = run_gemm(m, m->gu[l], EPI_SILU, kv->tm_u, M, g, kv->status, st, next_trace(kv)))) return s);
+    r.hidden_out = hidden ? hidden + static_cast<size_t>(l + 1) * M * H : nullptr;
+    TIMED(VSD_K_DOWN, if ((s = run_gemm(m, m->down[l], EPI_RESID, kv->tm_a, M, r, kv->status, st, next_trace(kv)))) return s);
   }
   {
     GemmArgs a{};
+    set_norm_input(a, kv);
     a.keys = kv->keys;
     a.logits = logits;
-    if ((s = run_gemm(kv, m->lm, EPI_ARGMAX, kv->tm_u, M, a, st))) return s;
+    TIMED(VSD_K_LM_HEAD, if ((s = run_gemm(m, m->lm, EPI_ARGMAX, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
   }
-  CommitArgs ca{};
-  ca.vocab = c.vocab;
-  ca.layers = c.layers;
-  ca.n_kv = c.n_kv;
-  ca.hd = c.head_dim;
-  ca.batch_cap = kv->max_batch;
-  ca.num_pages = kv->num_pages;
-  ca.pages_per_req = kv->ppr;
-  ca.max_tokens = kv->max_tokens;
-  ca.keys = kv->keys;
-  ca.drafts = drafts;
-  ca.seq_lens = seq_lens;
-  ca.pending = pending;
-  ca.accepted = accepted;
-  ca.out_tokens = out_tokens;
-  ca.page_table = kv->page_table;
-  ca.k_new = kv->k_new;
-  ca.v_new = kv->v_new;
-  ca.k_pool = kv->k_pool;
-  ca.v_pool = kv->v_pool;
-  ca.status = kv->status;
-  CK(launch_ex(accept_commit_kernel, dim3(B), dim3(256), 0, st, use_pdl(st), ca));
+  CommitArgs ca = commit_args(kv, drafts, seq_lens, pending, accepted, out_tokens);
+  ca.trace = next_trace(kv);
+  TIMED(VSD_K_COMMIT, CK(launch_ex(accept_commit_kernel, dim3(B, c.layers), dim3(256), 0, st, use_pdl(st), ca)));
+#undef TIMED
+  return VSD_OK;
+}
+
+vsd_status vsd_verify_step_profiled(const vsd_model* m, vsd_kv* kv, int32_t batch, int32_t* seq_lens,
+                                    int32_t* pending, const int32_t* drafts, int32_t* accepted,
+                                    int32_t* out_tokens, int32_t max_launches, int32_t* kinds, float* ms,
+                                    int32_t* n_launches, vsd_stream stream) {
+  if (!kinds || !ms || !n_launches || max_launches < 1) return fail(VSD_ERR_ARG, "NULL pointer or no room");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LaunchTimer t;
+  t.st = st;
+  vsd_status s = verify_impl(m, kv, batch, seq_lens, pending, drafts, accepted, out_tokens, nullptr, nullptr, st, &t);
+  if (s) return s;
+  CK(cudaStreamSynchronize(st));
+  const int n = std::min<int>(max_launches, static_cast<int>(t.kinds.size()));
+  for (int i = 0; i < n; ++i) {
+    kinds[i] = t.kinds[i];
+    CK(cudaEventElapsedTime(&ms[i], t.ev[2 * i], t.ev[2 * i + 1]));
+  }
+  *n_launches = static_cast<int>(t.kinds.size());
   return VSD_OK;
 }
 
@@ -725,36 +878,27 @@ vsd_status vsd_linear(const vsd_weight* w, int32_t n, int32_t k, const uint16_t*
   Linear L;
   vsd_status s = build_linear(&w, &n, 1, k, identity_perm(n), st, &L);
   if (s) return s;
-  CUtensorMap tm{};
-  if ((s = tmap_2d(&tm, x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k, mtok, 64, 16))) {
+  CUtensorMap tm[kActBoxes]{};
+  for (int j = 0; j < kActBoxes; ++j) {
+    if ((s = tmap_2d(&tm[j], x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k, mtok, 64, 16u * (j + 1)))) {
+      free_linear(L);
+      return s;
+    }
+  }
+  int* status = nullptr;
+  if ((s = dalloc(&status, 1))) {
     free_linear(L);
     return s;
   }
-  // a throw-away workspace sized like a cache's
-  vsd_kv kv;
   vsd_model mm;
   mm.sms = sm_count();
-  kv.m = &mm;
-  kv.partials_cap = static_cast<size_t>(mm.sms) * 128 * 256;
-  kv.counters_cap = mm.sms;
-  if ((s = dalloc(&kv.partials, kv.partials_cap, false)) || (s = dalloc(&kv.counters, kv.counters_cap)) ||
-      (s = dalloc(&kv.status, 1))) {
-    free_linear(L);
-    return s;
-  }
   GemmArgs a{};
   a.out_f32 = y;
   a.ld_out = n;
-  s = run_gemm(&kv, L, EPI_STORE, tm, mtok, a, st);
+  s = run_gemm(&mm, L, EPI_STORE, tm, mtok, a, status, st);
   cudaStreamSynchronize(st);
-  cudaFree(kv.partials);
-  cudaFree(kv.counters);
-  cudaFree(kv.status);
-  kv.partials = nullptr;
-  kv.counters = nullptr;
-  kv.status = nullptr;
+  cudaFree(status);
   free_linear(L);
-  mm.lm.data = nullptr;
   return s;
 }
 
@@ -766,17 +910,14 @@ vsd_status vsd_block_attention(const vsd_model* m, vsd_kv* kv, int32_t layer, in
   const vsd_model_config& c = m->cfg;
   if (B < 1 || B > kv->max_batch || layer < 0 || layer >= c.layers) return fail(VSD_ERR_ARG, "batch or layer out of range");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const size_t nq = static_cast<size_t>(B) * kRows * c.n_q * c.head_dim;
   scatter_q_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), B, c.n_q, c.n_kv, c.head_dim,
                                         kv->q_tile);
   scatter_block_rows_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k_new), 1, B, c.n_kv,
                                                  c.head_dim, kv->max_batch, layer, kv->k_new);
   scatter_block_rows_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(v_new), 1, B, c.n_kv,
                                                  c.head_dim, kv->max_batch, layer, kv->v_new);
-  clamp_ctx_kernel<<<ceil_div(B, 128), 128, 0, st>>>(seq_lens, B, kv->max_tokens, kv->ctx_len, kv->status);
   CK(cudaGetLastError());
-  (void)nq;
-  vsd_status s = run_attention(kv, layer, B, st);
+  vsd_status s = run_attention(kv, layer, B, seq_lens, st);
   if (s) return s;
   CK(cudaMemcpyAsync(out, kv->act_o, static_cast<size_t>(B) * kRows * c.n_q * c.head_dim * 2,
                      cudaMemcpyDeviceToDevice, st));
@@ -798,28 +939,10 @@ vsd_status vsd_accept_commit(const vsd_model* m, vsd_kv* kv, int32_t B, const fl
                                                  c.head_dim, kv->max_batch, 0, kv->v_new);
   logits_argmax_kernel<<<B * kRows, 256, 0, st>>>(logits, c.vocab, kv->keys);
   CK(cudaGetLastError());
-  CommitArgs ca{};
-  ca.vocab = c.vocab;
-  ca.layers = c.layers;
-  ca.n_kv = c.n_kv;
-  ca.hd = c.head_dim;
-  ca.batch_cap = kv->max_batch;
-  ca.num_pages = kv->num_pages;
-  ca.pages_per_req = kv->ppr;
-  ca.max_tokens = kv->max_tokens;
-  ca.keys = kv->keys;
-  ca.drafts = drafts;
-  ca.seq_lens = seq_lens;
-  ca.pending = pending;
-  ca.accepted = accepted;
-  ca.out_tokens = out_tokens;
-  ca.page_table = kv->page_table;
-  ca.k_new = kv->k_new;
-  ca.v_new = kv->v_new;
-  ca.k_pool = kv->k_pool;
-  ca.v_pool = kv->v_pool;
-  ca.status = kv->status;
-  CK(launch_ex(accept_commit_kernel, dim3(B), dim3(256), 0, st, false, ca));
+  validate_requests_kernel<<<ceil_div(B, 128), 128, 0, st>>>(seq_lens, pending, B, c.vocab, kv->max_tokens,
+                                                            kv->ctx_len, kv->req_ok, kv->status);
+  CommitArgs ca = commit_args(kv, drafts, seq_lens, pending, accepted, out_tokens);
+  CK(launch_ex(accept_commit_kernel, dim3(B, c.layers), dim3(256), 0, st, false, ca));
   return VSD_OK;
 }
 

@@ -8,27 +8,35 @@
 // split into 128-key chunks (eight 16-token pages, fetched by TMA through
 // the page table -- paged KV as in "LLM inference acceleration", section
 // two); the block's own 17 keys form one more 32-key chunk read from the
-// step's scratch.  A CTA takes `chunks_per_split` consecutive chunks:
+// step's scratch.  Work items are (request, KV head, split of
+// `chunks_per_split` consecutive chunks); persistent CTAs (one per SM) walk
+// the item list, which every CTA derives from the caller's sequence lengths.
+// Per chunk:
 //   S = Q K^T     tcgen05.mma, bf16 in, fp32 in TMEM (two S buffers)
-//   softmax       one thread per row straight from TMEM, running max / sum
+//   softmax       two threads per row (each half of the chunk's columns)
+//                 straight from TMEM, running max shared through smem
 //   O_c = P V     P written as bf16 to shared memory, V read MN-major
 // and the per-chunk O_c is folded into registers with the running rescale.
-// Split partials (unnormalised O, max, sum) go to a workspace; the last CTA
-// of (b, h) merges them in split order and writes the f16 output row.
+// Context pages do not depend on the preceding kernels of the step, so the
+// first stages are fetched before the grid-dependency wait.  Split partials
+// (unnormalised O, max, sum) go to a workspace; the last CTA to finish a
+// (request, head) merges them in split order and writes the f16 output rows.
 #pragma once
 
 #include "vsd_common.cuh"
 
 namespace vsd {
 
-constexpr int kAttnThreads = 192;  // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kAttnThreads = 320;  // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kMaxReqs = 1024;     // requests whose item offsets fit in shared memory
 
 struct AttnArgs {
+  int batch;         // requests in this step
   int batch_cap;     // rows of the q tile / scratch buffers = max_batch
   int n_q, n_kv, hd, group, rows_valid;
   int chunks_per_split, max_splits;
-  int layer, num_pages, pages_per_req;
-  const int* ctx_len;      // [B]
+  int layer, num_pages, pages_per_req, max_tokens;
+  const int* seq_lens;     // [B] caller's committed lengths (validated here)
   const int* page_table;   // [max_batch][pages_per_req]
   float scale_log2;        // log2(e) / sqrt(hd)
   float* part_o;           // [B][n_kv][max_splits][128][hd]
@@ -36,12 +44,25 @@ struct AttnArgs {
   int* counters;           // [B][n_kv]
   __half* out;             // [B*17][n_q*hd]
   int* status;
+  Trace trace;
 };
 
 __host__ __device__ inline uint32_t attn_stages(int hd) { return hd == 64 ? 3u : 2u; }
+// q tile, K/V stages, P tile, then barriers (256 B), row statistics (4 KB) and item offsets
 __host__ __device__ inline uint32_t attn_smem_bytes(int hd) {
   const uint32_t q = 128u * hd * 2u, kv = 2u * 128u * hd * 2u;
-  return 1024u + q + attn_stages(hd) * kv + 32768u + 1024u;
+  return 1024u + q + attn_stages(hd) * kv + 32768u + 256u + 4096u + 4u * (kMaxReqs + 1);
+}
+
+__device__ __forceinline__ int valid_len(const AttnArgs& a, int b) {
+  const int L = a.seq_lens[b];
+  return (L >= 0 && L + kRows <= a.max_tokens) ? L : 0;
+}
+
+__device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation (ex2(-inf) = 0)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <int HD>
@@ -50,7 +71,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kn,
                 const __grid_constant__ CUtensorMap tm_vn, const AttnArgs a) {
   constexpr int NS = HD == 64 ? 3 : 2;
-  constexpr int NA = HD / 64;  // 64-wide swizzle atoms along head_dim
+  constexpr int NA = HD / 64;   // 64-wide swizzle atoms along head_dim
+  constexpr int HH = HD / 2;    // output columns per softmax thread
   constexpr uint32_t QB = 128u * HD * 2u, KVB = 128u * HD * 2u;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -61,7 +83,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* kvfull = bars;
   uint64_t* kvempty = bars + NS;
   uint64_t* qfull = bars + 2 * NS;
-  uint64_t* sfull = qfull + 1;   // [2]
+  uint64_t* qempty = qfull + 1;  // the item's S products are done with the q tile
+  uint64_t* sfull = qempty + 1;  // [2]
   uint64_t* sfree = sfull + 2;   // [2]
   uint64_t* pfull = sfree + 2;
   uint64_t* ofull = pfull + 1;
@@ -69,37 +92,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint32_t* tmem_p = reinterpret_cast<uint32_t*>(ofree + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_p + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_p + 2);
+  volatile int* n_items = reinterpret_cast<volatile int*>(tmem_p + 3);
+  float* xstat = reinterpret_cast<float*>(p_s + 32768 + 256);  // [2 parity][2 halves][128] maxima; then [2][2][128] sums
+  int* item_off = reinterpret_cast<int*>(p_s + 32768 + 256 + 4096);  // [B + 1] first item of each request
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  pdl_wait();  // ctx_len, q tile and block K/V are produced by earlier kernels of the step
-  pdl_launch_dependents();
-  const int L = a.ctx_len[b];
-  const int n_ctx = (L + 127) >> 7;
-  const int n_chunks = n_ctx + 1;
-  const int n_splits = (n_chunks + a.chunks_per_split - 1) / a.chunks_per_split;
-  if (split >= n_splits) return;
-  const int c_begin = split * a.chunks_per_split;
-  const int n = min(n_chunks, c_begin + a.chunks_per_split) - c_begin;
+  const int cps = a.chunks_per_split;
+  auto splits_of = [&](int b) { return ((valid_len(a, b) + 127) / 128 + 1 + cps - 1) / cps; };
 
   if (threadIdx.x == 0) {
+    trace_start(a.trace);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&kvfull[s], 1);
       mbar_init(&kvempty[s], 1);
     }
     mbar_init(qfull, 1);
+    mbar_init(qempty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sfree[i], 128);
+      mbar_init(&sfree[i], 256);
     }
-    mbar_init(pfull, 128);
+    mbar_init(pfull, 256);
     mbar_init(ofull, 1);
-    mbar_init(ofree, 128);
+    mbar_init(ofree, 256);
     *abort_flag = 0;
     fence_mbar_init();
+    // item list: request-major, then KV head, then split (seq_lens is the
+    // caller's input and does not change during the step)
+    int acc = 0;
+    for (int b = 0; b < a.batch; ++b) {
+      item_off[b] = acc;
+      acc += a.n_kv * splits_of(b);
+    }
+    item_off[a.batch] = acc;
+    *n_items = acc;
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_p, 512);
     tmem_relinquish();
   }
@@ -107,35 +135,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_p;
+  const int total = *n_items;
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) trace_point(a.trace, 1);
 
-  if (warp == 4) {
+  struct Item {
+    int b, h, split, n_splits, L, n_ctx, c_begin, n;
+  };
+  auto decode = [&](int it) {
+    Item x;
+    int lo = 0, hi = a.batch - 1;  // last request whose first item is <= it
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (item_off[mid] <= it) lo = mid;
+      else hi = mid - 1;
+    }
+    x.b = lo;
+    x.n_splits = splits_of(x.b);
+    const int rem = it - item_off[x.b];
+    x.h = rem / x.n_splits;
+    x.split = rem % x.n_splits;
+    x.L = valid_len(a, x.b);
+    x.n_ctx = (x.L + 127) >> 7;
+    x.c_begin = x.split * cps;
+    x.n = min(x.n_ctx + 1, x.c_begin + cps) - x.c_begin;
+    return x;
+  };
+
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      mbar_expect_tx(qfull, QB);
-      for (int at = 0; at < NA; ++at)
-        tma_load_2d(q_s + at * 16384, &tm_q, qfull, at * 64, (b * a.n_kv + h) * 128);
-      int issued = 0;
-      bool ok = true;
-      for (int i = 0; i < n; ++i, ++issued) {
-        const int st = i % NS;
-        if (i >= NS && !mbar_wait(&kvempty[st], ((i / NS) - 1) & 1, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
+      auto issue = [&](const Item& x, int i, int g) {  // chunk i of item x, global chunk number g
+        const int st = g % NS;
         uint8_t* ks = kv_s + st * 2 * KVB;
         uint8_t* vs = ks + KVB;
-        const int c = c_begin + i;
-        if (c < n_ctx) {
+        const int c = x.c_begin + i;
+        if (c < x.n_ctx) {
           mbar_expect_tx(&kvfull[st], 2u * 128u * HD * 2u);
           for (int p = 0; p < 8; ++p) {
             const int pi = min(c * 8 + p, a.pages_per_req - 1);
-            int page = a.page_table[b * a.pages_per_req + pi];
+            int page = a.page_table[x.b * a.pages_per_req + pi];
             if (page < 0 || page >= a.num_pages) {
               atomicOr(a.status, VSD_DEV_BAD_PAGE);
               page = 0;
             }
-            const int row0 = ((a.layer * a.num_pages + page) * a.n_kv + h) * kPage;
+            const int row0 = ((a.layer * a.num_pages + page) * a.n_kv + x.h) * kPage;
             for (int at = 0; at < NA; ++at) {
               tma_load_2d_hint(ks + at * 16384 + p * 2048, &tm_kc, &kvfull[st], at * 64, row0, pol);
               tma_load_2d_hint(vs + at * 16384 + p * 2048, &tm_vc, &kvfull[st], at * 64, row0, pol);
@@ -143,153 +188,219 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         } else {
           mbar_expect_tx(&kvfull[st], 2u * 32u * HD * 2u);
-          const int row0 = ((a.layer * a.batch_cap + b) * a.n_kv + h) * 32;
+          const int row0 = ((a.layer * a.batch_cap + x.b) * a.n_kv + x.h) * 32;
           for (int at = 0; at < NA; ++at) {
             tma_load_2d(ks + at * 16384, &tm_kn, &kvfull[st], at * 64, row0);
             tma_load_2d(vs + at * 16384, &tm_vn, &kvfull[st], at * 64, row0);
           }
         }
+      };
+      // context pages of the first item: committed by earlier steps, safe before the dependency wait
+      int pre = 0;
+      if (static_cast<int>(blockIdx.x) < total) {
+        const Item x = decode(blockIdx.x);
+        while (pre < min(x.n, NS) && x.c_begin + pre < x.n_ctx) {
+          issue(x, pre, pre);
+          ++pre;
+        }
+      }
+      pdl_wait();  // q tiles and the block's K/V come from the QKV kernel
+      trace_point(a.trace, 2);
+      int g = 0, ic = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++ic) {
+        const Item x = decode(it);
+        if (ic > 0 && !mbar_wait(qempty, (ic - 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(qfull, QB);
+        for (int at = 0; at < NA; ++at)
+          tma_load_2d(q_s + at * 16384, &tm_q, qfull, at * 64, (x.b * a.n_kv + x.h) * 128);
+        for (int i = 0; i < x.n; ++i, ++g) {
+          if (g < pre) continue;  // fetched before the dependency wait
+          const int st = g % NS;
+          if (g >= NS && !mbar_wait(&kvempty[st], ((g / NS) - 1) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          issue(x, i, g);
+        }
       }
       if (!ok) {
         volatile int never = 0;
-        mbar_wait(qfull, 0, &never, nullptr);
-        for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&kvfull[i % NS], (i / NS) & 1, &never, nullptr);
+        mbar_wait(qfull, ic & 1, &never, nullptr);
+        for (int i = max(0, g - NS); i < g; ++i) mbar_wait(&kvfull[i % NS], (i / NS) & 1, &never, nullptr);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       const uint32_t id_s128 = idesc_f16(128, 128, true, true, false);
       const uint32_t id_s32 = idesc_f16(128, 32, true, true, false);
       const uint32_t id_pv = idesc_f16(128, HD, true, true, true);
       const uint32_t qa = smem_u32(q_s), pa = smem_u32(p_s);
-      bool ok = mbar_wait(qfull, 0, abort_flag, a.status);
-      auto issue_s = [&](int i) -> bool {
-        const int st = i % NS;
-        if (!mbar_wait(&kvfull[st], (i / NS) & 1, abort_flag, a.status)) return false;
-        if (i >= 2 && !mbar_wait(&sfree[i & 1], ((i >> 1) - 1) & 1, abort_flag, a.status)) return false;
-        tc_fence_after();
-        const uint32_t ka = smem_u32(kv_s + st * 2 * KVB);
-        const bool blk = (c_begin + i) >= n_ctx;
-        const uint32_t d = tmem + (i & 1) * 128;
+      int g0 = 0, ic = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++ic) {
+        const Item x = decode(it);
+        if (!mbar_wait(qfull, ic & 1, abort_flag, a.status)) break;
+        auto issue_s = [&](int i) -> bool {
+          const int g = g0 + i, st = g % NS;
+          if (!mbar_wait(&kvfull[st], (g / NS) & 1, abort_flag, a.status)) return false;
+          if (g >= 2 && !mbar_wait(&sfree[g & 1], ((g >> 1) - 1) & 1, abort_flag, a.status)) return false;
+          tc_fence_after();
+          const uint32_t ka = smem_u32(kv_s + st * 2 * KVB);
+          const bool blk = (x.c_begin + i) >= x.n_ctx;
+          const uint32_t d = tmem + (g & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_f16(d, sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024), blk ? id_s32 : id_s128,
-                   kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_f16(d, sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024), blk ? id_s32 : id_s128,
+                     kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&sfull[g & 1]);
+          if (i + 1 == x.n) umma_commit(qempty);  // last use of this item's q tile
+          return true;
+        };
+        ok = issue_s(0);
+        if (ic == 0) trace_point(a.trace, 3);
+        for (int i = 0; ok && i < x.n; ++i) {
+          const int g = g0 + i;
+          if (i + 1 < x.n && !issue_s(i + 1)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(pfull, g & 1, abort_flag, a.status) ||
+              (g >= 1 && !mbar_wait(ofree, (g - 1) & 1, abort_flag, a.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int st = g % NS;
+          const uint32_t va = smem_u32(kv_s + st * 2 * KVB + KVB);
+          const bool blk = (x.c_begin + i) >= x.n_ctx;
+          const int ksteps = blk ? 2 : 8;
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_f16(tmem + 256, sw128_desc(pa + aoff, 16, 1024), sw128_desc(va + kk * 2048, 16384, 1024), id_pv,
+                     kk > 0 ? 1u : 0u);
+          }
+          umma_commit(ofull);
+          umma_commit(&kvempty[st]);
         }
-        umma_commit(&sfull[i & 1]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n && !issue_s(i + 1)) break;
-        if (!mbar_wait(pfull, i & 1, abort_flag, a.status)) break;
-        if (i >= 1 && !mbar_wait(ofree, (i - 1) & 1, abort_flag, a.status)) break;
-        tc_fence_after();
-        const int st = i % NS;
-        const uint32_t va = smem_u32(kv_s + st * 2 * KVB + KVB);
-        const bool blk = (c_begin + i) >= n_ctx;
-        const int ksteps = blk ? 2 : 8;
-        for (int kk = 0; kk < ksteps; ++kk) {
-          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_f16(tmem + 256, sw128_desc(pa + aoff, 16, 1024), sw128_desc(va + kk * 2048, 16384, 1024), id_pv,
-                   kk > 0 ? 1u : 0u);
-        }
-        umma_commit(ofull);
-        umma_commit(&kvempty[st]);
+        g0 += x.n;
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax rows (warps 0-3)
-    const int r = threadIdx.x;  // row == TMEM lane
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int q4 = warp & 3, hf = warp >> 2;  // TMEM lane quarter, column half
+    const int r = q4 * 32 + lane;             // row == TMEM lane
     const bool row_ok = r < a.rows_valid;
     const int jr = row_ok ? r / a.group : 0;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    float o[HD];
-#pragma unroll
-    for (int d = 0; d < HD; ++d) o[d] = 0.0f;
-    float m = -INFINITY, l = 0.0f;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const int bar_id = 2 + q4;  // the 64 threads that share these rows
+    int g0 = 0, ic = 0;
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      if (!mbar_wait(&sfull[i & 1], (i >> 1) & 1, abort_flag, a.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int c = c_begin + i;
-      const bool blk = c >= n_ctx;
-      const int ncol = blk ? 32 : 128;
-      const uint32_t sa = tmem + lane_base + (i & 1) * 128;
-      float v[16];
-      // pass 1: row max of the chunk
-      float cm = -INFINITY;
-      for (int c0 = 0; c0 < ncol; c0 += 16) {
-        tmem_ld16(sa + c0, v);
-        tmem_ld_wait();
+    for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++ic) {
+      const Item x = decode(it);
+      float o[HH];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const int key = c0 + t;
-          const bool vis = blk ? (key <= jr) : (c * 128 + key < L);
-          if (vis && row_ok) cm = fmaxf(cm, v[t] * a.scale_log2);
+      for (int d = 0; d < HH; ++d) o[d] = 0.0f;
+      float m = -INFINITY, l = 0.0f;
+      for (int i = 0; i < x.n; ++i) {
+        const int g = g0 + i;
+        if (!mbar_wait(&sfull[g & 1], (g >> 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
         }
-      }
-      const float m_new = fmaxf(m, cm);
-      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-      const float alpha = exp2f(m - m_use);  // 0 on the first visible chunk (m = -inf)
-      // pass 2: probabilities -> bf16 P in shared memory
-      float psum = 0.0f;
-      for (int c0 = 0; c0 < ncol; c0 += 16) {
-        tmem_ld16(sa + c0, v);
-        tmem_ld_wait();
-        uint32_t w[8];
+        if (threadIdx.x == 0 && ic == 0) trace_point(a.trace, i == 0 ? 4 : 5);
+        tc_fence_after();
+        const int c = x.c_begin + i;
+        const bool blk = c >= x.n_ctx;
+        const bool need_mask = blk || (c * 128 + 128 > x.L) || !row_ok;
+        const int ncol = blk ? 16 : 64;        // this thread's columns of the chunk
+        const int col0 = hf * ncol;
+        const uint32_t sa = tmem + lane_base + (g & 1) * 128 + col0;
+        float s[64];
 #pragma unroll
-        for (int t = 0; t < 16; t += 2) {
-          const int key = c0 + t;
-          const bool v0 = row_ok && (blk ? (key <= jr) : (c * 128 + key < L));
-          const bool v1 = row_ok && (blk ? (key + 1 <= jr) : (c * 128 + key + 1 < L));
-          const float p0 = v0 ? exp2f(v[t] * a.scale_log2 - m_use) : 0.0f;
-          const float p1 = v1 ? exp2f(v[t + 1] * a.scale_log2 - m_use) : 0.0f;
-          w[t >> 1] = f32x2_to_bf16x2(p0, p1);
-          // the sum uses the bf16-rounded probabilities that the PV product uses
-          psum += __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(w[t >> 1] & 0xFFFF))) +
-                  __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(w[t >> 1] >> 16)));
+        for (int q = 0; q < 4; ++q)
+          if (q * 16 < ncol) tmem_ld16(sa + q * 16, s + q * 16);
+        tmem_ld_wait();
+        float cm = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < 64; ++t) {
+          if (t < ncol) {
+            const int key = col0 + t;
+            const bool vis = !need_mask || (row_ok && (blk ? (key <= jr) : (c * 128 + key < x.L)));
+            s[t] = vis ? s[t] * a.scale_log2 : -INFINITY;
+            cm = fmaxf(cm, s[t]);
+          }
         }
-        const int atom = c0 >> 6, ch = (c0 & 63) >> 3;
-        uint8_t* prow = p_s + atom * 16384;
-        *reinterpret_cast<uint4*>(prow + sw128_off(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(prow + sw128_off(r, ch + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-      tc_fence_before();
-      mbar_arrive(&sfree[i & 1]);
-      fence_proxy_async();
-      mbar_arrive(pfull);
-      l = l * alpha + psum;
-      m = m_new;
-      if (!mbar_wait(ofull, i & 1, abort_flag, a.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+        float* xs = xstat + (g & 1) * 256;
+        xs[hf * 128 + r] = cm;
+        named_bar_sync(bar_id, 64);
+        cm = fmaxf(xs[r], xs[128 + r]);
+        const float m_new = fmaxf(m, cm);
+        const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+        const float alpha = ex2(m - m_use);  // 0 on the first chunk (m = -inf)
+        float psum = 0.0f;
+        // probabilities -> bf16 P, one 16-byte chunk (8 keys) at a time:
+        // keys [col0, col0 + ncol) of row r live in atom col0 / 64
 #pragma unroll
-      for (int d0 = 0; d0 < HD; d0 += 16) {
-        tmem_ld16(tmem + lane_base + 256 + d0, v);
-        tmem_ld_wait();
+        for (int t = 0; t < 64; t += 8) {
+          if (t < ncol) {
+            uint32_t w[4];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) o[d0 + t] = o[d0 + t] * alpha + v[t];
+            for (int e = 0; e < 8; e += 2) {
+              w[e >> 1] = f32x2_to_bf16x2(ex2(s[t + e] - m_use), ex2(s[t + e + 1] - m_use));
+              // the row sum uses the bf16-rounded probabilities that the PV product uses
+              psum += __uint_as_float(w[e >> 1] << 16) + __uint_as_float(w[e >> 1] & 0xFFFF0000u);
+            }
+            const int key = col0 + t;
+            *reinterpret_cast<uint4*>(p_s + (key >> 6) * 16384 + sw128_off(r, (key & 63) >> 3)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sfree[g & 1]);
+        fence_proxy_async();
+        mbar_arrive(pfull);
+        l = l * alpha + psum;
+        m = m_new;
+        if (!mbar_wait(ofull, g & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float v[16];
+#pragma unroll
+        for (int d0 = 0; d0 < HH; d0 += 16) {
+          tmem_ld16(tmem + lane_base + 256 + hf * HH + d0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < 16; ++t) o[d0 + t] = o[d0 + t] * alpha + v[t];
+        }
+        tc_fence_before();
+        mbar_arrive(ofree);
       }
-      tc_fence_before();
-      mbar_arrive(ofree);
-    }
-    if (ok) {
-      const size_t pair = static_cast<size_t>(b) * a.n_kv + h;
+      g0 += x.n;
+      if (!ok) break;
+      if (threadIdx.x == 0 && ic == 0) trace_point(a.trace, 6);
+      // row sum over both halves
+      float* xl = xstat + 512 + (ic & 1) * 256;
+      xl[hf * 128 + r] = l;
+      named_bar_sync(bar_id, 64);
+      const float lt = xl[r] + xl[128 + r];
+      const size_t pair = static_cast<size_t>(x.b) * a.n_kv + x.h;
       const int hq = row_ok ? r % a.group : 0;
-      __half* dst = a.out + (static_cast<size_t>(b) * kRows + jr) * (a.n_q * HD) + (h * a.group + hq) * HD;
-      if (n_splits == 1) {
+      __half* dst =
+          a.out + (static_cast<size_t>(x.b) * kRows + jr) * (a.n_q * HD) + (x.h * a.group + hq) * HD + hf * HH;
+      if (x.n_splits == 1) {
         if (row_ok) {
-          const float inv = 1.0f / l;
+          const float inv = 1.0f / lt;
 #pragma unroll
-          for (int d = 0; d < HD; d += 8) {
+          for (int d = 0; d < HH; d += 8) {
             uint4 u;
             u.x = f32x2_to_f16x2(o[d] * inv, o[d + 1] * inv);
             u.y = f32x2_to_f16x2(o[d + 2] * inv, o[d + 3] * inv);
@@ -298,61 +409,81 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             *reinterpret_cast<uint4*>(dst + d) = u;
           }
         }
-      } else {
-        float* po = a.part_o + ((pair * a.max_splits + split) * 128 + r) * HD;
-        float* pml = a.part_ml + ((pair * a.max_splits + split) * 128 + r) * 2;
+        continue;
+      }
+      const size_t base = (pair * a.max_splits) * 128;
+      float* po = a.part_o + ((base + x.split * 128 + r) * HD) + hf * HH;
 #pragma unroll
-        for (int d = 0; d < HD; d += 4) __stcg(reinterpret_cast<float4*>(po + d), make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]));
-        __stcg(reinterpret_cast<float2*>(pml), make_float2(m, l));
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (r == 0) *last_flag = (atomicAdd(&a.counters[pair], 1) == n_splits - 1) ? 1 : 0;
-        named_bar_sync(1, 128);
-        if (*last_flag) {
-          __threadfence();
-          float mm = -INFINITY;
-          for (int s = 0; s < n_splits; ++s)
-            mm = fmaxf(mm, __ldcg(a.part_ml + ((pair * a.max_splits + s) * 128 + r) * 2));
-          if (mm == -INFINITY) mm = 0.0f;
-          float acc[HD];
+      for (int d = 0; d < HH; d += 4)
+        __stcg(reinterpret_cast<float4*>(po + d), make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]));
+      if (hf == 0) __stcg(reinterpret_cast<float2*>(a.part_ml + (base + x.split * 128 + r) * 2), make_float2(m, lt));
+      __threadfence();
+      named_bar_sync(1, 256);
+      if (threadIdx.x == 0) *last_flag = (atomicAdd(&a.counters[pair], 1) == x.n_splits - 1) ? 1 : 0;
+      named_bar_sync(1, 256);
+      const bool last = *last_flag;
+      named_bar_sync(1, 256);  // everyone read the flag before the next item may set it
+      if (!last) continue;
+      __threadfence();
+      float mm = -INFINITY;
+#pragma unroll 8
+      for (int sp = 0; sp < x.n_splits; ++sp) mm = fmaxf(mm, __ldcg(a.part_ml + (base + sp * 128 + r) * 2));
+      if (mm == -INFINITY) mm = 0.0f;
+      float accv[HH];
 #pragma unroll
-          for (int d = 0; d < HD; ++d) acc[d] = 0.0f;
-          float ls = 0.0f;
-          for (int s = 0; s < n_splits; ++s) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + ((pair * a.max_splits + s) * 128 + r) * 2));
-            const float w = exp2f(ml.x - mm);
-            ls += ml.y * w;
-            const float* ps = a.part_o + ((pair * a.max_splits + s) * 128 + r) * HD;
+      for (int d = 0; d < HH; ++d) accv[d] = 0.0f;
+      float ls = 0.0f;
+      constexpr int U = HD == 64 ? 2 : 1;  // splits whose loads are in flight together
+      for (int s0 = 0; s0 < x.n_splits; s0 += U) {
+        float4 xv[U][HH / 4];
+        float wgt[U];
 #pragma unroll
-            for (int d = 0; d < HD; d += 4) {
-              const float4 x = __ldcg(reinterpret_cast<const float4*>(ps + d));
-              acc[d] += x.x * w;
-              acc[d + 1] += x.y * w;
-              acc[d + 2] += x.z * w;
-              acc[d + 3] += x.w * w;
+        for (int u = 0; u < U; ++u) {
+          const int sp = s0 + u;
+          wgt[u] = 0.0f;
+          if (sp < x.n_splits) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (base + sp * 128 + r) * 2));
+            wgt[u] = ex2(ml.x - mm);
+            ls += ml.y * wgt[u];
+            const float* ps = a.part_o + (base + sp * 128 + r) * HD + hf * HH;
+#pragma unroll
+            for (int d = 0; d < HH / 4; ++d) xv[u][d] = __ldcg(reinterpret_cast<const float4*>(ps) + d);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (s0 + u < x.n_splits) {
+#pragma unroll
+            for (int d = 0; d < HH / 4; ++d) {
+              accv[4 * d] += xv[u][d].x * wgt[u];
+              accv[4 * d + 1] += xv[u][d].y * wgt[u];
+              accv[4 * d + 2] += xv[u][d].z * wgt[u];
+              accv[4 * d + 3] += xv[u][d].w * wgt[u];
             }
           }
-          if (row_ok) {
-            const float inv = 1.0f / ls;
-#pragma unroll
-            for (int d = 0; d < HD; d += 8) {
-              uint4 u;
-              u.x = f32x2_to_f16x2(acc[d] * inv, acc[d + 1] * inv);
-              u.y = f32x2_to_f16x2(acc[d + 2] * inv, acc[d + 3] * inv);
-              u.z = f32x2_to_f16x2(acc[d + 4] * inv, acc[d + 5] * inv);
-              u.w = f32x2_to_f16x2(acc[d + 6] * inv, acc[d + 7] * inv);
-              *reinterpret_cast<uint4*>(dst + d) = u;
-            }
-          }
-          if (r == 0) a.counters[pair] = 0;
         }
       }
+      if (row_ok) {
+        const float inv = 1.0f / ls;
+#pragma unroll
+        for (int d = 0; d < HH; d += 8) {
+          uint4 u;
+          u.x = f32x2_to_f16x2(accv[d] * inv, accv[d + 1] * inv);
+          u.y = f32x2_to_f16x2(accv[d + 2] * inv, accv[d + 3] * inv);
+          u.z = f32x2_to_f16x2(accv[d + 4] * inv, accv[d + 5] * inv);
+          u.w = f32x2_to_f16x2(accv[d + 6] * inv, accv[d + 7] * inv);
+          *reinterpret_cast<uint4*>(dst + d) = u;
+        }
+      }
+      if (threadIdx.x == 0) a.counters[pair] = 0;
+      if (threadIdx.x == 0 && ic == 0) trace_point(a.trace, 7);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (threadIdx.x == 0) trace_end(a.trace, 11);
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);

@@ -1,4 +1,5 @@
 // gemm.cu -- instantiations and launcher of the weight-streaming GEMM.
+#include <algorithm>
 #include <utility>
 
 #include "launch.h"
@@ -8,12 +9,31 @@ namespace vsd {
 template <int WF, int EPI>
 static cudaError_t launch_one(const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a, int grid,
                               cudaStream_t st, bool pdl) {
-  const uint32_t smem = gemm_smem_bytes(WF, a.n_tok, a.stages);
-  static uint32_t configured = 0;  // largest dynamic shared memory set so far
-  if (smem > configured) {
+  const uint32_t smem = gemm_smem_bytes(WF, a.n_tok, a.rd, a.da, a.db, a.cs);
+  static bool configured = false;
+  if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<WF, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
-    configured = 232448;
+    configured = true;
+  }
+  if (a.cs > 1) {
+    // no more clusters than can be resident together (the CTAs loop over items)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = a.cs;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<WF, EPI>, &cfg) == cudaSuccess && max_clusters > 0)
+      grid = std::min(grid, max_clusters * a.cs);
+    return launch_ex_cluster(gemm_kernel<WF, EPI>, dim3(grid), dim3(kGemmThreads), smem, a.cs, st, pdl, tm_act,
+                             tm_w, a);
   }
   return launch_ex(gemm_kernel<WF, EPI>, dim3(grid), dim3(kGemmThreads), smem, st, pdl, tm_act, tm_w, a);
 }

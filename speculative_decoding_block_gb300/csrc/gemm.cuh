@@ -7,26 +7,36 @@
 //
 // Swap-AB: the weight tile is the 128-row A operand and the tokens are the
 // MMA's N dimension, so one CTA covers 128 output features x n_tok tokens.
-// Weight tiles arrive by TMA (BF16: tiled tensor copy with the 128-byte
-// swizzle, converted to f16 in place; FP8 / NVFP4: one 1-D bulk copy of a
-// pre-packed tile, expanded exactly to f16 -- E4M3 and E2M1 x E4M3 values are
-// all exact f16 numbers).  Activation tiles arrive by TMA with the same
+// Weight tiles arrive by TMA (BF16 matrices, repacked once as f16 when the
+// model is created: tiled tensor copy with the 128-byte swizzle straight into
+// the MMA operand; FP8 / NVFP4: one 1-D bulk copy of a pre-packed tile,
+// expanded exactly to f16 in shared memory -- E4M3 and E2M1 x E4M3 values
+// are all exact f16 numbers).  Activation tiles arrive by TMA with the same
 // swizzle.  The fp32 accumulator sits in TMEM (double-buffered so the
-// epilogue of one tile overlaps the MMAs of the next).  Per-row and
-// per-tensor scales are applied in the epilogue.
+// epilogue of one tile overlaps the MMAs of the next).  Per-row (FP8) and
+// per-tensor (NVFP4) fp32 scales are applied in the epilogue.
 //
 // Warp roles (320 threads): warps 0-3 expand weights into the f16 A tile,
 // warps 4-7 run the epilogue (warp w reads TMEM lanes 32*(w%4)..), warp 8
-// issues TMA, warp 9 allocates TMEM and issues the MMAs.  CTAs are
-// persistent over work items (tile, token tile, k split); split-K partial
-// sums go to a workspace and the last CTA of a tile adds them in split order
-// (deterministic) before running the epilogue.
+// issues TMA, warp 9 allocates TMEM and issues the MMAs.
+//
+// When the output tiles alone cannot fill the GPU, the k dimension is split
+// over a thread-block cluster of cs CTAs: rank r accumulates k tiles
+// [r*kps, (r+1)*kps), stores its partial tile in shared memory, and every CTA
+// then sums the cs partials of its own column groups straight from the peers'
+// shared memory (distributed shared memory), in rank order -- deterministic,
+// no global-memory round trip.  Clusters are persistent over output tiles.
+//
+// The RMSNorm in front of QKV, gate/up and lm_head is folded into the GEMM:
+// the input rows arrive unnormalised (f16 copy of the fp32 residual) and the
+// result of token t is scaled by r_t = 1/sqrt(sum(x_t^2)/hidden + eps), from
+// sums of squares that the residual epilogue writes per 128-feature tile.
 //
 // Epilogues fuse the neighbouring element-wise steps of the decoder layer
 // ("The Inference Stack Behind OCRia", section "Avoiding unnecessary memory
 // transfers": intermediates stay on chip):
 //   STORE  : y = acc * scale                       (component entry point)
-//   RESID  : x_resid += acc * scale                (O and down projections)
+//   RESID  : x += acc * scale; f16 copy of x; sums of squares of x per tile
 //   QKV    : RoPE on q and k, q -> attention tile layout, k / v -> block scratch
 //   SILU   : silu(gate) * up -> f16 MLP activation (gate/up rows interleaved)
 //   ARGMAX : per token, max over vocab rows -> 64-bit argmax key (atomicMax)
@@ -41,6 +51,7 @@ enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SILU = 3, EPI_ARGMAX =
 
 constexpr int kGemmThreads = 320;
 constexpr int kTileN = 128;   // weight rows per tile (MMA M)
+constexpr int kActBoxes = 16;  // activation box heights 16..256 rows (MMA N)
 constexpr int kTileK = 64;    // k per stage (one 128-byte swizzle row of f16)
 constexpr uint32_t kFp8TileBytes = kTileN * kTileK;                  // 8192
 constexpr uint32_t kFp4ValBytes = kTileN * kTileK / 2;               // 4096
@@ -57,12 +68,20 @@ struct GemmArgs {
   int n_rows;              // valid packed rows
   int n_tiles, k_tiles;
   int tok_tiles, n_tok;    // token tiles, tokens per tile (MMA N)
-  int splits, kt_per_split;
+  int cs, kps;             // cluster size = k splits, k tiles per split
   int m_tokens;            // valid token rows
-  int stages;
+  int rd, da, db;          // depths of the weight / expanded-weight / activation rings
+  // RMSNorm of the input rows, folded in as a per-token scale of the result:
+  // r[t] = 1 / sqrt(sum_i ssq_in[i][t] / hidden + eps)  (ssq_in == nullptr: no scale)
+  const float* ssq_in;
+  int n_ssq, ssq_ld;
+  float inv_hidden, eps;
   // STORE / RESID
   float* out_f32;
   int ld_out;
+  __half* x16_out;         // RESID: f16 copy of the updated rows (next GEMM's input)
+  float* ssq_out;          // RESID: [tile][ssq_ld] sum of squares of the updated rows per 128-feature tile
+  float* hidden_out;       // RESID (optional): copy of the updated rows
   // QKV
   __nv_bfloat16* q_tile;   // [B][n_kv][128][hd]
   __nv_bfloat16* k_new;    // [B][n_kv][32][hd] (this layer)
@@ -76,52 +95,87 @@ struct GemmArgs {
   // ARGMAX
   unsigned long long* keys;  // [M]
   float* logits;             // optional [M][vocab]
-  // split-K
-  float* partials;
-  int* counters;
   int* status;
+  Trace trace;
 };
 
+// Shared memory rings (sizes chosen by the host):
+//   W ring (rd slots): weight tiles as loaded -- f16 tiles (16 KB, MMA-ready)
+//          or raw FP8 (8 KB) / NVFP4 (4.5 KB) tiles; deep enough to hold a
+//          CTA's whole weight stream, so it fills before the grid-dependency
+//          wait while the previous kernel still runs;
+//   A ring (da slots, FP8 / NVFP4 only): 16 KB f16 expansions of raw tiles;
+//   B ring (db slots): activation tiles, n_tok x 128 bytes;
+//   R: split-K exchange buffer (cs > 1: n_tok columns x (128 + 4) fp32,
+//      column-major so a warp's read of one column from a peer is one
+//      contiguous 128-byte segment); then the control block.
 struct GemmSmem {
-  // offsets inside the dynamic shared memory (after 1024-byte alignment)
-  uint32_t stage_bytes, b_off, ctrl_off;
+  uint32_t a_off, b_off, b_bytes, w_off, w_bytes, r_off, r_ld, ctrl_off;
 };
 
-__host__ __device__ inline GemmSmem gemm_smem_layout(int wf, int n_tok, int stages) {
+__host__ __device__ inline uint32_t weight_slot_bytes(int wf) {
+  return wf == W_BF16 ? 16384u : (wf == W_FP8 ? kFp8TileBytes : kFp4TileBytes);
+}
+
+__host__ __device__ inline GemmSmem gemm_smem_layout(int wf, int n_tok, int rd, int da, int db, int cs) {
   GemmSmem s;
-  s.b_off = 16384u + raw_region_bytes(wf);
-  s.stage_bytes = s.b_off + static_cast<uint32_t>(n_tok) * 128u;
-  s.ctrl_off = s.stage_bytes * static_cast<uint32_t>(stages);
+  s.w_bytes = weight_slot_bytes(wf);
+  s.b_bytes = static_cast<uint32_t>(n_tok) * 128u;
+  uint32_t off = 0;
+  if (wf == W_BF16) {  // weight slots are MMA operands: 1024-byte aligned, first
+    s.w_off = 0;
+    off = s.w_bytes * rd;
+    s.a_off = 0;
+  } else {
+    s.a_off = 0;
+    off = 16384u * da;
+  }
+  s.b_off = off;
+  off += s.b_bytes * db;
+  if (wf != W_BF16) {
+    s.w_off = off;
+    off += s.w_bytes * rd;
+    off = (off + 1023u) & ~1023u;
+  }
+  s.r_off = off;
+  s.r_ld = 128u + 4u;
+  const uint32_t r_bytes = cs > 1 ? static_cast<uint32_t>(n_tok) * s.r_ld * 4u : 0u;
+  s.ctrl_off = s.r_off + ((r_bytes + 1023u) & ~1023u);
   return s;
 }
-// control block: 4*stages+4 barriers, tmem base, abort flag, last flag, argmax reduction
-__host__ __device__ inline uint32_t gemm_ctrl_bytes() { return 1024u + 8192u; }
-__host__ __device__ inline uint32_t gemm_smem_bytes(int wf, int n_tok, int stages) {
-  return 1024u + gemm_smem_layout(wf, n_tok, stages).ctrl_off + gemm_ctrl_bytes();
+
+// control block: barriers (1 KB), argmax transpose tile 128 x 17 fp32 (9 KB),
+// running argmax keys (8 KB), sums of squares (4 KB), row scales (1 KB)
+constexpr uint32_t kCtrlT = 1024, kCtrlBest = kCtrlT + 9216, kCtrlSq = kCtrlBest + 8192, kCtrlRs = kCtrlSq + 4096;
+constexpr int kBestCap = 1024;  // token columns whose running argmax fits in shared memory
+constexpr int kMaxRd = 32, kMaxDb = 16, kMaxDa = 4;
+constexpr uint32_t kSleepLongWaitNs = 128;  // back-off of the epilogue's wait for the accumulator
+__host__ __device__ inline uint32_t gemm_ctrl_bytes() { return kCtrlRs + 1024u; }
+__host__ __device__ inline uint32_t gemm_smem_bytes(int wf, int n_tok, int rd, int da, int db, int cs) {
+  return 1024u + gemm_smem_layout(wf, n_tok, rd, da, db, cs).ctrl_off + gemm_ctrl_bytes();
 }
 
-// Iterates over the (item, k-tile) sequence of one CTA.
+// Iterates over the (item, k-tile) sequence of one CTA: items (tile, token
+// tile) are dealt to clusters; the CTA of rank r covers k tiles
+// [r * kps, (r + 1) * kps) of every item.
 struct ItemIter {
-  int item, total, stride, kt, kt_end;
+  int item, total, stride, kt, kt_begin, kt_end;
   const GemmArgs* a;
-  __device__ void set_item() {
-    const int split = item % a->splits;
-    kt = split * a->kt_per_split;
-    kt_end = min(a->k_tiles, kt + a->kt_per_split);
+  __device__ ItemIter(const GemmArgs* args, int first, int stride_, int total_, int rank)
+      : item(first), total(total_), stride(stride_), a(args) {
+    kt_begin = rank * args->kps;
+    kt_end = min(args->k_tiles, kt_begin + args->kps);
+    kt = kt_begin;
   }
-  __device__ ItemIter(const GemmArgs* args, int first, int stride_, int total_)
-      : item(first), total(total_), stride(stride_), kt(0), kt_end(0), a(args) {
-    if (item < total) set_item();
-  }
-  __device__ bool done() const { return item >= total; }
-  __device__ bool first_k() const { return kt == (item % a->splits) * a->kt_per_split; }
+  __device__ bool done() const { return item >= total || kt_begin >= kt_end; }
+  __device__ bool first_k() const { return kt == kt_begin; }
   __device__ bool last_k() const { return kt + 1 == kt_end; }
-  __device__ int tile() const { return item / (a->splits * a->tok_tiles); }
-  __device__ int tok_tile() const { return (item / a->splits) % a->tok_tiles; }
+  __device__ int tile() const { return item / a->tok_tiles; }
+  __device__ int tok_tile() const { return item % a->tok_tiles; }
   __device__ void next() {
     if (++kt >= kt_end) {
       item += stride;
-      if (item < total) set_item();
+      kt = kt_begin;
     }
   }
 };
@@ -134,15 +188,7 @@ __device__ __forceinline__ void expand_weights(uint8_t* a_tile, const uint8_t* r
     const int q = t + 128 * i;
     const int r = q >> 3, c = q & 7;
     uint4 o;
-    if constexpr (WF == W_BF16) {
-      uint4* p = reinterpret_cast<uint4*>(a_tile + q * 16);  // in place, position unchanged
-      const uint4 v = *p;
-      o.x = bf16x2_to_f16x2(v.x);
-      o.y = bf16x2_to_f16x2(v.y);
-      o.z = bf16x2_to_f16x2(v.z);
-      o.w = bf16x2_to_f16x2(v.w);
-      *p = o;
-    } else if constexpr (WF == W_FP8) {
+    if constexpr (WF == W_FP8) {
       const uint2 v = *reinterpret_cast<const uint2*>(raw + r * 64 + c * 8);
       o.x = e4m3x2_to_f16x2(static_cast<uint16_t>(v.x & 0xFFFF));
       o.y = e4m3x2_to_f16x2(static_cast<uint16_t>(v.x >> 16));
@@ -175,25 +221,46 @@ __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v,
 }
 
 // Epilogue of one 16-column group: v[i] is the fp32 result of packed row
-// `row` (0..127 inside the tile) for token column c0 + i.
+// `row` (0..127 inside the tile) for token column c0 + i; rs holds the
+// per-column row scales of the item (1 when the input is not normalised).
 template <int EPI, int WF>
-__device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int tt, int row, int c0,
-                                              float* v, unsigned long long* red, int warp_e, int lane) {
+__device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int tt, int row, int c0, float* v,
+                                              const float* rs, float* tbuf, float* sq_red, int warp_e, int lane) {
   const int prow = tile * kTileN + row;  // packed row
   const bool row_ok = prow < a.n_rows;
   float scale = 1.0f;
   if constexpr (WF != W_BF16) scale = row_ok ? a.row_scale[prow] : 0.0f;
   const int tok0 = tt * a.n_tok + c0;
 
-  if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+  if constexpr (EPI == EPI_STORE) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int tok = tok0 + i;
+      if (row_ok && tok < a.m_tokens)
+        a.out_f32[static_cast<size_t>(tok) * a.ld_out + prow] = v[i] * scale * rs[c0 + i];
+    }
+  } else if constexpr (EPI == EPI_RESID) {
+    float old[16];  // every load issued before the first store
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int tok = tok0 + i;
+      old[i] = (row_ok && tok < a.m_tokens) ? a.out_f32[static_cast<size_t>(tok) * a.ld_out + prow] : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int tok = tok0 + i;
+      float sq = 0.0f;
       if (row_ok && tok < a.m_tokens) {
-        float* p = a.out_f32 + static_cast<size_t>(tok) * a.ld_out + prow;
-        if constexpr (EPI == EPI_RESID) *p += v[i] * scale;
-        else *p = v[i] * scale;
+        const size_t o = static_cast<size_t>(tok) * a.ld_out + prow;
+        const float x = old[i] + v[i] * scale;
+        a.out_f32[o] = x;
+        a.x16_out[o] = __float2half_rn(x);
+        if (a.hidden_out) a.hidden_out[o] = x;
+        sq = x * x;
       }
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, m);
+      if (lane == 0) sq_red[warp_e * 256 + c0 + i] = sq;
     }
   } else if constexpr (EPI == EPI_QKV) {
     const int hd = a.head_dim, half = hd >> 1;
@@ -201,16 +268,23 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
     const int d = (r & 1) ? (r >> 1) + half : (r >> 1);
     const int fi = r >> 1;  // rotation frequency index
     const int group = a.n_q / a.n_kv;
+    const bool rotate = head < a.n_q + a.n_kv;
+    float2 cs[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {  // all table loads first
+      const int tok = min(tok0 + i, a.m_tokens - 1);
+      const int b = tok / kRows, j = tok % kRows;
+      cs[i] = rotate ? a.rope[static_cast<size_t>(a.ctx_len[b] + j) * half + fi] : make_float2(1.0f, 0.0f);
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float x = v[i] * scale;
+      const float x = v[i] * scale * rs[c0 + i];
       const float xp = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
       const int tok = tok0 + i;
       if (!row_ok || tok >= a.m_tokens) continue;
       const int b = tok / kRows, j = tok % kRows;
-      if (head < a.n_q + a.n_kv) {  // q or k: rotate
-        const float2 cs = a.rope[static_cast<size_t>(a.ctx_len[b] + j) * half + fi];
-        const float y = (r & 1) ? (x * cs.x + xp * cs.y) : (x * cs.x - xp * cs.y);
+      if (rotate) {
+        const float y = (r & 1) ? (x * cs[i].x + xp * cs[i].y) : (x * cs[i].x - xp * cs[i].y);
         if (head < a.n_q) {
           const int kvh = head / group, hq = head % group;
           a.q_tile[((static_cast<size_t>(b) * a.n_kv + kvh) * 128 + j * group + hq) * hd + d] =
@@ -228,7 +302,7 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
     const int feat = tile * 64 + (row >> 1);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float x = v[i] * scale;
+      const float x = v[i] * scale * rs[c0 + i];
       const float up = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
       const int tok = tok0 + i;
       if ((row & 1) == 0 && feat < a.ffn && tok < a.m_tokens) {
@@ -237,20 +311,38 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
       }
     }
   } else if constexpr (EPI == EPI_ARGMAX) {
+    // scaled logits -> transpose tile tbuf[row][16]; argmax_group reduces the columns
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int tok = tok0 + i;
-      const float x = v[i] * scale;
+      const float x = v[i] * rs[c0 + i];
       if (a.logits && row_ok && tok < a.m_tokens) a.logits[static_cast<size_t>(tok) * a.n_rows + prow] = x;
-      unsigned long long key = row_ok ? argmax_key(x, static_cast<uint32_t>(prow)) : 0ull;
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) {
-        const unsigned long long o = shfl_xor_u64(key, m);
-        key = o > key ? o : key;
-      }
-      if (lane == 0) red[warp_e * 256 + c0 + i] = key;
+      tbuf[row * 17 + i] = row_ok ? x : -INFINITY;
     }
   }
+}
+
+// Max over the 128 rows of each of the 16 columns of tbuf, 8 threads per
+// column (et = epilogue thread 0..127); the winner of column cc is folded
+// into best[cc] (largest logit, lowest vocabulary row among equals).
+__device__ __forceinline__ void argmax_group(const float* tbuf, unsigned long long* best, int tile, int et) {
+  const int cc = et >> 3, part = et & 7;
+  unsigned long long key = 0ull;
+#pragma unroll 4
+  for (int k = 0; k < 16; ++k) {
+    const int r = part * 16 + k;
+    const float x = tbuf[r * 17 + cc];
+    if (x != -INFINITY) {
+      const unsigned long long kk = argmax_key(x, static_cast<uint32_t>(tile * kTileN + r));
+      key = kk > key ? kk : key;
+    }
+  }
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const unsigned long long o = shfl_xor_u64(key, m);
+    key = o > key ? o : key;
+  }
+  if (part == 0 && key > best[cc]) best[cc] = key;
 }
 
 template <int WF, int EPI>
@@ -259,36 +351,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const GemmSmem L = gemm_smem_layout(WF, a.n_tok, a.stages);
-  const int S = a.stages;
+  const GemmSmem L = gemm_smem_layout(WF, a.n_tok, a.rd, a.da, a.db, a.cs);
+  const int RD = a.rd, DA = a.da, DB = a.db;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.ctrl_off);
-  uint64_t* wfull = bars;
-  uint64_t* afull = bars + S;
-  uint64_t* conv = bars + 2 * S;
-  uint64_t* empty = bars + 3 * S;
-  uint64_t* tfull = bars + 4 * S;
-  uint64_t* tempty = bars + 4 * S + 2;
-  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(bars + 4 * S + 4);
+  uint64_t* wfull = bars;                // weight tile landed
+  uint64_t* wempty = wfull + kMaxRd;     // weight slot free again
+  uint64_t* bfull = wempty + kMaxRd;     // activation tile landed
+  uint64_t* bempty = bfull + kMaxDb;     // activation slot free again
+  uint64_t* conv = bempty + kMaxDb;      // expanded tile ready (FP8 / NVFP4)
+  uint64_t* cempty = conv + kMaxDa;      // expanded slot free again
+  uint64_t* tfull = cempty + kMaxDa;     // [2] accumulator complete
+  uint64_t* tempty = tfull + 2;          // [2] accumulator read out
+  uint64_t* rfull = tempty + 2;          // peers' partials are in their R buffers
+  uint64_t* rfree = rfull + 1;           // peers finished reading this CTA's R buffer
+  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(rfree + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_base_p + 2);
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(smem + L.ctrl_off + 1024);
+  float* tbuf = reinterpret_cast<float*>(smem + L.ctrl_off + kCtrlT);
+  unsigned long long* best = reinterpret_cast<unsigned long long*>(smem + L.ctrl_off + kCtrlBest);
+  float* sq_red = reinterpret_cast<float*>(smem + L.ctrl_off + kCtrlSq);
+  float* rs = reinterpret_cast<float*>(smem + L.ctrl_off + kCtrlRs);
+  float* R = reinterpret_cast<float*>(smem + L.r_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = a.n_tiles * a.tok_tiles * a.splits;
+  const int cs = a.cs;
+  const int rank = cs > 1 ? static_cast<int>(cluster_rank()) : 0;
+  const int cluster = cs > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int n_clusters = cs > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+  const int total = a.n_tiles * a.tok_tiles;
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(2 * a.n_tok)) tmem_cols <<= 1;
+  if (threadIdx.x == 0) trace_start(a.trace);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&wfull[s], 1);
-      mbar_init(&afull[s], 1);
-      mbar_init(&conv[s], 128);
-      mbar_init(&empty[s], 1);
+    for (int i = 0; i < RD; ++i) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wempty[i], WF == W_BF16 ? 1 : 128);
+    }
+    for (int i = 0; i < DB; ++i) {
+      mbar_init(&bfull[i], 1);
+      mbar_init(&bempty[i], 1);
+    }
+    for (int i = 0; i < DA; ++i) {
+      mbar_init(&conv[i], 128);
+      mbar_init(&cempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 128);
     }
+    mbar_init(rfull, cs);
+    mbar_init(rfree, cs);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -298,78 +410,101 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (cs > 1) cluster_sync();  // every CTA of the cluster has its barriers initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_p;
   pdl_launch_dependents();
+  if (threadIdx.x == 0) trace_point(a.trace, 1);
 
   if (warp == 8) {
-    // ---------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------- TMA producer (weights + activations)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
-      const uint32_t wbytes = WF == W_BF16 ? 16384u : (WF == W_FP8 ? kFp8TileBytes : kFp4TileBytes);
-      auto issue_w = [&](int cnt, const ItemIter& it) {
-        const int s = cnt % S;
-        uint8_t* st = smem + s * L.stage_bytes;
-        mbar_expect_tx(&wfull[s], wbytes);
+      auto issue_w = [&](int i, const ItemIter& it) {
+        const int r = i % RD;
+        uint8_t* dst = smem + L.w_off + r * L.w_bytes;
+        mbar_expect_tx(&wfull[r], L.w_bytes);
         if constexpr (WF == W_BF16) {
-          tma_load_2d_hint(st, &tm_w, &wfull[s], it.kt * kTileK, it.tile() * kTileN, pol_w);
+          tma_load_2d_hint(dst, &tm_w, &wfull[r], it.kt * kTileK, it.tile() * kTileN, pol_w);
         } else {
-          const uint8_t* src = a.w_tiles + (static_cast<size_t>(it.tile()) * a.k_tiles + it.kt) * wbytes;
-          bulk_load(st + 16384, src, wbytes, &wfull[s], pol_w);
+          const uint8_t* src = a.w_tiles + (static_cast<size_t>(it.tile()) * a.k_tiles + it.kt) * L.w_bytes;
+          bulk_load(dst, src, L.w_bytes, &wfull[r], pol_w);
         }
       };
-      // weights do not depend on the previous kernel: start them before the grid dependency wait
-      int pre = 0;
-      {
-        ItemIter it(&a, blockIdx.x, gridDim.x, total);
-        for (; pre < S && !it.done(); ++pre, it.next()) issue_w(pre, it);
-      }
+      auto issue_b = [&](int i, const ItemIter& it) {
+        const int b = i % DB;
+        uint8_t* dst = smem + L.b_off + b * L.b_bytes;
+        mbar_expect_tx(&bfull[b], L.b_bytes);
+        // one box of n_tok rows (the host encodes the map with that box height)
+        tma_load_2d_hint(dst, &tm_act, &bfull[b], it.kt * kTileK, it.tok_tile() * a.n_tok, pol_a);
+      };
+      // weights do not depend on the previous kernel: fill the weight ring before the grid dependency wait
+      ItemIter itw(&a, cluster, n_clusters, total, rank), itb(&a, cluster, n_clusters, total, rank);
+      int wi = 0, bi = 0;
+      for (; wi < RD && !itw.done(); ++wi, itw.next()) issue_w(wi, itw);
       pdl_wait();
-      ItemIter it(&a, blockIdx.x, gridDim.x, total);
-      int cnt = 0;
+      trace_point(a.trace, 2);
+      // then serve both rings as their slots free up, never blocking on one while the other could proceed
+      long long t_last = cycles();
       bool ok = true;
-      for (; !it.done(); it.next(), ++cnt) {
-        const int s = cnt % S;
-        if (cnt >= S && !mbar_wait(&empty[s], ((cnt / S) - 1) & 1, abort_flag, a.status)) {
+      while (!itw.done() || !itb.done()) {
+        bool progress = false;
+        if (!itb.done() && (bi < DB || mbar_test_wait(&bempty[bi % DB], ((bi / DB) - 1) & 1))) {
+          issue_b(bi, itb);
+          ++bi;
+          itb.next();
+          progress = true;
+        }
+        if (!itw.done() && (wi < RD || mbar_test_wait(&wempty[wi % RD], ((wi / RD) - 1) & 1))) {
+          issue_w(wi, itw);
+          ++wi;
+          itw.next();
+          progress = true;
+        }
+        if (progress) {
+          t_last = cycles();
+          continue;
+        }
+        // nothing to issue: back off briefly, so that this thread does not
+        // take shared-memory and issue slots from the expansion warps
+        __nanosleep(64);
+        if (*abort_flag || cycles() - t_last > kWaitLimitCycles) {
+          if (!*abort_flag) atomicOr(a.status, VSD_DEV_TIMEOUT);
+          *abort_flag = 1;
           ok = false;
           break;
         }
-        if (cnt >= pre) issue_w(cnt, it);
-        uint8_t* bt = smem + s * L.stage_bytes + L.b_off;
-        mbar_expect_tx(&afull[s], static_cast<uint32_t>(a.n_tok) * 128u);
-        const int r0 = it.tok_tile() * a.n_tok;
-        for (int i = 0; i < a.n_tok / 16; ++i)
-          tma_load_2d_hint(bt + i * 2048, &tm_act, &afull[s], it.kt * kTileK, r0 + 16 * i, pol_a);
       }
       if (!ok) {
         // drain: let the copies already in flight land before the CTA exits
-        const int issued = max(cnt, pre);
-        for (int c = max(0, issued - S); c < issued; ++c) {
-          volatile int never = 0;
-          mbar_wait(&wfull[c % S], (c / S) & 1, &never, nullptr);
-          if (c < cnt) mbar_wait(&afull[c % S], (c / S) & 1, &never, nullptr);
-        }
+        volatile int never = 0;
+        for (int i = max(0, wi - RD); i < wi; ++i) mbar_wait(&wfull[i % RD], (i / RD) & 1, &never, nullptr);
+        for (int i = max(0, bi - DB); i < bi; ++i) mbar_wait(&bfull[i % DB], (i / DB) & 1, &never, nullptr);
       }
     }
   } else if (warp < 4) {
-    // ---------------------------------------------------------- weight expansion
-    const int t = threadIdx.x;
-    ItemIter it(&a, blockIdx.x, gridDim.x, total);
-    for (int cnt = 0; !it.done(); it.next(), ++cnt) {
-      const int s = cnt % S;
-      if (!mbar_wait(&wfull[s], (cnt / S) & 1, abort_flag, a.status)) break;
-      uint8_t* st = smem + s * L.stage_bytes;
-      expand_weights<WF>(st, st + 16384, t);
-      fence_proxy_async();
-      mbar_arrive(&conv[s]);
+    // ---------------------------------------------------------- weight expansion (FP8 / NVFP4)
+    if constexpr (WF != W_BF16) {
+      const int t = threadIdx.x;
+      ItemIter it(&a, cluster, n_clusters, total, rank);
+      for (int i = 0; !it.done(); it.next(), ++i) {
+        const int r = i % RD, c = i % DA;
+        if (!mbar_wait(&wfull[r], (i / RD) & 1, abort_flag, a.status)) break;
+        if (i >= DA && !mbar_wait(&cempty[c], ((i / DA) - 1) & 1, abort_flag, a.status)) break;
+        if (t == 0 && i == 0) trace_point(a.trace, 3);
+        expand_weights<WF>(smem + L.a_off + c * 16384, smem + L.w_off + r * L.w_bytes, t);
+        fence_proxy_async();
+        mbar_arrive(&conv[c]);
+        mbar_arrive(&wempty[r]);
+      }
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, a.n_tok, false, false, false);
-      ItemIter it(&a, blockIdx.x, gridDim.x, total);
-      int cnt = 0, acc = 0;
+      ItemIter it(&a, cluster, n_clusters, total, rank);
+      int i = 0, acc = 0;
       bool ok = true;
       while (ok && !it.done()) {
         const int ab = acc & 1;
@@ -378,29 +513,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d = tmem_base + static_cast<uint32_t>(ab * a.n_tok);
         bool last = false;
         do {
-          const int s = cnt % S;
-          const uint32_t par = (cnt / S) & 1;
-          if (!mbar_wait(&conv[s], par, abort_flag, a.status) ||
-              !mbar_wait(&afull[s], par, abort_flag, a.status)) {
+          // 16-bit weights are MMA-ready on arrival; FP8 / NVFP4 after expansion
+          const int s = WF == W_BF16 ? i % RD : i % DA;
+          const uint32_t par = WF == W_BF16 ? (i / RD) & 1 : (i / DA) & 1;
+          const int b = i % DB;
+          if (!mbar_wait(WF == W_BF16 ? &wfull[s] : &conv[s], par, abort_flag, a.status) ||
+              !mbar_wait(&bfull[b], (i / DB) & 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
+          if (i == 0) trace_point(a.trace, 4);
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + s * L.stage_bytes);
-          const uint32_t sb = smem_u32(smem + s * L.stage_bytes + L.b_off);
+          const uint32_t sa = smem_u32(smem + (WF == W_BF16 ? L.w_off + s * L.w_bytes : L.a_off + s * 16384));
+          const uint32_t sb = smem_u32(smem + L.b_off + b * L.b_bytes);
           const bool first = it.first_k();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             umma_f16(d, sw128_desc(sa + kk * 32, 16, 1024), sw128_desc(sb + kk * 32, 16, 1024), idesc,
                      (first && kk == 0) ? 0u : 1u);
           }
-          umma_commit(&empty[s]);
+          umma_commit(WF == W_BF16 ? &wempty[s] : &cempty[s]);
+          umma_commit(&bempty[b]);
           last = it.last_k();
           it.next();
-          ++cnt;
+          ++i;
         } while (!last);
         if (!ok) break;
         umma_commit(&tfull[ab]);
+        if (acc == 0) trace_point(a.trace, 5);
         ++acc;
       }
     }
@@ -409,73 +549,139 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int we = warp - 4;  // == warp % 4: TMEM lane quarter
     const int row = we * 32 + lane;
     const int et = threadIdx.x - 128;
+    const int groups = a.n_tok / 16;
+    const bool alive = rank * a.kps < a.k_tiles;
+    // ARGMAX: running best key per token column of this CTA, flushed once at the end
+    const bool keep_best = a.tok_tiles * a.n_tok <= kBestCap;
+    if constexpr (EPI == EPI_ARGMAX)
+      for (int c = et; c < kBestCap; c += 128) best[c] = 0ull;
+    pdl_wait();  // the row scales read what the previous kernels wrote
+    named_bar_sync(1, 128);
     int acc = 0;
-    for (int item = blockIdx.x; item < total; item += gridDim.x, ++acc) {
+    for (int item = cluster; alive && item < total; item += n_clusters, ++acc) {
       const int ab = acc & 1;
-      if (!mbar_wait(&tfull[ab], (acc >> 1) & 1, abort_flag, a.status)) break;
+      const int tile = item / a.tok_tiles, tt = item % a.tok_tiles;
+      // per-token scale of the normalised input rows, while the MMAs run
+      for (int c = et; c < a.n_tok; c += 128) {
+        float r = 1.0f;
+        const int tok = tt * a.n_tok + c;
+        if (a.ssq_in && tok < a.m_tokens) {
+          float ss = 0.0f;
+#pragma unroll 8
+          for (int k = 0; k < a.n_ssq; ++k) ss += a.ssq_in[static_cast<size_t>(k) * a.ssq_ld + tok];
+          r = 1.0f / sqrtf(ss * a.inv_hidden + a.eps);
+        }
+        rs[c] = r;
+      }
+      named_bar_sync(1, 128);
+      if (et == 0 && acc == 0) trace_point(a.trace, 8);
+      if (cs > 1 && acc > 0 && !mbar_wait_cluster(rfree, (acc - 1) & 1, abort_flag, a.status)) break;
+      if (!mbar_wait(&tfull[ab], (acc >> 1) & 1, abort_flag, a.status, kSleepLongWaitNs)) break;
+      if (et == 0 && acc == 0) trace_point(a.trace, 6);
       tc_fence_after();
-      const int tile = item / (a.splits * a.tok_tiles);
-      const int tt = (item / a.splits) % a.tok_tiles;
-      const int split = item % a.splits;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(we * 32) << 16) + static_cast<uint32_t>(ab * a.n_tok);
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(we * 32) << 16) + static_cast<uint32_t>(ab * a.n_tok);
       float v[16];
-      if (a.splits == 1) {
-        for (int c0 = 0; c0 < a.n_tok; c0 += 16) {
-          tmem_ld16(taddr + c0, v);
-          tmem_ld_wait();
-          epilogue_cols<EPI, WF>(a, tile, tt, row, c0, v, red, we, lane);
-        }
-        tc_fence_before();
-        mbar_arrive(&tempty[ab]);
-      } else {
-        const int tid = tile * a.tok_tiles + tt;
-        float* base = a.partials + static_cast<size_t>(tid) * a.splits * 128 * a.n_tok;
-        float* mine = base + static_cast<size_t>(split) * 128 * a.n_tok;
+      if (cs > 1) {
+        // partial sums of this CTA's k range -> R (column-major), then tell every CTA of the cluster
         for (int c0 = 0; c0 < a.n_tok; c0 += 16) {
           tmem_ld16(taddr + c0, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) __stcg(mine + (c0 + i) * 128 + row, v[i]);
+          for (int i = 0; i < 16; ++i) R[(c0 + i) * L.r_ld + row] = v[i];
         }
         tc_fence_before();
         mbar_arrive(&tempty[ab]);
-        __threadfence();
         named_bar_sync(1, 128);
-        if (et == 0) *last_flag = (atomicAdd(&a.counters[tid], 1) == a.splits - 1) ? 1 : 0;
-        named_bar_sync(1, 128);
-        if (*last_flag) {
-          __threadfence();
-          for (int c0 = 0; c0 < a.n_tok; c0 += 16) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-            for (int sp = 0; sp < a.splits; ++sp) {
-              const float* p = base + static_cast<size_t>(sp) * 128 * a.n_tok + c0 * 128 + row;
-#pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] += __ldcg(p + i * 128);
-            }
-            epilogue_cols<EPI, WF>(a, tile, tt, row, c0, v, red, we, lane);
-          }
-          if (et == 0) a.counters[tid] = 0;
+        if (et == 0) {
+          fence_acq_rel_cluster();
+          for (int p = 0; p < cs; ++p) mbar_arrive_remote(mapa_shared(smem_u32(rfull), p));
+        }
+        if (!mbar_wait_cluster(rfull, acc & 1, abort_flag, a.status)) break;
+        if (et == 0 && acc == 0) trace_point(a.trace, 7);
+      }
+      // column groups of this CTA: all of them (cs == 1) or every cs-th (split-K)
+      for (int g = rank; g < groups; g += cs) {
+        const int c0 = g * 16;
+        if (cs == 1) {
+          tmem_ld16(taddr + c0, v);
+          tmem_ld_wait();
         } else {
-          continue;  // this CTA's split is done; the last CTA runs the epilogue
+          const uint32_t local = smem_u32(R + c0 * L.r_ld + row);
+#pragma unroll
+          for (int h4 = 0; h4 < 16; h4 += 4) {  // 4 columns at a time, every peer's loads in flight
+            float x[8][4];
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+              if (p < cs) {
+                const uint32_t ra = mapa_shared(local, p) + h4 * L.r_ld * 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) x[p][i] = ld_dsmem_f32(ra + i * L.r_ld * 4);
+              }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[h4 + i] = 0.0f;
+#pragma unroll
+            for (int p = 0; p < 8; ++p)  // fixed order: deterministic sum
+              if (p < cs) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[h4 + i] += x[p][i];
+              }
+          }
+        }
+        if (et == 0 && acc == 0 && g == rank) trace_point(a.trace, 12);
+        epilogue_cols<EPI, WF>(a, tile, tt, row, c0, v, rs, tbuf, sq_red, we, lane);
+        if (et == 0 && acc == 0 && g == rank) trace_point(a.trace, 14);
+        if constexpr (EPI == EPI_ARGMAX) {
+          named_bar_sync(1, 128);
+          const int col = tt * a.n_tok + c0;
+          if (keep_best) {
+            argmax_group(tbuf, best + col, tile, et);
+          } else {  // too many tokens for the running best: one atomic per column and tile
+            argmax_group(tbuf, best, tile, et);
+            if ((et & 7) == 0) {
+              const int tok = col + (et >> 3);
+              if (tok < a.m_tokens && best[et >> 3]) atomicMax(a.keys + tok, best[et >> 3]);
+              best[et >> 3] = 0ull;
+            }
+          }
+          named_bar_sync(1, 128);
+          if (et == 0 && acc == 0 && g == rank) trace_point(a.trace, 15);
         }
       }
-      if constexpr (EPI == EPI_ARGMAX) {
-        named_bar_sync(1, 128);
+      if (cs == 1) {
+        tc_fence_before();
+        mbar_arrive(&tempty[ab]);
+      }
+      named_bar_sync(1, 128);
+      if (et == 0 && acc == 0) trace_point(a.trace, 9);
+      if (cs > 1 && et == 0) {
+        fence_acq_rel_cluster();
+        for (int p = 0; p < cs; ++p) mbar_arrive_remote(mapa_shared(smem_u32(rfree), p));
+      }
+      if constexpr (EPI == EPI_RESID) {
         for (int c = et; c < a.n_tok; c += 128) {
-          unsigned long long k = red[c];
-          for (int w = 1; w < 4; ++w) k = red[w * 256 + c] > k ? red[w * 256 + c] : k;
           const int tok = tt * a.n_tok + c;
-          if (tok < a.m_tokens) atomicMax(a.keys + tok, k);
+          if ((c / 16) % cs == rank && tok < a.m_tokens)
+            a.ssq_out[static_cast<size_t>(tile) * a.ssq_ld + tok] =
+                sq_red[c] + sq_red[256 + c] + sq_red[512 + c] + sq_red[768 + c];
         }
-        named_bar_sync(1, 128);
       }
+      named_bar_sync(1, 128);
+      if (et == 0 && acc == 0) trace_point(a.trace, 10);
+    }
+    if constexpr (EPI == EPI_ARGMAX) {
+      if (keep_best)
+        for (int c = et; c < a.tok_tiles * a.n_tok; c += 128)
+          if (c < a.m_tokens && best[c]) atomicMax(a.keys + c, best[c]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (cs > 1) cluster_sync();  // no CTA leaves while a peer may still read its R buffer
+  if (threadIdx.x == 0) trace_end(a.trace, 11);
   if (warp == 9) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, tmem_cols);
   }

@@ -9,11 +9,38 @@ namespace vsd {
 
 // Launches gemm_kernel<wf, epi> on `grid` persistent CTAs; programmatic
 // dependent launch when pdl is set.
+// Launches gemm_kernel<wf, epi> as a.cs-CTA clusters; `grid` is a multiple of
+// a.cs and is clamped to the clusters that can be resident at once.
 cudaError_t launch_gemm(int wf, int epi, const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
                         int grid, cudaStream_t st, bool pdl);
 cudaError_t launch_attn(int hd, const CUtensorMap& tm_q, const CUtensorMap& tm_kc, const CUtensorMap& tm_vc,
                         const CUtensorMap& tm_kn, const CUtensorMap& tm_vn, const AttnArgs& a, dim3 grid,
                         cudaStream_t st, bool pdl);
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex_cluster(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, int cluster, cudaStream_t st,
+                              bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeClusterDimension;
+  attr[n].val.clusterDim.x = cluster;
+  attr[n].val.clusterDim.y = 1;
+  attr[n].val.clusterDim.z = 1;
+  ++n;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,

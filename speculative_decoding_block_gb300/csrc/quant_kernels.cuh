@@ -148,14 +148,16 @@ __global__ void pack_row_scale_kernel(const float* src_scale, const int* perm, i
   if (p < n_packed) row_scale[p] = perm[p] >= 0 ? src_scale[perm[p]] : 0.0f;
 }
 
-// BF16: row gather [n_packed][K].
+// BF16 -> f16 row gather [n_packed][K] (the GEMM consumes 16-bit weights as
+// f16: exact for magnitudes in [2^-14, 65504], nearest f16 below 2^-14).
 __global__ void pack_bf16_kernel(const uint16_t* w, const int* perm, int n_packed, int K, uint16_t* out) {
   const size_t n = static_cast<size_t>(n_packed) * K;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int p = static_cast<int>(i / K), k = static_cast<int>(i % K);
     const int src = perm[p];
-    out[i] = src >= 0 ? w[static_cast<size_t>(src) * K + k] : 0;
+    const float v = src >= 0 ? __uint_as_float(static_cast<uint32_t>(w[static_cast<size_t>(src) * K + k]) << 16) : 0.0f;
+    out[i] = __half_as_ushort(__float2half_rn(v));
   }
 }
 

@@ -1,6 +1,6 @@
-// step_kernels.cuh -- the light kernels of the verify step: embedding gather
-// with the first RMSNorm, RMSNorm, the fused argmax / prefix-accept / KV
-// commit, and helpers of the component entry points.
+// step_kernels.cuh -- the light kernels of the verify step: embedding gather,
+// the fused argmax / prefix-accept / KV commit, and helpers of the component
+// entry points.
 #pragma once
 
 #include "vsd_common.cuh"
@@ -18,16 +18,6 @@ __device__ __forceinline__ float block_sum_128(float v, float* red) {
   return s;
 }
 
-// x / sqrt(mean(x^2) + eps) * gamma of one row held in x (global), written as f16.
-__device__ __forceinline__ void rmsnorm_row(const float* x, int H, float eps, const float* gamma, __half* u,
-                                            float* red) {
-  float ss = 0.0f;
-  for (int i = threadIdx.x; i < H; i += 128) ss += x[i] * x[i];
-  ss = block_sum_128(ss, red);
-  const float r = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
-  for (int i = threadIdx.x; i < H; i += 128) u[i] = __float2half_rn(x[i] * r * gamma[i]);
-}
-
 struct EmbedArgs {
   const uint16_t* embed;  // [V][H] bf16
   int vocab, hidden;
@@ -35,60 +25,98 @@ struct EmbedArgs {
   const int* pending;     // [B]
   const int* drafts;      // [B][16]
   int max_tokens;
-  float eps;
-  const float* gamma;
   float* x;               // [M][H] residual stream
-  __half* u;              // [M][H] normalised (layer-0 input)
+  __half* x16;            // [M][H] f16 copy (first GEMM's input)
+  float* ssq;             // [ceil(H/128)][ssq_ld] sums of squares per 128-feature slice
+  int ssq_ld;
   int* ctx_len;           // [B] validated context length (0 if invalid)
+  int* req_ok;            // [B] 1 if seq_len and pending token are valid
+  unsigned long long* keys;  // [M] argmax keys of the step, cleared here
   float* hidden0;         // optional [M][H]
   int* status;
+  Trace trace;
 };
 
+constexpr int kMaxSlices = 128;  // hidden <= 128 * 128
+
 // One CTA (128 threads) per row b*17 + j: token = pending (j = 0) or draft j-1.
-__global__ void __launch_bounds__(128) embed_norm_kernel(const EmbedArgs a) {
-  __shared__ float red[4];
+// The row's RMSNorm is not applied here: the consuming GEMM scales its
+// result per token by 1/sqrt(mean(x^2) + eps), from the sums of squares
+// written here per 128-feature slice.
+__global__ void __launch_bounds__(128) embed_kernel(const EmbedArgs a) {
+  __shared__ float part[kMaxSlices][4];
   pdl_wait();
   pdl_launch_dependents();
+  if (threadIdx.x == 0) trace_start(a.trace);
   const int row = blockIdx.x, b = row / kRows, j = row % kRows;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   int tok = j == 0 ? a.pending[b] : a.drafts[b * kBlock + j - 1];
-  if (tok < 0 || tok >= a.vocab) {
-    if (threadIdx.x == 0) atomicOr(a.status, VSD_DEV_BAD_TOKEN);
+  const bool tok_ok = tok >= 0 && tok < a.vocab;
+  if (!tok_ok) {
+    if (t == 0) atomicOr(a.status, VSD_DEV_BAD_TOKEN);
     tok = 0;
   }
-  if (j == 0 && threadIdx.x == 0) {
-    const int L = a.seq_lens[b];
-    const bool ok = L >= 0 && L + kRows <= a.max_tokens;
-    if (!ok) atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
-    a.ctx_len[b] = ok ? L : 0;
+  if (t == 0) {
+    a.keys[row] = 0ull;
+    if (j == 0) {
+      const int L = a.seq_lens[b];
+      const bool ok = L >= 0 && L + kRows <= a.max_tokens;
+      if (!ok) atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
+      a.ctx_len[b] = ok ? L : 0;
+      a.req_ok[b] = (ok && tok_ok) ? 1 : 0;
+    }
   }
   const uint16_t* e = a.embed + static_cast<size_t>(tok) * a.hidden;
-  float* x = a.x + static_cast<size_t>(row) * a.hidden;
-  for (int i = threadIdx.x; i < a.hidden; i += 128) {
-    const float v = __uint_as_float(static_cast<uint32_t>(e[i]) << 16);
-    x[i] = v;
-    if (a.hidden0) a.hidden0[static_cast<size_t>(row) * a.hidden + i] = v;
+  const size_t o = static_cast<size_t>(row) * a.hidden;
+  const int slices = (a.hidden + 127) / 128;
+  for (int k0 = 0; k0 < slices; k0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {  // loads first
+      const int i = (k0 + k) * 128 + t;
+      v[k] = (k0 + k < slices && i < a.hidden) ? __uint_as_float(static_cast<uint32_t>(e[i]) << 16) : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = (k0 + k) * 128 + t;
+      if (k0 + k < slices && i < a.hidden) {
+        a.x[o + i] = v[k];
+        a.x16[o + i] = __float2half_rn(v[k]);
+        if (a.hidden0) a.hidden0[o + i] = v[k];
+      }
+      float sq = v[k] * v[k];
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, m);
+      if (lane == 0 && k0 + k < slices) part[k0 + k][warp] = sq;
+    }
   }
   __syncthreads();
-  rmsnorm_row(x, a.hidden, a.eps, a.gamma, a.u + static_cast<size_t>(row) * a.hidden, red);
+  if (t < slices)
+    a.ssq[static_cast<size_t>(t) * a.ssq_ld + row] = part[t][0] + part[t][1] + part[t][2] + part[t][3];
 }
 
-__global__ void __launch_bounds__(128) rmsnorm_kernel(const float* x, int hidden, float eps, const float* gamma,
-                                                      __half* u, float* copy_out) {
-  __shared__ float red[4];
-  pdl_wait();
-  pdl_launch_dependents();
-  const size_t row = blockIdx.x;
-  if (copy_out)
-    for (int i = threadIdx.x; i < hidden; i += 128) copy_out[row * hidden + i] = x[row * hidden + i];
-  rmsnorm_row(x + row * hidden, hidden, eps, gamma, u + row * hidden, red);
+// Validation of the caller's per-request state (component entry points that
+// run without the embedding kernel).
+__global__ void validate_requests_kernel(const int* seq_lens, const int* pending, int B, int vocab, int max_tokens,
+                                         int* ctx_len, int* req_ok, int* status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int L = seq_lens[b], p = pending[b];
+  const bool ok = L >= 0 && L + kRows <= max_tokens;
+  if (!ok) atomicOr(status, VSD_DEV_BAD_SEQLEN);
+  if (p < 0 || p >= vocab) atomicOr(status, VSD_DEV_BAD_TOKEN);
+  ctx_len[b] = ok ? L : 0;
+  req_ok[b] = (ok && p >= 0 && p < vocab) ? 1 : 0;
 }
 
 struct CommitArgs {
-  int vocab, layers, n_kv, hd, batch_cap, num_pages, pages_per_req, max_tokens;
-  unsigned long long* keys;       // [B*17], reset to 0 after use
+  int vocab, layers, n_kv, hd, batch_cap, num_pages, pages_per_req;
+  const unsigned long long* keys;  // [B*17]
   const int* drafts;              // [B][16]
-  int* seq_lens;                  // [B] in/out
-  int* pending;                   // [B] in/out
+  const int* ctx_len;             // [B] validated committed length
+  const int* req_ok;              // [B]
+  int* seq_lens;                  // [B] out (written by the layer-0 CTA only)
+  int* pending;                   // [B] out
   int* accepted;                  // [B]
   int* out_tokens;                // [B][17]
   const int* page_table;          // [max_batch][ppr]
@@ -97,18 +125,24 @@ struct CommitArgs {
   __nv_bfloat16* k_pool;          // [layers][pages][n_kv][16][hd]
   __nv_bfloat16* v_pool;
   int* status;
+  Trace trace;
 };
 
-// Greedy tokens from the argmax keys, accepted length = first draft that
-// differs (16 if none), outputs, then the K/V rows 0..a of the block move from
-// scratch into the request's cache pages at positions L..L+a, and finally
-// seq_len += a+1 and pending = g_a.  One CTA per request.
+// Greedy tokens from the argmax keys, accepted length a = first draft that
+// differs (16 if none); CTA (b, l) moves the K/V rows 0..a of layer l from
+// scratch into request b's cache pages at positions L..L+a; CTA (b, 0) also
+// writes the outputs and then seq_len = L + a + 1, pending = g_a.  All CTAs
+// read L from the step's validated copy, so the in-place update races with
+// nothing.
 __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) {
   __shared__ int g[kRows];
-  __shared__ int s_acc, s_valid, s_len;
+  __shared__ int page[kRows];
+  __shared__ int s_acc, s_valid;
   pdl_wait();
   pdl_launch_dependents();
-  const int b = blockIdx.x, t = threadIdx.x;
+  const int b = blockIdx.x, l = blockIdx.y, t = threadIdx.x;
+  if (t == 0 && l == 0) trace_start(a.trace);
+  const int L = a.ctx_len[b];
   if (t < 32) {
     int gt = -1, dt = -1;
     bool bad = false;
@@ -118,64 +152,64 @@ __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) 
       if (gt < 0 || gt >= a.vocab) bad = true;
       g[t] = gt;
     }
+    int pg = 0;
+    if (t < kRows) {
+      pg = a.page_table[b * a.pages_per_req + (L + t) / kPage];
+      page[t] = pg;
+    }
     if (t < kBlock) {
       dt = a.drafts[b * kBlock + t];
       if (dt < 0 || dt >= a.vocab) bad = true;
     }
     const unsigned mism = __ballot_sync(0xFFFFFFFFu, t < kBlock && dt != gt);
     const unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
+    const unsigned pbad = __ballot_sync(0xFFFFFFFFu, t < kRows && (pg < 0 || pg >= a.num_pages));
     if (t == 0) {
-      const int L = a.seq_lens[b];
-      const int p = a.pending[b];
-      const bool ok = badm == 0 && L >= 0 && L + kRows <= a.max_tokens && p >= 0 && p < a.vocab;
-      s_valid = ok ? 1 : 0;
-      s_acc = mism ? (__ffs(mism) - 1) : kBlock;
-      s_len = L;
+      const int acc0 = mism ? (__ffs(mism) - 1) : kBlock;
+      const bool pages_ok = (pbad & ((2u << acc0) - 1u)) == 0;  // only the committed rows need pages
+      if (!pages_ok && l == 0) atomicOr(a.status, VSD_DEV_BAD_PAGE);
+      s_valid = (badm == 0 && a.req_ok[b] && pages_ok) ? 1 : 0;
+      s_acc = acc0;
     }
   }
   __syncthreads();
-  const int acc = s_acc, L = s_len;
+  const int acc = s_acc;
   if (!s_valid) {
-    if (t < kRows) a.out_tokens[b * kRows + t] = -1;
-    if (t == 0) a.accepted[b] = -1;
-    __syncthreads();
-    if (t < kRows) a.keys[b * kRows + t] = 0;
+    if (l == 0) {
+      if (t < kRows) a.out_tokens[b * kRows + t] = -1;
+      if (t == 0) a.accepted[b] = -1;
+    }
     return;
   }
-  if (t < kRows) a.out_tokens[b * kRows + t] = t <= acc ? g[t] : -1;
-  if (t == 0) a.accepted[b] = acc;
-  // KV commit: rows 0..acc of every layer / K,V / head, 16-byte pieces
+  // KV commit of layer l: rows 0..acc, K and V, every head, 16-byte pieces
   const int pieces = a.hd / 8;
-  const int per_row = 2 * a.n_kv * pieces;
-  const int total = (acc + 1) * a.layers * per_row;
+  const int total = (acc + 1) * 2 * a.n_kv * pieces;
+#pragma unroll 4
   for (int idx = t; idx < total; idx += blockDim.x) {
     const int piece = idx % pieces;
     int rest = idx / pieces;
     const int h = rest % a.n_kv;
     rest /= a.n_kv;
     const int kv = rest & 1;
-    rest >>= 1;
-    const int j = rest % (acc + 1);
-    const int l = rest / (acc + 1);
+    const int j = rest >> 1;
     const int pos = L + j;
-    int page = a.page_table[b * a.pages_per_req + pos / kPage];
-    if (page < 0 || page >= a.num_pages) {
-      atomicOr(a.status, VSD_DEV_BAD_PAGE);
-      continue;
-    }
-    const __nv_bfloat16* src = (kv ? a.v_new : a.k_new) +
-                               ((((static_cast<size_t>(l) * a.batch_cap + b) * a.n_kv + h) * 32 + j) * a.hd) + piece * 8;
+    const __nv_bfloat16* src =
+        (kv ? a.v_new : a.k_new) + ((((static_cast<size_t>(l) * a.batch_cap + b) * a.n_kv + h) * 32 + j) * a.hd) +
+        piece * 8;
     __nv_bfloat16* dst = (kv ? a.v_pool : a.k_pool) +
-                         ((((static_cast<size_t>(l) * a.num_pages + page) * a.n_kv + h) * kPage + pos % kPage) * a.hd) +
+                         ((((static_cast<size_t>(l) * a.num_pages + page[j]) * a.n_kv + h) * kPage + pos % kPage) *
+                          a.hd) +
                          piece * 8;
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
   }
-  __syncthreads();
-  if (t == 0) {
-    a.seq_lens[b] = L + acc + 1;
-    a.pending[b] = g[acc];
+  if (l == 0) {
+    if (t < kRows) a.out_tokens[b * kRows + t] = t <= acc ? g[t] : -1;
+    if (t == 0) {
+      a.accepted[b] = acc;
+      a.seq_lens[b] = L + acc + 1;
+      a.pending[b] = g[acc];
+    }
   }
-  if (t < kRows) a.keys[b * kRows + t] = 0;
 }
 
 // Argmax keys of given float32 logits (component entry point): one CTA per row.
@@ -230,16 +264,6 @@ __global__ void scatter_q_kernel(const __nv_bfloat16* q, int B, int n_q, int n_k
     const int j = r % kRows;
     const int b = static_cast<int>(r / kRows);
     tile[((static_cast<size_t>(b) * n_kv + hh / group) * 128 + j * group + hh % group) * hd + d] = q[i];
-  }
-}
-
-__global__ void clamp_ctx_kernel(const int* seq_lens, int B, int max_tokens, int* ctx_len, int* status) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b < B) {
-    const int L = seq_lens[b];
-    const bool ok = L >= 0 && L + kRows <= max_tokens;
-    if (!ok) atomicOr(status, VSD_DEV_BAD_SEQLEN);
-    ctx_len[b] = ok ? L : 0;
   }
 }
 

@@ -15,9 +15,11 @@
 
 namespace vsd {
 
-// A device-side wait gives up after this many nanoseconds, records
-// VSD_DEV_TIMEOUT and lets the kernel wind down instead of hanging.
-constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// A device-side wait gives up after this many SM clock cycles (about 1 s at
+// the GB300's 2 GHz), records VSD_DEV_TIMEOUT and lets the kernel wind down
+// instead of hanging.  The SM-local cycle counter is used because reading
+// %globaltimer is slow enough to pace a spin loop.
+constexpr long long kWaitLimitCycles = 2000ll * 1000ll * 1000ll;
 
 constexpr int kRows = 17;    // rows per request: pending token + 16 drafts
 constexpr int kBlock = 16;   // drafted tokens per request
@@ -31,6 +33,43 @@ __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+__device__ __forceinline__ long long cycles() { return clock64(); }
+
+// ------------------------------------------------------------------ tracing
+// Optional per-CTA phase stamps (off when buf == nullptr): a plain store of
+// the SM cycle counter into the fixed slot [launch id][CTA][tag] -- no
+// atomics and no slow timer reads, so recording barely perturbs the kernel.
+// trace_start also stores %globaltimer (ns, common to all SMs) in the last
+// tag slot so that CTAs can be aligned with each other.
+constexpr int kTraceCtas = 1024, kTraceTags = 64;
+struct Trace {
+  unsigned long long* buf;
+  int max_launches;
+  int id;  // launch sequence number within the step
+};
+__device__ __forceinline__ unsigned long long* trace_slot(const Trace& t, int tag) {
+  if (t.buf == nullptr || t.id >= t.max_launches) return nullptr;
+  const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  if (cta >= static_cast<unsigned>(kTraceCtas) || tag >= kTraceTags) return nullptr;
+  return t.buf + (static_cast<size_t>(t.id) * kTraceCtas + cta) * kTraceTags + tag;
+}
+__device__ __forceinline__ void trace_point(const Trace& t, int tag) {
+  if (unsigned long long* p = trace_slot(t, tag)) *p = static_cast<unsigned long long>(clock64());
+}
+__device__ __forceinline__ void trace_start(const Trace& t) {
+  if (unsigned long long* p = trace_slot(t, 0)) {
+    p[kTraceTags - 1] = globaltimer();
+    p[0] = static_cast<unsigned long long>(clock64());
+  }
+}
+// Closing stamp: clock64 at `tag` and %globaltimer in the second-to-last
+// slot, which gives the SM clock rate over the CTA's lifetime.
+__device__ __forceinline__ void trace_end(const Trace& t, int tag) {
+  if (unsigned long long* p = trace_slot(t, tag)) {
+    *p = static_cast<unsigned long long>(clock64());
+    p[kTraceTags - 2 - tag] = globaltimer();
+  }
 }
 
 // ------------------------------------------------------------------ mbarrier
@@ -47,10 +86,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Non-suspending probe of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
@@ -61,21 +101,101 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete.  Returns false if
 // the CTA-wide abort flag is raised or the time limit runs out (then the
 // abort flag is raised and VSD_DEV_TIMEOUT is recorded in *status).
+// Bounded wait for the phase of `parity` to complete.  Polls with the
+// non-suspending test_wait (a suspended try_wait was seen to miss wake-ups
+// from TMA and MMA completions by microseconds); `sleep_ns` > 0 backs off
+// between probes, for long waits whose polling would otherwise take shared
+// memory and issue slots from the warps doing the work.  Gives up (sets the
+// abort flag and VSD_DEV_TIMEOUT) after kWaitLimitCycles or when another
+// thread of the CTA has given up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
+                                          int* status, uint32_t sleep_ns = 0) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = cycles();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 32; ++i) {
+      if (sleep_ns) __nanosleep(sleep_ns);
+      if (mbar_test_wait(bar, parity)) return true;
+    }
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (cycles() - t0 > kWaitLimitCycles) {
       *abort_flag = 1;
       if (status) atomicOr(status, VSD_DEV_TIMEOUT);
       return false;
     }
   }
+}
+
+// ------------------------------------------------------------------ clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  int* status) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  const long long t0 = cycles();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_test_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (cycles() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1;
+      if (status) atomicOr(status, VSD_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// All threads of all CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ TMA
