@@ -259,6 +259,36 @@ vsd_status vsd_block_attention(const vsd_model* m, vsd_kv* kv, int32_t layer, in
                                const uint16_t* k_new_dev, const uint16_t* v_new_dev,
                                uint16_t* out_dev, vsd_stream stream);
 
+/* vsd_block_attention without any device allocation (no counterpart in the
+ * method's description; an addition for callers that cannot allocate).
+ * Some callers must not call cudaMalloc once they are running: a serving
+ * process whose device memory is handed out up front by another allocator,
+ * or code that runs where allocation is forbidden or would synchronise the
+ * device.  This entry point takes the same arguments and computes the same
+ * result as vsd_block_attention, but its scratch (query tiles, the block's
+ * staged K/V rows, split partials and their counters) lives in one static
+ * device array of 16 MiB that every device loading this library holds from
+ * load until the process exits; the cache's own step workspace is not
+ * touched.  It calls no allocating routine.
+ *   - Limit: B * n_kv tiles of 128 x head_dim query rows plus the split
+ *     partials must fit in 16 MiB (the call coarsens the context split until
+ *     the partials fit); beyond that it returns VSD_ERR_UNSUPPORTED and
+ *     names the bytes it needed.
+ *   - The array is shared by all calls on a device and keeps the last
+ *     call's contents; each call clears what must start at zero (split
+ *     counters, padding rows of the staged block).  Calls whose work
+ *     overlaps on the GPU (other streams, other threads) race on it: order
+ *     them on one stream.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, no allocation); make that first call before
+ *     any stream capture.
+ * Device-side errors (bad page numbers) go to the cache's status word, as
+ * for vsd_block_attention. */
+vsd_status vsd_block_attention_static(const vsd_model* m, vsd_kv* kv, int32_t layer, int32_t batch,
+                                      const int32_t* seq_lens_dev, const uint16_t* q_dev,
+                                      const uint16_t* k_new_dev, const uint16_t* v_new_dev,
+                                      uint16_t* out_dev, vsd_stream stream);
+
 /* The accept-and-commit tail of the step driven by given float32 logits
  * [B*17, vocab] and block K/V rows k_new_dev / v_new_dev BF16
  * [layers, B, 17, n_kv, hd]: per-row argmax, prefix accept, outputs, KV

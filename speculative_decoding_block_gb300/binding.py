@@ -25,7 +25,8 @@ EXPORTS = [
     "vsd_model_create", "vsd_model_destroy", "vsd_kv_create", "vsd_kv_destroy",
     "vsd_kv_pages_per_req", "vsd_kv_num_pages", "vsd_kv_set_page_table", "vsd_kv_write",
     "vsd_kv_read", "vsd_get_device_status", "vsd_verify_step", "vsd_verify_step_debug",
-    "vsd_linear", "vsd_block_attention", "vsd_accept_commit", "vsd_verify_step_profiled",
+    "vsd_linear", "vsd_block_attention", "vsd_block_attention_static", "vsd_accept_commit",
+    "vsd_verify_step_profiled",
     "vsd_trace_enable", "vsd_trace_read",
 ]
 KERNEL_KINDS = ["embed", "qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm",
@@ -92,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "vsd_trace_enable": ([p, c_int], c_int),
             "vsd_trace_read": ([p, p, c_int, ctypes.POINTER(c_int), p], c_int),
             "vsd_block_attention": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
+            "vsd_block_attention_static": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
             "vsd_accept_commit": ([p, p, c_int, p, p, p, p, p, p, p, p, p], c_int),
         }
         for name, (args, res) in sig.items():
@@ -296,6 +298,18 @@ def vsd_block_attention(model: Model, kv: KV, layer: int, batch: int, seq_lens, 
                                      _dev(seq_lens, I32, "seq_lens", batch), _dev(q, B16, "q"),
                                      _dev(k_new, B16, "k_new"), _dev(v_new, B16, "v_new"),
                                      _dev(out, (torch.float16,), "out"), _stream(stream)))
+
+
+def vsd_block_attention_static(model: Model, kv: KV, layer: int, batch: int, seq_lens, q, k_new, v_new, out,
+                               stream=None) -> None:
+    """vsd_block_attention with its scratch in the library's static device
+    array: no device allocation on any call (for callers that cannot
+    allocate while running).  Calls on one device share that array, so they
+    must not overlap on the GPU."""
+    _check(lib().vsd_block_attention_static(model.handle, kv.handle, layer, batch,
+                                            _dev(seq_lens, I32, "seq_lens", batch), _dev(q, B16, "q"),
+                                            _dev(k_new, B16, "k_new"), _dev(v_new, B16, "v_new"),
+                                            _dev(out, (torch.float16,), "out"), _stream(stream)))
 
 
 def vsd_accept_commit(model: Model, kv: KV, batch: int, logits, k_new, v_new, seq_lens, pending, drafts,

@@ -924,6 +924,133 @@ vsd_status vsd_block_attention(const vsd_model* m, vsd_kv* kv, int32_t layer, in
   return VSD_OK;
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------ attention without allocation
+// Scratch memory of vsd_block_attention_static: one fixed array in every
+// device's copy of this library's module, present from load until the
+// process exits, shared by all calls on that device.  Host code must not
+// hand `g_static_scratch` itself to a kernel (on the host it names a
+// stand-in, not device memory); it uses the device address looked up below.
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(16) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device, looked up with
+// cudaGetSymbolAddress on the first call per device (no allocation).
+vsd_status static_scratch_address(void** out) {
+  int dev = -1;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return fail(VSD_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(VSD_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed: %s", cudaGetErrorString(e));
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return VSD_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+vsd_status vsd_block_attention_static(const vsd_model* m, vsd_kv* kv, int32_t layer, int32_t B,
+                                      const int32_t* seq_lens, const uint16_t* q, const uint16_t* k_new,
+                                      const uint16_t* v_new, uint16_t* out, vsd_stream stream) {
+  if (!m || !kv || !seq_lens || !q || !k_new || !v_new || !out) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (kv->m != m) return fail(VSD_ERR_ARG, "the cache was created for another model");
+  const vsd_model_config& c = m->cfg;
+  if (B < 1 || B > kv->max_batch || layer < 0 || layer >= c.layers) return fail(VSD_ERR_ARG, "batch or layer out of range");
+  if (B > kMaxReqs) return fail(VSD_ERR_UNSUPPORTED, "at most %d requests per call", kMaxReqs);
+  const int hd = c.head_dim;
+  const size_t pairs = static_cast<size_t>(B) * c.n_kv;
+  // scratch layout: split counters | q tiles | block K rows | block V rows | split partials (O, then m / l)
+  const size_t o_cnt = 0;
+  const size_t o_q = align256(o_cnt + pairs * sizeof(int));
+  const size_t o_k = align256(o_q + pairs * 128 * hd * 2);
+  const size_t o_v = align256(o_k + pairs * 32 * hd * 2);
+  const size_t o_part = align256(o_v + pairs * 32 * hd * 2);
+  const size_t per_split = align256(pairs * 128 * hd * 4) + align256(pairs * 128 * 2 * 4);
+  const int max_chunks = ceil_div(kv->max_tokens, 128) + 1;
+  // same work split as the step's attention, coarsened until the partials fit
+  int cps = std::max(1, ceil_div(B * c.n_kv * max_chunks, 2 * m->sms));
+  while (o_part + static_cast<size_t>(ceil_div(max_chunks, cps)) * per_split > kStaticScratchBytes && cps < max_chunks)
+    ++cps;
+  const int max_splits = ceil_div(max_chunks, cps);
+  const size_t need = o_part + static_cast<size_t>(max_splits) * per_split;
+  if (need > kStaticScratchBytes)
+    return fail(VSD_ERR_UNSUPPORTED,
+                "%d requests x %d KV heads x head_dim %d need %zu bytes of scratch; the static array holds %zu",
+                B, c.n_kv, hd, need, kStaticScratchBytes);
+  void* base_v = nullptr;
+  vsd_status s = static_scratch_address(&base_v);
+  if (s) return s;
+  uint8_t* base = static_cast<uint8_t*>(base_v);
+  auto* q_tile = reinterpret_cast<__nv_bfloat16*>(base + o_q);
+  auto* k_stage = reinterpret_cast<__nv_bfloat16*>(base + o_k);
+  auto* v_stage = reinterpret_cast<__nv_bfloat16*>(base + o_v);
+  float* part_o = reinterpret_cast<float*>(base + o_part);
+  float* part_ml = reinterpret_cast<float*>(base + o_part + static_cast<size_t>(max_splits) * align256(pairs * 128 * hd * 4));
+  // tensor maps: the layer's slice of the cache pool (so the kernel's layer index is 0), the staged tiles
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const size_t layer_rows = static_cast<size_t>(kv->num_pages) * c.n_kv * kPage;
+  CUtensorMap tm_q, tm_kc, tm_vc, tm_kn, tm_vn;
+  if ((s = tmap_2d(&tm_q, q_tile, BF16, hd, pairs * 128, 64, 128)) ||
+      (s = tmap_2d(&tm_kc, kv->k_pool + layer * layer_rows * hd, BF16, hd, layer_rows, 64, 16)) ||
+      (s = tmap_2d(&tm_vc, kv->v_pool + layer * layer_rows * hd, BF16, hd, layer_rows, 64, 16)) ||
+      (s = tmap_2d(&tm_kn, k_stage, BF16, hd, pairs * 32, 64, 32)) ||
+      (s = tmap_2d(&tm_vn, v_stage, BF16, hd, pairs * 32, 64, 32)))
+    return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // what must start at zero: the split counters, and the staged block rows
+  // 17..31 of every 32-row group (loaded with the block, masked by the kernel)
+  CK(cudaMemsetAsync(base + o_cnt, 0, pairs * sizeof(int), st));
+  CK(cudaMemsetAsync(base + o_k, 0, o_part - o_k, st));
+  scatter_q_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), B, c.n_q, c.n_kv, hd, q_tile);
+  scatter_block_rows_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k_new), 1, B, c.n_kv, hd, B,
+                                                 0, k_stage);
+  scatter_block_rows_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(v_new), 1, B, c.n_kv, hd, B,
+                                                 0, v_stage);
+  CK(cudaGetLastError());
+  AttnArgs a{};
+  a.batch = B;
+  a.batch_cap = B;
+  a.n_q = c.n_q;
+  a.n_kv = c.n_kv;
+  a.hd = hd;
+  a.group = c.n_q / c.n_kv;
+  a.rows_valid = kRows * a.group;
+  a.chunks_per_split = cps;
+  a.max_splits = max_splits;
+  a.layer = 0;
+  a.num_pages = kv->num_pages;
+  a.pages_per_req = kv->ppr;
+  a.max_tokens = kv->max_tokens;
+  a.seq_lens = seq_lens;
+  a.page_table = kv->page_table;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));
+  a.part_o = part_o;
+  a.part_ml = part_ml;
+  a.counters = reinterpret_cast<int*>(base + o_cnt);
+  a.out = reinterpret_cast<__half*>(out);
+  a.status = kv->status;
+  const int grid = std::min(static_cast<int>(pairs) * max_splits, m->sms);
+  const cudaError_t e = launch_attn(hd, tm_q, tm_kc, tm_vc, tm_kn, tm_vn, a, dim3(grid), st, false);
+  if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  return VSD_OK;
+}
+
 vsd_status vsd_accept_commit(const vsd_model* m, vsd_kv* kv, int32_t B, const float* logits, const uint16_t* k_new,
                              const uint16_t* v_new, int32_t* seq_lens, int32_t* pending, const int32_t* drafts,
                              int32_t* accepted, int32_t* out_tokens, vsd_stream stream) {
