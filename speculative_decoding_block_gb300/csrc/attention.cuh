@@ -34,12 +34,12 @@ struct AttnArgs {
   int batch;         // requests in this step
   int batch_cap;     // rows of the q tile / scratch buffers = max_batch
   int n_q, n_kv, hd, group, rows_valid;
-  int chunks_per_split, max_splits;
+  int chunks_per_split, max_splits;  // smallest split the host allows; capacity of the partials
   int layer, num_pages, pages_per_req, max_tokens;
   const int* seq_lens;     // [B] caller's committed lengths (validated here)
   const int* page_table;   // [max_batch][pages_per_req]
   float scale_log2;        // log2(e) / sqrt(hd)
-  float* part_o;           // [B][n_kv][max_splits][128][hd]
+  float* part_o;           // [B][n_kv][max_splits][2 halves][128][hd / 2] unnormalised partial O
   float* part_ml;          // [B][n_kv][max_splits][128][2]
   int* counters;           // [B][n_kv]
   __half* out;             // [B*17][n_q*hd]
@@ -97,8 +97,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   int* item_off = reinterpret_cast<int*>(p_s + 32768 + 256 + 4096);  // [B + 1] first item of each request
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cps = a.chunks_per_split;
-  auto splits_of = [&](int b) { return ((valid_len(a, b) + 127) / 128 + 1 + cps - 1) / cps; };
+  volatile int* cps_s = reinterpret_cast<volatile int*>(tmem_p + 4);
+  volatile int* sum_s = reinterpret_cast<volatile int*>(tmem_p + 5);
+  auto chunks_of = [&](int b) { return (valid_len(a, b) + 127) / 128 + 1; };
 
   if (threadIdx.x == 0) {
     trace_start(a.trace);
@@ -116,16 +117,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(ofull, 1);
     mbar_init(ofree, 256);
     *abort_flag = 0;
+    *sum_s = 0;
     fence_mbar_init();
-    // item list: request-major, then KV head, then split (seq_lens is the
-    // caller's input and does not change during the step)
-    int acc = 0;
-    for (int b = 0; b < a.batch; ++b) {
-      item_off[b] = acc;
-      acc += a.n_kv * splits_of(b);
-    }
-    item_off[a.batch] = acc;
-    *n_items = acc;
   }
   if (warp == 9) {
     tmem_alloc(tmem_p, 512);
@@ -134,8 +127,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Split size: the smallest number of chunks per split (at least the
+  // host's) whose items fit in one round of the grid, so that each CTA
+  // walks about one item.  seq_lens is the caller's input and does not
+  // change during the step, so every CTA derives the same split.
+  {
+    int mine = 0;
+    for (int b = threadIdx.x; b < a.batch; b += blockDim.x) mine += chunks_of(b);
+    if (mine) atomicAdd(const_cast<int*>(sum_s), mine);
+    __syncthreads();
+    const int total_chunks = *sum_s * a.n_kv;
+    int c = max(a.chunks_per_split, (total_chunks + gridDim.x - 1) / gridDim.x);
+    for (;; ++c) {  // ends: at c = the longest request's chunk count every request is one split
+      __syncthreads();
+      if (threadIdx.x == 0) *sum_s = 0;
+      __syncthreads();
+      int items = 0;
+      for (int b = threadIdx.x; b < a.batch; b += blockDim.x) items += (chunks_of(b) + c - 1) / c;
+      if (items) atomicAdd(const_cast<int*>(sum_s), items);
+      __syncthreads();
+      if (*sum_s * a.n_kv <= static_cast<int>(gridDim.x) || *sum_s == a.batch) break;
+    }
+    if (threadIdx.x == 0) {
+      *cps_s = c;
+      // item list: request-major, then KV head, then split
+      int acc = 0;
+      for (int b = 0; b < a.batch; ++b) {
+        item_off[b] = acc;
+        acc += a.n_kv * ((chunks_of(b) + c - 1) / c);
+      }
+      item_off[a.batch] = acc;
+      *n_items = acc;
+    }
+    __syncthreads();
+  }
   const uint32_t tmem = *tmem_p;
   const int total = *n_items;
+  const int cps = *cps_s;
+  auto splits_of = [&](int b) { return (chunks_of(b) + cps - 1) / cps; };
   pdl_launch_dependents();
   if (threadIdx.x == 0) trace_point(a.trace, 1);
 
@@ -163,8 +192,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   };
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ TMA producer (whole warp)
+    // Lanes 0..7 each fetch one 16-row page of a context chunk (page-table
+    // read and K/V copies in parallel); lane 0 arms the barriers and fetches
+    // the q tile and the block's own rows.
+    {
       const uint64_t pol = policy_evict_first();
       auto issue = [&](const Item& x, int i, int g) {  // chunk i of item x, global chunk number g
         const int st = g % NS;
@@ -172,21 +204,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint8_t* vs = ks + KVB;
         const int c = x.c_begin + i;
         if (c < x.n_ctx) {
-          mbar_expect_tx(&kvfull[st], 2u * 128u * HD * 2u);
-          for (int p = 0; p < 8; ++p) {
-            const int pi = min(c * 8 + p, a.pages_per_req - 1);
+          if (lane == 0) mbar_expect_tx(&kvfull[st], 2u * 128u * HD * 2u);
+          __syncwarp();
+          if (lane < 8) {
+            const int pi = min(c * 8 + lane, a.pages_per_req - 1);
             int page = a.page_table[x.b * a.pages_per_req + pi];
             if (page < 0 || page >= a.num_pages) {
               atomicOr(a.status, VSD_DEV_BAD_PAGE);
               page = 0;
             }
             const int row0 = ((a.layer * a.num_pages + page) * a.n_kv + x.h) * kPage;
+#pragma unroll
             for (int at = 0; at < NA; ++at) {
-              tma_load_2d_hint(ks + at * 16384 + p * 2048, &tm_kc, &kvfull[st], at * 64, row0, pol);
-              tma_load_2d_hint(vs + at * 16384 + p * 2048, &tm_vc, &kvfull[st], at * 64, row0, pol);
+              tma_load_2d_hint(ks + at * 16384 + lane * 2048, &tm_kc, &kvfull[st], at * 64, row0, pol);
+              tma_load_2d_hint(vs + at * 16384 + lane * 2048, &tm_vc, &kvfull[st], at * 64, row0, pol);
             }
           }
-        } else {
+        } else if (lane == 0) {
           mbar_expect_tx(&kvfull[st], 2u * 32u * HD * 2u);
           const int row0 = ((a.layer * a.batch_cap + x.b) * a.n_kv + x.h) * 32;
           for (int at = 0; at < NA; ++at) {
@@ -194,6 +228,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tma_load_2d(vs + at * 16384, &tm_vn, &kvfull[st], at * 64, row0);
           }
         }
+        __syncwarp();
       };
       // context pages of the first item: committed by earlier steps, safe before the dependency wait
       int pre = 0;
@@ -205,7 +240,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
       pdl_wait();  // q tiles and the block's K/V come from the QKV kernel
-      trace_point(a.trace, 2);
+      if (lane == 0) trace_point(a.trace, 2);
       int g = 0, ic = 0;
       bool ok = true;
       for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++ic) {
@@ -214,9 +249,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ok = false;
           break;
         }
-        mbar_expect_tx(qfull, QB);
-        for (int at = 0; at < NA; ++at)
-          tma_load_2d(q_s + at * 16384, &tm_q, qfull, at * 64, (x.b * a.n_kv + x.h) * 128);
+        if (lane == 0) {
+          mbar_expect_tx(qfull, QB);
+          for (int at = 0; at < NA; ++at)
+            tma_load_2d(q_s + at * 16384, &tm_q, qfull, at * 64, (x.b * a.n_kv + x.h) * 128);
+        }
         for (int i = 0; i < x.n; ++i, ++g) {
           if (g < pre) continue;  // fetched before the dependency wait
           const int st = g % NS;
@@ -327,15 +364,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int q = 0; q < 4; ++q)
           if (q * 16 < ncol) tmem_ld16(sa + q * 16, s + q * 16);
         tmem_ld_wait();
+        // visible keys of this row form a prefix [0, lim) of the thread's columns:
+        // block keys 0..j (causal), context keys below L, nothing for padding rows
+        int lim = ncol;
+        if (need_mask) lim = !row_ok ? 0 : min(ncol, blk ? jr + 1 - col0 : x.L - c * 128 - col0);
+        const float sl = a.scale_log2;
         float cm = -INFINITY;
 #pragma unroll
         for (int t = 0; t < 64; ++t) {
-          if (t < ncol) {
-            const int key = col0 + t;
-            const bool vis = !need_mask || (row_ok && (blk ? (key <= jr) : (c * 128 + key < x.L)));
-            s[t] = vis ? s[t] * a.scale_log2 : -INFINITY;
-            cm = fmaxf(cm, s[t]);
-          }
+          s[t] = t < lim ? s[t] * sl : -INFINITY;
+          cm = fmaxf(cm, s[t]);
         }
         float* xs = xstat + (g & 1) * 256;
         xs[hf * 128 + r] = cm;
@@ -411,12 +449,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         continue;
       }
-      const size_t base = (pair * a.max_splits) * 128;
-      float* po = a.part_o + ((base + x.split * 128 + r) * HD) + hf * HH;
+      // split partial: unnormalised O as [2 halves][128 rows][HD/2] fp32 per
+      // (pair, split), staged through shared memory (the P tile is free once
+      // the last PV product is done) so that the global writes are coalesced
+      constexpr int Q4 = HH / 4;                 // float4 per half row
+      constexpr int NF4 = 128 * Q4;              // float4 per half tile
+      float4* stage = reinterpret_cast<float4*>(p_s);
+      auto slot = [&](int row, int d4) { return row * Q4 + (d4 ^ (row & 7)); };  // bank-spread
+      const size_t split_idx = pair * a.max_splits + x.split;
+      float4* po = reinterpret_cast<float4*>(a.part_o + split_idx * 128 * HD);
+      for (int hh = 0; hh < 2; ++hh) {
+        if (hf == hh) {
 #pragma unroll
-      for (int d = 0; d < HH; d += 4)
-        __stcg(reinterpret_cast<float4*>(po + d), make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]));
-      if (hf == 0) __stcg(reinterpret_cast<float2*>(a.part_ml + (base + x.split * 128 + r) * 2), make_float2(m, lt));
+          for (int d4 = 0; d4 < Q4; ++d4)
+            stage[slot(r, d4)] = make_float4(o[4 * d4], o[4 * d4 + 1], o[4 * d4 + 2], o[4 * d4 + 3]);
+        }
+        named_bar_sync(1, 256);
+#pragma unroll
+        for (int j = threadIdx.x; j < NF4; j += 256) __stcg(po + hh * NF4 + j, stage[slot(j / Q4, j % Q4)]);
+        named_bar_sync(1, 256);
+      }
+      if (hf == 0) __stcg(reinterpret_cast<float2*>(a.part_ml) + split_idx * 128 + r, make_float2(m, lt));
       __threadfence();
       named_bar_sync(1, 256);
       if (threadIdx.x == 0) *last_flag = (atomicAdd(&a.counters[pair], 1) == x.n_splits - 1) ? 1 : 0;
@@ -425,56 +478,73 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       named_bar_sync(1, 256);  // everyone read the flag before the next item may set it
       if (!last) continue;
       __threadfence();
-      float mm = -INFINITY;
-#pragma unroll 8
-      for (int sp = 0; sp < x.n_splits; ++sp) mm = fmaxf(mm, __ldcg(a.part_ml + (base + sp * 128 + r) * 2));
-      if (mm == -INFINITY) mm = 0.0f;
-      float accv[HH];
+      // merge of the pair's splits (split order fixed: deterministic).
+      // Per row: mm = max of the split maxima, 1 / sum of the rescaled sums.
+      const size_t first = pair * a.max_splits;
+      const float2* pml = reinterpret_cast<const float2*>(a.part_ml) + first * 128;
+      float* row_mm = xstat;         // [128]
+      float* row_inv = xstat + 128;  // [128]
+      if (hf == 0) {
+        float mm = -INFINITY;
+        for (int sp = 0; sp < x.n_splits; ++sp) mm = fmaxf(mm, __ldcg(pml + sp * 128 + r).x);
+        if (mm == -INFINITY) mm = 0.0f;
+        float ls = 0.0f;
+        for (int sp = 0; sp < x.n_splits; ++sp) {
+          const float2 ml = __ldcg(pml + sp * 128 + r);
+          ls += ml.y * ex2(ml.x - mm);
+        }
+        row_mm[r] = mm;
+        row_inv[r] = ls > 0.0f ? 1.0f / ls : 0.0f;
+      }
+      named_bar_sync(1, 256);
+      // Per half: every thread owns NF4 / 256 float4 of the half tile
+      // (coalesced across the warp) and sums them over the splits.
+      constexpr int PER = NF4 / 256;
+      const float4* pbase = reinterpret_cast<const float4*>(a.part_o + first * 128 * HD);
+      for (int hh = 0; hh < 2; ++hh) {
+        float4 acc4[PER];
+        int rows[PER];
+        float mrow[PER];
 #pragma unroll
-      for (int d = 0; d < HH; ++d) accv[d] = 0.0f;
-      float ls = 0.0f;
-      constexpr int U = HD == 64 ? 2 : 1;  // splits whose loads are in flight together
-      for (int s0 = 0; s0 < x.n_splits; s0 += U) {
-        float4 xv[U][HH / 4];
-        float wgt[U];
+        for (int k = 0; k < PER; ++k) {
+          acc4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          rows[k] = (threadIdx.x + 256 * k) / Q4;
+          mrow[k] = row_mm[rows[k]];
+        }
+        for (int sp = 0; sp < x.n_splits; ++sp) {
+          float4 xv[PER];
+          float mv[PER];
+          const float4* ps = pbase + static_cast<size_t>(sp) * 2 * NF4 + hh * NF4;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int sp = s0 + u;
-          wgt[u] = 0.0f;
-          if (sp < x.n_splits) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (base + sp * 128 + r) * 2));
-            wgt[u] = ex2(ml.x - mm);
-            ls += ml.y * wgt[u];
-            const float* ps = a.part_o + (base + sp * 128 + r) * HD + hf * HH;
+          for (int k = 0; k < PER; ++k) {
+            xv[k] = __ldcg(ps + threadIdx.x + 256 * k);
+            mv[k] = __ldcg(pml + sp * 128 + rows[k]).x;
+          }
 #pragma unroll
-            for (int d = 0; d < HH / 4; ++d) xv[u][d] = __ldcg(reinterpret_cast<const float4*>(ps) + d);
+          for (int k = 0; k < PER; ++k) {
+            const float w = ex2(mv[k] - mrow[k]);
+            acc4[k].x += xv[k].x * w;
+            acc4[k].y += xv[k].y * w;
+            acc4[k].z += xv[k].z * w;
+            acc4[k].w += xv[k].w * w;
           }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (s0 + u < x.n_splits) {
-#pragma unroll
-            for (int d = 0; d < HH / 4; ++d) {
-              accv[4 * d] += xv[u][d].x * wgt[u];
-              accv[4 * d + 1] += xv[u][d].y * wgt[u];
-              accv[4 * d + 2] += xv[u][d].z * wgt[u];
-              accv[4 * d + 3] += xv[u][d].w * wgt[u];
-            }
+        for (int k = 0; k < PER; ++k) {
+          const int row = rows[k];
+          if (row < a.rows_valid) {
+            const int d = hh * HH + ((threadIdx.x + 256 * k) % Q4) * 4;
+            const float inv = row_inv[row];
+            __half* o_dst = a.out + (static_cast<size_t>(x.b) * kRows + row / a.group) * (a.n_q * HD) +
+                            (x.h * a.group + row % a.group) * HD + d;
+            uint2 u;
+            u.x = f32x2_to_f16x2(acc4[k].x * inv, acc4[k].y * inv);
+            u.y = f32x2_to_f16x2(acc4[k].z * inv, acc4[k].w * inv);
+            *reinterpret_cast<uint2*>(o_dst) = u;
           }
         }
       }
-      if (row_ok) {
-        const float inv = 1.0f / ls;
-#pragma unroll
-        for (int d = 0; d < HH; d += 8) {
-          uint4 u;
-          u.x = f32x2_to_f16x2(accv[d] * inv, accv[d + 1] * inv);
-          u.y = f32x2_to_f16x2(accv[d + 2] * inv, accv[d + 3] * inv);
-          u.z = f32x2_to_f16x2(accv[d + 4] * inv, accv[d + 5] * inv);
-          u.w = f32x2_to_f16x2(accv[d + 6] * inv, accv[d + 7] * inv);
-          *reinterpret_cast<uint4*>(dst + d) = u;
-        }
-      }
+      named_bar_sync(1, 256);  // row statistics read by all before the next item reuses them
       if (threadIdx.x == 0) a.counters[pair] = 0;
       if (threadIdx.x == 0 && ic == 0) trace_point(a.trace, 7);
     }
