@@ -119,6 +119,7 @@ struct vsd_model {
   std::vector<Linear> qkv, o, gu, down;
   float2* rope = nullptr;
   int sms = 1;
+  int max_clusters[4] = {1, 1, 1, 1};  // resident GEMM clusters of 1, 2, 4, 8 CTAs
 };
 
 struct vsd_kv {
@@ -287,30 +288,35 @@ struct Plan {
 };
 
 // Chooses token tiles (MMA N <= 256) and the k split (cluster of 1..8 CTAs)
-// with a small latency model: every CTA pays a fixed start-up and drain
-// cost, streams its weight k tiles plus the matching activation tiles, and
-// a split pays for the cluster reduction.  Token tiles re-read the same
-// weight tile (from L2), which costs far less than a reduction.
-Plan plan_gemm(const Linear& w, int M, bool no_split, int sms) {
-  const double wbytes = w.fmt == VSD_FMT_BF16 ? 16384.0 : (w.fmt == VSD_FMT_FP8 ? 8192.0 : 4608.0);
-  const double fixed_us = 3.0, bytes_per_us = 120e3, reduce_us = 1.5, reduce_per_cta_us = 0.3;
+// with a latency model fitted to traced steps (microseconds): each CTA pays
+// a fixed launch / start-up / drain cost, about 0.6 us per k tile (weight
+// expansion and MMA pipeline; 0.5 for 16-bit weights), and its share of the
+// epilogue's 16-column groups; a split adds the cluster reduction, which
+// grows with the columns exchanged.  Clusters beyond what can be resident
+// at once run in further waves.
+Plan plan_gemm(const vsd_model* m, const Linear& w, int M, int epi) {
+  const bool no_split = epi == EPI_ARGMAX;
+  const double t_tile = w.fmt == VSD_FMT_BF16 ? 0.5 : 0.6;
+  const double t_group = epi == EPI_QKV ? 1.5 : (epi == EPI_ARGMAX || epi == EPI_STORE ? 0.3 : 0.5);
   Plan best{};
   double best_cost = 1e30;
   const int max_t = std::max(1, ceil_div(M, 16));
   for (int t = ceil_div(M, 256); t <= max_t; ++t) {
     const int n_tok = std::max(16, round_up(ceil_div(M, t), 16));
     if (n_tok > 256 || (t > 1 && round_up(ceil_div(M, t - 1), 16) == n_tok)) continue;
-    for (int want : {1, 2, 4, 8}) {
+    for (int li = 0; li < 4; ++li) {
+      const int want = 1 << li;
       if (no_split && want > 1) break;
       if (want > w.k_tiles) break;
       const int kps = ceil_div(w.k_tiles, want);
       const int cs = ceil_div(w.k_tiles, kps);  // every rank gets at least one k tile
+      const int csi = cs <= 1 ? 0 : (cs <= 2 ? 1 : (cs <= 4 ? 2 : 3));
       const int items = w.n_tiles * t;
-      const int ctas = items * cs;
-      const int waves = ceil_div(ctas, sms);
-      const double per_cta = kps * (wbytes + n_tok * 128.0);
-      double cost = fixed_us + waves * per_cta / bytes_per_us;
-      if (cs > 1) cost += reduce_us + reduce_per_cta_us * cs;
+      const int resident = std::max(1, std::min(m->max_clusters[csi], m->sms / cs));
+      const int waves = ceil_div(items, resident);
+      const int groups = ceil_div(ceil_div(n_tok, 16), cs);
+      double cost = waves * (6.0 + kps * t_tile + groups * t_group);
+      if (cs > 1) cost += 2.5 + 0.035 * n_tok + 0.1 * cs;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best.tok_tiles = t;
@@ -320,8 +326,9 @@ Plan plan_gemm(const Linear& w, int M, bool no_split, int sms) {
       }
     }
   }
+  const int csi = best.cs <= 1 ? 0 : (best.cs <= 2 ? 1 : (best.cs <= 4 ? 2 : 3));
   const int items = w.n_tiles * best.tok_tiles;
-  const int clusters = std::max(1, std::min(items, sms / best.cs));
+  const int clusters = std::max(1, std::min({items, m->sms / best.cs, std::max(1, m->max_clusters[csi])}));
   best.grid = clusters * best.cs;
   // ring depths: the weight ring holds the CTA's whole weight stream when it fits
   const int ki = ceil_div(items, clusters) * best.kps;  // k iterations of one CTA
@@ -354,7 +361,7 @@ void set_norm_input(GemmArgs& a, const vsd_kv* kv) {
 
 vsd_status run_gemm(const vsd_model* m, const Linear& w, int epi, const CUtensorMap* tm_acts, int M, GemmArgs a,
                     int* status, cudaStream_t st, Trace trace = Trace{}) {
-  const Plan p = plan_gemm(w, M, epi == EPI_ARGMAX, m->sms);
+  const Plan p = plan_gemm(m, w, M, epi);
   a.w_tiles = static_cast<const uint8_t*>(w.data);
   a.row_scale = w.row_scale;
   a.n_rows = w.n_rows;
@@ -510,6 +517,7 @@ vsd_status vsd_model_create(const vsd_model_config* cfg, const vsd_weights* w, v
   vsd_model* m = new vsd_model();
   m->cfg = c;
   m->sms = sm_count();
+  for (int i = 0; i < 4; ++i) m->max_clusters[i] = gemm_max_clusters(1 << i);
   auto cleanup = [&](vsd_status e) {
     vsd_model_destroy(m);
     return e;
@@ -892,6 +900,7 @@ vsd_status vsd_linear(const vsd_weight* w, int32_t n, int32_t k, const uint16_t*
   }
   vsd_model mm;
   mm.sms = sm_count();
+  for (int i = 0; i < 4; ++i) mm.max_clusters[i] = gemm_max_clusters(1 << i);
   GemmArgs a{};
   a.out_f32 = y;
   a.ld_out = n;

@@ -51,6 +51,31 @@ static cudaError_t launch_fmt(int epi, const CUtensorMap& tm_act, const CUtensor
   return cudaErrorInvalidValue;
 }
 
+int gemm_max_clusters(int cs) {
+  if (cs <= 1) {
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+  }
+  auto k = gemm_kernel<W_FP8, EPI_RESID>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) != cudaSuccess) return 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs * 64);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = 232448;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = cs;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n < 1) return 1;
+  return n;
+}
+
 cudaError_t launch_gemm(int wf, int epi, const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
                         int grid, cudaStream_t st, bool pdl) {
   switch (wf) {

@@ -42,6 +42,8 @@
 //   ARGMAX : per token, max over vocab rows -> 64-bit argmax key (atomicMax)
 #pragma once
 
+#include <type_traits>
+
 #include "vsd_common.cuh"
 
 namespace vsd {
@@ -145,12 +147,14 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int wf, int n_tok, int rd, 
 }
 
 // control block: barriers (1 KB), argmax transpose tile 128 x 17 fp32 (9 KB),
-// running argmax keys (8 KB), sums of squares (4 KB), row scales (1 KB)
-constexpr uint32_t kCtrlT = 1024, kCtrlBest = kCtrlT + 9216, kCtrlSq = kCtrlBest + 8192, kCtrlRs = kCtrlSq + 4096;
+// running argmax keys (8 KB), sums of squares (4 KB), per-token row scales
+// (1 KB), per-token positions (1 KB, QKV)
+constexpr uint32_t kCtrlT = 1024, kCtrlBest = kCtrlT + 9216, kCtrlSq = kCtrlBest + 8192, kCtrlRs = kCtrlSq + 4096,
+                   kCtrlPos = kCtrlRs + 1024;
 constexpr int kBestCap = 1024;  // token columns whose running argmax fits in shared memory
 constexpr int kMaxRd = 32, kMaxDb = 16, kMaxDa = 4;
 constexpr uint32_t kSleepLongWaitNs = 128;  // back-off of the epilogue's wait for the accumulator
-__host__ __device__ inline uint32_t gemm_ctrl_bytes() { return kCtrlRs + 1024u; }
+__host__ __device__ inline uint32_t gemm_ctrl_bytes() { return kCtrlPos + 1024u; }
 __host__ __device__ inline uint32_t gemm_smem_bytes(int wf, int n_tok, int rd, int da, int db, int cs) {
   return 1024u + gemm_smem_layout(wf, n_tok, rd, da, db, cs).ctrl_off + gemm_ctrl_bytes();
 }
@@ -180,12 +184,12 @@ struct ItemIter {
   }
 };
 
-template <int WF>
+template <int WF, int NT>
 __device__ __forceinline__ void expand_weights(uint8_t* a_tile, const uint8_t* raw, int t) {
-  // 1024 chunks of 8 f16 (16 bytes); thread t handles chunks t + 128 i.
+  // 1024 chunks of 8 f16 (16 bytes); thread t of NT handles chunks t + NT i.
 #pragma unroll 4
-  for (int i = 0; i < 8; ++i) {
-    const int q = t + 128 * i;
+  for (int i = 0; i < 1024 / NT; ++i) {
+    const int q = t + NT * i;
     const int r = q >> 3, c = q & 7;
     uint4 o;
     if constexpr (WF == W_FP8) {
@@ -214,30 +218,67 @@ __device__ __forceinline__ void expand_weights(uint8_t* a_tile, const uint8_t* r
   }
 }
 
-__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
+__device__ __forceinline__ float shfl_xor_any(float v, int m) { return __shfl_xor_sync(0xFFFFFFFFu, v, m); }
+__device__ __forceinline__ unsigned long long shfl_xor_any(unsigned long long v, int m) {
   const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), m);
   const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), m);
   return (static_cast<unsigned long long>(hi) << 32) | lo;
 }
 
+// Reduce-scatter of 16 per-lane values over the 32 lanes of a warp: after
+// four halving exchanges (lane bits 4..1) and one final pair exchange, lane L
+// holds the combination over all 32 lanes of element
+// T(L) = 8*b4 + 4*b3 + 2*b2 + b1 (lanes L and L^1 hold the same element).
+// 16 shuffles instead of 16 x 5 for sixteen butterfly reductions.
+template <typename T, typename Op>
+__device__ __forceinline__ T warp_reduce_scatter16(const T (&x)[16], int lane, Op op) {
+  T y[8], z[4], w[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const T keep = b4 ? x[k + 8] : x[k], send = b4 ? x[k] : x[k + 8];
+    y[k] = op(keep, shfl_xor_any(send, 16));
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const T keep = b3 ? y[k + 4] : y[k], send = b3 ? y[k] : y[k + 4];
+    z[k] = op(keep, shfl_xor_any(send, 8));
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const T keep = b2 ? z[k + 2] : z[k], send = b2 ? z[k] : z[k + 2];
+    w[k] = op(keep, shfl_xor_any(send, 4));
+  }
+  const T keep = b1 ? w[1] : w[0], send = b1 ? w[0] : w[1];
+  const T u = op(keep, shfl_xor_any(send, 2));
+  return op(u, shfl_xor_any(u, 1));
+}
+__device__ __forceinline__ int scatter16_element(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
 // Epilogue of one 16-column group: v[i] is the fp32 result of packed row
-// `row` (0..127 inside the tile) for token column c0 + i; rs holds the
-// per-column row scales of the item (1 when the input is not normalised).
+// `row` (0..127 inside the tile) for token column c0 + i; `scale` is the
+// weight row's scale, rs the per-column token scales (1 when the input is not
+// normalised), pos the per-column cache positions (QKV).  Every variant
+// computes all sixteen values first and stores with predicates, so the
+// sixteen columns overlap instead of running one branch at a time.
 template <int EPI, int WF>
 __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int tt, int row, int c0, float* v,
-                                              const float* rs, float* tbuf, float* sq_red, int warp_e, int lane) {
+                                              float scale, const float* rs, const int* pos,
+                                              unsigned long long* wbest, float* sq_red, int warp_e, int lane) {
   const int prow = tile * kTileN + row;  // packed row
   const bool row_ok = prow < a.n_rows;
-  float scale = 1.0f;
-  if constexpr (WF != W_BF16) scale = row_ok ? a.row_scale[prow] : 0.0f;
   const int tok0 = tt * a.n_tok + c0;
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = v[i] * scale * rs[c0 + i];
 
   if constexpr (EPI == EPI_STORE) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int tok = tok0 + i;
-      if (row_ok && tok < a.m_tokens)
-        a.out_f32[static_cast<size_t>(tok) * a.ld_out + prow] = v[i] * scale * rs[c0 + i];
+      if (row_ok && tok < a.m_tokens) a.out_f32[static_cast<size_t>(tok) * a.ld_out + prow] = x[i];
     }
   } else if constexpr (EPI == EPI_RESID) {
     float old[16];  // every load issued before the first store
@@ -246,103 +287,95 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
       const int tok = tok0 + i;
       old[i] = (row_ok && tok < a.m_tokens) ? a.out_f32[static_cast<size_t>(tok) * a.ld_out + prow] : 0.0f;
     }
+    float sq[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int tok = tok0 + i;
-      float sq = 0.0f;
-      if (row_ok && tok < a.m_tokens) {
+      const bool ok = row_ok && tok < a.m_tokens;
+      const float r = old[i] + x[i];  // residual GEMM inputs are not normalised: rs == 1
+      sq[i] = ok ? r * r : 0.0f;
+      if (ok) {
         const size_t o = static_cast<size_t>(tok) * a.ld_out + prow;
-        const float x = old[i] + v[i] * scale;
-        a.out_f32[o] = x;
-        a.x16_out[o] = __float2half_rn(x);
-        if (a.hidden_out) a.hidden_out[o] = x;
-        sq = x * x;
+        a.out_f32[o] = r;
+        a.x16_out[o] = __float2half_rn(r);
+        if (a.hidden_out) a.hidden_out[o] = r;
       }
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, m);
-      if (lane == 0) sq_red[warp_e * 256 + c0 + i] = sq;
     }
+    const float tot = warp_reduce_scatter16(sq, lane, [](float p, float q) { return p + q; });
+    if ((lane & 1) == 0) sq_red[warp_e * 256 + c0 + scatter16_element(lane)] = tot;
   } else if constexpr (EPI == EPI_QKV) {
     const int hd = a.head_dim, half = hd >> 1;
-    const int head = prow / hd, r = prow % hd;
+    const int head = prow / hd, r = prow - head * hd;
     const int d = (r & 1) ? (r >> 1) + half : (r >> 1);
     const int fi = r >> 1;  // rotation frequency index
     const int group = a.n_q / a.n_kv;
     const bool rotate = head < a.n_q + a.n_kv;
-    float2 cs[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {  // all table loads first
-      const int tok = min(tok0 + i, a.m_tokens - 1);
-      const int b = tok / kRows, j = tok % kRows;
-      cs[i] = rotate ? a.rope[static_cast<size_t>(a.ctx_len[b] + j) * half + fi] : make_float2(1.0f, 0.0f);
-    }
+    const bool is_q = head < a.n_q;
+    float y[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float x = v[i] * scale * rs[c0 + i];
-      const float xp = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+      const float2 c = rotate ? a.rope[static_cast<size_t>(pos[c0 + i]) * half + fi] : make_float2(1.0f, 0.0f);
+      const float xp = __shfl_xor_sync(0xFFFFFFFFu, x[i], 1);
+      y[i] = (r & 1) ? (x[i] * c.x + xp * c.y) : (x[i] * c.x - xp * c.y);
+    }
+    // destination: q tile [B][n_kv][128][hd] (row j * group + hq) or block K / V [B][n_kv][32][hd]
+    __nv_bfloat16* dst;
+    int kvh, rstride, roff;
+    if (is_q) {
+      kvh = head / group;
+      dst = a.q_tile;
+      rstride = 128;
+      roff = head - kvh * group;  // + j * group
+    } else {
+      kvh = rotate ? head - a.n_q : head - a.n_q - a.n_kv;
+      dst = rotate ? a.k_new : a.v_new;
+      rstride = 32;
+      roff = 0;
+    }
+    const int jmul = is_q ? group : 1;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
       const int tok = tok0 + i;
-      if (!row_ok || tok >= a.m_tokens) continue;
-      const int b = tok / kRows, j = tok % kRows;
-      if (rotate) {
-        const float y = (r & 1) ? (x * cs[i].x + xp * cs[i].y) : (x * cs[i].x - xp * cs[i].y);
-        if (head < a.n_q) {
-          const int kvh = head / group, hq = head % group;
-          a.q_tile[((static_cast<size_t>(b) * a.n_kv + kvh) * 128 + j * group + hq) * hd + d] =
-              __float2bfloat16_rn(y);
-        } else {
-          const int kvh = head - a.n_q;
-          a.k_new[((static_cast<size_t>(b) * a.n_kv + kvh) * 32 + j) * hd + d] = __float2bfloat16_rn(y);
-        }
-      } else {
-        const int kvh = head - a.n_q - a.n_kv;
-        a.v_new[((static_cast<size_t>(b) * a.n_kv + kvh) * 32 + j) * hd + d] = __float2bfloat16_rn(x);
+      if (row_ok && tok < a.m_tokens) {
+        const int b = tok / kRows, j = tok - b * kRows;
+        dst[((static_cast<size_t>(b) * a.n_kv + kvh) * rstride + j * jmul + roff) * hd + d] =
+            __float2bfloat16_rn(rotate ? y[i] : x[i]);
       }
     }
   } else if constexpr (EPI == EPI_SILU) {
+    // rows 2f / 2f+1 of the tile are gate / up of feature f: the pair of
+    // lanes splits the sixteen columns (even lane 0..7, odd lane 8..15)
     const int feat = tile * 64 + (row >> 1);
+    const bool odd = row & 1;
+    float g[8], u[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float x = v[i] * scale * rs[c0 + i];
-      const float up = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
-      const int tok = tok0 + i;
-      if ((row & 1) == 0 && feat < a.ffn && tok < a.m_tokens) {
-        const float g = x / (1.0f + expf(-x));
-        a.act_out[static_cast<size_t>(tok) * a.ffn + feat] = __float2half_rn(g * up);
-      }
+    for (int k = 0; k < 8; ++k) {
+      const float send = odd ? x[k] : x[k + 8];  // partner's half
+      const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+      const float mine = odd ? x[k + 8] : x[k];
+      g[k] = odd ? recv : mine;   // gate lives on the even lane
+      u[k] = odd ? mine : recv;   // up on the odd lane
+    }
+    const int cbase = odd ? 8 : 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int tok = tok0 + cbase + k;
+      const float sg = __fdividef(g[k], 1.0f + __expf(-g[k]));
+      if (feat < a.ffn && tok < a.m_tokens)
+        a.act_out[static_cast<size_t>(tok) * a.ffn + feat] = __float2half_rn(sg * u[k]);
     }
   } else if constexpr (EPI == EPI_ARGMAX) {
-    // scaled logits -> transpose tile tbuf[row][16]; argmax_group reduces the columns
+    unsigned long long key[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int tok = tok0 + i;
-      const float x = v[i] * rs[c0 + i];
-      if (a.logits && row_ok && tok < a.m_tokens) a.logits[static_cast<size_t>(tok) * a.n_rows + prow] = x;
-      tbuf[row * 17 + i] = row_ok ? x : -INFINITY;
+      if (a.logits && row_ok && tok < a.m_tokens) a.logits[static_cast<size_t>(tok) * a.n_rows + prow] = x[i];
+      key[i] = row_ok ? argmax_key(x[i], static_cast<uint32_t>(prow)) : 0ull;
     }
+    const unsigned long long best =
+        warp_reduce_scatter16(key, lane, [](unsigned long long p, unsigned long long q) { return p > q ? p : q; });
+    if ((lane & 1) == 0) wbest[warp_e * 16 + scatter16_element(lane)] = best;
   }
-}
-
-// Max over the 128 rows of each of the 16 columns of tbuf, 8 threads per
-// column (et = epilogue thread 0..127); the winner of column cc is folded
-// into best[cc] (largest logit, lowest vocabulary row among equals).
-__device__ __forceinline__ void argmax_group(const float* tbuf, unsigned long long* best, int tile, int et) {
-  const int cc = et >> 3, part = et & 7;
-  unsigned long long key = 0ull;
-#pragma unroll 4
-  for (int k = 0; k < 16; ++k) {
-    const int r = part * 16 + k;
-    const float x = tbuf[r * 17 + cc];
-    if (x != -INFINITY) {
-      const unsigned long long kk = argmax_key(x, static_cast<uint32_t>(tile * kTileN + r));
-      key = kk > key ? kk : key;
-    }
-  }
-#pragma unroll
-  for (int m = 4; m >= 1; m >>= 1) {
-    const unsigned long long o = shfl_xor_u64(key, m);
-    key = o > key ? o : key;
-  }
-  if (part == 0 && key > best[cc]) best[cc] = key;
 }
 
 template <int WF, int EPI>
@@ -366,10 +399,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* rfree = rfull + 1;           // peers finished reading this CTA's R buffer
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(rfree + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_p + 1);
-  float* tbuf = reinterpret_cast<float*>(smem + L.ctrl_off + kCtrlT);
+  // ARGMAX: per-warp column maxima of a 16-column group, two parities [2][4 warps][16]
+  unsigned long long* wbest = reinterpret_cast<unsigned long long*>(smem + L.ctrl_off + kCtrlT);
   unsigned long long* best = reinterpret_cast<unsigned long long*>(smem + L.ctrl_off + kCtrlBest);
   float* sq_red = reinterpret_cast<float*>(smem + L.ctrl_off + kCtrlSq);
   float* rs = reinterpret_cast<float*>(smem + L.ctrl_off + kCtrlRs);
+  int* pos_s = reinterpret_cast<int*>(smem + L.ctrl_off + kCtrlPos);
   float* R = reinterpret_cast<float*>(smem + L.r_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -378,6 +413,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int cluster = cs > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
   const int n_clusters = cs > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
   const int total = a.n_tiles * a.tok_tiles;
+  // One item per CTA (the usual case for the FP8 / NVFP4 layer GEMMs): the
+  // epilogue warps have nothing to do during the k loop, so warps 0-7 share
+  // the weight expansion, and warps 0-3 also compute the per-token scales.
+  const bool wide = WF != W_BF16 && total <= n_clusters;
+  const bool has_item = cluster < total;
+  const int conv_n = wide ? 256 : 128;
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(2 * a.n_tok)) tmem_cols <<= 1;
   if (threadIdx.x == 0) trace_start(a.trace);
@@ -385,14 +426,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < RD; ++i) {
       mbar_init(&wfull[i], 1);
-      mbar_init(&wempty[i], WF == W_BF16 ? 1 : 128);
+      mbar_init(&wempty[i], WF == W_BF16 ? 1 : conv_n);
     }
     for (int i = 0; i < DB; ++i) {
       mbar_init(&bfull[i], 1);
       mbar_init(&bempty[i], 1);
     }
     for (int i = 0; i < DA; ++i) {
-      mbar_init(&conv[i], 128);
+      mbar_init(&conv[i], conv_n);
       mbar_init(&cempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -415,6 +456,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_base_p;
   pdl_launch_dependents();
   if (threadIdx.x == 0) trace_point(a.trace, 1);
+
+  // per-token scale of the normalised input rows (and, for QKV, the cache
+  // position of each token, whose RoPE row is pulled into L2 early); reads
+  // what the previous kernels wrote, so only after the grid dependency wait
+  auto token_scales = [&](int item, int t0, int nt) {
+    const int tt = item % a.tok_tiles;
+    for (int c = t0; c < a.n_tok; c += nt) {
+      float r = 1.0f;
+      const int tok = tt * a.n_tok + c;
+      if (a.ssq_in && tok < a.m_tokens) {
+        float ss = 0.0f;
+#pragma unroll 8
+        for (int k = 0; k < a.n_ssq; ++k) ss += a.ssq_in[static_cast<size_t>(k) * a.ssq_ld + tok];
+        r = 1.0f / sqrtf(ss * a.inv_hidden + a.eps);
+      }
+      rs[c] = r;
+      if constexpr (EPI == EPI_QKV) {
+        int p = 0;
+        if (tok < a.m_tokens) {
+          p = a.ctx_len[tok / kRows] + tok % kRows;
+          const char* row_p = reinterpret_cast<const char*>(a.rope + static_cast<size_t>(p) * (a.head_dim >> 1));
+          for (int off = 0; off < (a.head_dim >> 1) * 8; off += 128) prefetch_l2(row_p + off);
+        }
+        pos_s[c] = p;
+      }
+    }
+  };
+  // weight expansion of the CTA's k tiles by NT threads (t = 0..NT-1); in the
+  // wide mode warps 0-3 compute the token scales once the first expanded
+  // tiles are ready, and publish them on named barrier 3
+  auto expand_all = [&](auto nt_const, int t) {
+    constexpr int NT = decltype(nt_const)::value;
+    bool scales_done = !(wide && has_item && warp < 4);
+    ItemIter it(&a, cluster, n_clusters, total, rank);
+    for (int i = 0; !it.done(); it.next(), ++i) {
+      if (!scales_done && i == DA) {
+        pdl_wait();
+        token_scales(cluster, t, 128);
+        named_bar_arrive(3, 256);
+        scales_done = true;
+      }
+      const int r = i % RD, c = i % DA;
+      if (!mbar_wait(&wfull[r], (i / RD) & 1, abort_flag, a.status)) break;
+      if (i >= DA && !mbar_wait(&cempty[c], ((i / DA) - 1) & 1, abort_flag, a.status)) break;
+      if (t == 0 && i == 0) trace_point(a.trace, 3);
+      expand_weights<WF, NT>(smem + L.a_off + c * 16384, smem + L.w_off + r * L.w_bytes, t);
+      fence_proxy_async();
+      mbar_arrive(&conv[c]);
+      mbar_arrive(&wempty[r]);
+    }
+    if (!scales_done) {
+      pdl_wait();
+      token_scales(cluster, t, 128);
+      named_bar_arrive(3, 256);
+    }
+  };
 
   if (warp == 8) {
     // ---------------------------------------------------------- TMA producer (weights + activations)
@@ -486,18 +583,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp < 4) {
     // ---------------------------------------------------------- weight expansion (FP8 / NVFP4)
     if constexpr (WF != W_BF16) {
-      const int t = threadIdx.x;
-      ItemIter it(&a, cluster, n_clusters, total, rank);
-      for (int i = 0; !it.done(); it.next(), ++i) {
-        const int r = i % RD, c = i % DA;
-        if (!mbar_wait(&wfull[r], (i / RD) & 1, abort_flag, a.status)) break;
-        if (i >= DA && !mbar_wait(&cempty[c], ((i / DA) - 1) & 1, abort_flag, a.status)) break;
-        if (t == 0 && i == 0) trace_point(a.trace, 3);
-        expand_weights<WF>(smem + L.a_off + c * 16384, smem + L.w_off + r * L.w_bytes, t);
-        fence_proxy_async();
-        mbar_arrive(&conv[c]);
-        mbar_arrive(&wempty[r]);
-      }
+      if (wide)
+        expand_all(std::integral_constant<int, 256>{}, static_cast<int>(threadIdx.x));
+      else
+        expand_all(std::integral_constant<int, 128>{}, static_cast<int>(threadIdx.x));
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issue
@@ -555,23 +644,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool keep_best = a.tok_tiles * a.n_tok <= kBestCap;
     if constexpr (EPI == EPI_ARGMAX)
       for (int c = et; c < kBestCap; c += 128) best[c] = 0ull;
-    pdl_wait();  // the row scales read what the previous kernels wrote
+    if constexpr (WF != W_BF16)
+      if (wide) expand_all(std::integral_constant<int, 256>{}, static_cast<int>(threadIdx.x));
+    // weight row scales are constant: the first item's is read before the grid dependency wait
+    auto row_scale_of = [&](int item) -> float {
+      if constexpr (WF == W_BF16) {
+        return 1.0f;
+      } else {
+        const int prow = (item / a.tok_tiles) * kTileN + row;
+        return prow < a.n_rows ? a.row_scale[prow] : 0.0f;
+      }
+    };
+    float scale_next = (alive && cluster < total) ? row_scale_of(cluster) : 0.0f;
+    pdl_wait();  // the token scales and positions read what the previous kernels wrote
     named_bar_sync(1, 128);
     int acc = 0;
     for (int item = cluster; alive && item < total; item += n_clusters, ++acc) {
       const int ab = acc & 1;
       const int tile = item / a.tok_tiles, tt = item % a.tok_tiles;
-      // per-token scale of the normalised input rows, while the MMAs run
-      for (int c = et; c < a.n_tok; c += 128) {
-        float r = 1.0f;
-        const int tok = tt * a.n_tok + c;
-        if (a.ssq_in && tok < a.m_tokens) {
-          float ss = 0.0f;
-#pragma unroll 8
-          for (int k = 0; k < a.n_ssq; ++k) ss += a.ssq_in[static_cast<size_t>(k) * a.ssq_ld + tok];
-          r = 1.0f / sqrtf(ss * a.inv_hidden + a.eps);
-        }
-        rs[c] = r;
+      const float scale = scale_next;
+      if (item + n_clusters < total) scale_next = row_scale_of(item + n_clusters);
+      // per-token scales: computed here while the MMAs run, or (wide mode) by warps 0-3
+      if (wide) {
+        named_bar_sync(3, 256);
+      } else {
+        token_scales(item, et, 128);
       }
       named_bar_sync(1, 128);
       if (et == 0 && acc == 0) trace_point(a.trace, 8);
@@ -629,22 +726,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (et == 0 && acc == 0 && g == rank) trace_point(a.trace, 12);
-        epilogue_cols<EPI, WF>(a, tile, tt, row, c0, v, rs, tbuf, sq_red, we, lane);
+        unsigned long long* wb = wbest + (g & 1) * 64;
+        epilogue_cols<EPI, WF>(a, tile, tt, row, c0, v, scale, rs, pos_s, wb, sq_red, we, lane);
         if (et == 0 && acc == 0 && g == rank) trace_point(a.trace, 14);
         if constexpr (EPI == EPI_ARGMAX) {
           named_bar_sync(1, 128);
-          const int col = tt * a.n_tok + c0;
-          if (keep_best) {
-            argmax_group(tbuf, best + col, tile, et);
-          } else {  // too many tokens for the running best: one atomic per column and tile
-            argmax_group(tbuf, best, tile, et);
-            if ((et & 7) == 0) {
-              const int tok = col + (et >> 3);
-              if (tok < a.m_tokens && best[et >> 3]) atomicMax(a.keys + tok, best[et >> 3]);
-              best[et >> 3] = 0ull;
+          if (et < 16) {  // fold the four warps' maxima of column c0 + et (the other parity is written next)
+            unsigned long long k = wb[et];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) k = wb[w * 16 + et] > k ? wb[w * 16 + et] : k;
+            const int col = tt * a.n_tok + c0 + et;
+            if (keep_best) {
+              if (k > best[col]) best[col] = k;
+            } else if (col < a.m_tokens && k) {
+              atomicMax(a.keys + col, k);
             }
           }
-          named_bar_sync(1, 128);
           if (et == 0 && acc == 0 && g == rank) trace_point(a.trace, 15);
         }
       }
@@ -669,6 +766,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       named_bar_sync(1, 128);
       if (et == 0 && acc == 0) trace_point(a.trace, 10);
     }
+    // the peers read this CTA's R buffer until they arrive on rfree: wait for
+    // that before the CTA may exit (its shared memory must stay valid)
+    if (cs > 1 && acc > 0) mbar_wait_cluster(rfree, (acc - 1) & 1, abort_flag, a.status);
     if constexpr (EPI == EPI_ARGMAX) {
       if (keep_best)
         for (int c = et; c < a.tok_tiles * a.n_tok; c += 128)
@@ -678,7 +778,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (cs > 1) cluster_sync();  // no CTA leaves while a peer may still read its R buffer
   if (threadIdx.x == 0) trace_end(a.trace, 11);
   if (warp == 9) {
     __syncwarp();

@@ -11,6 +11,8 @@ namespace vsd {
 // dependent launch when pdl is set.
 // Launches gemm_kernel<wf, epi> as a.cs-CTA clusters; `grid` is a multiple of
 // a.cs and is clamped to the clusters that can be resident at once.
+// Clusters of `cs` GEMM CTAs (full shared memory each) that can be resident at once.
+int gemm_max_clusters(int cs);
 cudaError_t launch_gemm(int wf, int epi, const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
                         int grid, cudaStream_t st, bool pdl);
 cudaError_t launch_attn(int hd, const CUtensorMap& tm_q, const CUtensorMap& tm_kc, const CUtensorMap& tm_vc,
