@@ -294,7 +294,7 @@ struct Plan {
 // epilogue's 16-column groups; a split adds the cluster reduction, which
 // grows with the columns exchanged.  Clusters beyond what can be resident
 // at once run in further waves.
-Plan plan_gemm(const vsd_model* m, const Linear& w, int M, int epi) {
+Plan plan_gemm(const vsd_model* m, const Linear& w, int M, int epi, bool lo) {
   const bool no_split = epi == EPI_ARGMAX;
   const double t_tile = w.fmt == VSD_FMT_BF16 ? 0.5 : 0.6;
   const double t_group = epi == EPI_QKV ? 1.5 : (epi == EPI_ARGMAX || epi == EPI_STORE ? 0.3 : 0.5);
@@ -332,7 +332,7 @@ Plan plan_gemm(const vsd_model* m, const Linear& w, int M, int epi) {
   best.grid = clusters * best.cs;
   // ring depths: the weight ring holds the CTA's whole weight stream when it fits
   const int ki = ceil_div(items, clusters) * best.kps;  // k iterations of one CTA
-  const int wslot = static_cast<int>(weight_slot_bytes(w.fmt)), bslot = best.n_tok * 128;
+  const int wslot = static_cast<int>(weight_slot_bytes(w.fmt)), bslot = best.n_tok * 128 * (lo ? 2 : 1);
   const int r_bytes = best.cs > 1 ? round_up(best.n_tok * 132 * 4, 1024) : 0;
   const int budget = 232448 - 1024 - static_cast<int>(gemm_ctrl_bytes()) - r_bytes - 1024;
   if (w.fmt == VSD_FMT_BF16) {
@@ -361,7 +361,8 @@ void set_norm_input(GemmArgs& a, const vsd_kv* kv) {
 
 vsd_status run_gemm(const vsd_model* m, const Linear& w, int epi, const CUtensorMap* tm_acts, int M, GemmArgs a,
                     int* status, cudaStream_t st, Trace trace = Trace{}) {
-  const Plan p = plan_gemm(m, w, M, epi);
+  const bool lo = a.act_lo_rows > 0;
+  const Plan p = plan_gemm(m, w, M, epi, lo);
   a.w_tiles = static_cast<const uint8_t*>(w.data);
   a.row_scale = w.row_scale;
   a.n_rows = w.n_rows;
@@ -377,14 +378,16 @@ vsd_status run_gemm(const vsd_model* m, const Linear& w, int epi, const CUtensor
   a.db = p.db;
   a.status = status;
   a.trace = trace;
-  if (gemm_smem_bytes(w.fmt, p.n_tok, p.rd, p.da, p.db, p.cs) > 232448)
+  if (gemm_smem_bytes(w.fmt, p.n_tok, p.rd, p.da, p.db, p.cs, lo) > 232448)
     return fail(VSD_ERR_UNSUPPORTED, "GEMM tile does not fit in shared memory");
   const cudaError_t e = launch_gemm(w.fmt, epi, tm_acts[p.n_tok / 16 - 1], w.tm, a, p.grid, st, use_pdl(st));
   if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
   return VSD_OK;
 }
 
-vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cudaStream_t st) {
+// lo: the q tiles carry lo halves and the output gets its lo copy (the step);
+// otherwise hi only (the single-layer entry point, whose inputs are BF16)
+vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cudaStream_t st, bool lo) {
   const vsd_model* m = kv->m;
   const vsd_model_config& c = m->cfg;
   if (B > kMaxReqs) return fail(VSD_ERR_UNSUPPORTED, "at most %d requests per step", kMaxReqs);
@@ -416,6 +419,10 @@ vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cuda
   a.part_ml = kv->attn_ml;
   a.counters = kv->attn_counters;
   a.out = kv->act_o;
+  if (lo) {
+    a.out_lo = static_cast<size_t>(kv->m_alloc) * c.n_q * c.head_dim;
+    a.q_lo_rows = kv->max_batch * c.n_kv * 128;
+  }
   a.status = kv->status;
   a.trace = next_trace(kv);
   const cudaError_t e = launch_attn(c.head_dim, kv->tm_q, kv->tm_kc, kv->tm_vc, kv->tm_kn, kv->tm_vn, a,
@@ -616,10 +623,12 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
   }
   const int M = kRows * max_batch;
   kv->m_alloc = round_up(M, 16);
-  if ((s = dalloc(&kv->x, static_cast<size_t>(kv->m_alloc) * H)) || (s = dalloc(&kv->u, static_cast<size_t>(kv->m_alloc) * H)) ||
-      (s = dalloc(&kv->act_o, static_cast<size_t>(kv->m_alloc) * nqd)) ||
-      (s = dalloc(&kv->act_a, static_cast<size_t>(kv->m_alloc) * F)) ||
-      (s = dalloc(&kv->q_tile, static_cast<size_t>(max_batch) * c.n_kv * 128 * hd)) ||
+  // GEMM inputs and the attention's q tiles are hi / lo pairs: [2][rows][cols]
+  if ((s = dalloc(&kv->x, static_cast<size_t>(kv->m_alloc) * H)) ||
+      (s = dalloc(&kv->u, static_cast<size_t>(2) * kv->m_alloc * H)) ||
+      (s = dalloc(&kv->act_o, static_cast<size_t>(2) * kv->m_alloc * nqd)) ||
+      (s = dalloc(&kv->act_a, static_cast<size_t>(2) * kv->m_alloc * F)) ||
+      (s = dalloc(&kv->q_tile, static_cast<size_t>(2) * max_batch * c.n_kv * 128 * hd)) ||
       (s = dalloc(&kv->k_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
       (s = dalloc(&kv->v_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
       (s = dalloc(&kv->keys, M)) || (s = dalloc(&kv->ctx_len, max_batch)) || (s = dalloc(&kv->req_ok, max_batch)) ||
@@ -634,12 +643,12 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
   const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16, BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   for (int j = 0; j < kActBoxes; ++j) {
     const uint32_t rows = 16u * (j + 1);
-    if ((s = tmap_2d(&kv->tm_u[j], kv->u, F16, H, kv->m_alloc, 64, rows)) ||
-        (s = tmap_2d(&kv->tm_o[j], kv->act_o, F16, nqd, kv->m_alloc, 64, rows)) ||
-        (s = tmap_2d(&kv->tm_a[j], kv->act_a, F16, F, kv->m_alloc, 64, rows)))
+    if ((s = tmap_2d(&kv->tm_u[j], kv->u, F16, H, 2 * kv->m_alloc, 64, rows)) ||
+        (s = tmap_2d(&kv->tm_o[j], kv->act_o, F16, nqd, 2 * kv->m_alloc, 64, rows)) ||
+        (s = tmap_2d(&kv->tm_a[j], kv->act_a, F16, F, 2 * kv->m_alloc, 64, rows)))
       return cleanup(s);
   }
-  if ((s = tmap_2d(&kv->tm_q, kv->q_tile, BF16, hd, static_cast<uint64_t>(max_batch) * c.n_kv * 128, 64, 128)) ||
+  if ((s = tmap_2d(&kv->tm_q, kv->q_tile, BF16, hd, static_cast<uint64_t>(2) * max_batch * c.n_kv * 128, 64, 128)) ||
       (s = tmap_2d(&kv->tm_kc, kv->k_pool, BF16, hd, pool / hd, 64, 16)) ||
       (s = tmap_2d(&kv->tm_vc, kv->v_pool, BF16, hd, pool / hd, 64, 16)) ||
       (s = tmap_2d(&kv->tm_kn, kv->k_new, BF16, hd, static_cast<uint64_t>(c.layers) * max_batch * c.n_kv * 32, 64, 32)) ||
@@ -791,6 +800,7 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     e.max_tokens = kv->max_tokens;
     e.x = kv->x;
     e.x16 = kv->u;
+    e.x16_lo = static_cast<size_t>(kv->m_alloc) * H;
     e.ssq = kv->ssq;
     e.ssq_ld = kv->m_alloc;
     e.ctx_len = kv->ctx_len;
@@ -806,6 +816,8 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     GemmArgs a{};
     set_norm_input(a, kv);
     a.q_tile = kv->q_tile;
+    a.act_lo_rows = kv->m_alloc;
+    a.out_lo = static_cast<size_t>(kv->max_batch) * c.n_kv * 128 * c.head_dim;
     a.k_new = kv->k_new + l * layer_scratch;
     a.v_new = kv->v_new + l * layer_scratch;
     a.ctx_len = kv->ctx_len;
@@ -814,17 +826,21 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     a.n_kv = c.n_kv;
     a.head_dim = c.head_dim;
     TIMED(VSD_K_QKV, if ((s = run_gemm(m, m->qkv[l], EPI_QKV, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
-    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, seq_lens, st))) return s);
+    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, seq_lens, st, true))) return s);
     GemmArgs r{};
     r.out_f32 = kv->x;
     r.ld_out = H;
     r.x16_out = kv->u;
+    r.act_lo_rows = kv->m_alloc;
+    r.out_lo = static_cast<size_t>(kv->m_alloc) * H;
     r.ssq_out = kv->ssq;
     r.ssq_ld = kv->m_alloc;
     TIMED(VSD_K_O_PROJ, if ((s = run_gemm(m, m->o[l], EPI_RESID, kv->tm_o, M, r, kv->status, st, next_trace(kv)))) return s);
     GemmArgs g{};
     set_norm_input(g, kv);
     g.act_out = kv->act_a;
+    g.act_lo_rows = kv->m_alloc;
+    g.out_lo = static_cast<size_t>(kv->m_alloc) * c.ffn;
     g.ffn = c.ffn;
     TIMED(VSD_K_GATE_UP, if ((s = run_gemm(m, m->gu[l], EPI_SILU, kv->tm_u, M, g, kv->status, st, next_trace(kv)))) return s);
     r.hidden_out = hidden ? hidden + static_cast<size_t>(l + 1) * M * H : nullptr;
@@ -835,6 +851,7 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     set_norm_input(a, kv);
     a.keys = kv->keys;
     a.logits = logits;
+    a.act_lo_rows = kv->m_alloc;
     TIMED(VSD_K_LM_HEAD, if ((s = run_gemm(m, m->lm, EPI_ARGMAX, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
   }
   CommitArgs ca = commit_args(kv, drafts, seq_lens, pending, accepted, out_tokens);
@@ -926,7 +943,7 @@ vsd_status vsd_block_attention(const vsd_model* m, vsd_kv* kv, int32_t layer, in
   scatter_block_rows_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(v_new), 1, B, c.n_kv,
                                                  c.head_dim, kv->max_batch, layer, kv->v_new);
   CK(cudaGetLastError());
-  vsd_status s = run_attention(kv, layer, B, seq_lens, st);
+  vsd_status s = run_attention(kv, layer, B, seq_lens, st, false);
   if (s) return s;
   CK(cudaMemcpyAsync(out, kv->act_o, static_cast<size_t>(B) * kRows * c.n_q * c.head_dim * 2,
                      cudaMemcpyDeviceToDevice, st));

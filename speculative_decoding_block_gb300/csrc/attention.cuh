@@ -42,21 +42,37 @@ struct AttnArgs {
   float* part_o;           // [B][n_kv][max_splits][2 halves][128][hd / 2] unnormalised partial O
   float* part_ml;          // [B][n_kv][max_splits][128][2]
   int* counters;           // [B][n_kv]
-  __half* out;             // [B*17][n_q*hd]
+  __half* out;             // [B*17][n_q*hd] f16 (hi)
+  size_t out_lo;           // elements from a hi output value to its lo copy, f16(o - hi) (0: hi only)
+  int q_lo_rows;           // rows of the q-tile map from a hi tile to its lo tile (0: no lo tile)
   int* status;
   Trace trace;
 };
 
-__host__ __device__ inline uint32_t attn_stages(int hd) { return hd == 64 ? 3u : 2u; }
-// q tile, K/V stages, P tile, then barriers (256 B), row statistics (4 KB) and item offsets
+// K and V of a chunk travel in separate rings of this depth (a K slot frees
+// when its S product is done, a V slot when its PV product is done)
+__host__ __device__ inline uint32_t attn_stages(int hd) { return hd == 64 ? 3u : 1u; }
+// q tile (hi, lo), K/V stages, P tile (hi, lo), then barriers (256 B), row
+// statistics (4 KB) and item offsets
 __host__ __device__ inline uint32_t attn_smem_bytes(int hd) {
   const uint32_t q = 128u * hd * 2u, kv = 2u * 128u * hd * 2u;
-  return 1024u + q + attn_stages(hd) * kv + 32768u + 256u + 4096u + 4u * (kMaxReqs + 1);
+  return 1024u + 2u * q + attn_stages(hd) * kv + 2u * 32768u + 256u + 4096u + 4u * (kMaxReqs + 1);
 }
 
 __device__ __forceinline__ int valid_len(const AttnArgs& a, int b) {
   const int L = a.seq_lens[b];
   return (L >= 0 && L + kRows <= a.max_tokens) ? L : 0;
+}
+
+// Eight values v[i] * scale as f16 hi words and f16 lo words (v*scale - hi), packed in pairs.
+__device__ __forceinline__ void f16_pairs8(const float* v, float scale, uint32_t* hw, uint32_t* lw) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float y0 = v[2 * e] * scale, y1 = v[2 * e + 1] * scale;
+    hw[e] = f32x2_to_f16x2(y0, y1);
+    const __half2 h2 = *reinterpret_cast<const __half2*>(&hw[e]);
+    lw[e] = f32x2_to_f16x2(y0 - __low2float(h2), y1 - __high2float(h2));
+  }
 }
 
 __device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation (ex2(-inf) = 0)
@@ -70,19 +86,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                 const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kn,
                 const __grid_constant__ CUtensorMap tm_vn, const AttnArgs a) {
-  constexpr int NS = HD == 64 ? 3 : 2;
+  constexpr int NS = HD == 64 ? 3 : 1;
   constexpr int NA = HD / 64;   // 64-wide swizzle atoms along head_dim
   constexpr int HH = HD / 2;    // output columns per softmax thread
   constexpr uint32_t QB = 128u * HD * 2u, KVB = 128u * HD * 2u;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = smem;
-  uint8_t* kv_s = smem + QB;                 // stage st: K at st*2*KVB, V at +KVB
-  uint8_t* p_s = kv_s + NS * 2 * KVB;        // 2 atoms of [128 rows x 64 keys]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(p_s + 32768);
-  uint64_t* kvfull = bars;
-  uint64_t* kvempty = bars + NS;
-  uint64_t* qfull = bars + 2 * NS;
+  // Q and P enter the MMAs as BF16 pairs hi = bf16(x), lo = bf16(x - hi)
+  // (two MMAs each), so that scores and weights carry about 16 significant bits
+  uint8_t* q_s = smem;                       // hi tile, lo tile at + QB
+  uint8_t* kv_s = smem + 2 * QB;             // K slot st at st*KVB, V slot st at (NS + st)*KVB
+  uint8_t* p_s = kv_s + NS * 2 * KVB;        // hi: 2 atoms of [128 rows x 64 keys]; lo at + 32768
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p_s + 2 * 32768);
+  uint64_t* kfull = bars;
+  uint64_t* kempty = bars + NS;
+  uint64_t* vfull = bars + 2 * NS;
+  uint64_t* vempty = bars + 3 * NS;
+  uint64_t* qfull = bars + 4 * NS;
   uint64_t* qempty = qfull + 1;  // the item's S products are done with the q tile
   uint64_t* sfull = qempty + 1;  // [2]
   uint64_t* sfree = sfull + 2;   // [2]
@@ -93,8 +113,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_p + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_p + 2);
   volatile int* n_items = reinterpret_cast<volatile int*>(tmem_p + 3);
-  float* xstat = reinterpret_cast<float*>(p_s + 32768 + 256);  // [2 parity][2 halves][128] maxima; then [2][2][128] sums
-  int* item_off = reinterpret_cast<int*>(p_s + 32768 + 256 + 4096);  // [B + 1] first item of each request
+  float* xstat = reinterpret_cast<float*>(p_s + 2 * 32768 + 256);  // [2 parity][2 halves][128] maxima; then [2][2][128] sums
+  int* item_off = reinterpret_cast<int*>(p_s + 2 * 32768 + 256 + 4096);  // [B + 1] first item of each request
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* cps_s = reinterpret_cast<volatile int*>(tmem_p + 4);
@@ -104,8 +124,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (threadIdx.x == 0) {
     trace_start(a.trace);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&kvfull[s], 1);
-      mbar_init(&kvempty[s], 1);
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
     }
     mbar_init(qfull, 1);
     mbar_init(qempty, 1);
@@ -198,44 +220,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // the q tile and the block's own rows.
     {
       const uint64_t pol = policy_evict_first();
-      auto issue = [&](const Item& x, int i, int g) {  // chunk i of item x, global chunk number g
+      // chunk i of item x, global chunk number g: K then V, each once its slot is free
+      auto issue = [&](const Item& x, int i, int g) -> bool {
         const int st = g % NS;
-        uint8_t* ks = kv_s + st * 2 * KVB;
-        uint8_t* vs = ks + KVB;
+        uint8_t* ks = kv_s + st * KVB;
+        uint8_t* vs = kv_s + (NS + st) * KVB;
         const int c = x.c_begin + i;
-        if (c < x.n_ctx) {
-          if (lane == 0) mbar_expect_tx(&kvfull[st], 2u * 128u * HD * 2u);
-          __syncwarp();
-          if (lane < 8) {
-            const int pi = min(c * 8 + lane, a.pages_per_req - 1);
-            int page = a.page_table[x.b * a.pages_per_req + pi];
-            if (page < 0 || page >= a.num_pages) {
-              atomicOr(a.status, VSD_DEV_BAD_PAGE);
-              page = 0;
-            }
-            const int row0 = ((a.layer * a.num_pages + page) * a.n_kv + x.h) * kPage;
-#pragma unroll
-            for (int at = 0; at < NA; ++at) {
-              tma_load_2d_hint(ks + at * 16384 + lane * 2048, &tm_kc, &kvfull[st], at * 64, row0, pol);
-              tma_load_2d_hint(vs + at * 16384 + lane * 2048, &tm_vc, &kvfull[st], at * 64, row0, pol);
-            }
+        const bool ctx = c < x.n_ctx;
+        int row0 = 0;
+        if (ctx && lane < 8) {  // lane p: page p of the chunk
+          const int pi = min(c * 8 + lane, a.pages_per_req - 1);
+          int page = a.page_table[x.b * a.pages_per_req + pi];
+          if (page < 0 || page >= a.num_pages) {
+            atomicOr(a.status, VSD_DEV_BAD_PAGE);
+            page = 0;
           }
-        } else if (lane == 0) {
-          mbar_expect_tx(&kvfull[st], 2u * 32u * HD * 2u);
-          const int row0 = ((a.layer * a.batch_cap + x.b) * a.n_kv + x.h) * 32;
-          for (int at = 0; at < NA; ++at) {
-            tma_load_2d(ks + at * 16384, &tm_kn, &kvfull[st], at * 64, row0);
-            tma_load_2d(vs + at * 16384, &tm_vn, &kvfull[st], at * 64, row0);
-          }
+          row0 = ((a.layer * a.num_pages + page) * a.n_kv + x.h) * kPage;
+        } else if (!ctx) {
+          row0 = ((a.layer * a.batch_cap + x.b) * a.n_kv + x.h) * 32;
         }
-        __syncwarp();
+        const uint32_t bytes = (ctx ? 128u : 32u) * HD * 2u;
+        for (int part = 0; part < 2; ++part) {  // 0: K, 1: V
+          uint64_t* full = part ? &vfull[st] : &kfull[st];
+          uint64_t* empty = part ? &vempty[st] : &kempty[st];
+          uint8_t* dst = part ? vs : ks;
+          if (g >= NS && !mbar_wait(empty, ((g / NS) - 1) & 1, abort_flag, a.status)) return false;
+          if (lane == 0) mbar_expect_tx(full, bytes);
+          __syncwarp();
+          if (ctx && lane < 8) {
+#pragma unroll
+            for (int at = 0; at < NA; ++at)
+              tma_load_2d_hint(dst + at * 16384 + lane * 2048, part ? &tm_vc : &tm_kc, full, at * 64, row0, pol);
+          } else if (!ctx && lane == 0) {
+            for (int at = 0; at < NA; ++at) tma_load_2d(dst + at * 16384, part ? &tm_vn : &tm_kn, full, at * 64, row0);
+          }
+          __syncwarp();
+        }
+        return true;
       };
       // context pages of the first item: committed by earlier steps, safe before the dependency wait
       int pre = 0;
       if (static_cast<int>(blockIdx.x) < total) {
         const Item x = decode(blockIdx.x);
         while (pre < min(x.n, NS) && x.c_begin + pre < x.n_ctx) {
-          issue(x, pre, pre);
+          issue(x, pre, pre);  // g < NS: no slot waits
           ++pre;
         }
       }
@@ -250,24 +278,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         if (lane == 0) {
-          mbar_expect_tx(qfull, QB);
-          for (int at = 0; at < NA; ++at)
-            tma_load_2d(q_s + at * 16384, &tm_q, qfull, at * 64, (x.b * a.n_kv + x.h) * 128);
+          const int q_row = (x.b * a.n_kv + x.h) * 128;
+          mbar_expect_tx(qfull, a.q_lo_rows ? 2 * QB : QB);
+          for (int at = 0; at < NA; ++at) {
+            tma_load_2d(q_s + at * 16384, &tm_q, qfull, at * 64, q_row);
+            if (a.q_lo_rows) tma_load_2d(q_s + QB + at * 16384, &tm_q, qfull, at * 64, a.q_lo_rows + q_row);
+          }
         }
         for (int i = 0; i < x.n; ++i, ++g) {
           if (g < pre) continue;  // fetched before the dependency wait
-          const int st = g % NS;
-          if (g >= NS && !mbar_wait(&kvempty[st], ((g / NS) - 1) & 1, abort_flag, a.status)) {
+          if (!issue(x, i, g)) {
             ok = false;
             break;
           }
-          issue(x, i, g);
         }
       }
       if (!ok) {
         volatile int never = 0;
         mbar_wait(qfull, ic & 1, &never, nullptr);
-        for (int i = max(0, g - NS); i < g; ++i) mbar_wait(&kvfull[i % NS], (i / NS) & 1, &never, nullptr);
+        for (int i = max(0, g - NS); i < g; ++i) {
+          mbar_wait(&kfull[i % NS], (i / NS) & 1, &never, nullptr);
+          mbar_wait(&vfull[i % NS], (i / NS) & 1, &never, nullptr);
+        }
       }
     }
   } else if (warp == 9) {
@@ -284,19 +316,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!mbar_wait(qfull, ic & 1, abort_flag, a.status)) break;
         auto issue_s = [&](int i) -> bool {
           const int g = g0 + i, st = g % NS;
-          if (!mbar_wait(&kvfull[st], (g / NS) & 1, abort_flag, a.status)) return false;
+          if (!mbar_wait(&kfull[st], (g / NS) & 1, abort_flag, a.status)) return false;
           if (g >= 2 && !mbar_wait(&sfree[g & 1], ((g >> 1) - 1) & 1, abort_flag, a.status)) return false;
           tc_fence_after();
-          const uint32_t ka = smem_u32(kv_s + st * 2 * KVB);
+          const uint32_t ka = smem_u32(kv_s + st * KVB);
           const bool blk = (x.c_begin + i) >= x.n_ctx;
           const uint32_t d = tmem + (g & 1) * 128;
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_f16(d, sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024), blk ? id_s32 : id_s128,
-                     kk > 0 ? 1u : 0u);
+            const uint64_t kd = sw128_desc(ka + off, 16, 1024);
+            umma_f16(d, sw128_desc(qa + off, 16, 1024), kd, blk ? id_s32 : id_s128, kk > 0 ? 1u : 0u);
+            if (a.q_lo_rows) umma_f16(d, sw128_desc(qa + QB + off, 16, 1024), kd, blk ? id_s32 : id_s128, 1u);
           }
           umma_commit(&sfull[g & 1]);
+          umma_commit(&kempty[st]);
           if (i + 1 == x.n) umma_commit(qempty);  // last use of this item's q tile
           return true;
         };
@@ -313,18 +347,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ok = false;
             break;
           }
-          tc_fence_after();
           const int st = g % NS;
-          const uint32_t va = smem_u32(kv_s + st * 2 * KVB + KVB);
+          if (!mbar_wait(&vfull[st], (g / NS) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t va = smem_u32(kv_s + (NS + st) * KVB);
           const bool blk = (x.c_begin + i) >= x.n_ctx;
           const int ksteps = blk ? 2 : 8;
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_f16(tmem + 256, sw128_desc(pa + aoff, 16, 1024), sw128_desc(va + kk * 2048, 16384, 1024), id_pv,
-                     kk > 0 ? 1u : 0u);
+            const uint64_t vd = sw128_desc(va + kk * 2048, 16384, 1024);
+            umma_f16(tmem + 256, sw128_desc(pa + aoff, 16, 1024), vd, id_pv, kk > 0 ? 1u : 0u);
+            umma_f16(tmem + 256, sw128_desc(pa + 32768 + aoff, 16, 1024), vd, id_pv, 1u);
           }
           umma_commit(ofull);
-          umma_commit(&kvempty[st]);
+          umma_commit(&vempty[st]);
         }
         g0 += x.n;
       }
@@ -383,21 +422,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
         const float alpha = ex2(m - m_use);  // 0 on the first chunk (m = -inf)
         float psum = 0.0f;
-        // probabilities -> bf16 P, one 16-byte chunk (8 keys) at a time:
-        // keys [col0, col0 + ncol) of row r live in atom col0 / 64
+        // probabilities -> BF16 pairs P_hi, P_lo, one 16-byte chunk (8 keys) at a
+        // time: keys [col0, col0 + ncol) of row r live in atom col0 / 64
 #pragma unroll
         for (int t = 0; t < 64; t += 8) {
           if (t < ncol) {
-            uint32_t w[4];
+            uint32_t w[4], wl[4];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-              w[e >> 1] = f32x2_to_bf16x2(ex2(s[t + e] - m_use), ex2(s[t + e + 1] - m_use));
-              // the row sum uses the bf16-rounded probabilities that the PV product uses
-              psum += __uint_as_float(w[e >> 1] << 16) + __uint_as_float(w[e >> 1] & 0xFFFF0000u);
+              const float p0 = ex2(s[t + e] - m_use), p1 = ex2(s[t + e + 1] - m_use);
+              w[e >> 1] = f32x2_to_bf16x2(p0, p1);
+              const float h0 = __uint_as_float(w[e >> 1] << 16), h1 = __uint_as_float(w[e >> 1] & 0xFFFF0000u);
+              wl[e >> 1] = f32x2_to_bf16x2(p0 - h0, p1 - h1);
+              psum += p0 + p1;
             }
             const int key = col0 + t;
-            *reinterpret_cast<uint4*>(p_s + (key >> 6) * 16384 + sw128_off(r, (key & 63) >> 3)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+            const uint32_t o = (key >> 6) * 16384 + sw128_off(r, (key & 63) >> 3);
+            *reinterpret_cast<uint4*>(p_s + o) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(p_s + 32768 + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
           }
         }
         tc_fence_before();
@@ -439,12 +481,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float inv = 1.0f / lt;
 #pragma unroll
           for (int d = 0; d < HH; d += 8) {
-            uint4 u;
-            u.x = f32x2_to_f16x2(o[d] * inv, o[d + 1] * inv);
-            u.y = f32x2_to_f16x2(o[d + 2] * inv, o[d + 3] * inv);
-            u.z = f32x2_to_f16x2(o[d + 4] * inv, o[d + 5] * inv);
-            u.w = f32x2_to_f16x2(o[d + 6] * inv, o[d + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + d) = u;
+            uint32_t hw[4], lw[4];
+            f16_pairs8(o + d, inv, hw, lw);
+            *reinterpret_cast<uint4*>(dst + d) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            if (a.out_lo) *reinterpret_cast<uint4*>(dst + a.out_lo + d) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
         continue;
@@ -537,10 +577,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float inv = row_inv[row];
             __half* o_dst = a.out + (static_cast<size_t>(x.b) * kRows + row / a.group) * (a.n_q * HD) +
                             (x.h * a.group + row % a.group) * HD + d;
-            uint2 u;
-            u.x = f32x2_to_f16x2(acc4[k].x * inv, acc4[k].y * inv);
-            u.y = f32x2_to_f16x2(acc4[k].z * inv, acc4[k].w * inv);
-            *reinterpret_cast<uint2*>(o_dst) = u;
+            const float y[4] = {acc4[k].x * inv, acc4[k].y * inv, acc4[k].z * inv, acc4[k].w * inv};
+            uint32_t hw[2], lw[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              hw[e] = f32x2_to_f16x2(y[2 * e], y[2 * e + 1]);
+              const __half2 h2 = *reinterpret_cast<const __half2*>(&hw[e]);
+              lw[e] = f32x2_to_f16x2(y[2 * e] - __low2float(h2), y[2 * e + 1] - __high2float(h2));
+            }
+            *reinterpret_cast<uint2*>(o_dst) = make_uint2(hw[0], hw[1]);
+            if (a.out_lo) *reinterpret_cast<uint2*>(o_dst + a.out_lo) = make_uint2(lw[0], lw[1]);
           }
         }
       }

@@ -73,6 +73,14 @@ struct GemmArgs {
   int cs, kps;             // cluster size = k splits, k tiles per split
   int m_tokens;            // valid token rows
   int rd, da, db;          // depths of the weight / expanded-weight / activation rings
+  // Activations are pairs of f16 rows, hi = f16(x) and lo = f16(x - hi), so
+  // that the 16-bit MMA inputs carry about 22 significant bits: the
+  // activation map holds the lo rows act_lo_rows rows after the hi rows
+  // (0: hi only, one MMA per k step instead of two).  Epilogues that write
+  // activations (x16_out, act_out, q_tile) put the lo copy out_lo elements
+  // after the hi copy (0: hi only).
+  int act_lo_rows;
+  size_t out_lo;
   // RMSNorm of the input rows, folded in as a per-token scale of the result:
   // r[t] = 1 / sqrt(sum_i ssq_in[i][t] / hidden + eps)  (ssq_in == nullptr: no scale)
   const float* ssq_in;
@@ -119,10 +127,11 @@ __host__ __device__ inline uint32_t weight_slot_bytes(int wf) {
   return wf == W_BF16 ? 16384u : (wf == W_FP8 ? kFp8TileBytes : kFp4TileBytes);
 }
 
-__host__ __device__ inline GemmSmem gemm_smem_layout(int wf, int n_tok, int rd, int da, int db, int cs) {
+__host__ __device__ inline GemmSmem gemm_smem_layout(int wf, int n_tok, int rd, int da, int db, int cs,
+                                                    bool lo) {
   GemmSmem s;
   s.w_bytes = weight_slot_bytes(wf);
-  s.b_bytes = static_cast<uint32_t>(n_tok) * 128u;
+  s.b_bytes = static_cast<uint32_t>(n_tok) * 128u * (lo ? 2u : 1u);  // hi tile, then lo tile
   uint32_t off = 0;
   if (wf == W_BF16) {  // weight slots are MMA operands: 1024-byte aligned, first
     s.w_off = 0;
@@ -155,8 +164,8 @@ constexpr int kBestCap = 1024;  // token columns whose running argmax fits in sh
 constexpr int kMaxRd = 32, kMaxDb = 16, kMaxDa = 4;
 constexpr uint32_t kSleepLongWaitNs = 128;  // back-off of the epilogue's wait for the accumulator
 __host__ __device__ inline uint32_t gemm_ctrl_bytes() { return kCtrlPos + 1024u; }
-__host__ __device__ inline uint32_t gemm_smem_bytes(int wf, int n_tok, int rd, int da, int db, int cs) {
-  return 1024u + gemm_smem_layout(wf, n_tok, rd, da, db, cs).ctrl_off + gemm_ctrl_bytes();
+__host__ __device__ inline uint32_t gemm_smem_bytes(int wf, int n_tok, int rd, int da, int db, int cs, bool lo) {
+  return 1024u + gemm_smem_layout(wf, n_tok, rd, da, db, cs, lo).ctrl_off + gemm_ctrl_bytes();
 }
 
 // Iterates over the (item, k-tile) sequence of one CTA: items (tile, token
@@ -297,7 +306,9 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
       if (ok) {
         const size_t o = static_cast<size_t>(tok) * a.ld_out + prow;
         a.out_f32[o] = r;
-        a.x16_out[o] = __float2half_rn(r);
+        const __half hi = __float2half_rn(r);
+        a.x16_out[o] = hi;
+        if (a.out_lo) a.x16_out[o + a.out_lo] = __float2half_rn(r - __half2float(hi));
         if (a.hidden_out) a.hidden_out[o] = r;
       }
     }
@@ -338,8 +349,11 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
       const int tok = tok0 + i;
       if (row_ok && tok < a.m_tokens) {
         const int b = tok / kRows, j = tok - b * kRows;
-        dst[((static_cast<size_t>(b) * a.n_kv + kvh) * rstride + j * jmul + roff) * hd + d] =
-            __float2bfloat16_rn(rotate ? y[i] : x[i]);
+        const size_t o = ((static_cast<size_t>(b) * a.n_kv + kvh) * rstride + j * jmul + roff) * hd + d;
+        const float val = rotate ? y[i] : x[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(val);
+        dst[o] = hi;  // K / V: the cache format; q: the hi half of the attention's q tile
+        if (is_q && a.out_lo) dst[o + a.out_lo] = __float2bfloat16_rn(val - __bfloat162float(hi));
       }
     }
   } else if constexpr (EPI == EPI_SILU) {
@@ -361,8 +375,13 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
     for (int k = 0; k < 8; ++k) {
       const int tok = tok0 + cbase + k;
       const float sg = __fdividef(g[k], 1.0f + __expf(-g[k]));
-      if (feat < a.ffn && tok < a.m_tokens)
-        a.act_out[static_cast<size_t>(tok) * a.ffn + feat] = __float2half_rn(sg * u[k]);
+      if (feat < a.ffn && tok < a.m_tokens) {
+        const size_t o = static_cast<size_t>(tok) * a.ffn + feat;
+        const float y = sg * u[k];
+        const __half hi = __float2half_rn(y);
+        a.act_out[o] = hi;
+        if (a.out_lo) a.act_out[o + a.out_lo] = __float2half_rn(y - __half2float(hi));
+      }
     }
   } else if constexpr (EPI == EPI_ARGMAX) {
     unsigned long long key[16];
@@ -384,7 +403,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const GemmSmem L = gemm_smem_layout(WF, a.n_tok, a.rd, a.da, a.db, a.cs);
+  const bool act_lo = a.act_lo_rows > 0;
+  const GemmSmem L = gemm_smem_layout(WF, a.n_tok, a.rd, a.da, a.db, a.cs, act_lo);
   const int RD = a.rd, DA = a.da, DB = a.db;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.ctrl_off);
   uint64_t* wfull = bars;                // weight tile landed
@@ -533,8 +553,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int b = i % DB;
         uint8_t* dst = smem + L.b_off + b * L.b_bytes;
         mbar_expect_tx(&bfull[b], L.b_bytes);
-        // one box of n_tok rows (the host encodes the map with that box height)
-        tma_load_2d_hint(dst, &tm_act, &bfull[b], it.kt * kTileK, it.tok_tile() * a.n_tok, pol_a);
+        // one box of n_tok rows (the host encodes the map with that box height); lo rows follow the hi tile
+        const int r0 = it.tok_tile() * a.n_tok;
+        tma_load_2d_hint(dst, &tm_act, &bfull[b], it.kt * kTileK, r0, pol_a);
+        if (act_lo) tma_load_2d_hint(dst + a.n_tok * 128, &tm_act, &bfull[b], it.kt * kTileK, a.act_lo_rows + r0, pol_a);
       };
       // weights do not depend on the previous kernel: fill the weight ring before the grid dependency wait
       ItemIter itw(&a, cluster, n_clusters, total, rank), itb(&a, cluster, n_clusters, total, rank);
@@ -615,11 +637,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (WF == W_BF16 ? L.w_off + s * L.w_bytes : L.a_off + s * 16384));
           const uint32_t sb = smem_u32(smem + L.b_off + b * L.b_bytes);
+          const uint32_t sb_lo = sb + static_cast<uint32_t>(a.n_tok) * 128u;
           const bool first = it.first_k();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            umma_f16(d, sw128_desc(sa + kk * 32, 16, 1024), sw128_desc(sb + kk * 32, 16, 1024), idesc,
-                     (first && kk == 0) ? 0u : 1u);
+            const uint64_t ad = sw128_desc(sa + kk * 32, 16, 1024);
+            umma_f16(d, ad, sw128_desc(sb + kk * 32, 16, 1024), idesc, (first && kk == 0) ? 0u : 1u);
+            if (act_lo) umma_f16(d, ad, sw128_desc(sb_lo + kk * 32, 16, 1024), idesc, 1u);
           }
           umma_commit(WF == W_BF16 ? &wempty[s] : &cempty[s]);
           umma_commit(&bempty[b]);

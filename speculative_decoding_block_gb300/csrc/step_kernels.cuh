@@ -26,7 +26,8 @@ struct EmbedArgs {
   const int* drafts;      // [B][16]
   int max_tokens;
   float* x;               // [M][H] residual stream
-  __half* x16;            // [M][H] f16 copy (first GEMM's input)
+  __half* x16;            // [M][H] f16 copy (first GEMM's input), hi = f16(x)
+  size_t x16_lo;          // elements from a hi value to its lo copy f16(x - hi) (0: hi only)
   float* ssq;             // [ceil(H/128)][ssq_ld] sums of squares per 128-feature slice
   int ssq_ld;
   int* ctx_len;           // [B] validated context length (0 if invalid)
@@ -81,7 +82,9 @@ __global__ void __launch_bounds__(128) embed_kernel(const EmbedArgs a) {
       const int i = (k0 + k) * 128 + t;
       if (k0 + k < slices && i < a.hidden) {
         a.x[o + i] = v[k];
-        a.x16[o + i] = __float2half_rn(v[k]);
+        const __half hi = __float2half_rn(v[k]);
+        a.x16[o + i] = hi;
+        if (a.x16_lo) a.x16[o + i + a.x16_lo] = __float2half_rn(v[k] - __half2float(hi));
         if (a.hidden0) a.hidden0[o + i] = v[k];
       }
       float sq = v[k] * v[k];

@@ -11,62 +11,11 @@ import torch
 
 from oracle import model as OM
 from tests.gpu_helpers import StepIO, gpu, load_state, read_rows, rel_rows, require_gpu
-from tests.oracle_helpers import near_tie_check, oracle_model, oracle_state_from_kv
-from workload import HALF_B_BF16, HALF_B_MIXED, TINY, WORKLOADS, ModelShape, gen
+from tests.oracle_helpers import near_tie_check, oracle_model
+from tests.step_check import KV_TOL, check_request, run_step
+from workload import TINY, WORKLOADS, gen
 
 pytestmark = gpu
-
-LOGIT_TOL, HIDDEN_TOL, KV_TOL = 2e-2, 2e-2, 1e-2
-
-
-def _check_request(B, kv, shape, b, st_before, drafts, res_gpu, logits, hidden, report):
-    """Compares request b of a finished GPU step with the oracle (advances nothing)."""
-    st = st_before.copy()
-    L = st.length
-    ref = OM.verify_step(_check_request.model, st, drafts, keep_hidden=hidden is not None)
-    acc, out, seq, pend = res_gpu
-    ok, tie = near_tie_check(ref, acc, out)
-    assert ok, (b, acc, out, ref["accepted"], ref["out"])
-    if tie is not None:
-        report.append((b, tie))
-    rows = slice(b * 17, b * 17 + 17)
-    if logits is not None:
-        e = rel_rows(logits[rows], ref["logits"])
-        assert e.max() < LOGIT_TOL, e.max()
-    if hidden is not None:
-        for l in range(shape.layers + 1):
-            e = rel_rows(hidden[l, rows], ref["hidden"][l])
-            assert e.max() < HIDDEN_TOL, (l, e.max())
-    if tie is None:
-        a = ref["accepted"]
-        assert seq == L + a + 1 and pend == ref["out"][a]
-        k_all, v_all = read_rows(B, kv, b, 0, L + 17, shape)
-        # untouched: rows before L and the 16 - a rows after the committed ones
-        for l in range(shape.layers):
-            assert np.array_equal(k_all[l, :L], st_before.k[l][:L])
-            assert np.array_equal(v_all[l, :L], st_before.v[l][:L])
-            assert not np.any(k_all[l, L + a + 1:]) and not np.any(v_all[l, L + a + 1:])
-            for kvref, got in ((ref["new_k"][l], k_all[l]), (ref["new_v"][l], v_all[l])):
-                e = rel_rows(got[L: L + a + 1], kvref[: a + 1])
-                assert e.max() < KV_TOL, (l, e.max())
-    return ref
-
-
-def _run(B, model, kv, shape, states, drafts, debug=True):
-    Bn = len(states)
-    io = StepIO(Bn, [s.length for s in states], [s.pending for s in states], np.stack(drafts))
-    M = 17 * Bn
-    logits = hidden = None
-    if debug:
-        logits = torch.full((M, shape.vocab), float("nan"), dtype=torch.float32, device="cuda")
-        hidden = torch.full((shape.layers + 1, M, shape.hidden), float("nan"), dtype=torch.float32, device="cuda")
-        B.vsd_verify_step_debug(model, kv, Bn, io.seq, io.pending, io.drafts, io.acc, io.out, logits, hidden)
-    else:
-        B.vsd_verify_step(model, kv, Bn, io.seq, io.pending, io.drafts, io.acc, io.out)
-    torch.cuda.synchronize()
-    assert B.vsd_get_device_status(kv) == 0
-    res = [(int(io.acc[b]), io.out[b].cpu().numpy(), int(io.seq[b]), int(io.pending[b])) for b in range(Bn)]
-    return res, (logits.cpu().numpy() if debug else None), (hidden.cpu().numpy() if debug else None)
 
 
 @pytest.fixture(scope="module")
@@ -83,23 +32,21 @@ def tiny_setup():
 def test_tiny_workload_single_request(tiny_setup):
     B, om, model = tiny_setup
     w = WORKLOADS["tiny_b1_ctx128"]
-    _check_request.model = om
     st = OM.prefill(om, gen.prompt_ids(TINY.vocab, 128, w.seed, 0))
     k = int(gen.prefix_lengths(w)[0])
     g = OM.ar_greedy(om, st.copy(), min(k + 1, 17))
     drafts = gen.plant_drafts(g, k, TINY.vocab, "tiny", w.seed)
     kv = B.vsd_kv_create(model, 1, 1024)
     load_state(B, kv, 0, st)
-    res, logits, hidden = _run(B, model, kv, TINY, [st], [drafts])
+    res, logits, hidden = run_step(B, model, kv, TINY, [st], [drafts])
     ties = []
-    ref = _check_request(B, kv, TINY, 0, st, drafts, res[0], logits, hidden, ties)
+    ref = check_request(om, B, kv, TINY, 0, st, drafts, res[0], logits, hidden, ties)
     assert ref["accepted"] == k or ties
 
 
 def test_tiny_batch_every_prefix_length(tiny_setup):
     """17 requests, planted k = 0..16, contexts of mixed length incl. empty."""
     B, om, model = tiny_setup
-    _check_request.model = om
     lens = [0, 1, 15, 16, 17, 31, 64, 127, 128, 129, 200, 255, 256, 300, 40, 90, 5]
     states, drafts = [], []
     for b, L in enumerate(lens):
@@ -111,17 +58,16 @@ def test_tiny_batch_every_prefix_length(tiny_setup):
     kv = B.vsd_kv_create(model, len(lens), 400)
     for b, st in enumerate(states):
         load_state(B, kv, b, st)
-    res, logits, hidden = _run(B, model, kv, TINY, states, drafts)
+    res, logits, hidden = run_step(B, model, kv, TINY, states, drafts)
     ties = []
     for b in range(len(lens)):
-        _check_request(B, kv, TINY, b, states[b], drafts[b], res[b], logits, hidden, ties)
+        check_request(om, B, kv, TINY, b, states[b], drafts[b], res[b], logits, hidden, ties)
     print("near ties:", ties)
 
 
 def test_tiny_consecutive_steps_match_oracle(tiny_setup):
     """Eight committing steps in a row on a paged (shuffled) cache."""
     B, om, model = tiny_setup
-    _check_request.model = om
     Bn = 3
     states = [OM.prefill(om, gen.prompt_ids(TINY.vocab, 50 + 30 * b, 91, b)) for b in range(Bn)]
     kv = B.vsd_kv_create(model, Bn, 400)
