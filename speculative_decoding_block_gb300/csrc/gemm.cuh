@@ -194,26 +194,43 @@ struct ItemIter {
 };
 
 template <int WF, int NT>
-__device__ __forceinline__ void expand_weights(uint8_t* a_tile, const uint8_t* raw, int t) {
+__device__ __forceinline__ void expand_weights(uint8_t* __restrict__ a_tile, const uint8_t* __restrict__ raw,
+                                               int t) {
   // 1024 chunks of 8 f16 (16 bytes); thread t of NT handles chunks t + NT i.
-#pragma unroll 4
-  for (int i = 0; i < 1024 / NT; ++i) {
-    const int q = t + NT * i;
-    const int r = q >> 3, c = q & 7;
-    uint4 o;
-    if constexpr (WF == W_FP8) {
-      const uint2 v = *reinterpret_cast<const uint2*>(raw + r * 64 + c * 8);
-      o.x = e4m3x2_to_f16x2(static_cast<uint16_t>(v.x & 0xFFFF));
-      o.y = e4m3x2_to_f16x2(static_cast<uint16_t>(v.x >> 16));
-      o.z = e4m3x2_to_f16x2(static_cast<uint16_t>(v.y & 0xFFFF));
-      o.w = e4m3x2_to_f16x2(static_cast<uint16_t>(v.y >> 16));
-      *reinterpret_cast<uint4*>(a_tile + sw128_off(r, c)) = o;
-    } else {
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(raw + r * 32 + c * 4);
-      const uint32_t sb = raw[kFp4ValBytes + r * 4 + (c >> 1)];
-      const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint16_t>(sb | (sb << 8)));
+  // All raw words are loaded first so that the loads overlap each other.
+  constexpr int N = 1024 / NT;
+  if constexpr (WF == W_FP8) {
+    uint2 v[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int q = t + NT * i;
+      v[i] = *reinterpret_cast<const uint2*>(raw + (q >> 3) * 64 + (q & 7) * 8);
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int q = t + NT * i;
+      uint4 o;
+      o.x = e4m3x2_to_f16x2(static_cast<uint16_t>(v[i].x & 0xFFFF));
+      o.y = e4m3x2_to_f16x2(static_cast<uint16_t>(v[i].x >> 16));
+      o.z = e4m3x2_to_f16x2(static_cast<uint16_t>(v[i].y & 0xFFFF));
+      o.w = e4m3x2_to_f16x2(static_cast<uint16_t>(v[i].y >> 16));
+      *reinterpret_cast<uint4*>(a_tile + sw128_off(q >> 3, q & 7)) = o;
+    }
+  } else {
+    uint32_t v[N], sb[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int q = t + NT * i;
+      const int r = q >> 3, c = q & 7;
+      v[i] = *reinterpret_cast<const uint32_t*>(raw + r * 32 + c * 4);
+      sb[i] = raw[kFp4ValBytes + r * 4 + (c >> 1)];
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int q = t + NT * i;
+      const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint16_t>(sb[i] | (sb[i] << 8)));
       uint32_t h[4];
-      e2m1x8_to_f16x8(v, h);
+      e2m1x8_to_f16x8(v[i], h);
       const __half2 sc = *reinterpret_cast<const __half2*>(&s2);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -221,8 +238,7 @@ __device__ __forceinline__ void expand_weights(uint8_t* a_tile, const uint8_t* r
         x = __hmul2(x, sc);  // exact: both factors have <= 4 significant bits
         h[j] = *reinterpret_cast<uint32_t*>(&x);
       }
-      o = make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(a_tile + sw128_off(r, c)) = o;
+      *reinterpret_cast<uint4*>(a_tile + sw128_off(q >> 3, q & 7)) = make_uint4(h[0], h[1], h[2], h[3]);
     }
   }
 }
