@@ -103,6 +103,12 @@ struct Linear {
   CUtensorMap tm{};            // BF16 only
 };
 
+// Bytes of the packed weight data of a Linear (one contiguous range).
+size_t linear_bytes(const Linear& l) {
+  if (l.fmt == VSD_FMT_BF16) return static_cast<size_t>(l.n_rows) * l.k * 2;
+  return static_cast<size_t>(l.n_tiles) * l.k_tiles * (l.fmt == VSD_FMT_FP8 ? kFp8TileBytes : kFp4TileBytes);
+}
+
 void free_linear(Linear& l) {
   if (l.owns && l.data) cudaFree(l.data);
   if (l.row_scale) cudaFree(l.row_scale);
@@ -285,6 +291,7 @@ bool use_pdl(cudaStream_t st) { return st != nullptr; }
 
 struct Plan {
   int n_tok, tok_tiles, cs, kps, rd, da, db, grid;
+  bool r_alias;
 };
 
 // Chooses token tiles (MMA N <= 256) and the k split (cluster of 1..8 CTAs)
@@ -296,7 +303,6 @@ struct Plan {
 // at once run in further waves.
 Plan plan_gemm(const vsd_model* m, const Linear& w, int M, int epi, bool lo) {
   const bool no_split = epi == EPI_ARGMAX;
-  const double t_tile = w.fmt == VSD_FMT_BF16 ? 0.5 : 0.6;
   const double t_group = epi == EPI_QKV ? 1.5 : (epi == EPI_ARGMAX || epi == EPI_STORE ? 0.3 : 0.5);
   Plan best{};
   double best_cost = 1e30;
@@ -304,6 +310,9 @@ Plan plan_gemm(const vsd_model* m, const Linear& w, int M, int epi, bool lo) {
   for (int t = ceil_div(M, 256); t <= max_t; ++t) {
     const int n_tok = std::max(16, round_up(ceil_div(M, t), 16));
     if (n_tok > 256 || (t > 1 && round_up(ceil_div(M, t - 1), 16) == n_tok)) continue;
+    // MMA instructions per k tile: 4, or 8 when lo rows do not fit beside the hi rows (N <= 256)
+    const int n_mma = (lo && 2 * n_tok > 256) ? 8 : 4;
+    const double t_tile = (w.fmt == VSD_FMT_BF16 ? 0.26 : 0.36) + 0.06 * n_mma;
     for (int li = 0; li < 4; ++li) {
       const int want = 1 << li;
       if (no_split && want > 1) break;
@@ -330,21 +339,34 @@ Plan plan_gemm(const vsd_model* m, const Linear& w, int M, int epi, bool lo) {
   const int items = w.n_tiles * best.tok_tiles;
   const int clusters = std::max(1, std::min({items, m->sms / best.cs, std::max(1, m->max_clusters[csi])}));
   best.grid = clusters * best.cs;
-  // ring depths: the weight ring holds the CTA's whole weight stream when it fits
+  // ring depths: as deep as the CTA's k stream, trimmed until the shared
+  // memory fits -- weights beyond 6 slots first, then activations beyond 4
   const int ki = ceil_div(items, clusters) * best.kps;  // k iterations of one CTA
-  const int wslot = static_cast<int>(weight_slot_bytes(w.fmt)), bslot = best.n_tok * 128 * (lo ? 2 : 1);
-  const int r_bytes = best.cs > 1 ? round_up(best.n_tok * 132 * 4, 1024) : 0;
-  const int budget = 232448 - 1024 - static_cast<int>(gemm_ctrl_bytes()) - r_bytes - 1024;
+  best.r_alias = best.cs > 1 && items <= clusters;
+  auto fits = [&](int da, int db, int rd) {
+    return gemm_smem_bytes(w.fmt, best.n_tok, rd, da, db, best.cs, lo, best.r_alias) <= 232448;
+  };
   if (w.fmt == VSD_FMT_BF16) {
     best.da = 1;
-    const int d = std::max(2, std::min({8, ki, budget / (wslot + bslot)}));
+    int d = std::max(2, std::min(8, ki));
+    while (d > 2 && !fits(1, d, d)) --d;
     best.rd = best.db = d;
   } else {
-    // expanded tiles: deep enough that expansion runs ahead of the MMAs
-    best.da = std::max(2, std::min(kMaxDa, ki));
-    const int rest = budget - best.da * 16384;
-    best.db = std::max(2, std::min({kMaxDb, ki, std::max(2, (rest - std::min(ki, kMaxRd) * wslot) / bslot)}));
-    best.rd = std::max(2, std::min({kMaxRd, ki, (rest - best.db * bslot) / wslot}));
+    int da = std::max(2, std::min(kMaxDa, ki)), db = std::max(2, std::min(kMaxDb, ki));
+    int rd = std::max(2, std::min(kMaxRd, ki));
+    while (!fits(da, db, rd)) {
+      if (rd > 6) --rd;
+      else if (db > 4) --db;
+      else if (rd > 4) --rd;
+      else if (db > 3) --db;
+      else if (da > 2) --da;
+      else if (rd > 2) --rd;
+      else if (db > 2) --db;
+      else break;
+    }
+    best.da = da;
+    best.db = db;
+    best.rd = rd;
   }
   return best;
 }
@@ -378,7 +400,8 @@ vsd_status run_gemm(const vsd_model* m, const Linear& w, int epi, const CUtensor
   a.db = p.db;
   a.status = status;
   a.trace = trace;
-  if (gemm_smem_bytes(w.fmt, p.n_tok, p.rd, p.da, p.db, p.cs, lo) > 232448)
+  a.r_alias = p.r_alias ? 1 : 0;
+  if (gemm_smem_bytes(w.fmt, p.n_tok, p.rd, p.da, p.db, p.cs, lo, p.r_alias) > 232448)
     return fail(VSD_ERR_UNSUPPORTED, "GEMM tile does not fit in shared memory");
   const cudaError_t e = launch_gemm(w.fmt, epi, tm_acts[p.n_tok / 16 - 1], w.tm, a, p.grid, st, use_pdl(st));
   if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
@@ -387,7 +410,8 @@ vsd_status run_gemm(const vsd_model* m, const Linear& w, int epi, const CUtensor
 
 // lo: the q tiles carry lo halves and the output gets its lo copy (the step);
 // otherwise hi only (the single-layer entry point, whose inputs are BF16)
-vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cudaStream_t st, bool lo) {
+vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cudaStream_t st, bool lo,
+                         const L2Prefetch* pf = nullptr) {
   const vsd_model* m = kv->m;
   const vsd_model_config& c = m->cfg;
   if (B > kMaxReqs) return fail(VSD_ERR_UNSUPPORTED, "at most %d requests per step", kMaxReqs);
@@ -424,6 +448,7 @@ vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cuda
     a.q_lo_rows = kv->max_batch * c.n_kv * 128;
   }
   a.status = kv->status;
+  if (pf) a.pf = *pf;
   a.trace = next_trace(kv);
   const cudaError_t e = launch_attn(c.head_dim, kv->tm_q, kv->tm_kc, kv->tm_vc, kv->tm_kn, kv->tm_vn, a,
                                     dim3(grid), st, use_pdl(st));
@@ -808,6 +833,8 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     e.keys = kv->keys;
     e.hidden0 = hidden;
     e.status = kv->status;
+    e.pf.ptr[0] = m->qkv[0].data;
+    e.pf.bytes[0] = linear_bytes(m->qkv[0]);
     e.trace = next_trace(kv);
     TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), e)));
   }
@@ -826,7 +853,16 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     a.n_kv = c.n_kv;
     a.head_dim = c.head_dim;
     TIMED(VSD_K_QKV, if ((s = run_gemm(m, m->qkv[l], EPI_QKV, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
-    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, seq_lens, st, true))) return s);
+    // while attention runs (latency-bound), the rest of this layer's weights
+    // and the next layer's QKV weights are pulled into L2
+    L2Prefetch pf{};
+    const Linear* next[4] = {&m->o[l], &m->gu[l], &m->down[l], l + 1 < c.layers ? &m->qkv[l + 1] : nullptr};
+    for (int i = 0; i < 4; ++i)
+      if (next[i]) {
+        pf.ptr[i] = next[i]->data;
+        pf.bytes[i] = linear_bytes(*next[i]);
+      }
+    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, seq_lens, st, true, &pf))) return s);
     GemmArgs r{};
     r.out_f32 = kv->x;
     r.ld_out = H;

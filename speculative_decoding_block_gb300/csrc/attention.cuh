@@ -46,6 +46,7 @@ struct AttnArgs {
   size_t out_lo;           // elements from a hi output value to its lo copy, f16(o - hi) (0: hi only)
   int q_lo_rows;           // rows of the q-tile map from a hi tile to its lo tile (0: no lo tile)
   int* status;
+  L2Prefetch pf;           // next layers' weights to pull into L2
   Trace trace;
 };
 
@@ -188,7 +189,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int cps = *cps_s;
   auto splits_of = [&](int b) { return (chunks_of(b) + cps - 1) / cps; };
   pdl_launch_dependents();
-  if (threadIdx.x == 0) trace_point(a.trace, 1);
+  if (threadIdx.x == 0) {
+    trace_point(a.trace, 1);
+    l2_prefetch_share(a.pf, blockIdx.x, gridDim.x);
+  }
 
   struct Item {
     int b, h, split, n_splits, L, n_ctx, c_begin, n;

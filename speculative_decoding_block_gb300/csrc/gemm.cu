@@ -9,7 +9,7 @@ namespace vsd {
 template <int WF, int EPI>
 static cudaError_t launch_one(const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a, int grid,
                               cudaStream_t st, bool pdl) {
-  const uint32_t smem = gemm_smem_bytes(WF, a.n_tok, a.rd, a.da, a.db, a.cs, a.act_lo_rows > 0);
+  const uint32_t smem = gemm_smem_bytes(WF, a.n_tok, a.rd, a.da, a.db, a.cs, a.act_lo_rows > 0, a.r_alias != 0);
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<WF, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);

@@ -81,6 +81,7 @@ struct GemmArgs {
   // after the hi copy (0: hi only).
   int act_lo_rows;
   size_t out_lo;
+  int r_alias;             // split-K buffer shares the rings' space (host sets it when a CTA has one item)
   // RMSNorm of the input rows, folded in as a per-token scale of the result:
   // r[t] = 1 / sqrt(sum_i ssq_in[i][t] / hidden + eps)  (ssq_in == nullptr: no scale)
   const float* ssq_in;
@@ -128,7 +129,7 @@ __host__ __device__ inline uint32_t weight_slot_bytes(int wf) {
 }
 
 __host__ __device__ inline GemmSmem gemm_smem_layout(int wf, int n_tok, int rd, int da, int db, int cs,
-                                                    bool lo) {
+                                                    bool lo, bool r_alias) {
   GemmSmem s;
   s.w_bytes = weight_slot_bytes(wf);
   s.b_bytes = static_cast<uint32_t>(n_tok) * 128u * (lo ? 2u : 1u);  // hi tile, then lo tile
@@ -148,24 +149,32 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int wf, int n_tok, int rd, 
     off += s.w_bytes * rd;
     off = (off + 1023u) & ~1023u;
   }
-  s.r_off = off;
   s.r_ld = 128u + 4u;
-  const uint32_t r_bytes = cs > 1 ? static_cast<uint32_t>(n_tok) * s.r_ld * 4u : 0u;
-  s.ctrl_off = s.r_off + ((r_bytes + 1023u) & ~1023u);
+  const uint32_t r_bytes = cs > 1 ? ((static_cast<uint32_t>(n_tok) * s.r_ld * 4u + 1023u) & ~1023u) : 0u;
+  if (r_alias) {
+    // one item per CTA: the rings are idle once its accumulator is complete,
+    // so the split-K exchange buffer reuses their space
+    s.r_off = 0;
+    s.ctrl_off = off > r_bytes ? off : r_bytes;
+  } else {
+    s.r_off = off;
+    s.ctrl_off = off + r_bytes;
+  }
   return s;
 }
 
-// control block: barriers (1 KB), argmax transpose tile 128 x 17 fp32 (9 KB),
+// control block: barriers (1 KB), per-warp argmax keys [2][4][16] (1 KB),
 // running argmax keys (8 KB), sums of squares (4 KB), per-token row scales
 // (1 KB), per-token positions (1 KB, QKV)
-constexpr uint32_t kCtrlT = 1024, kCtrlBest = kCtrlT + 9216, kCtrlSq = kCtrlBest + 8192, kCtrlRs = kCtrlSq + 4096,
+constexpr uint32_t kCtrlT = 1024, kCtrlBest = kCtrlT + 1024, kCtrlSq = kCtrlBest + 8192, kCtrlRs = kCtrlSq + 4096,
                    kCtrlPos = kCtrlRs + 1024;
 constexpr int kBestCap = 1024;  // token columns whose running argmax fits in shared memory
 constexpr int kMaxRd = 32, kMaxDb = 16, kMaxDa = 4;
 constexpr uint32_t kSleepLongWaitNs = 128;  // back-off of the epilogue's wait for the accumulator
 __host__ __device__ inline uint32_t gemm_ctrl_bytes() { return kCtrlPos + 1024u; }
-__host__ __device__ inline uint32_t gemm_smem_bytes(int wf, int n_tok, int rd, int da, int db, int cs, bool lo) {
-  return 1024u + gemm_smem_layout(wf, n_tok, rd, da, db, cs, lo).ctrl_off + gemm_ctrl_bytes();
+__host__ __device__ inline uint32_t gemm_smem_bytes(int wf, int n_tok, int rd, int da, int db, int cs, bool lo,
+                                                    bool r_alias) {
+  return 1024u + gemm_smem_layout(wf, n_tok, rd, da, db, cs, lo, r_alias).ctrl_off + gemm_ctrl_bytes();
 }
 
 // Iterates over the (item, k-tile) sequence of one CTA: items (tile, token
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const bool act_lo = a.act_lo_rows > 0;
-  const GemmSmem L = gemm_smem_layout(WF, a.n_tok, a.rd, a.da, a.db, a.cs, act_lo);
+  const GemmSmem L = gemm_smem_layout(WF, a.n_tok, a.rd, a.da, a.db, a.cs, act_lo, a.r_alias != 0);
   const int RD = a.rd, DA = a.da, DB = a.db;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.ctrl_off);
   uint64_t* wfull = bars;                // weight tile landed
@@ -455,8 +464,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const bool wide = WF != W_BF16 && total <= n_clusters;
   const bool has_item = cluster < total;
   const int conv_n = wide ? 256 : 128;
+  // With lo rows and n_tok <= 128, the hi and lo rows form one B operand of
+  // 2 n_tok rows: one MMA per k step yields W x_hi in accumulator columns
+  // [0, n_tok) and W x_lo in [n_tok, 2 n_tok), summed by the epilogue (MMA
+  // instructions cost about the same for any N, so this halves them).  For
+  // wider tiles the lo product is a second MMA into the same columns.  Two
+  // accumulator buffers.
+  const bool stacked = act_lo && 2 * a.n_tok <= 256;
+  const int acc_w = stacked ? 2 * a.n_tok : a.n_tok;
   uint32_t tmem_cols = 32;
-  while (tmem_cols < static_cast<uint32_t>(2 * a.n_tok)) tmem_cols <<= 1;
+  while (tmem_cols < static_cast<uint32_t>(2 * acc_w)) tmem_cols <<= 1;
   if (threadIdx.x == 0) trace_start(a.trace);
 
   if (threadIdx.x == 0) {
@@ -629,7 +646,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(128, a.n_tok, false, false, false);
+      const uint32_t idesc = idesc_f16(128, acc_w, false, false, false);
       ItemIter it(&a, cluster, n_clusters, total, rank);
       int i = 0, acc = 0;
       bool ok = true;
@@ -637,7 +654,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int ab = acc & 1;
         if (acc >= 2 && !mbar_wait(&tempty[ab], ((acc >> 1) - 1) & 1, abort_flag, a.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(ab * a.n_tok);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(ab * acc_w);
         bool last = false;
         do {
           // 16-bit weights are MMA-ready on arrival; FP8 / NVFP4 after expansion
@@ -653,13 +670,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (WF == W_BF16 ? L.w_off + s * L.w_bytes : L.a_off + s * 16384));
           const uint32_t sb = smem_u32(smem + L.b_off + b * L.b_bytes);
-          const uint32_t sb_lo = sb + static_cast<uint32_t>(a.n_tok) * 128u;
           const bool first = it.first_k();
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < 4; ++kk) {  // stacked: B = hi rows then lo rows, one operand of acc_w rows
             const uint64_t ad = sw128_desc(sa + kk * 32, 16, 1024);
             umma_f16(d, ad, sw128_desc(sb + kk * 32, 16, 1024), idesc, (first && kk == 0) ? 0u : 1u);
-            if (act_lo) umma_f16(d, ad, sw128_desc(sb_lo + kk * 32, 16, 1024), idesc, 1u);
+            if (act_lo && !stacked)
+              umma_f16(d, ad, sw128_desc(sb + a.n_tok * 128 + kk * 32, 16, 1024), idesc, 1u);
           }
           umma_commit(WF == W_BF16 ? &wempty[s] : &cempty[s]);
           umma_commit(&bempty[b]);
@@ -717,13 +734,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (et == 0 && acc == 0) trace_point(a.trace, 6);
       tc_fence_after();
       const uint32_t taddr =
-          tmem_base + (static_cast<uint32_t>(we * 32) << 16) + static_cast<uint32_t>(ab * a.n_tok);
+          tmem_base + (static_cast<uint32_t>(we * 32) << 16) + static_cast<uint32_t>(ab * acc_w);
+      // 16 columns of the result: the hi product plus, if present, the lo product
+      auto load_cols = [&](int c0, float* v) {
+        tmem_ld16(taddr + c0, v);
+        if (stacked) {
+          float w[16];
+          tmem_ld16(taddr + a.n_tok + c0, w);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] += w[i];
+        } else {
+          tmem_ld_wait();
+        }
+      };
       float v[16];
       if (cs > 1) {
         // partial sums of this CTA's k range -> R (column-major), then tell every CTA of the cluster
         for (int c0 = 0; c0 < a.n_tok; c0 += 16) {
-          tmem_ld16(taddr + c0, v);
-          tmem_ld_wait();
+          load_cols(c0, v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) R[(c0 + i) * L.r_ld + row] = v[i];
         }
@@ -741,8 +770,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int g = rank; g < groups; g += cs) {
         const int c0 = g * 16;
         if (cs == 1) {
-          tmem_ld16(taddr + c0, v);
-          tmem_ld_wait();
+          load_cols(c0, v);
         } else {
           const uint32_t local = smem_u32(R + c0 * L.r_ld + row);
 #pragma unroll
