@@ -103,12 +103,6 @@ struct Linear {
   CUtensorMap tm{};            // BF16 only
 };
 
-// Bytes of the packed weight data of a Linear (one contiguous range).
-size_t linear_bytes(const Linear& l) {
-  if (l.fmt == VSD_FMT_BF16) return static_cast<size_t>(l.n_rows) * l.k * 2;
-  return static_cast<size_t>(l.n_tiles) * l.k_tiles * (l.fmt == VSD_FMT_FP8 ? kFp8TileBytes : kFp4TileBytes);
-}
-
 void free_linear(Linear& l) {
   if (l.owns && l.data) cudaFree(l.data);
   if (l.row_scale) cudaFree(l.row_scale);
@@ -410,8 +404,7 @@ vsd_status run_gemm(const vsd_model* m, const Linear& w, int epi, const CUtensor
 
 // lo: the q tiles carry lo halves and the output gets its lo copy (the step);
 // otherwise hi only (the single-layer entry point, whose inputs are BF16)
-vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cudaStream_t st, bool lo,
-                         const L2Prefetch* pf = nullptr) {
+vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cudaStream_t st, bool lo) {
   const vsd_model* m = kv->m;
   const vsd_model_config& c = m->cfg;
   if (B > kMaxReqs) return fail(VSD_ERR_UNSUPPORTED, "at most %d requests per step", kMaxReqs);
@@ -448,7 +441,6 @@ vsd_status run_attention(vsd_kv* kv, int layer, int B, const int* seq_lens, cuda
     a.q_lo_rows = kv->max_batch * c.n_kv * 128;
   }
   a.status = kv->status;
-  if (pf) a.pf = *pf;
   a.trace = next_trace(kv);
   const cudaError_t e = launch_attn(c.head_dim, kv->tm_q, kv->tm_kc, kv->tm_vc, kv->tm_kn, kv->tm_vn, a,
                                     dim3(grid), st, use_pdl(st));
@@ -833,8 +825,6 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     e.keys = kv->keys;
     e.hidden0 = hidden;
     e.status = kv->status;
-    e.pf.ptr[0] = m->qkv[0].data;
-    e.pf.bytes[0] = linear_bytes(m->qkv[0]);
     e.trace = next_trace(kv);
     TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), e)));
   }
@@ -853,16 +843,7 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     a.n_kv = c.n_kv;
     a.head_dim = c.head_dim;
     TIMED(VSD_K_QKV, if ((s = run_gemm(m, m->qkv[l], EPI_QKV, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
-    // while attention runs (latency-bound), the rest of this layer's weights
-    // and the next layer's QKV weights are pulled into L2
-    L2Prefetch pf{};
-    const Linear* next[4] = {&m->o[l], &m->gu[l], &m->down[l], l + 1 < c.layers ? &m->qkv[l + 1] : nullptr};
-    for (int i = 0; i < 4; ++i)
-      if (next[i]) {
-        pf.ptr[i] = next[i]->data;
-        pf.bytes[i] = linear_bytes(*next[i]);
-      }
-    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, seq_lens, st, true, &pf))) return s);
+    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, seq_lens, st, true))) return s);
     GemmArgs r{};
     r.out_f32 = kv->x;
     r.ld_out = H;

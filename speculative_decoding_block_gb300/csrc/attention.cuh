@@ -46,7 +46,6 @@ struct AttnArgs {
   size_t out_lo;           // elements from a hi output value to its lo copy, f16(o - hi) (0: hi only)
   int q_lo_rows;           // rows of the q-tile map from a hi tile to its lo tile (0: no lo tile)
   int* status;
-  L2Prefetch pf;           // next layers' weights to pull into L2
   Trace trace;
 };
 
@@ -189,10 +188,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int cps = *cps_s;
   auto splits_of = [&](int b) { return (chunks_of(b) + cps - 1) / cps; };
   pdl_launch_dependents();
-  if (threadIdx.x == 0) {
-    trace_point(a.trace, 1);
-    l2_prefetch_share(a.pf, blockIdx.x, gridDim.x);
-  }
+  if (threadIdx.x == 0) trace_point(a.trace, 1);
 
   struct Item {
     int b, h, split, n_splits, L, n_ctx, c_begin, n;
@@ -528,51 +524,72 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float2* pml = reinterpret_cast<const float2*>(a.part_ml) + first * 128;
       float* row_mm = xstat;         // [128]
       float* row_inv = xstat + 128;  // [128]
-      if (hf == 0) {
-        float mm = -INFINITY;
-        for (int sp = 0; sp < x.n_splits; ++sp) mm = fmaxf(mm, __ldcg(pml + sp * 128 + r).x);
-        if (mm == -INFINITY) mm = 0.0f;
-        float ls = 0.0f;
-        for (int sp = 0; sp < x.n_splits; ++sp) {
-          const float2 ml = __ldcg(pml + sp * 128 + r);
-          ls += ml.y * ex2(ml.x - mm);
+      if (hf == 0) {  // row statistics in one pass (running max, rescaled sum), eight splits in flight
+        float mm = -INFINITY, ls = 0.0f;
+        for (int s0 = 0; s0 < x.n_splits; s0 += 8) {
+          float2 ml[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            ml[j] = s0 + j < x.n_splits ? __ldcg(pml + (s0 + j) * 128 + r) : make_float2(-INFINITY, 0.0f);
+          float bm = mm;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) bm = fmaxf(bm, ml[j].x);
+          const float bu = bm == -INFINITY ? 0.0f : bm;
+          ls = ls * ex2(mm - bu);  // 0 while mm = -inf
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ls += ml[j].y * ex2(ml[j].x - bu);
+          mm = bm;
         }
+        if (mm == -INFINITY) mm = 0.0f;
         row_mm[r] = mm;
         row_inv[r] = ls > 0.0f ? 1.0f / ls : 0.0f;
       }
       named_bar_sync(1, 256);
-      // Per half: every thread owns NF4 / 256 float4 of the half tile
-      // (coalesced across the warp) and sums them over the splits.
+      // Every thread owns PER float4 of each half tile (coalesced across the
+      // warp) and sums them over the splits, two splits' loads in flight.
       constexpr int PER = NF4 / 256;
       const float4* pbase = reinterpret_cast<const float4*>(a.part_o + first * 128 * HD);
+      float4 acc4[2][PER];
+      int rows[PER];
+      float mrow[PER];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        acc4[0][k] = acc4[1][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        rows[k] = (threadIdx.x + 256 * k) / Q4;
+        mrow[k] = row_mm[rows[k]];
+      }
+      for (int s0 = 0; s0 < x.n_splits; s0 += 2) {
+        float4 xv[2][2][PER];
+        float mv[2][PER];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int sp = min(s0 + u, x.n_splits - 1);
+          const float4* ps = pbase + static_cast<size_t>(sp) * 2 * NF4;
+#pragma unroll
+          for (int k = 0; k < PER; ++k) {
+            xv[u][0][k] = __ldcg(ps + threadIdx.x + 256 * k);
+            xv[u][1][k] = __ldcg(ps + NF4 + threadIdx.x + 256 * k);
+            mv[u][k] = __ldcg(pml + sp * 128 + rows[k]).x;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (s0 + u >= x.n_splits) break;
+#pragma unroll
+          for (int k = 0; k < PER; ++k) {
+            const float w = ex2(mv[u][k] - mrow[k]);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              acc4[hh][k].x += xv[u][hh][k].x * w;
+              acc4[hh][k].y += xv[u][hh][k].y * w;
+              acc4[hh][k].z += xv[u][hh][k].z * w;
+              acc4[hh][k].w += xv[u][hh][k].w * w;
+            }
+          }
+        }
+      }
+#pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        float4 acc4[PER];
-        int rows[PER];
-        float mrow[PER];
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-          acc4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          rows[k] = (threadIdx.x + 256 * k) / Q4;
-          mrow[k] = row_mm[rows[k]];
-        }
-        for (int sp = 0; sp < x.n_splits; ++sp) {
-          float4 xv[PER];
-          float mv[PER];
-          const float4* ps = pbase + static_cast<size_t>(sp) * 2 * NF4 + hh * NF4;
-#pragma unroll
-          for (int k = 0; k < PER; ++k) {
-            xv[k] = __ldcg(ps + threadIdx.x + 256 * k);
-            mv[k] = __ldcg(pml + sp * 128 + rows[k]).x;
-          }
-#pragma unroll
-          for (int k = 0; k < PER; ++k) {
-            const float w = ex2(mv[k] - mrow[k]);
-            acc4[k].x += xv[k].x * w;
-            acc4[k].y += xv[k].y * w;
-            acc4[k].z += xv[k].z * w;
-            acc4[k].w += xv[k].w * w;
-          }
-        }
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
           const int row = rows[k];
@@ -581,7 +598,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float inv = row_inv[row];
             __half* o_dst = a.out + (static_cast<size_t>(x.b) * kRows + row / a.group) * (a.n_q * HD) +
                             (x.h * a.group + row % a.group) * HD + d;
-            const float y[4] = {acc4[k].x * inv, acc4[k].y * inv, acc4[k].z * inv, acc4[k].w * inv};
+            const float y[4] = {acc4[hh][k].x * inv, acc4[hh][k].y * inv, acc4[hh][k].z * inv, acc4[hh][k].w * inv};
             uint32_t hw[2], lw[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {

@@ -35,7 +35,6 @@ struct EmbedArgs {
   unsigned long long* keys;  // [M] argmax keys of the step, cleared here
   float* hidden0;         // optional [M][H]
   int* status;
-  L2Prefetch pf;          // first layer's weights to pull into L2
   Trace trace;
 };
 
@@ -47,7 +46,6 @@ constexpr int kMaxSlices = 128;  // hidden <= 128 * 128
 // written here per 128-feature slice.
 __global__ void __launch_bounds__(128) embed_kernel(const EmbedArgs a) {
   __shared__ float part[kMaxSlices][4];
-  if (threadIdx.x == 0) l2_prefetch_share(a.pf, blockIdx.x, gridDim.x);  // constant weights
   pdl_wait();
   pdl_launch_dependents();
   if (threadIdx.x == 0) trace_start(a.trace);

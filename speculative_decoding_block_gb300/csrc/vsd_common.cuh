@@ -239,28 +239,6 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
 }
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (tensor cores, TMA).
-// Weight bytes a kernel pulls into L2 for the kernels after it (constant
-// data, so it may be fetched before the grid dependency wait): up to four
-// contiguous ranges, split evenly over the CTAs of the grid.
-struct L2Prefetch {
-  const void* ptr[4];
-  unsigned long long bytes[4];
-};
-__device__ __forceinline__ void l2_prefetch_share(const L2Prefetch& pf, int cta, int ctas) {
-  for (int i = 0; i < 4; ++i) {
-    const unsigned long long n = pf.bytes[i];
-    if (!pf.ptr[i] || n < 16) continue;
-    // this CTA's share, in 16-byte units, issued in pieces of at most 64 KB
-    const unsigned long long units = n / 16;
-    const unsigned long long lo = units * cta / ctas * 16, hi = units * (cta + 1) / ctas * 16;
-    const char* base = static_cast<const char*>(pf.ptr[i]);
-    for (unsigned long long off = lo; off < hi; off += 65536) {
-      const uint32_t len = static_cast<uint32_t>(hi - off < 65536 ? hi - off : 65536);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(len) : "memory");
-    }
-  }
-}
-
 // Hint: bring the 128-byte line holding `p` into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
