@@ -19,6 +19,7 @@ workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import multiprocessing as mp
@@ -125,52 +126,61 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms from before the warm-up; the summary keeps
+    the samples whose timestamps fall inside the timed region (or, when the
+    region is shorter than the sampling interval, the two nearest)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.lines = []
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         return self
 
-    def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
+    def stop(self):
+        proc, self.proc = self.proc, None
+        if proc is not None:
+            proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                out, _ = proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
+                proc.kill()
+                out, _ = proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    def summary(self, t0: float, t1: float):
+        import datetime
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 8:
+            if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[0]))
-                mx = float(f[1])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[1]), float(f[2]), [n for n, v in zip(names, f[5:9]) if v.lower() == "active"]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside and rows:  # region shorter than the interval: the nearest samples on either side
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
+        sm = [r[1] for r in inside]
+        reasons = sorted({n for r in inside for n in r[3]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": inside[0][2] if inside else None,
+                "samples": len(sm), "samples_in_region": sum(t0 <= r[0] <= t1 for r in rows),
+                "region_s": round(t1 - t0, 4), "reasons": reasons}
 
 
 # ------------------------------------------------------------------ oracle (CPU) sample
@@ -327,6 +337,8 @@ def run_gpu(args, rank: int, world: int):
             if timed_events:
                 timed_events[1].record(stream)
 
+    clk = ClockSampler(torch.cuda.current_device()).start()
+    atexit.register(clk.stop)  # never leave the sampler running
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
@@ -337,10 +349,12 @@ def run_gpu(args, rank: int, world: int):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        for i in range(args.steps):
-            one_step(evs[i])
-        torch.cuda.synchronize()
+    t_region0 = time.time()
+    for i in range(args.steps):
+        one_step(evs[i])
+    torch.cuda.synchronize()
+    t_region1 = time.time()
+    clk.stop()
     if world > 1:
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in evs]
@@ -444,7 +458,7 @@ def run_gpu(args, rank: int, world: int):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * statistics.mean(e2e_times), 4),
                 "call": "vsd_verify_step (direct launches, no graph)"},
         "gpu_launches": len(prof),
-        "clocks": clk.summary(),
+        "clocks": clk.summary(t_region0, t_region1),
     }
     if oracle_handle is not None:
         r = finish_oracle(oracle_handle)
