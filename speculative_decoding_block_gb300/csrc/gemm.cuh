@@ -543,6 +543,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr int NT = decltype(nt_const)::value;
     bool scales_done = !(wide && has_item && warp < 4);
     ItemIter it(&a, cluster, n_clusters, total, rank);
+    int r = 0, c = 0;           // weight and expansion slots of tile i
+    uint32_t rp = 0, cp = 0;    // their phase parities
     for (int i = 0; !it.done(); it.next(), ++i) {
       if (!scales_done && i == DA) {
         pdl_wait();
@@ -550,14 +552,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         named_bar_arrive(3, 256);
         scales_done = true;
       }
-      const int r = i % RD, c = i % DA;
-      if (!mbar_wait(&wfull[r], (i / RD) & 1, abort_flag, a.status)) break;
-      if (i >= DA && !mbar_wait(&cempty[c], ((i / DA) - 1) & 1, abort_flag, a.status)) break;
+      if (!mbar_wait(&wfull[r], rp, abort_flag, a.status)) break;
+      if (i >= DA && !mbar_wait(&cempty[c], cp ^ 1u, abort_flag, a.status)) break;
       if (t == 0 && i == 0) trace_point(a.trace, 3);
       expand_weights<WF, NT>(smem + L.a_off + c * 16384, smem + L.w_off + r * L.w_bytes, t);
       fence_proxy_async();
       mbar_arrive(&conv[c]);
       mbar_arrive(&wempty[r]);
+      if (++r == RD) {
+        r = 0;
+        rp ^= 1u;
+      }
+      if (++c == DA) {
+        c = 0;
+        cp ^= 1u;
+      }
     }
     if (!scales_done) {
       pdl_wait();
@@ -571,8 +580,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
-      auto issue_w = [&](int i, const ItemIter& it) {
-        const int r = i % RD;
+      auto issue_w = [&](int r, const ItemIter& it) {
         uint8_t* dst = smem + L.w_off + r * L.w_bytes;
         mbar_expect_tx(&wfull[r], L.w_bytes);
         if constexpr (WF == W_BF16) {
@@ -582,8 +590,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           bulk_load(dst, src, L.w_bytes, &wfull[r], pol_w);
         }
       };
-      auto issue_b = [&](int i, const ItemIter& it) {
-        const int b = i % DB;
+      auto issue_b = [&](int b, const ItemIter& it) {
         uint8_t* dst = smem + L.b_off + b * L.b_bytes;
         mbar_expect_tx(&bfull[b], L.b_bytes);
         // one box of n_tok rows (the host encodes the map with that box height); lo rows follow the hi tile
@@ -593,8 +600,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       };
       // weights do not depend on the previous kernel: fill the weight ring before the grid dependency wait
       ItemIter itw(&a, cluster, n_clusters, total, rank), itb(&a, cluster, n_clusters, total, rank);
-      int wi = 0, bi = 0;
+      // (wi, bi: tiles issued; ws, bs: next slot; wp, bp: parity of the release
+      // of that slot's previous tile)
+      int wi = 0, bi = 0, bs = 0;
+      uint32_t wp = 0, bp = 0;
       for (; wi < RD && !itw.done(); ++wi, itw.next()) issue_w(wi, itw);
+      int ws = wi == RD ? 0 : wi;
       pdl_wait();
       trace_point(a.trace, 2);
       // then serve both rings as their slots free up, never blocking on one while the other could proceed
@@ -602,15 +613,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       while (!itw.done() || !itb.done()) {
         bool progress = false;
-        if (!itb.done() && (bi < DB || mbar_test_wait(&bempty[bi % DB], ((bi / DB) - 1) & 1))) {
-          issue_b(bi, itb);
+        if (!itb.done() && (bi < DB || mbar_test_wait(&bempty[bs], bp))) {
+          issue_b(bs, itb);
           ++bi;
+          if (++bs == DB) {  // slot 0 again: wait for the previous round's release
+            bs = 0;
+            bp = bi == DB ? 0u : bp ^ 1u;
+          }
           itb.next();
           progress = true;
         }
-        if (!itw.done() && (wi < RD || mbar_test_wait(&wempty[wi % RD], ((wi / RD) - 1) & 1))) {
-          issue_w(wi, itw);
+        if (!itw.done() && (wi < RD || mbar_test_wait(&wempty[ws], wp))) {
+          issue_w(ws, itw);
           ++wi;
+          if (++ws == RD) {
+            ws = 0;
+            wp ^= 1u;
+          }
           itw.next();
           progress = true;
         }
@@ -648,41 +667,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, acc_w, false, false, false);
       ItemIter it(&a, cluster, n_clusters, total, rank);
-      int i = 0, acc = 0;
-      bool ok = true;
+      // 16-bit weights are MMA-ready on arrival; FP8 / NVFP4 after expansion.
+      // Ring slots and phases advance by counting (no division per k tile);
+      // descriptors are the slot's base descriptor plus the address offset
+      // (bits 0-13 hold address / 16).
+      const int NA = WF == W_BF16 ? RD : DA;
+      uint64_t* afull = WF == W_BF16 ? wfull : conv;
+      uint64_t* aempty = WF == W_BF16 ? wempty : cempty;
+      const uint64_t a_desc0 = sw128_desc(smem_u32(smem + (WF == W_BF16 ? L.w_off : L.a_off)), 16, 1024);
+      const uint64_t b_desc0 = sw128_desc(smem_u32(smem + L.b_off), 16, 1024);
+      const uint32_t b_step = L.b_bytes >> 4, lo_step = static_cast<uint32_t>(a.n_tok) * 8u;
+      int s = 0, b = 0, acc = 0;
+      uint32_t sp = 0, bp = 0;
+      bool ok = true, first_tile = true;
       while (ok && !it.done()) {
         const int ab = acc & 1;
         if (acc >= 2 && !mbar_wait(&tempty[ab], ((acc >> 1) - 1) & 1, abort_flag, a.status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(ab * acc_w);
+        uint32_t accum = 0;
         bool last = false;
         do {
-          // 16-bit weights are MMA-ready on arrival; FP8 / NVFP4 after expansion
-          const int s = WF == W_BF16 ? i % RD : i % DA;
-          const uint32_t par = WF == W_BF16 ? (i / RD) & 1 : (i / DA) & 1;
-          const int b = i % DB;
-          if (!mbar_wait(WF == W_BF16 ? &wfull[s] : &conv[s], par, abort_flag, a.status) ||
-              !mbar_wait(&bfull[b], (i / DB) & 1, abort_flag, a.status)) {
+          if (!mbar_wait(&afull[s], sp, abort_flag, a.status) || !mbar_wait(&bfull[b], bp, abort_flag, a.status)) {
             ok = false;
             break;
           }
-          if (i == 0) trace_point(a.trace, 4);
+          if (first_tile) {
+            trace_point(a.trace, 4);
+            first_tile = false;
+          }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + (WF == W_BF16 ? L.w_off + s * L.w_bytes : L.a_off + s * 16384));
-          const uint32_t sb = smem_u32(smem + L.b_off + b * L.b_bytes);
-          const bool first = it.first_k();
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>(s) * 1024u;
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>(b) * b_step;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // stacked: B = hi rows then lo rows, one operand of acc_w rows
-            const uint64_t ad = sw128_desc(sa + kk * 32, 16, 1024);
-            umma_f16(d, ad, sw128_desc(sb + kk * 32, 16, 1024), idesc, (first && kk == 0) ? 0u : 1u);
-            if (act_lo && !stacked)
-              umma_f16(d, ad, sw128_desc(sb + a.n_tok * 128 + kk * 32, 16, 1024), idesc, 1u);
+            umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, accum | kk);
+            if (act_lo && !stacked) umma_f16(d, ad + 2 * kk, bd + lo_step + 2 * kk, idesc, 1u);
           }
-          umma_commit(WF == W_BF16 ? &wempty[s] : &cempty[s]);
+          accum = 1;
+          umma_commit(&aempty[s]);
           umma_commit(&bempty[b]);
           last = it.last_k();
           it.next();
-          ++i;
+          if (++s == NA) {
+            s = 0;
+            sp ^= 1u;
+          }
+          if (++b == DB) {
+            b = 0;
+            bp ^= 1u;
+          }
         } while (!last);
         if (!ok) break;
         umma_commit(&tfull[ab]);

@@ -98,19 +98,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Returns false if
-// the CTA-wide abort flag is raised or the time limit runs out (then the
-// abort flag is raised and VSD_DEV_TIMEOUT is recorded in *status).
-// Bounded wait for the phase of `parity` to complete.  Polls with the
-// non-suspending test_wait (a suspended try_wait was seen to miss wake-ups
-// from TMA and MMA completions by microseconds); `sleep_ns` > 0 backs off
-// between probes, for long waits whose polling would otherwise take shared
-// memory and issue slots from the warps doing the work.  Gives up (sets the
-// abort flag and VSD_DEV_TIMEOUT) after kWaitLimitCycles or when another
-// thread of the CTA has given up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, uint32_t sleep_ns = 0) {
-  if (mbar_test_wait(bar, parity)) return true;
+// Polling part of mbar_wait, out of line: the waits sit in the hot loops of
+// every warp role, and keeping only the first probe inline keeps those loops
+// short.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   int* status, uint32_t sleep_ns) {
   const long long t0 = cycles();
   while (true) {
 #pragma unroll 1
@@ -125,6 +117,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       return false;
     }
   }
+}
+
+// Bounded wait for the phase of `parity` to complete.  Polls with the
+// non-suspending test_wait (a suspended try_wait was seen to miss wake-ups
+// from TMA and MMA completions by microseconds); `sleep_ns` > 0 backs off
+// between probes, for long waits whose polling would otherwise take shared
+// memory and issue slots from the warps doing the work.  Returns false when
+// another thread of the CTA has raised the abort flag, or after
+// kWaitLimitCycles (then it raises the flag and records VSD_DEV_TIMEOUT in
+// *status).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, uint32_t sleep_ns = 0) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, status, sleep_ns);
 }
 
 // ------------------------------------------------------------------ clusters
