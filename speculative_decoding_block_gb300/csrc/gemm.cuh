@@ -163,10 +163,10 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int wf, int n_tok, int rd, 
   return s;
 }
 
-// control block: barriers (1 KB), per-warp argmax keys [2][4][16] (1 KB),
+// control block: barriers (1 KB), per-warp argmax keys [2][2][4][16] (2 KB),
 // running argmax keys (8 KB), sums of squares (4 KB), per-token row scales
 // (1 KB), per-token positions (1 KB, QKV)
-constexpr uint32_t kCtrlT = 1024, kCtrlBest = kCtrlT + 1024, kCtrlSq = kCtrlBest + 8192, kCtrlRs = kCtrlSq + 4096,
+constexpr uint32_t kCtrlT = 1024, kCtrlBest = kCtrlT + 2048, kCtrlSq = kCtrlBest + 8192, kCtrlRs = kCtrlSq + 4096,
                    kCtrlPos = kCtrlRs + 1024;
 constexpr int kBestCap = 1024;  // token columns whose running argmax fits in shared memory
 constexpr int kMaxRd = 32, kMaxDb = 16, kMaxDa = 4;
@@ -464,6 +464,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const bool wide = WF != W_BF16 && total <= n_clusters;
   const bool has_item = cluster < total;
   const int conv_n = wide ? 256 : 128;
+  // warps 0-3 join the epilogue when they have no expansion to run meanwhile
+  const bool ep8 = WF == W_BF16 || wide;
   // With lo rows and n_tok <= 128, the hi and lo rows form one B operand of
   // 2 n_tok rows: one MMA per k step yields W x_hi in accumulator columns
   // [0, n_tok) and W x_lo in [n_tok, 2 n_tok), summed by the epilogue (MMA
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
+      mbar_init(&tempty[i], ep8 ? 256 : 128);
     }
     mbar_init(rfull, cs);
     mbar_init(rfree, cs);
@@ -654,14 +656,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int i = max(0, bi - DB); i < bi; ++i) mbar_wait(&bfull[i % DB], (i / DB) & 1, &never, nullptr);
       }
     }
-  } else if (warp < 4) {
-    // ---------------------------------------------------------- weight expansion (FP8 / NVFP4)
-    if constexpr (WF != W_BF16) {
-      if (wide)
-        expand_all(std::integral_constant<int, 256>{}, static_cast<int>(threadIdx.x));
-      else
-        expand_all(std::integral_constant<int, 128>{}, static_cast<int>(threadIdx.x));
-    }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
@@ -725,159 +719,176 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
-    // ---------------------------------------------------------- epilogue (warps 4..7)
-    const int we = warp - 4;  // == warp % 4: TMEM lane quarter
-    const int row = we * 32 + lane;
-    const int et = threadIdx.x - 128;
-    const int groups = a.n_tok / 16;
-    const bool alive = rank * a.kps < a.k_tiles;
-    // ARGMAX: running best key per token column of this CTA, flushed once at the end
-    const bool keep_best = a.tok_tiles * a.n_tok <= kBestCap;
-    if constexpr (EPI == EPI_ARGMAX)
-      for (int c = et; c < kBestCap; c += 128) best[c] = 0ull;
-    if constexpr (WF != W_BF16)
-      if (wide) expand_all(std::integral_constant<int, 256>{}, static_cast<int>(threadIdx.x));
-    // weight row scales are constant: the first item's is read before the grid dependency wait
-    auto row_scale_of = [&](int item) -> float {
-      if constexpr (WF == W_BF16) {
-        return 1.0f;
-      } else {
-        const int prow = (item / a.tok_tiles) * kTileN + row;
-        return prow < a.n_rows ? a.row_scale[prow] : 0.0f;
-      }
-    };
-    float scale_next = (alive && cluster < total) ? row_scale_of(cluster) : 0.0f;
-    pdl_wait();  // the token scales and positions read what the previous kernels wrote
-    named_bar_sync(1, 128);
-    int acc = 0;
-    for (int item = cluster; alive && item < total; item += n_clusters, ++acc) {
-      const int ab = acc & 1;
-      const int tile = item / a.tok_tiles, tt = item % a.tok_tiles;
-      const float scale = scale_next;
-      if (item + n_clusters < total) scale_next = row_scale_of(item + n_clusters);
-      // per-token scales: computed here while the MMAs run, or (wide mode) by warps 0-3
-      if (wide) {
-        named_bar_sync(3, 256);
-      } else {
-        token_scales(item, et, 128);
-      }
-      named_bar_sync(1, 128);
-      if (et == 0 && acc == 0) trace_point(a.trace, 8);
-      if (cs > 1 && acc > 0 && !mbar_wait_cluster(rfree, (acc - 1) & 1, abort_flag, a.status)) break;
-      if (!mbar_wait(&tfull[ab], (acc >> 1) & 1, abort_flag, a.status, kSleepLongWaitNs)) break;
-      if (et == 0 && acc == 0) trace_point(a.trace, 6);
-      tc_fence_after();
-      const uint32_t taddr =
-          tmem_base + (static_cast<uint32_t>(we * 32) << 16) + static_cast<uint32_t>(ab * acc_w);
-      // 16 columns of the result: the hi product plus, if present, the lo product
-      auto load_cols = [&](int c0, float* v) {
-        tmem_ld16(taddr + c0, v);
-        if (stacked) {
-          float w[16];
-          tmem_ld16(taddr + a.n_tok + c0, w);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] += w[i];
+    // ---------------------------------------------------------- epilogue
+    // Warps 4-7 always; warps 0-3 too once they are free (16-bit weights: no
+    // expansion; wide mode: expansion finished with the k loop).  Each set of
+    // four warps covers the 128 TMEM lanes, and the two sets take alternate
+    // 16-column groups, so two warps per scheduler hide each other's latency.
+    const int half = warp < 4 ? 1 : 0;
+    if constexpr (WF != W_BF16) {
+      if (wide)
+        expand_all(std::integral_constant<int, 256>{}, static_cast<int>(threadIdx.x));
+      else if (half)
+        expand_all(std::integral_constant<int, 128>{}, static_cast<int>(threadIdx.x));
+    }
+    if (!half || ep8) {
+      const int we = warp & 3;  // TMEM lane quarter
+      const int row = we * 32 + lane;
+      const int et = threadIdx.x & 127;     // thread of this set
+      const int et2 = half * 128 + et;      // thread of the epilogue
+      const int n_sets = ep8 ? 2 : 1;
+      const int ep_n = 128 * n_sets;        // epilogue threads
+      const int groups = a.n_tok / 16;
+      const bool alive = rank * a.kps < a.k_tiles;
+      // ARGMAX: running best key per token column of this CTA, flushed once at the end
+      const bool keep_best = a.tok_tiles * a.n_tok <= kBestCap;
+      if constexpr (EPI == EPI_ARGMAX)
+        for (int c = et2; c < kBestCap; c += ep_n) best[c] = 0ull;
+      // weight row scales are constant: the first item's is read before the grid dependency wait
+      auto row_scale_of = [&](int item) -> float {
+        if constexpr (WF == W_BF16) {
+          return 1.0f;
         } else {
-          tmem_ld_wait();
+          const int prow = (item / a.tok_tiles) * kTileN + row;
+          return prow < a.n_rows ? a.row_scale[prow] : 0.0f;
         }
       };
-      float v[16];
-      if (cs > 1) {
-        // partial sums of this CTA's k range -> R (column-major), then tell every CTA of the cluster
-        for (int c0 = 0; c0 < a.n_tok; c0 += 16) {
-          load_cols(c0, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) R[(c0 + i) * L.r_ld + row] = v[i];
-        }
-        tc_fence_before();
-        mbar_arrive(&tempty[ab]);
-        named_bar_sync(1, 128);
-        if (et == 0) {
-          fence_acq_rel_cluster();
-          for (int p = 0; p < cs; ++p) mbar_arrive_remote(mapa_shared(smem_u32(rfull), p));
-        }
-        if (!mbar_wait_cluster(rfull, acc & 1, abort_flag, a.status)) break;
-        if (et == 0 && acc == 0) trace_point(a.trace, 7);
-      }
-      // column groups of this CTA: all of them (cs == 1) or every cs-th (split-K)
-      for (int g = rank; g < groups; g += cs) {
-        const int c0 = g * 16;
-        if (cs == 1) {
-          load_cols(c0, v);
+      float scale_next = (alive && cluster < total) ? row_scale_of(cluster) : 0.0f;
+      pdl_wait();  // the token scales and positions read what the previous kernels wrote
+      named_bar_sync(1, ep_n);
+      int acc = 0;
+      for (int item = cluster; alive && item < total; item += n_clusters, ++acc) {
+        const int ab = acc & 1;
+        const int tile = item / a.tok_tiles, tt = item % a.tok_tiles;
+        const float scale = scale_next;
+        if (item + n_clusters < total) scale_next = row_scale_of(item + n_clusters);
+        // per-token scales: computed here while the MMAs run, or (wide mode)
+        // by warps 0-3 during the expansion, published on barrier 3
+        if (wide) {
+          if (!half) named_bar_sync(3, 256);
         } else {
-          const uint32_t local = smem_u32(R + c0 * L.r_ld + row);
-#pragma unroll
-          for (int h4 = 0; h4 < 16; h4 += 4) {  // 4 columns at a time, every peer's loads in flight
-            float x[8][4];
-#pragma unroll
-            for (int p = 0; p < 8; ++p)
-              if (p < cs) {
-                const uint32_t ra = mapa_shared(local, p) + h4 * L.r_ld * 4;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) x[p][i] = ld_dsmem_f32(ra + i * L.r_ld * 4);
-              }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[h4 + i] = 0.0f;
-#pragma unroll
-            for (int p = 0; p < 8; ++p)  // fixed order: deterministic sum
-              if (p < cs) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) v[h4 + i] += x[p][i];
-              }
-          }
+          token_scales(item, et2, ep_n);
         }
-        if (et == 0 && acc == 0 && g == rank) trace_point(a.trace, 12);
-        unsigned long long* wb = wbest + (g & 1) * 64;
-        epilogue_cols<EPI, WF>(a, tile, tt, row, c0, v, scale, rs, pos_s, wb, sq_red, we, lane);
-        if (et == 0 && acc == 0 && g == rank) trace_point(a.trace, 14);
-        if constexpr (EPI == EPI_ARGMAX) {
-          named_bar_sync(1, 128);
-          if (et < 16) {  // fold the four warps' maxima of column c0 + et (the other parity is written next)
-            unsigned long long k = wb[et];
-#pragma unroll
-            for (int w = 1; w < 4; ++w) k = wb[w * 16 + et] > k ? wb[w * 16 + et] : k;
-            const int col = tt * a.n_tok + c0 + et;
-            if (keep_best) {
-              if (k > best[col]) best[col] = k;
-            } else if (col < a.m_tokens && k) {
-              atomicMax(a.keys + col, k);
+        named_bar_sync(1, ep_n);
+        if (et2 == 0 && acc == 0) trace_point(a.trace, 8);
+        if (cs > 1 && acc > 0 && !mbar_wait_cluster(rfree, (acc - 1) & 1, abort_flag, a.status)) break;
+        if (!mbar_wait(&tfull[ab], (acc >> 1) & 1, abort_flag, a.status, kSleepLongWaitNs)) break;
+        if (et2 == 0 && acc == 0) trace_point(a.trace, 6);
+        tc_fence_after();
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(we * 32) << 16) + static_cast<uint32_t>(ab * acc_w);
+        // 16 columns of the result: the hi product plus, if present, the lo product
+        auto load_cols = [&](int c0, float* v) {
+          tmem_ld16(taddr + c0, v);
+          if (stacked) {
+            float w[16];
+            tmem_ld16(taddr + a.n_tok + c0, w);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] += w[i];
+          } else {
+            tmem_ld_wait();
+          }
+        };
+        float v[16];
+        if (cs > 1) {
+          // partial sums of this CTA's k range -> R (column-major), then tell every CTA of the cluster
+          for (int c0 = half * 16; c0 < a.n_tok; c0 += 16 * n_sets) {
+            load_cols(c0, v);
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) R[(c0 + i) * L.r_ld + row] = v[i];
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty[ab]);
+          named_bar_sync(1, ep_n);
+          if (et2 == 0) {
+            fence_acq_rel_cluster();
+            for (int p = 0; p < cs; ++p) mbar_arrive_remote(mapa_shared(smem_u32(rfull), p));
+          }
+          if (!mbar_wait_cluster(rfull, acc & 1, abort_flag, a.status)) break;
+          if (et2 == 0 && acc == 0) trace_point(a.trace, 7);
+        }
+        // column groups of this set: every n_sets-th of this CTA's (all groups
+        // when cs == 1, every cs-th for a split-K rank)
+        int gi = 0;
+        for (int g = rank + cs * half; g < groups; g += cs * n_sets, ++gi) {
+          const int c0 = g * 16;
+          if (cs == 1) {
+            load_cols(c0, v);
+          } else {
+            const uint32_t local = smem_u32(R + c0 * L.r_ld + row);
+  #pragma unroll
+            for (int h4 = 0; h4 < 16; h4 += 4) {  // 4 columns at a time, every peer's loads in flight
+              float x[8][4];
+  #pragma unroll
+              for (int p = 0; p < 8; ++p)
+                if (p < cs) {
+                  const uint32_t ra = mapa_shared(local, p) + h4 * L.r_ld * 4;
+  #pragma unroll
+                  for (int i = 0; i < 4; ++i) x[p][i] = ld_dsmem_f32(ra + i * L.r_ld * 4);
+                }
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) v[h4 + i] = 0.0f;
+  #pragma unroll
+              for (int p = 0; p < 8; ++p)  // fixed order: deterministic sum
+                if (p < cs) {
+  #pragma unroll
+                  for (int i = 0; i < 4; ++i) v[h4 + i] += x[p][i];
+                }
             }
           }
-          if (et == 0 && acc == 0 && g == rank) trace_point(a.trace, 15);
+          if (et2 == 0 && acc == 0 && g == rank) trace_point(a.trace, 12);
+          // ARGMAX: per-warp maxima, [set][parity][4 warps][16]
+          unsigned long long* wb = wbest + half * 128 + (gi & 1) * 64;
+          epilogue_cols<EPI, WF>(a, tile, tt, row, c0, v, scale, rs, pos_s, wb, sq_red, we, lane);
+          if (et2 == 0 && acc == 0 && g == rank) trace_point(a.trace, 14);
+          if constexpr (EPI == EPI_ARGMAX) {
+            named_bar_sync(4 + half, 128);  // this set's four warps only
+            if (et < 16) {  // fold the four warps' maxima of column c0 + et (the other parity is written next)
+              unsigned long long k = wb[et];
+  #pragma unroll
+              for (int w = 1; w < 4; ++w) k = wb[w * 16 + et] > k ? wb[w * 16 + et] : k;
+              const int col = tt * a.n_tok + c0 + et;
+              if (keep_best) {
+                if (k > best[col]) best[col] = k;
+              } else if (col < a.m_tokens && k) {
+                atomicMax(a.keys + col, k);
+              }
+            }
+            if (et2 == 0 && acc == 0 && g == rank) trace_point(a.trace, 15);
+          }
         }
-      }
-      if (cs == 1) {
-        tc_fence_before();
-        mbar_arrive(&tempty[ab]);
-      }
-      named_bar_sync(1, 128);
-      if (et == 0 && acc == 0) trace_point(a.trace, 9);
-      if (cs > 1 && et == 0) {
-        fence_acq_rel_cluster();
-        for (int p = 0; p < cs; ++p) mbar_arrive_remote(mapa_shared(smem_u32(rfree), p));
-      }
-      if constexpr (EPI == EPI_RESID) {
-        for (int c = et; c < a.n_tok; c += 128) {
-          const int tok = tt * a.n_tok + c;
-          if ((c / 16) % cs == rank && tok < a.m_tokens)
-            a.ssq_out[static_cast<size_t>(tile) * a.ssq_ld + tok] =
-                sq_red[c] + sq_red[256 + c] + sq_red[512 + c] + sq_red[768 + c];
+        if (cs == 1) {
+          tc_fence_before();
+          mbar_arrive(&tempty[ab]);
         }
+        named_bar_sync(1, ep_n);
+        if (et2 == 0 && acc == 0) trace_point(a.trace, 9);
+        if (cs > 1 && et2 == 0) {
+          fence_acq_rel_cluster();
+          for (int p = 0; p < cs; ++p) mbar_arrive_remote(mapa_shared(smem_u32(rfree), p));
+        }
+        if constexpr (EPI == EPI_RESID) {
+          for (int c = et2; c < a.n_tok; c += ep_n) {
+            const int tok = tt * a.n_tok + c;
+            if ((c / 16) % cs == rank && tok < a.m_tokens)
+              a.ssq_out[static_cast<size_t>(tile) * a.ssq_ld + tok] =
+                  sq_red[c] + sq_red[256 + c] + sq_red[512 + c] + sq_red[768 + c];
+          }
+        }
+        named_bar_sync(1, ep_n);
+        if (et2 == 0 && acc == 0) trace_point(a.trace, 10);
       }
-      named_bar_sync(1, 128);
-      if (et == 0 && acc == 0) trace_point(a.trace, 10);
-    }
-    // the peers read this CTA's R buffer until they arrive on rfree: wait for
-    // that before the CTA may exit (its shared memory must stay valid)
-    if (cs > 1 && acc > 0) mbar_wait_cluster(rfree, (acc - 1) & 1, abort_flag, a.status);
-    if constexpr (EPI == EPI_ARGMAX) {
-      if (keep_best)
-        for (int c = et; c < a.tok_tiles * a.n_tok; c += 128)
-          if (c < a.m_tokens && best[c]) atomicMax(a.keys + c, best[c]);
+      // the peers read this CTA's R buffer until they arrive on rfree: wait for
+      // that before the CTA may exit (its shared memory must stay valid)
+      if (cs > 1 && acc > 0) mbar_wait_cluster(rfree, (acc - 1) & 1, abort_flag, a.status);
+      if constexpr (EPI == EPI_ARGMAX) {
+        if (keep_best)
+          for (int c = et2; c < a.tok_tiles * a.n_tok; c += ep_n)
+            if (c < a.m_tokens && best[c]) atomicMax(a.keys + c, best[c]);
+      }
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) trace_end(a.trace, 11);
