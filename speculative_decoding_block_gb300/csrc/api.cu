@@ -655,7 +655,7 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
   kv->attn_items_cap = static_cast<size_t>(4) * m->sms + static_cast<size_t>(2) * max_batch * c.n_kv;
   if ((s = dalloc(&kv->attn_o, kv->attn_items_cap * 128 * hd, false)) ||
       (s = dalloc(&kv->attn_ml, kv->attn_items_cap * 128 * 2, false)) ||
-      (s = dalloc(&kv->attn_counters, static_cast<size_t>(max_batch) * c.n_kv)))
+      (s = dalloc(&kv->attn_counters, static_cast<size_t>(2) * max_batch * c.n_kv)))
     return cleanup(s);
   const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16, BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   for (int j = 0; j < kActBoxes; ++j) {
@@ -1020,7 +1020,7 @@ vsd_status vsd_block_attention_static(const vsd_model* m, vsd_kv* kv, int32_t la
   const size_t pairs = static_cast<size_t>(B) * c.n_kv;
   // scratch layout: split counters | q tiles | block K rows | block V rows | split partials (O, then m / l)
   const size_t o_cnt = 0;
-  const size_t o_q = align256(o_cnt + pairs * sizeof(int));
+  const size_t o_q = align256(o_cnt + 2 * pairs * sizeof(int));  // arrived / done counters per pair
   const size_t o_k = align256(o_q + pairs * 128 * hd * 2);
   const size_t o_v = align256(o_k + pairs * 32 * hd * 2);
   const size_t o_part = align256(o_v + pairs * 32 * hd * 2);
@@ -1058,7 +1058,7 @@ vsd_status vsd_block_attention_static(const vsd_model* m, vsd_kv* kv, int32_t la
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // what must start at zero: the split counters, and the staged block rows
   // 17..31 of every 32-row group (loaded with the block, masked by the kernel)
-  CK(cudaMemsetAsync(base + o_cnt, 0, pairs * sizeof(int), st));
+  CK(cudaMemsetAsync(base + o_cnt, 0, 2 * pairs * sizeof(int), st));
   CK(cudaMemsetAsync(base + o_k, 0, o_part - o_k, st));
   scatter_q_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), B, c.n_q, c.n_kv, hd, q_tile);
   scatter_block_rows_kernel<<<256, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k_new), 1, B, c.n_kv, hd, B,

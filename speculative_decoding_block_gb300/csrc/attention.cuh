@@ -41,7 +41,7 @@ struct AttnArgs {
   float scale_log2;        // log2(e) / sqrt(hd)
   float* part_o;           // [B][n_kv][max_splits][2 halves][128][hd / 2] unnormalised partial O
   float* part_ml;          // [B][n_kv][max_splits][128][2]
-  int* counters;           // [B][n_kv]
+  int* counters;           // [2][batch_cap][n_kv]: splits arrived / done merging, per pair (zero between launches)
   __half* out;             // [B*17][n_q*hd] f16 (hi)
   size_t out_lo;           // elements from a hi output value to its lo copy, f16(o - hi) (0: hi only)
   int q_lo_rows;           // rows of the q-tile map from a hi tile to its lo tile (0: no lo tile)
@@ -111,7 +111,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* ofree = ofull + 1;
   uint32_t* tmem_p = reinterpret_cast<uint32_t*>(ofree + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_p + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_p + 2);
   volatile int* n_items = reinterpret_cast<volatile int*>(tmem_p + 3);
   float* xstat = reinterpret_cast<float*>(p_s + 2 * 32768 + 256);  // [2 parity][2 halves][128] maxima; then [2][2][128] sums
   int* item_off = reinterpret_cast<int*>(p_s + 2 * 32768 + 256 + 4096);  // [B + 1] first item of each request
@@ -221,7 +220,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     {
       const uint64_t pol = policy_evict_first();
       // chunk i of item x, global chunk number g: K then V, each once its slot is free
-      auto issue = [&](const Item& x, int i, int g) -> bool {
+      // (page_pre: lane p's page of the chunk when the caller has read it, else -1)
+      auto issue = [&](const Item& x, int i, int g, int page_pre) -> bool {
         const int st = g % NS;
         uint8_t* ks = kv_s + st * KVB;
         uint8_t* vs = kv_s + (NS + st) * KVB;
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         int row0 = 0;
         if (ctx && lane < 8) {  // lane p: page p of the chunk
           const int pi = min(c * 8 + lane, a.pages_per_req - 1);
-          int page = a.page_table[x.b * a.pages_per_req + pi];
+          int page = page_pre >= 0 ? page_pre : a.page_table[x.b * a.pages_per_req + pi];
           if (page < 0 || page >= a.num_pages) {
             atomicOr(a.status, VSD_DEV_BAD_PAGE);
             page = 0;
@@ -262,10 +262,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int pre = 0;
       if (static_cast<int>(blockIdx.x) < total) {
         const Item x = decode(blockIdx.x);
-        while (pre < min(x.n, NS) && x.c_begin + pre < x.n_ctx) {
-          issue(x, pre, pre);  // g < NS: no slot waits
-          ++pre;
-        }
+        int npre = 0;
+        while (npre < min(x.n, NS) && x.c_begin + npre < x.n_ctx) ++npre;
+        // the page-table entries of all of these chunks in one round trip (lane 8 i + p: page p of chunk i)
+        int pg = -1;
+        if (lane < 8 * npre)
+          pg = a.page_table[x.b * a.pages_per_req + min((x.c_begin + lane / 8) * 8 + lane % 8, a.pages_per_req - 1)];
+        for (; pre < npre; ++pre) issue(x, pre, pre, __shfl_sync(0xFFFFFFFFu, pg, (pre * 8 + lane) & 31));  // g < NS: no slot waits
       }
       pdl_wait();  // q tiles and the block's K/V come from the QKV kernel
       if (lane == 0) trace_point(a.trace, 2);
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         for (int i = 0; i < x.n; ++i, ++g) {
           if (g < pre) continue;  // fetched before the dependency wait
-          if (!issue(x, i, g)) {
+          if (!issue(x, i, g, -1)) {
             ok = false;
             break;
           }
@@ -510,109 +513,96 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         named_bar_sync(1, 256);
       }
       if (hf == 0) __stcg(reinterpret_cast<float2*>(a.part_ml) + split_idx * 128 + r, make_float2(m, lt));
+      // Every split of the pair then merges a slice of the pair's rows, once
+      // all of the pair's partials are written.  The splits of a pair run at
+      // the same time: with more than one split per request every CTA has at
+      // most one item (the split size is chosen so), and the grid (at most
+      // one CTA per SM) is resident as a whole once the previous kernel's
+      // CTAs have left.  The wait is bounded all the same.
       __threadfence();
       named_bar_sync(1, 256);
-      if (threadIdx.x == 0) *last_flag = (atomicAdd(&a.counters[pair], 1) == x.n_splits - 1) ? 1 : 0;
-      named_bar_sync(1, 256);
-      const bool last = *last_flag;
-      named_bar_sync(1, 256);  // everyone read the flag before the next item may set it
-      if (!last) continue;
-      __threadfence();
-      // merge of the pair's splits (split order fixed: deterministic).
-      // Per row: mm = max of the split maxima, 1 / sum of the rescaled sums.
-      const size_t first = pair * a.max_splits;
-      const float2* pml = reinterpret_cast<const float2*>(a.part_ml) + first * 128;
-      float* row_mm = xstat;         // [128]
-      float* row_inv = xstat + 128;  // [128]
-      if (hf == 0) {  // row statistics in one pass (running max, rescaled sum), eight splits in flight
-        float mm = -INFINITY, ls = 0.0f;
-        for (int s0 = 0; s0 < x.n_splits; s0 += 8) {
-          float2 ml[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            ml[j] = s0 + j < x.n_splits ? __ldcg(pml + (s0 + j) * 128 + r) : make_float2(-INFINITY, 0.0f);
-          float bm = mm;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) bm = fmaxf(bm, ml[j].x);
-          const float bu = bm == -INFINITY ? 0.0f : bm;
-          ls = ls * ex2(mm - bu);  // 0 while mm = -inf
-#pragma unroll
-          for (int j = 0; j < 8; ++j) ls += ml[j].y * ex2(ml[j].x - bu);
-          mm = bm;
+      int* arrived = a.counters + pair;
+      int* departed = a.counters + static_cast<size_t>(a.batch_cap) * a.n_kv + pair;
+      if (threadIdx.x == 0) {
+        atomicAdd(arrived, 1);
+        const long long t0 = cycles();
+        while (ld_acquire_gpu(arrived) < x.n_splits) {
+          __nanosleep(64);
+          if (cycles() - t0 > kWaitLimitCycles) {
+            atomicOr(a.status, VSD_DEV_TIMEOUT);
+            break;
+          }
         }
-        if (mm == -INFINITY) mm = 0.0f;
-        row_mm[r] = mm;
-        row_inv[r] = ls > 0.0f ? 1.0f / ls : 0.0f;
       }
       named_bar_sync(1, 256);
-      // Every thread owns PER float4 of each half tile (coalesced across the
-      // warp) and sums them over the splits, two splits' loads in flight.
-      constexpr int PER = NF4 / 256;
-      const float4* pbase = reinterpret_cast<const float4*>(a.part_o + first * 128 * HD);
-      float4 acc4[2][PER];
-      int rows[PER];
-      float mrow[PER];
+      // rows [r0, r1) of the valid rows; per row and float4 of the output:
+      // running maximum over the splits and the rescaled sums of l and O,
+      // eight splits' loads in flight (split order fixed: deterministic)
+      {
+        const int r0 = x.split * a.rows_valid / x.n_splits, r1 = (x.split + 1) * a.rows_valid / x.n_splits;
+        constexpr int Q = HD / 4;  // float4 per row
+        const size_t first = pair * a.max_splits;
+        const float2* pml = reinterpret_cast<const float2*>(a.part_ml) + first * 128;
+        const float4* pbase = reinterpret_cast<const float4*>(a.part_o + first * 128 * HD);
+        for (int idx = threadIdx.x; idx < (r1 - r0) * Q; idx += 256) {
+          const int row = r0 + idx / Q, d4 = idx % Q;
+          const int hh = d4 / Q4, w4 = d4 % Q4;
+          const float4* po_row = pbase + hh * NF4 + row * Q4 + w4;
+          float mm = -INFINITY, ls = 0.0f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int s0 = 0; s0 < x.n_splits; s0 += 8) {
+            float2 ml[8];
+            float4 ov[8];
 #pragma unroll
-      for (int k = 0; k < PER; ++k) {
-        acc4[0][k] = acc4[1][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        rows[k] = (threadIdx.x + 256 * k) / Q4;
-        mrow[k] = row_mm[rows[k]];
-      }
-      for (int s0 = 0; s0 < x.n_splits; s0 += 2) {
-        float4 xv[2][2][PER];
-        float mv[2][PER];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int sp = min(s0 + u, x.n_splits - 1);
-          const float4* ps = pbase + static_cast<size_t>(sp) * 2 * NF4;
-#pragma unroll
-          for (int k = 0; k < PER; ++k) {
-            xv[u][0][k] = __ldcg(ps + threadIdx.x + 256 * k);
-            xv[u][1][k] = __ldcg(ps + NF4 + threadIdx.x + 256 * k);
-            mv[u][k] = __ldcg(pml + sp * 128 + rows[k]).x;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (s0 + u >= x.n_splits) break;
-#pragma unroll
-          for (int k = 0; k < PER; ++k) {
-            const float w = ex2(mv[u][k] - mrow[k]);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              acc4[hh][k].x += xv[u][hh][k].x * w;
-              acc4[hh][k].y += xv[u][hh][k].y * w;
-              acc4[hh][k].z += xv[u][hh][k].z * w;
-              acc4[hh][k].w += xv[u][hh][k].w * w;
+            for (int j = 0; j < 8; ++j) {
+              const bool in = s0 + j < x.n_splits;
+              ml[j] = in ? __ldcg(pml + (s0 + j) * 128 + row) : make_float2(-INFINITY, 0.0f);
+              ov[j] = in ? __ldcg(po_row + static_cast<size_t>(s0 + j) * 2 * NF4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-          }
-        }
-      }
+            float bm = mm;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+            for (int j = 0; j < 8; ++j) bm = fmaxf(bm, ml[j].x);
+            const float bu = bm == -INFINITY ? 0.0f : bm;
+            const float sc = ex2(mm - bu);  // 0 while mm = -inf
+            ls *= sc;
+            acc.x *= sc;
+            acc.y *= sc;
+            acc.z *= sc;
+            acc.w *= sc;
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-          const int row = rows[k];
-          if (row < a.rows_valid) {
-            const int d = hh * HH + ((threadIdx.x + 256 * k) % Q4) * 4;
-            const float inv = row_inv[row];
-            __half* o_dst = a.out + (static_cast<size_t>(x.b) * kRows + row / a.group) * (a.n_q * HD) +
-                            (x.h * a.group + row % a.group) * HD + d;
-            const float y[4] = {acc4[hh][k].x * inv, acc4[hh][k].y * inv, acc4[hh][k].z * inv, acc4[hh][k].w * inv};
-            uint32_t hw[2], lw[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              hw[e] = f32x2_to_f16x2(y[2 * e], y[2 * e + 1]);
-              const __half2 h2 = *reinterpret_cast<const __half2*>(&hw[e]);
-              lw[e] = f32x2_to_f16x2(y[2 * e] - __low2float(h2), y[2 * e + 1] - __high2float(h2));
+            for (int j = 0; j < 8; ++j) {
+              const float w = ex2(ml[j].x - bu);
+              ls += ml[j].y * w;
+              acc.x += ov[j].x * w;
+              acc.y += ov[j].y * w;
+              acc.z += ov[j].z * w;
+              acc.w += ov[j].w * w;
             }
-            *reinterpret_cast<uint2*>(o_dst) = make_uint2(hw[0], hw[1]);
-            if (a.out_lo) *reinterpret_cast<uint2*>(o_dst + a.out_lo) = make_uint2(lw[0], lw[1]);
+            mm = bm;
           }
+          const float inv = ls > 0.0f ? 1.0f / ls : 0.0f;
+          const int d = hh * HH + w4 * 4;
+          __half* o_dst = a.out + (static_cast<size_t>(x.b) * kRows + row / a.group) * (a.n_q * HD) +
+                          (x.h * a.group + row % a.group) * HD + d;
+          const float y[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+          uint32_t hw[2], lw[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            hw[e] = f32x2_to_f16x2(y[2 * e], y[2 * e + 1]);
+            const __half2 h2 = *reinterpret_cast<const __half2*>(&hw[e]);
+            lw[e] = f32x2_to_f16x2(y[2 * e] - __low2float(h2), y[2 * e + 1] - __high2float(h2));
+          }
+          *reinterpret_cast<uint2*>(o_dst) = make_uint2(hw[0], hw[1]);
+          if (a.out_lo) *reinterpret_cast<uint2*>(o_dst + a.out_lo) = make_uint2(lw[0], lw[1]);
         }
       }
-      named_bar_sync(1, 256);  // row statistics read by all before the next item reuses them
-      if (threadIdx.x == 0) a.counters[pair] = 0;
+      // the last split to finish resets the pair's counters for the next launch
+      // (every split has passed its wait by then)
+      named_bar_sync(1, 256);
+      if (threadIdx.x == 0 && atomicAdd(departed, 1) == x.n_splits - 1) {
+        *arrived = 0;
+        *departed = 0;
+      }
       if (threadIdx.x == 0 && ic == 0) trace_point(a.trace, 7);
     }
   }

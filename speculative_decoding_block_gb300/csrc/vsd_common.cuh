@@ -35,6 +35,11 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 __device__ __forceinline__ long long cycles() { return clock64(); }
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // ------------------------------------------------------------------ tracing
 // Optional per-CTA phase stamps (off when buf == nullptr): a plain store of
