@@ -826,7 +826,7 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     e.hidden0 = hidden;
     e.status = kv->status;
     e.trace = next_trace(kv);
-    TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), e)));
+    TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), false, e)));
   }
   const size_t layer_scratch = static_cast<size_t>(kv->max_batch) * c.n_kv * 32 * c.head_dim;
   for (int l = 0; l < c.layers; ++l) {
@@ -873,7 +873,7 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
   }
   CommitArgs ca = commit_args(kv, drafts, seq_lens, pending, accepted, out_tokens);
   ca.trace = next_trace(kv);
-  TIMED(VSD_K_COMMIT, CK(launch_ex(accept_commit_kernel, dim3(B, c.layers), dim3(256), 0, st, use_pdl(st), ca)));
+  TIMED(VSD_K_COMMIT, CK(launch_ex(accept_commit_kernel, dim3(B, c.layers), dim3(256), 0, st, use_pdl(st), false, ca)));
 #undef TIMED
   return VSD_OK;
 }
@@ -1112,7 +1112,7 @@ vsd_status vsd_accept_commit(const vsd_model* m, vsd_kv* kv, int32_t B, const fl
   validate_requests_kernel<<<ceil_div(B, 128), 128, 0, st>>>(seq_lens, pending, B, c.vocab, kv->max_tokens,
                                                             kv->ctx_len, kv->req_ok, kv->status);
   CommitArgs ca = commit_args(kv, drafts, seq_lens, pending, accepted, out_tokens);
-  CK(launch_ex(accept_commit_kernel, dim3(B, c.layers), dim3(256), 0, st, false, ca));
+  CK(launch_ex(accept_commit_kernel, dim3(B, c.layers), dim3(256), 0, st, false, false, ca));
   return VSD_OK;
 }
 

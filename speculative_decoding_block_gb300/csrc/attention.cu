@@ -16,7 +16,9 @@ static cudaError_t launch_hd(const CUtensorMap& tm_q, const CUtensorMap& tm_kc, 
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_ex(attn_kernel<HD>, grid, dim3(kAttnThreads), smem, st, pdl, tm_q, tm_kc, tm_vc, tm_kn, tm_vn, a);
+  // cooperative: the splits of a request wait for one another before merging
+  return launch_ex(attn_kernel<HD>, grid, dim3(kAttnThreads), smem, st, pdl, true, tm_q, tm_kc, tm_vc, tm_kn, tm_vn,
+                   a);
 }
 
 cudaError_t launch_attn(int hd, const CUtensorMap& tm_q, const CUtensorMap& tm_kc, const CUtensorMap& tm_vc,

@@ -35,7 +35,7 @@ static cudaError_t launch_one(const CUtensorMap& tm_act, const CUtensorMap& tm_w
     return launch_ex_cluster(gemm_kernel<WF, EPI>, dim3(grid), dim3(kGemmThreads), smem, a.cs, st, pdl, tm_act,
                              tm_w, a);
   }
-  return launch_ex(gemm_kernel<WF, EPI>, dim3(grid), dim3(kGemmThreads), smem, st, pdl, tm_act, tm_w, a);
+  return launch_ex(gemm_kernel<WF, EPI>, dim3(grid), dim3(kGemmThreads), smem, st, pdl, false, tm_act, tm_w, a);
 }
 
 template <int WF>
