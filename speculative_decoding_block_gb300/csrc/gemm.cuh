@@ -774,6 +774,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (cs > 1 && acc > 0 && !mbar_wait_cluster(rfree, (acc - 1) & 1, abort_flag, a.status)) break;
         if (!mbar_wait(&tfull[ab], (acc >> 1) & 1, abort_flag, a.status, kSleepLongWaitNs)) break;
         if (et2 == 0 && acc == 0) trace_point(a.trace, 6);
+        if constexpr (EPI == EPI_RESID) {
+          // the residual rows this thread updates: into L1 now, read after the reduction
+          const int prow = tile * kTileN + row;
+          if (prow < a.n_rows)
+            for (int g = rank + cs * half; g < groups; g += cs * n_sets)
+              for (int i = 0; i < 16; ++i) {
+                const int tok = tt * a.n_tok + g * 16 + i;
+                if (tok < a.m_tokens) prefetch_l1(a.out_f32 + static_cast<size_t>(tok) * a.ld_out + prow);
+              }
+        }
         tc_fence_after();
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(we * 32) << 16) + static_cast<uint32_t>(ab * acc_w);
@@ -801,9 +811,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_before();
           mbar_arrive(&tempty[ab]);
           named_bar_sync(1, ep_n);
-          if (et2 == 0) {
+          if (et2 < cs) {  // one thread per peer: the cluster-scope fence and remote arrive cost ~0.2-0.7 us each
             fence_acq_rel_cluster();
-            for (int p = 0; p < cs; ++p) mbar_arrive_remote(mapa_shared(smem_u32(rfull), p));
+            mbar_arrive_remote(mapa_shared(smem_u32(rfull), et2));
           }
           if (!mbar_wait_cluster(rfull, acc & 1, abort_flag, a.status)) break;
           if (et2 == 0 && acc == 0) trace_point(a.trace, 7);
@@ -864,9 +874,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         named_bar_sync(1, ep_n);
         if (et2 == 0 && acc == 0) trace_point(a.trace, 9);
-        if (cs > 1 && et2 == 0) {
+        if (cs > 1 && et2 < cs) {
           fence_acq_rel_cluster();
-          for (int p = 0; p < cs; ++p) mbar_arrive_remote(mapa_shared(smem_u32(rfree), p));
+          mbar_arrive_remote(mapa_shared(smem_u32(rfree), et2));
         }
         if constexpr (EPI == EPI_RESID) {
           for (int c = et2; c < a.n_tok; c += ep_n) {

@@ -251,6 +251,9 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (tensor cores, TMA).
 // Hint: bring the 128-byte line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
