@@ -146,11 +146,18 @@ def forward_block(m: Model, kc, vc, ctx_len: int, tokens, keep_hidden=False):
     BF16-rounded) and, if asked, hidden (list of [R, H], entry 0 = embeddings,
     entry l+1 = residual stream after layer l).
     """
-    s = m.shape
     tokens = np.asarray(tokens, np.int64)
-    R = len(tokens)
-    pos = ctx_len + np.arange(R)
-    h = m.embed[tokens].copy()
+    return forward_rows(m, kc, vc, ctx_len, m.embed[tokens], ctx_len + np.arange(len(tokens)), keep_hidden)
+
+
+def forward_rows(m: Model, kc, vc, ctx_len: int, rows, pos, keep_hidden=False):
+    """forward_block on given input rows [R, H] (the residual stream before
+    layer 0) at given positions pos [R]; block row j sees the ctx_len cached
+    rows and block rows 0..j."""
+    s = m.shape
+    h = np.array(rows, np.float64)
+    R = h.shape[0]
+    pos = np.asarray(pos, np.int64)
     hidden = [h.copy()] if keep_hidden else None
     new_k, new_v = [], []
     for l in range(s.layers):
@@ -258,6 +265,36 @@ def verify_step(m: Model, st: RequestState, drafts, keep_hidden=False) -> dict:
     st.commit(r["new_k"], r["new_v"], a + 1)
     st.pending = int(g[a])
     srt = np.sort(r["logits"], axis=-1)
-    return {"accepted": a, "out": out, "greedy": g, "logits": r["logits"],
-            "top2_gap": srt[:, -1] - srt[:, -2], "new_k": r["new_k"],
-            "new_v": r["new_v"], "hidden": r["hidden"], "ctx_len": L}
+    res = {"accepted": a, "out": out, "greedy": g, "logits": r["logits"],
+           "top2_gap": srt[:, -1] - srt[:, -2], "new_k": r["new_k"],
+           "new_v": r["new_v"], "hidden": r["hidden"], "ctx_len": L}
+    if keep_hidden:  # the drafter's next conditioning row: last layer's residual at row a
+        res["anchor"] = r["hidden"][-1][a].copy()
+    return res
+
+
+# ------------------------------------------------------------------ drafting
+def draft_step(d: Model, anchor, seq_len: int, mask_token: int, keep_hidden=False) -> dict:
+    """One pass of the block drafter over one request.
+
+    The pages: the DFlash drafter is a small transformer (5 layers,
+    initialised from the target's last five decoder layers) that takes the
+    target's hidden state at the anchor and proposes a whole block of 16
+    tokens in one forward pass -- HunyuanOCR-1.5 summary, section one; one
+    drafter pass per drafted block -- "The Inference Stack Behind OCRia",
+    speculative-decoding section.  Readings (the pages give no layer-level
+    detail): input rows [anchor, E[mask] x 16] at positions seq_len ..
+    seq_len+16, where anchor is the target's residual row (before the final
+    norm) at the last accepted position; the drafter's layers are the
+    target's kind of decoder layer; attention is causal among the 17 rows
+    with no cache; draft j = argmax of row 1+j of the head (ties to the
+    lowest id).  Returns drafts [16], logits [17, V] and, if asked, hidden.
+    """
+    s = d.shape
+    anchor = np.asarray(anchor, np.float64).reshape(1, s.hidden)
+    rows = np.concatenate([anchor, np.repeat(d.embed[[int(mask_token)]], BLOCK, axis=0)], axis=0)
+    empty = [np.zeros((0, s.n_kv, s.head_dim)) for _ in range(s.layers)]
+    r = forward_rows(d, empty, empty, 0, rows, seq_len + np.arange(BLOCK + 1), keep_hidden=keep_hidden)
+    srt = np.sort(r["logits"], axis=-1)
+    return {"drafts": greedy(r["logits"][1:]), "logits": r["logits"], "hidden": r["hidden"],
+            "top2_gap": srt[:, -1] - srt[:, -2]}

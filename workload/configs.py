@@ -18,7 +18,7 @@ Sources for the numbers:
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 BLOCK = 16          # drafted tokens per request per step
 ROWS = BLOCK + 1    # rows per request: the pending token plus the drafts
@@ -126,3 +126,17 @@ def linear_shapes(s: ModelShape) -> dict:
         "wu": (s.ffn, s.hidden, s.mlp_fmt),
         "wd": (s.hidden, s.ffn, s.mlp_fmt),
     }
+
+
+# ------------------------------------------------------------------ drafter
+DRAFTER_LAYERS = 5  # the block drafter copies the target's last five decoder layers
+
+
+def drafter_shape(s: ModelShape, layers: int = DRAFTER_LAYERS) -> ModelShape:
+    """The drafter: the target's layer shapes and formats, its last `layers` layers."""
+    return replace(s, name=s.name + "-drafter", layers=min(layers, s.layers))
+
+
+def mask_token(s: ModelShape) -> int:
+    """Token id whose embedding fills the drafter's 16 block rows (the last id)."""
+    return s.vocab - 1

@@ -142,3 +142,18 @@ def page_table(w: Workload, pages_per_req: int) -> np.ndarray:
     if w.paged:
         perm = _rng("pages", w.seed).permutation(n).astype(np.int32)
     return perm.reshape(w.batch, pages_per_req)
+
+
+def drafter_master(master: dict, target_layers: int, drafter_layers: int) -> dict:
+    """The drafter's master weights: the target's embedding (and head) and its last layers, renumbered."""
+    first = target_layers - drafter_layers
+    out = {"embed": master["embed"], "layers": {i: master["layers"][first + i] for i in range(drafter_layers)}}
+    if "lm_head" in master:
+        out["lm_head"] = master["lm_head"]
+    return out
+
+
+def anchor_rows(hidden: int, batch: int, seed: int) -> torch.Tensor:
+    """Synthetic drafter anchors [batch, hidden] float32: unit-RMS Gaussian rows (a residual row's scale)."""
+    r = _rng("anchor", seed, hidden, batch)
+    return torch.from_numpy(r.standard_normal((batch, hidden)).astype(np.float32))
