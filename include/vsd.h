@@ -240,6 +240,51 @@ vsd_status vsd_verify_step_profiled(const vsd_model* m, vsd_kv* kv, int32_t batc
                                     int32_t* kinds_host, float* ms_host,
                                     int32_t* n_launches_host, vsd_stream stream);
 
+/* ---------------------------------------------------------------- drafting
+ * One forward pass of a block drafter proposes the next 16 tokens of every
+ * request at once, conditioned on the target's hidden state at the anchor
+ * (the last accepted position) -- HunyuanOCR-1.5 summary, section one (the
+ * DFlash drafter: a 5-layer transformer initialised from the target's last
+ * five decoder layers, input the target's hidden state at the anchor, one
+ * pass per block of 16); "The Inference Stack Behind OCRia", section
+ * "Generate more tokens per target pass" (one drafter pass per block).
+ * Readings where the pages are silent: the drafter has the target's layer
+ * shapes and formats (any number of layers up to the target's); its input
+ * rows are [anchor_b, E[mask], ..., E[mask]] (16 mask rows) at positions
+ * L_b .. L_b+16, where anchor_b is the target's residual row (before the
+ * final norm) at the last accepted position; attention is causal among
+ * these 17 rows and reads no cache; draft j is the argmax (ties to the
+ * lowest id) of row 1+j of the drafter's head.  The drafter's weights are
+ * the caller's (random in this library's tests and benchmark).
+ *
+ * The pass runs in the target cache's scratch (activations, staging K/V of
+ * the first `layers` layers, argmax keys), so it must not overlap a verify
+ * step of the same cache on the GPU; vsd_verify_step leaves the anchor rows
+ * of its requests in the cache for the next draft pass.  */
+
+/* drafter: a model whose shape and formats equal the target's except for a
+ * layer count <= the target's (else VSD_ERR_ARG).
+ *   seq_lens_dev int32 [B]: committed lengths L_b (positions of row 0)
+ *   mask_token   id whose embedding fills rows 1..16
+ *   drafts_dev   int32 [B, 16] out: the proposed tokens (-1 and
+ *                VSD_DEV_BAD_TOKEN in the status word if a row had no key)
+ * Needs L_b + 17 <= max_tokens_per_req (else VSD_DEV_BAD_SEQLEN). */
+vsd_status vsd_draft_step(const vsd_model* drafter, vsd_kv* kv, int32_t batch,
+                          const int32_t* seq_lens_dev, int32_t mask_token,
+                          int32_t* drafts_dev, vsd_stream stream);
+
+/* The same pass with an explicit anchor (anchor_dev float32 [B, hidden], or
+ * NULL for the rows the last verify step left) and optional float32 logits
+ * [B*17, vocab] and residual stream [layers+1, B*17, hidden] outputs. */
+vsd_status vsd_draft_step_debug(const vsd_model* drafter, vsd_kv* kv, int32_t batch,
+                                const int32_t* seq_lens_dev, int32_t mask_token,
+                                const float* anchor_dev, int32_t* drafts_dev,
+                                float* logits_dev, float* hidden_dev, vsd_stream stream);
+
+/* Copies the anchor rows [B, hidden] float32 that the last verify step left
+ * (request b: the residual row of its last accepted position) to dst_dev. */
+vsd_status vsd_kv_get_anchor(const vsd_kv* kv, int32_t batch, float* dst_dev, vsd_stream stream);
+
 /* ---------------------------------------------------------------- components
  * Single kernels of the step, exposed so that each can be checked alone.  */
 

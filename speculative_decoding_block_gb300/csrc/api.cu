@@ -137,6 +137,8 @@ struct vsd_kv {
   float *attn_o = nullptr, *attn_ml = nullptr;
   int* attn_counters = nullptr;
   size_t attn_items_cap = 0;
+  float* anchor = nullptr;  // [max_batch][H] residual row of the last accepted position (drafter input)
+  int* zeros = nullptr;     // [max_batch] zero context lengths (the draft pass reads no cache)
   int* status = nullptr;
   unsigned long long* trace = nullptr;  // optional phase timestamps [launch][CTA][tag]
   int trace_launches = 0;
@@ -649,6 +651,7 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
       (s = dalloc(&kv->k_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
       (s = dalloc(&kv->v_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
       (s = dalloc(&kv->keys, M)) || (s = dalloc(&kv->ctx_len, max_batch)) || (s = dalloc(&kv->req_ok, max_batch)) ||
+      (s = dalloc(&kv->anchor, static_cast<size_t>(max_batch) * H)) || (s = dalloc(&kv->zeros, max_batch)) ||
       (s = dalloc(&kv->status, 1)))
     return cleanup(s);
   if ((s = dalloc(&kv->ssq, static_cast<size_t>(ceil_div(H, kTileN)) * kv->m_alloc))) return cleanup(s);
@@ -680,7 +683,7 @@ void vsd_kv_destroy(vsd_kv* kv) {
   if (!kv) return;
   void* ptrs[] = {kv->k_pool, kv->v_pool, kv->page_table, kv->x, kv->u, kv->act_o, kv->act_a, kv->q_tile,
                   kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->req_ok, kv->ssq, kv->attn_o,
-                  kv->attn_ml, kv->attn_counters, kv->status, kv->trace};
+                  kv->attn_ml, kv->attn_counters, kv->anchor, kv->zeros, kv->status, kv->trace};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete kv;
@@ -790,15 +793,73 @@ struct LaunchTimer {
   }
 };
 
-static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_lens, int* pending, const int* drafts,
-                              int* accepted, int* out_tokens, float* logits, float* hidden, cudaStream_t st,
-                              LaunchTimer* timer = nullptr) {
 #define TIMED(kind, ...)          \
   do {                            \
     if (timer) timer->before(kind); \
     __VA_ARGS__;                  \
     if (timer) timer->after();    \
   } while (0)
+
+// The decoder layers of model m over the M = 17 B rows already in the
+// residual scratch; attention reads attn_lens[b] cached rows per request.
+static vsd_status run_layers(const vsd_model* m, vsd_kv* kv, int B, const int* attn_lens, float* hidden,
+                             cudaStream_t st, LaunchTimer* timer) {
+  const vsd_model_config& c = m->cfg;
+  const int M = kRows * B, H = c.hidden;
+  vsd_status s;
+  const size_t layer_scratch = static_cast<size_t>(kv->max_batch) * c.n_kv * 32 * c.head_dim;
+  for (int l = 0; l < c.layers; ++l) {
+    GemmArgs a{};
+    set_norm_input(a, kv);
+    a.q_tile = kv->q_tile;
+    a.act_lo_rows = kv->m_alloc;
+    a.out_lo = static_cast<size_t>(kv->max_batch) * c.n_kv * 128 * c.head_dim;
+    a.k_new = kv->k_new + l * layer_scratch;
+    a.v_new = kv->v_new + l * layer_scratch;
+    a.ctx_len = kv->ctx_len;
+    a.rope = m->rope;
+    a.n_q = c.n_q;
+    a.n_kv = c.n_kv;
+    a.head_dim = c.head_dim;
+    TIMED(VSD_K_QKV, if ((s = run_gemm(m, m->qkv[l], EPI_QKV, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
+    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, attn_lens, st, true))) return s);
+    GemmArgs r{};
+    r.out_f32 = kv->x;
+    r.ld_out = H;
+    r.x16_out = kv->u;
+    r.act_lo_rows = kv->m_alloc;
+    r.out_lo = static_cast<size_t>(kv->m_alloc) * H;
+    r.ssq_out = kv->ssq;
+    r.ssq_ld = kv->m_alloc;
+    TIMED(VSD_K_O_PROJ, if ((s = run_gemm(m, m->o[l], EPI_RESID, kv->tm_o, M, r, kv->status, st, next_trace(kv)))) return s);
+    GemmArgs g{};
+    set_norm_input(g, kv);
+    g.act_out = kv->act_a;
+    g.act_lo_rows = kv->m_alloc;
+    g.out_lo = static_cast<size_t>(kv->m_alloc) * c.ffn;
+    g.ffn = c.ffn;
+    TIMED(VSD_K_GATE_UP, if ((s = run_gemm(m, m->gu[l], EPI_SILU, kv->tm_u, M, g, kv->status, st, next_trace(kv)))) return s);
+    r.hidden_out = hidden ? hidden + static_cast<size_t>(l + 1) * M * H : nullptr;
+    TIMED(VSD_K_DOWN, if ((s = run_gemm(m, m->down[l], EPI_RESID, kv->tm_a, M, r, kv->status, st, next_trace(kv)))) return s);
+  }
+  return VSD_OK;
+}
+
+// Final RMSNorm + lm_head + per-row argmax keys (kv->keys), logits optional.
+static vsd_status run_head(const vsd_model* m, vsd_kv* kv, int M, float* logits, cudaStream_t st, LaunchTimer* timer) {
+  vsd_status s;
+  GemmArgs a{};
+  set_norm_input(a, kv);
+  a.keys = kv->keys;
+  a.logits = logits;
+  a.act_lo_rows = kv->m_alloc;
+  TIMED(VSD_K_LM_HEAD, if ((s = run_gemm(m, m->lm, EPI_ARGMAX, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
+  return VSD_OK;
+}
+
+static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_lens, int* pending, const int* drafts,
+                              int* accepted, int* out_tokens, float* logits, float* hidden, cudaStream_t st,
+                              LaunchTimer* timer = nullptr) {
   if (!m || !kv || !seq_lens || !pending || !drafts || !accepted || !out_tokens)
     return fail(VSD_ERR_ARG, "NULL pointer");
   if (kv->m != m) return fail(VSD_ERR_ARG, "the cache was created for another model");
@@ -828,55 +889,65 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     e.trace = next_trace(kv);
     TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), false, e)));
   }
-  const size_t layer_scratch = static_cast<size_t>(kv->max_batch) * c.n_kv * 32 * c.head_dim;
-  for (int l = 0; l < c.layers; ++l) {
-    GemmArgs a{};
-    set_norm_input(a, kv);
-    a.q_tile = kv->q_tile;
-    a.act_lo_rows = kv->m_alloc;
-    a.out_lo = static_cast<size_t>(kv->max_batch) * c.n_kv * 128 * c.head_dim;
-    a.k_new = kv->k_new + l * layer_scratch;
-    a.v_new = kv->v_new + l * layer_scratch;
-    a.ctx_len = kv->ctx_len;
-    a.rope = m->rope;
-    a.n_q = c.n_q;
-    a.n_kv = c.n_kv;
-    a.head_dim = c.head_dim;
-    TIMED(VSD_K_QKV, if ((s = run_gemm(m, m->qkv[l], EPI_QKV, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
-    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, seq_lens, st, true))) return s);
-    GemmArgs r{};
-    r.out_f32 = kv->x;
-    r.ld_out = H;
-    r.x16_out = kv->u;
-    r.act_lo_rows = kv->m_alloc;
-    r.out_lo = static_cast<size_t>(kv->m_alloc) * H;
-    r.ssq_out = kv->ssq;
-    r.ssq_ld = kv->m_alloc;
-    TIMED(VSD_K_O_PROJ, if ((s = run_gemm(m, m->o[l], EPI_RESID, kv->tm_o, M, r, kv->status, st, next_trace(kv)))) return s);
-    GemmArgs g{};
-    set_norm_input(g, kv);
-    g.act_out = kv->act_a;
-    g.act_lo_rows = kv->m_alloc;
-    g.out_lo = static_cast<size_t>(kv->m_alloc) * c.ffn;
-    g.ffn = c.ffn;
-    TIMED(VSD_K_GATE_UP, if ((s = run_gemm(m, m->gu[l], EPI_SILU, kv->tm_u, M, g, kv->status, st, next_trace(kv)))) return s);
-    r.hidden_out = hidden ? hidden + static_cast<size_t>(l + 1) * M * H : nullptr;
-    TIMED(VSD_K_DOWN, if ((s = run_gemm(m, m->down[l], EPI_RESID, kv->tm_a, M, r, kv->status, st, next_trace(kv)))) return s);
-  }
-  {
-    GemmArgs a{};
-    set_norm_input(a, kv);
-    a.keys = kv->keys;
-    a.logits = logits;
-    a.act_lo_rows = kv->m_alloc;
-    TIMED(VSD_K_LM_HEAD, if ((s = run_gemm(m, m->lm, EPI_ARGMAX, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
-  }
+  if ((s = run_layers(m, kv, B, seq_lens, hidden, st, timer))) return s;
+  if ((s = run_head(m, kv, M, logits, st, timer))) return s;
   CommitArgs ca = commit_args(kv, drafts, seq_lens, pending, accepted, out_tokens);
+  ca.x = kv->x;  // the drafter's next conditioning row
+  ca.anchor = kv->anchor;
+  ca.hidden = H;
   ca.trace = next_trace(kv);
   TIMED(VSD_K_COMMIT, CK(launch_ex(accept_commit_kernel, dim3(B, c.layers), dim3(256), 0, st, use_pdl(st), false, ca)));
-#undef TIMED
   return VSD_OK;
 }
+
+// One draft pass: the drafter's layers over rows [anchor_b, mask x 16] at
+// positions L_b .. L_b+16 with no cached context (block-causal attention
+// among the 17 rows only), then the head; drafts[b][j] = argmax of row 1+j.
+// Runs in the target cache's scratch (its staging K/V of layers 0..layers-1
+// included), which no other call uses meanwhile on the stream.
+static vsd_status draft_impl(const vsd_model* d, vsd_kv* kv, int B, const int* seq_lens, int mask_token,
+                             const float* anchor, int* drafts, float* logits, float* hidden, cudaStream_t st,
+                             LaunchTimer* timer = nullptr) {
+  if (!d || !kv || !seq_lens || !drafts) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (B < 1 || B > kv->max_batch) return fail(VSD_ERR_ARG, "batch %d outside [1, %d]", B, kv->max_batch);
+  const vsd_model_config& c = d->cfg;
+  const vsd_model_config& t = kv->m->cfg;
+  if (c.hidden != t.hidden || c.n_q != t.n_q || c.n_kv != t.n_kv || c.head_dim != t.head_dim || c.ffn != t.ffn ||
+      c.vocab != t.vocab || c.layers > t.layers || c.attn_fmt != t.attn_fmt || c.mlp_fmt != t.mlp_fmt)
+    return fail(VSD_ERR_ARG, "the drafter's shape does not fit the target cache's scratch");
+  if (mask_token < 0 || mask_token >= c.vocab) return fail(VSD_ERR_ARG, "mask token %d outside the vocabulary", mask_token);
+  const int M = kRows * B, H = c.hidden;
+  vsd_status s;
+  {
+    EmbedArgs e{};
+    e.embed = d->embed;
+    e.vocab = c.vocab;
+    e.hidden = H;
+    e.seq_lens = seq_lens;
+    e.max_tokens = kv->max_tokens;
+    e.x = kv->x;
+    e.x16 = kv->u;
+    e.x16_lo = static_cast<size_t>(kv->m_alloc) * H;
+    e.ssq = kv->ssq;
+    e.ssq_ld = kv->m_alloc;
+    e.ctx_len = kv->ctx_len;  // positions L_b + j for RoPE
+    e.req_ok = kv->req_ok;
+    e.keys = kv->keys;
+    e.hidden0 = hidden;
+    e.anchor = anchor ? anchor : kv->anchor;
+    e.mask_token = mask_token;
+    e.status = kv->status;
+    e.trace = next_trace(kv);
+    TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), false, e)));
+  }
+  if ((s = run_layers(d, kv, B, kv->zeros, hidden, st, timer))) return s;
+  if ((s = run_head(d, kv, M, logits, st, timer))) return s;
+  TIMED(VSD_K_COMMIT, CK(launch_ex(draft_pick_kernel, dim3(ceil_div(B * kBlock, 128)), dim3(128), 0, st, use_pdl(st),
+                                   false, static_cast<const unsigned long long*>(kv->keys), B, c.vocab, drafts,
+                                   kv->status)));
+  return VSD_OK;
+}
+#undef TIMED
 
 vsd_status vsd_verify_step_profiled(const vsd_model* m, vsd_kv* kv, int32_t batch, int32_t* seq_lens,
                                     int32_t* pending, const int32_t* drafts, int32_t* accepted,
@@ -909,6 +980,27 @@ vsd_status vsd_verify_step_debug(const vsd_model* m, vsd_kv* kv, int32_t batch, 
                                  float* hidden, vsd_stream stream) {
   return verify_impl(m, kv, batch, seq_lens, pending, drafts, accepted, out_tokens, logits, hidden,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+vsd_status vsd_draft_step(const vsd_model* drafter, vsd_kv* kv, int32_t batch, const int32_t* seq_lens,
+                          int32_t mask_token, int32_t* drafts, vsd_stream stream) {
+  return draft_impl(drafter, kv, batch, seq_lens, mask_token, nullptr, drafts, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+vsd_status vsd_draft_step_debug(const vsd_model* drafter, vsd_kv* kv, int32_t batch, const int32_t* seq_lens,
+                                int32_t mask_token, const float* anchor, int32_t* drafts, float* logits,
+                                float* hidden, vsd_stream stream) {
+  return draft_impl(drafter, kv, batch, seq_lens, mask_token, anchor, drafts, logits, hidden,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+vsd_status vsd_kv_get_anchor(const vsd_kv* kv, int32_t batch, float* dst, vsd_stream stream) {
+  if (!kv || !dst) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (batch < 1 || batch > kv->max_batch) return fail(VSD_ERR_ARG, "batch %d outside [1, %d]", batch, kv->max_batch);
+  CK(cudaMemcpyAsync(dst, kv->anchor, static_cast<size_t>(batch) * kv->m->cfg.hidden * sizeof(float),
+                     cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
+  return VSD_OK;
 }
 
 // ------------------------------------------------------------------ components

@@ -34,6 +34,11 @@ struct EmbedArgs {
   int* req_ok;            // [B] 1 if seq_len and pending token are valid
   unsigned long long* keys;  // [M] argmax keys of the step, cleared here
   float* hidden0;         // optional [M][H]
+  // draft mode (anchor != nullptr): row 0 of request b is anchor[b] (the
+  // target's last residual row, fp32 [B][H]) and rows 1..16 embed mask_token;
+  // pending and drafts are not read
+  const float* anchor;
+  int mask_token;
   int* status;
   Trace trace;
 };
@@ -51,7 +56,8 @@ __global__ void __launch_bounds__(128) embed_kernel(const EmbedArgs a) {
   if (threadIdx.x == 0) trace_start(a.trace);
   const int row = blockIdx.x, b = row / kRows, j = row % kRows;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  int tok = j == 0 ? a.pending[b] : a.drafts[b * kBlock + j - 1];
+  const bool draft = a.anchor != nullptr;
+  int tok = draft ? a.mask_token : (j == 0 ? a.pending[b] : a.drafts[b * kBlock + j - 1]);
   const bool tok_ok = tok >= 0 && tok < a.vocab;
   if (!tok_ok) {
     if (t == 0) atomicOr(a.status, VSD_DEV_BAD_TOKEN);
@@ -68,6 +74,7 @@ __global__ void __launch_bounds__(128) embed_kernel(const EmbedArgs a) {
     }
   }
   const uint16_t* e = a.embed + static_cast<size_t>(tok) * a.hidden;
+  const float* anchor_row = (draft && j == 0) ? a.anchor + static_cast<size_t>(b) * a.hidden : nullptr;
   const size_t o = static_cast<size_t>(row) * a.hidden;
   const int slices = (a.hidden + 127) / 128;
   for (int k0 = 0; k0 < slices; k0 += 8) {
@@ -75,7 +82,9 @@ __global__ void __launch_bounds__(128) embed_kernel(const EmbedArgs a) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {  // loads first
       const int i = (k0 + k) * 128 + t;
-      v[k] = (k0 + k < slices && i < a.hidden) ? __uint_as_float(static_cast<uint32_t>(e[i]) << 16) : 0.0f;
+      v[k] = (k0 + k < slices && i < a.hidden)
+                 ? (anchor_row ? anchor_row[i] : __uint_as_float(static_cast<uint32_t>(e[i]) << 16))
+                 : 0.0f;
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -127,6 +136,11 @@ struct CommitArgs {
   const __nv_bfloat16* v_new;
   __nv_bfloat16* k_pool;          // [layers][pages][n_kv][16][hd]
   __nv_bfloat16* v_pool;
+  // optional: the residual row of the last accepted position, x[b*17 + a],
+  // copied to anchor[b] ([B][hidden] fp32) -- the drafter's conditioning input
+  const float* x;
+  float* anchor;
+  int hidden;
   int* status;
   Trace trace;
 };
@@ -212,7 +226,28 @@ __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) 
       a.seq_lens[b] = L + acc + 1;
       a.pending[b] = g[acc];
     }
+    if (a.anchor) {
+      const float* src = a.x + (static_cast<size_t>(b) * kRows + acc) * a.hidden;
+      for (int i = t; i < a.hidden; i += blockDim.x) a.anchor[static_cast<size_t>(b) * a.hidden + i] = src[i];
+    }
   }
+}
+
+// Drafts from the argmax keys of a draft pass: drafts[b][j] = token of row
+// b*17 + 1 + j (j = 0..15), -1 if the row has no key.
+__global__ void draft_pick_kernel(const unsigned long long* keys, int B, int vocab, int* drafts, int* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * kBlock) return;
+  const int b = i / kBlock, j = i % kBlock;
+  const unsigned long long k = keys[b * kRows + 1 + j];
+  int tok = k ? static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull)) : -1;
+  if (tok < 0 || tok >= vocab) {
+    atomicOr(status, VSD_DEV_BAD_TOKEN);
+    tok = -1;
+  }
+  drafts[i] = tok;
 }
 
 // Argmax keys of given float32 logits (component entry point): one CTA per row.
