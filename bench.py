@@ -35,7 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workload import ROWS, WORKLOADS, gen, linear_shapes  # noqa: E402
+from workload import ROWS, WORKLOADS, drafter_shape, gen, linear_shapes, mask_token  # noqa: E402
 
 DEFAULT_WORKLOAD = "0.5b_mixed_b8_ctx512-4096"
 METRIC = "verified tokens/sec per GB300, 0.5B target, block 16; verify-step HBM % peak"
@@ -83,6 +83,13 @@ def step_bytes(shape, lens, accepted) -> int:
     commit = int(np.sum(np.asarray(accepted) + 1)) * kv_row
     io = B * (16 * 4 + 8) + B * (4 + 17 * 4 + 8)
     return w + emb + kv + commit + io
+
+
+def draft_pass_bytes(shape, B: int) -> int:
+    """Algorithmic bytes of one drafter pass: its layers' weights once, the head, 17*B rows in, drafts out."""
+    ds = drafter_shape(shape)
+    w = sum(weight_bytes(ds, n) for n in linear_shapes(ds)) * ds.layers + shape.vocab * shape.hidden * 2
+    return w + ROWS * B * shape.hidden * 2 + B * shape.hidden * 4 + B * (4 + 16 * 4)
 
 
 def step_flops(shape, lens) -> float:
@@ -272,6 +279,10 @@ def run_gpu(args, rank: int, world: int):
     max_tok = w.max_tokens_per_req()
     master = gen.master_weights(shape, w.seed)
     model, _ = build_target(shape, master, max_positions=max_tok)
+    drafter = None
+    if not args.no_draft:
+        ds = drafter_shape(shape)
+        drafter, _ = build_target(ds, gen.drafter_master(master, shape.layers, ds.layers), max_positions=max_tok)
     del master
     Bn = w.batch
     kv = B.vsd_kv_create(model, Bn, max_tok)
@@ -460,6 +471,9 @@ def run_gpu(args, rank: int, world: int):
         "gpu_launches": len(prof),
         "clocks": clk.summary(t_region0, t_region1),
     }
+    if drafter is not None:
+        result["draft"] = time_draft(B, model, drafter, kv, shape, Bn, seq, pen, drafts, acc, out, seq0, pend0, g,
+                                     flush, stream, args)
     if oracle_handle is not None:
         r = finish_oracle(oracle_handle)
         if r and "tokens" in r:
@@ -473,6 +487,58 @@ def run_gpu(args, rank: int, world: int):
                                       "error": (r or {}).get("error", "no result")}
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def time_draft(B, model, drafter, kv, shape, Bn, seq, pen, drafts, acc, out, seq0, pend0, g_verify, flush, stream,
+               args):
+    """The drafter pass alone (graph replay, L2 flushed between passes) and one
+    speculative iteration (verify step, then a draft pass on its anchor rows)."""
+    import torch
+    mask = mask_token(shape)
+    dout = torch.empty((Bn, 16), dtype=torch.int32, device="cuda")
+    # anchor rows and lengths of a committed verify step
+    with torch.cuda.stream(stream):
+        seq.copy_(seq0)
+        pen.copy_(pend0)
+        g_verify.replay()
+    stream.synchronize()
+    seq_after = seq.clone()
+    gd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd, stream=stream):
+        B.vsd_draft_step(drafter, kv, Bn, seq_after, mask, dout, stream=stream)
+    gi = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gi, stream=stream):
+        B.vsd_verify_step(model, kv, Bn, seq, pen, drafts, acc, out, stream=stream)
+        B.vsd_draft_step(drafter, kv, Bn, seq, mask, dout, stream=stream)
+
+    def timed(graph, reset):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                if reset:
+                    seq.copy_(seq0)
+                    pen.copy_(pend0)
+                flush.fill_(1.0)
+                if i >= args.warmup:
+                    ev[i - args.warmup][0].record(stream)
+                graph.replay()
+                if i >= args.warmup:
+                    ev[i - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    ms_draft = timed(gd, False)
+    ms_iter = timed(gi, True)
+    if B.vsd_get_device_status(kv) != 0:
+        raise RuntimeError("draft pass reported a device error")
+    pb = draft_pass_bytes(shape, Bn)
+    hbm = peaks()[0]
+    return {"layers": drafter_shape(shape).layers, "weights": "the target's last layers (random init), its head",
+            "mask_token": mask, "ms_per_pass": round(ms_draft, 4),
+            "drafted_tokens_per_s": round(Bn * 16 / (ms_draft * 1e-3), 1),
+            "pass_bytes": pb, "pass_hbm_frac": round(pb / (ms_draft * 1e-3) / 1e9 / hbm, 4),
+            "ms_per_iteration": round(ms_iter, 4),
+            "iteration": "one CUDA graph: verify step, then a draft pass on its anchor rows"}
 
 
 # ------------------------------------------------------------------ reference arm
@@ -519,11 +585,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)  # ~0.6 s timed: clock samples land inside
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-draft", action="store_true", help="skip the drafter-pass measurement")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of timed oracle work")
     args = ap.parse_args()
     if args.warmup < 3:
