@@ -538,9 +538,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   };
-  // weight expansion of the CTA's k tiles by NT threads (t = 0..NT-1); in the
-  // wide mode warps 0-3 compute the token scales once the first expanded
-  // tiles are ready, and publish them on named barrier 3
+  // weight expansion of the CTA's k tiles: NT = 256 chunk slots, by 256
+  // threads (wide mode) or by 128 threads taking slots t and t + 128 (one
+  // instantiation keeps the kernel's code small); in the wide mode warps 0-3
+  // compute the token scales once the first expanded tiles are ready, and
+  // publish them on named barrier 3
   auto expand_all = [&](auto nt_const, int t) {
     constexpr int NT = decltype(nt_const)::value;
     bool scales_done = !(wide && has_item && warp < 4);
@@ -558,6 +560,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (i >= DA && !mbar_wait(&cempty[c], cp ^ 1u, abort_flag, a.status)) break;
       if (t == 0 && i == 0) trace_point(a.trace, 3);
       expand_weights<WF, NT>(smem + L.a_off + c * 16384, smem + L.w_off + r * L.w_bytes, t);
+      if (!wide)  // 128 threads: each also takes the chunks of thread t + 128
+        expand_weights<WF, NT>(smem + L.a_off + c * 16384, smem + L.w_off + r * L.w_bytes, t + 128);
       fence_proxy_async();
       mbar_arrive(&conv[c]);
       mbar_arrive(&wempty[r]);
@@ -726,10 +730,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // 16-column groups, so two warps per scheduler hide each other's latency.
     const int half = warp < 4 ? 1 : 0;
     if constexpr (WF != W_BF16) {
-      if (wide)
+      if (wide || half)  // one instantiation: 256 threads, or 128 threads taking two chunk sets each
         expand_all(std::integral_constant<int, 256>{}, static_cast<int>(threadIdx.x));
-      else if (half)
-        expand_all(std::integral_constant<int, 128>{}, static_cast<int>(threadIdx.x));
     }
     if (!half || ep8) {
       const int we = warp & 3;  // TMEM lane quarter
@@ -827,7 +829,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             load_cols(c0, v);
           } else {
             const uint32_t local = smem_u32(R + c0 * L.r_ld + row);
-  #pragma unroll
+  #pragma unroll 1
             for (int h4 = 0; h4 < 16; h4 += 4) {  // 4 columns at a time, every peer's loads in flight
               float x[8][4];
   #pragma unroll
