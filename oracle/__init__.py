@@ -13,5 +13,6 @@ Modules:
   model    -- float64 decoder forward, prefill, autoregressive greedy decode,
               greedy block verification with prefix accept and KV commit
   weights  -- canonical (quantised) weight entries from BF16 master weights
+  loop     -- slot scheduling of the device-resident draft / verify loop
 """
-from . import formats, quant, model, weights  # noqa: F401
+from . import formats, quant, model, weights, loop  # noqa: F401
