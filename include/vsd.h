@@ -281,6 +281,47 @@ vsd_status vsd_draft_step_debug(const vsd_model* drafter, vsd_kv* kv, int32_t ba
                                 const float* anchor_dev, int32_t* drafts_dev,
                                 float* logits_dev, float* hidden_dev, vsd_stream stream);
 
+/* ---------------------------------------------------------------- device-resident loop
+ * n_iters iterations of draft -> verify -> commit without the host: each
+ * iteration (1) retires the requests that have generated their budget and
+ * admits queued requests into empty slots in queue order, (2) runs the
+ * drafter pass on every slot's anchor row, (3) runs the verify step on the
+ * slots, (4) appends each slot's accepted tokens (the target's greedy
+ * tokens g_0..g_a) to its request's output.  The pages' serving loop:
+ * "LLM inference acceleration", section three (continuous batching: finished
+ * requests leave the running batch, waiting ones take their places, first
+ * come first served); "The Inference Stack Behind OCRia", "Fixing CPU-side
+ * preparation" (no host round trips between steps).  Everything is
+ * asynchronous on `stream` and capturable in one CUDA graph.
+ *
+ * Layout: the cache holds >= slots + queued requests; slots 0..slots-1 run,
+ * cache slot slots+q holds queued request q's context (written by the
+ * caller, e.g. vsd_kv_write at that index, with its page-table row).  On
+ * admission, slot b takes that page-table row, length req_len[q], pending
+ * token req_pending[q] and anchor row req_anchor[q] (float32 [queued,
+ * hidden]: the target's residual row at the request's last context
+ * position).  An empty slot runs with length -1: computed, never committed,
+ * not an error.  Requires req_len[q] + req_budget[q] + 16 + 17 <=
+ * max_tokens_per_req (not checked on the device beyond the step's own
+ * VSD_DEV_BAD_SEQLEN).
+ *   slot_req_dev   int32 [slots] in/out: request in each slot, -1 empty
+ *                  (start: all -1)
+ *   next_req_dev   int32 [1] in/out: first request not yet admitted (start 0)
+ *   iter_dev       int32 [1] in/out: iteration counter (start 0)
+ *   req_generated  int32 [queued] in/out: tokens generated (start 0)
+ *   req_admit_iter int32 [queued] out: iteration of admission (start -1)
+ *   req_out        int32 [queued, out_cap] out: generated tokens, in order
+ *                  (the first out_cap of them)
+ * A request stays in its slot until it has generated >= req_budget[q]
+ * tokens; the tokens of its last step beyond out_cap are not stored. */
+vsd_status vsd_spec_loop(const vsd_model* target, const vsd_model* drafter, vsd_kv* kv,
+                         int32_t slots, int32_t queued, const int32_t* req_len_dev,
+                         const int32_t* req_pending_dev, const int32_t* req_budget_dev,
+                         const float* req_anchor_dev, int32_t* slot_req_dev,
+                         int32_t* next_req_dev, int32_t* iter_dev, int32_t* req_generated_dev,
+                         int32_t* req_admit_iter_dev, int32_t* req_out_dev, int32_t out_cap,
+                         int32_t n_iters, int32_t mask_token, vsd_stream stream);
+
 /* Copies the anchor rows [B, hidden] float32 that the last verify step left
  * (request b: the residual row of its last accepted position) to dst_dev. */
 vsd_status vsd_kv_get_anchor(const vsd_kv* kv, int32_t batch, float* dst_dev, vsd_stream stream);

@@ -26,7 +26,7 @@ EXPORTS = [
     "vsd_kv_pages_per_req", "vsd_kv_num_pages", "vsd_kv_set_page_table", "vsd_kv_write",
     "vsd_kv_read", "vsd_get_device_status", "vsd_verify_step", "vsd_verify_step_debug",
     "vsd_linear", "vsd_block_attention", "vsd_block_attention_static", "vsd_accept_commit",
-    "vsd_verify_step_profiled", "vsd_draft_step", "vsd_draft_step_debug", "vsd_kv_get_anchor",
+    "vsd_verify_step_profiled", "vsd_draft_step", "vsd_draft_step_debug", "vsd_kv_get_anchor", "vsd_spec_loop",
     "vsd_trace_enable", "vsd_trace_read",
 ]
 KERNEL_KINDS = ["embed", "qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm",
@@ -92,6 +92,7 @@ def lib() -> ctypes.CDLL:
             "vsd_draft_step": ([p, p, c_int, p, c_int, p, p], c_int),
             "vsd_draft_step_debug": ([p, p, c_int, p, c_int, p, p, p, p, p], c_int),
             "vsd_kv_get_anchor": ([p, c_int, p, p], c_int),
+            "vsd_spec_loop": ([p, p, p, c_int, c_int, p, p, p, p, p, p, p, p, p, p, c_int, c_int, c_int, p], c_int),
             "vsd_linear": ([ctypes.POINTER(Weight), c_int, c_int, p, c_int, p, p], c_int),
             "vsd_trace_enable": ([p, c_int], c_int),
             "vsd_trace_read": ([p, p, c_int, ctypes.POINTER(c_int), p], c_int),
@@ -283,6 +284,38 @@ def vsd_draft_step_debug(drafter: Model, kv: KV, batch: int, seq_lens, mask_toke
                                       int(mask_token), _dev(anchor, F32, "anchor"),
                                       _dev(drafts, I32, "drafts", batch * 16), _dev(logits, F32, "logits"),
                                       _dev(hidden, F32, "hidden"), _stream(stream)))
+
+
+class LoopState:
+    """Device arrays of one device-resident loop: per-request inputs and outputs, slot state."""
+
+    def __init__(self, slots: int, req_len, req_pending, req_budget, req_anchor, out_cap: int):
+        q = int(req_len.numel())
+        self.slots, self.queued, self.out_cap = slots, q, out_cap
+        self.req_len = req_len.to(torch.int32).cuda().contiguous()
+        self.req_pending = req_pending.to(torch.int32).cuda().contiguous()
+        self.req_budget = req_budget.to(torch.int32).cuda().contiguous()
+        self.req_anchor = req_anchor.to(torch.float32).cuda().contiguous()
+        self.slot_req = torch.full((slots,), -1, dtype=torch.int32, device="cuda")
+        self.next_req = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.iter = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.req_generated = torch.zeros(q, dtype=torch.int32, device="cuda")
+        self.req_admit_iter = torch.full((q,), -1, dtype=torch.int32, device="cuda")
+        self.req_out = torch.full((q, out_cap), -1, dtype=torch.int32, device="cuda")
+
+
+def vsd_spec_loop(target: Model, drafter: Model, kv: KV, st: LoopState, n_iters: int, mask_token: int,
+                  stream=None) -> None:
+    q = st.queued
+    _check(lib().vsd_spec_loop(target.handle, drafter.handle, kv.handle, st.slots, q,
+                               _dev(st.req_len, I32, "req_len", q), _dev(st.req_pending, I32, "req_pending", q),
+                               _dev(st.req_budget, I32, "req_budget", q),
+                               _dev(st.req_anchor, F32, "req_anchor"), _dev(st.slot_req, I32, "slot_req", st.slots),
+                               _dev(st.next_req, I32, "next_req", 1), _dev(st.iter, I32, "iter", 1),
+                               _dev(st.req_generated, I32, "req_generated", q),
+                               _dev(st.req_admit_iter, I32, "req_admit_iter", q),
+                               _dev(st.req_out, I32, "req_out", q * st.out_cap), st.out_cap, int(n_iters),
+                               int(mask_token), _stream(stream)))
 
 
 def vsd_kv_get_anchor(kv: KV, batch: int, dst, stream=None) -> None:

@@ -139,6 +139,8 @@ struct vsd_kv {
   size_t attn_items_cap = 0;
   float* anchor = nullptr;  // [max_batch][H] residual row of the last accepted position (drafter input)
   int* zeros = nullptr;     // [max_batch] zero context lengths (the draft pass reads no cache)
+  // slot state of the device-resident loop: lengths, pending, drafts, accepted [max_batch], outputs [max_batch][17]
+  int *loop_seq = nullptr, *loop_pend = nullptr, *loop_drafts = nullptr, *loop_acc = nullptr, *loop_out = nullptr;
   int* status = nullptr;
   unsigned long long* trace = nullptr;  // optional phase timestamps [launch][CTA][tag]
   int trace_launches = 0;
@@ -652,6 +654,9 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
       (s = dalloc(&kv->v_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
       (s = dalloc(&kv->keys, M)) || (s = dalloc(&kv->ctx_len, max_batch)) || (s = dalloc(&kv->req_ok, max_batch)) ||
       (s = dalloc(&kv->anchor, static_cast<size_t>(max_batch) * H)) || (s = dalloc(&kv->zeros, max_batch)) ||
+      (s = dalloc(&kv->loop_seq, max_batch)) || (s = dalloc(&kv->loop_pend, max_batch)) ||
+      (s = dalloc(&kv->loop_drafts, static_cast<size_t>(max_batch) * kBlock)) ||
+      (s = dalloc(&kv->loop_acc, max_batch)) || (s = dalloc(&kv->loop_out, static_cast<size_t>(max_batch) * kRows)) ||
       (s = dalloc(&kv->status, 1)))
     return cleanup(s);
   if ((s = dalloc(&kv->ssq, static_cast<size_t>(ceil_div(H, kTileN)) * kv->m_alloc))) return cleanup(s);
@@ -683,7 +688,8 @@ void vsd_kv_destroy(vsd_kv* kv) {
   if (!kv) return;
   void* ptrs[] = {kv->k_pool, kv->v_pool, kv->page_table, kv->x, kv->u, kv->act_o, kv->act_a, kv->q_tile,
                   kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->req_ok, kv->ssq, kv->attn_o,
-                  kv->attn_ml, kv->attn_counters, kv->anchor, kv->zeros, kv->status, kv->trace};
+                  kv->attn_ml, kv->attn_counters, kv->anchor, kv->zeros, kv->loop_seq, kv->loop_pend,
+                  kv->loop_drafts, kv->loop_acc, kv->loop_out, kv->status, kv->trace};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete kv;
@@ -993,6 +999,57 @@ vsd_status vsd_draft_step_debug(const vsd_model* drafter, vsd_kv* kv, int32_t ba
                                 float* hidden, vsd_stream stream) {
   return draft_impl(drafter, kv, batch, seq_lens, mask_token, anchor, drafts, logits, hidden,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+vsd_status vsd_spec_loop(const vsd_model* target, const vsd_model* drafter, vsd_kv* kv, int32_t slots,
+                         int32_t queued, const int32_t* req_len, const int32_t* req_pending,
+                         const int32_t* req_budget, const float* req_anchor, int32_t* slot_req, int32_t* next_req,
+                         int32_t* iter, int32_t* req_generated, int32_t* req_admit_iter, int32_t* req_out,
+                         int32_t out_cap, int32_t n_iters, int32_t mask_token, vsd_stream stream) {
+  if (!target || !drafter || !kv || !req_len || !req_pending || !req_budget || !req_anchor || !slot_req ||
+      !next_req || !iter || !req_generated || !req_admit_iter || !req_out)
+    return fail(VSD_ERR_ARG, "NULL pointer");
+  if (kv->m != target) return fail(VSD_ERR_ARG, "the cache was created for another model");
+  if (slots < 1 || slots > kMaxLoopSlots || queued < 0 || out_cap < 1 || n_iters < 0)
+    return fail(VSD_ERR_ARG, "slots in [1, %d], queued >= 0, out_cap >= 1, n_iters >= 0", kMaxLoopSlots);
+  if (static_cast<int64_t>(slots) + queued > kv->max_batch)
+    return fail(VSD_ERR_ARG, "%d slots + %d queued requests exceed the cache's %d", slots, queued, kv->max_batch);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LoopArgs la{};
+  la.B = slots;
+  la.Q = queued;
+  la.out_cap = out_cap;
+  la.hidden = target->cfg.hidden;
+  la.pages_per_req = kv->ppr;
+  la.first_queued = slots;
+  la.slot_req = slot_req;
+  la.next_req = next_req;
+  la.req_len = req_len;
+  la.req_pending = req_pending;
+  la.req_budget = req_budget;
+  la.req_anchor = req_anchor;
+  la.req_generated = req_generated;
+  la.req_admit_iter = req_admit_iter;
+  la.req_out = req_out;
+  la.seq_lens = kv->loop_seq;
+  la.pending = kv->loop_pend;
+  la.accepted = kv->loop_acc;
+  la.out_tokens = kv->loop_out;
+  la.page_table = kv->page_table;
+  la.anchor = kv->anchor;
+  la.iter = iter;
+  la.status = kv->status;
+  vsd_status s;
+  for (int i = 0; i < n_iters; ++i) {
+    CK(launch_ex(loop_schedule_kernel, dim3(1), dim3(256), 0, st, use_pdl(st), false, la));
+    if ((s = draft_impl(drafter, kv, slots, kv->loop_seq, mask_token, nullptr, kv->loop_drafts, nullptr, nullptr, st)))
+      return s;
+    if ((s = verify_impl(target, kv, slots, kv->loop_seq, kv->loop_pend, kv->loop_drafts, kv->loop_acc, kv->loop_out,
+                         nullptr, nullptr, st)))
+      return s;
+    CK(launch_ex(loop_collect_kernel, dim3(slots), dim3(32), 0, st, use_pdl(st), false, la));
+  }
+  return VSD_OK;
 }
 
 vsd_status vsd_kv_get_anchor(const vsd_kv* kv, int32_t batch, float* dst, vsd_stream stream) {

@@ -57,18 +57,19 @@ __global__ void __launch_bounds__(128) embed_kernel(const EmbedArgs a) {
   const int row = blockIdx.x, b = row / kRows, j = row % kRows;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const bool draft = a.anchor != nullptr;
+  const int L = a.seq_lens[b];
+  const bool idle = L == kIdleSlot;  // an empty slot: computed on, never committed, not an error
   int tok = draft ? a.mask_token : (j == 0 ? a.pending[b] : a.drafts[b * kBlock + j - 1]);
   const bool tok_ok = tok >= 0 && tok < a.vocab;
   if (!tok_ok) {
-    if (t == 0) atomicOr(a.status, VSD_DEV_BAD_TOKEN);
+    if (t == 0 && !idle) atomicOr(a.status, VSD_DEV_BAD_TOKEN);
     tok = 0;
   }
   if (t == 0) {
     a.keys[row] = 0ull;
     if (j == 0) {
-      const int L = a.seq_lens[b];
       const bool ok = L >= 0 && L + kRows <= a.max_tokens;
-      if (!ok) atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
+      if (!ok && !idle) atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
       a.ctx_len[b] = ok ? L : 0;
       a.req_ok[b] = (ok && tok_ok) ? 1 : 0;
     }
@@ -231,6 +232,94 @@ __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) 
       for (int i = t; i < a.hidden; i += blockDim.x) a.anchor[static_cast<size_t>(b) * a.hidden + i] = src[i];
     }
   }
+}
+
+// ------------------------------------------------------------------ device-resident loop
+// Slots of the loop hold requests of a queue; request q's context sits in
+// cache slot first_queued + q (its page-table row), written by the caller.
+struct LoopArgs {
+  int B, Q, out_cap, hidden, pages_per_req, first_queued;
+  int* slot_req;          // [B] request in slot b, -1 empty
+  int* next_req;          // [1] queue head
+  const int* req_len;     // [Q] committed length at admission
+  const int* req_pending; // [Q] pending token at admission
+  const int* req_budget;  // [Q] tokens to generate
+  const float* req_anchor;// [Q][hidden] anchor row at admission
+  int* req_generated;     // [Q] out
+  int* req_admit_iter;    // [Q] out: loop iteration of admission (-1 never)
+  int* req_out;           // [Q][out_cap] out
+  int* seq_lens;          // [B] slot state (kIdleSlot when empty)
+  int* pending;           // [B]
+  const int* accepted;    // [B] of the step
+  const int* out_tokens;  // [B][17] of the step
+  int* page_table;        // [max_batch][ppr]
+  float* anchor;          // [max_batch][hidden] the cache's anchor rows
+  int* iter;              // [1] loop iteration counter
+  int* status;
+};
+
+// Before a step: retire requests that reached their budget, admit queued
+// requests into empty slots in queue order (page-table row, length,
+// pending token and anchor row of the request).  One CTA.
+__global__ void __launch_bounds__(256) loop_schedule_kernel(const LoopArgs a) {
+  __shared__ int admit_q[kMaxLoopSlots];
+  __shared__ int head;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = threadIdx.x;
+  if (t == 0) {
+    head = *a.next_req;
+    const int it = *a.iter;
+    for (int b = 0; b < a.B; ++b) {
+      int q = a.slot_req[b];
+      if (q >= 0 && a.req_generated[q] >= a.req_budget[q]) q = -1;  // retired
+      if (q < 0 && head < a.Q) {
+        q = head++;
+        a.req_admit_iter[q] = it;
+        admit_q[b] = q;
+      } else {
+        admit_q[b] = -1;
+      }
+      a.slot_req[b] = q;
+      if (q < 0) a.seq_lens[b] = kIdleSlot;
+    }
+    *a.next_req = head;
+  }
+  __syncthreads();
+  for (int b = 0; b < a.B; ++b) {
+    const int q = admit_q[b];
+    if (q < 0) continue;
+    for (int i = t; i < a.pages_per_req; i += blockDim.x)
+      a.page_table[static_cast<size_t>(b) * a.pages_per_req + i] =
+          a.page_table[static_cast<size_t>(a.first_queued + q) * a.pages_per_req + i];
+    for (int i = t; i < a.hidden; i += blockDim.x)
+      a.anchor[static_cast<size_t>(b) * a.hidden + i] = a.req_anchor[static_cast<size_t>(q) * a.hidden + i];
+    if (t == 0) {
+      a.seq_lens[b] = a.req_len[q];
+      a.pending[b] = a.req_pending[q];
+    }
+  }
+}
+
+// After a step: append each busy slot's accepted tokens to its request's
+// output (up to out_cap) and count them; advance the iteration counter.
+__global__ void loop_collect_kernel(const LoopArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x, t = threadIdx.x;  // one warp per slot
+  const int q = a.slot_req[b];
+  if (q >= 0) {
+    const int acc = a.accepted[b];
+    const int g0 = a.req_generated[q];
+    if (acc >= 0) {
+      if (t <= acc && g0 + t < a.out_cap) a.req_out[static_cast<size_t>(q) * a.out_cap + g0 + t] = a.out_tokens[b * kRows + t];
+      __syncwarp();
+      if (t == 0) a.req_generated[q] = g0 + acc + 1;
+    } else if (t == 0) {
+      atomicOr(a.status, VSD_DEV_BAD_SEQLEN);  // a busy slot whose step was rejected
+    }
+  }
+  if (b == 0 && t == 0) *a.iter += 1;
 }
 
 // Drafts from the argmax keys of a draft pass: drafts[b][j] = token of row

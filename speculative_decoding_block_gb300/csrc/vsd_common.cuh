@@ -24,6 +24,8 @@ constexpr long long kWaitLimitCycles = 2000ll * 1000ll * 1000ll;
 constexpr int kRows = 17;    // rows per request: pending token + 16 drafts
 constexpr int kBlock = 16;   // drafted tokens per request
 constexpr int kPage = 16;    // tokens per KV page
+constexpr int kIdleSlot = -1;      // seq_len of an empty slot: the step computes it but commits nothing
+constexpr int kMaxLoopSlots = 1024;  // slots of the device-resident loop
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
