@@ -474,6 +474,7 @@ def run_gpu(args, rank: int, world: int):
     if drafter is not None:
         result["draft"] = time_draft(B, model, drafter, kv, shape, Bn, seq, pen, drafts, acc, out, seq0, pend0, g,
                                      flush, stream, args)
+        result["loop"] = time_loop(B, model, drafter, shape, w, max_tok, flush, stream)
     if oracle_handle is not None:
         r = finish_oracle(oracle_handle)
         if r and "tokens" in r:
@@ -539,6 +540,59 @@ def time_draft(B, model, drafter, kv, shape, Bn, seq, pen, drafts, acc, out, seq
             "pass_bytes": pb, "pass_hbm_frac": round(pb / (ms_draft * 1e-3) / 1e9 / hbm, 4),
             "ms_per_iteration": round(ms_iter, 4),
             "iteration": "one CUDA graph: verify step, then a draft pass on its anchor rows"}
+
+
+def time_loop(B, model, drafter, shape, w, max_tok, flush, stream, queued=16, iters=64, budget=48, runs=3):
+    """The device-resident loop: w.batch slots, `queued` requests with synthetic contexts of the workload's
+    length mix and synthetic anchor rows, `iters` iterations of schedule -> draft -> verify -> collect in one
+    CUDA graph (L2 flushed before each run)."""
+    import torch
+    slots = w.batch
+    kv = B.vsd_kv_create(model, slots + queued, max_tok)
+    rng = np.random.default_rng(w.seed)
+    lens = rng.integers(w.ctx_lo, min(w.ctx_hi, max_tok - budget - 40) + 1, size=queued)
+    for q in range(queued):
+        kk, vv = gen.synthetic_kv(shape, int(lens[q]), w.seed + 1, q)
+        B.vsd_kv_write(kv, slots + q, 0, kk.cuda().contiguous(), vv.cuda().contiguous())
+        del kk, vv
+    pend = rng.integers(0, shape.vocab, size=queued)
+    anchors = gen.anchor_rows(shape.hidden, queued, w.seed)
+    ls = B.LoopState(slots, torch.tensor(lens), torch.tensor(pend), torch.full((queued,), budget),
+                     anchors, budget + 17)
+    fresh = {k: getattr(ls, k).clone() for k in ("slot_req", "next_req", "iter", "req_generated",
+                                                  "req_admit_iter", "req_out")}
+
+    def reset():
+        for k, v in fresh.items():
+            getattr(ls, k).copy_(v)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        B.vsd_spec_loop(model, drafter, kv, ls, iters, mask_token(shape), stream=stream)
+    times = []
+    for r in range(runs + 1):
+        with torch.cuda.stream(stream):
+            reset()
+            flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        if r:
+            times.append(e0.elapsed_time(e1))
+    if B.vsd_get_device_status(kv) != 0:
+        raise RuntimeError("loop reported a device error")
+    gen_tok = int(ls.req_generated.sum().item())
+    busy = int((ls.req_admit_iter >= 0).sum().item())
+    ms = statistics.mean(times)
+    return {"slots": slots, "queued": queued, "iterations": iters, "budget": budget,
+            "requests_admitted": busy, "requests_finished": int((ls.req_generated >= budget).sum().item()),
+            "generated_tokens": gen_tok, "ms_total": round(ms, 3), "ms_per_iteration": round(ms / iters, 4),
+            "tokens_per_s": round(gen_tok / (ms * 1e-3), 1),
+            "drafter": "random weights: drafts are accepted about as often as chance, ~1 token per slot-iteration",
+            "graph": f"{iters} iterations in one CUDA graph, L2 flushed before each run"}
 
 
 # ------------------------------------------------------------------ reference arm
