@@ -14,5 +14,6 @@ Modules:
               greedy block verification with prefix accept and KV commit
   weights  -- canonical (quantised) weight entries from BF16 master weights
   loop     -- slot scheduling of the device-resident draft / verify loop
+  sampling -- stochastic (temperature) block verification, random numbers as inputs
 """
-from . import formats, quant, model, weights, loop  # noqa: F401
+from . import formats, quant, model, weights, loop, sampling  # noqa: F401
