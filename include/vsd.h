@@ -218,6 +218,29 @@ vsd_status vsd_verify_step_debug(const vsd_model* m, vsd_kv* kv, int32_t batch,
                                  int32_t* out_tokens_dev, float* logits_dev,
                                  float* hidden_dev, vsd_stream stream);
 
+/* Stochastic verification at temperature T > 0: the pages require that the
+ * accepted tokens keep the target's output distribution ("The Inference
+ * Stack Behind OCRia", speculative-decoding section) and print a sampler at
+ * temperature 0.7 with accept / correction / bonus branches ("LLM inference
+ * acceleration", section 3.2).  The rule (from the speculative-sampling
+ * literature, for a drafter proposing single tokens): draft d_j is accepted
+ * iff u_accept[b][j] < p_j(d_j), p_j = softmax(logits_j / T); the first
+ * rejected row a gives out[a] = a sample of p_a without d_a; after 16
+ * acceptances out[16] = a sample of p_16.  Samples are drawn by inverse CDF
+ * over token ids in increasing order at u_sample[b][a] (the smallest id whose
+ * cumulative mass reaches u times the total).  Weights exp(min(logit / T, 80))
+ * in float32.  Commits as the greedy step.
+ *   u_accept_dev float32 [B, 16], u_sample_dev float32 [B, 17]: uniforms in
+ *                (0, 1), the caller's random numbers
+ *   logits_dev   optional float32 [B*17, vocab]
+ * VSD_ERR_UNSUPPORTED for a head that is not 16-bit or hidden % 16 != 0. */
+vsd_status vsd_verify_step_sampled(const vsd_model* m, vsd_kv* kv, int32_t batch,
+                                   int32_t* seq_lens_dev, int32_t* pending_dev,
+                                   const int32_t* drafts_dev, int32_t* accepted_dev,
+                                   int32_t* out_tokens_dev, const float* u_accept_dev,
+                                   const float* u_sample_dev, float temperature,
+                                   float* logits_dev, vsd_stream stream);
+
 /* Kernel kinds reported by vsd_verify_step_profiled. */
 #define VSD_K_EMBED      0  /* embedding gather (+ f16 copy, sums of squares) */
 #define VSD_K_QKV        1  /* QKV GEMM + RMSNorm scale + RoPE + block K/V to scratch */

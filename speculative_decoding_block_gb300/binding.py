@@ -26,7 +26,7 @@ EXPORTS = [
     "vsd_kv_pages_per_req", "vsd_kv_num_pages", "vsd_kv_set_page_table", "vsd_kv_write",
     "vsd_kv_read", "vsd_get_device_status", "vsd_verify_step", "vsd_verify_step_debug",
     "vsd_linear", "vsd_block_attention", "vsd_block_attention_static", "vsd_accept_commit",
-    "vsd_verify_step_profiled", "vsd_draft_step", "vsd_draft_step_debug", "vsd_kv_get_anchor", "vsd_spec_loop",
+    "vsd_verify_step_profiled", "vsd_draft_step", "vsd_draft_step_debug", "vsd_kv_get_anchor", "vsd_spec_loop", "vsd_verify_step_sampled",
     "vsd_trace_enable", "vsd_trace_read",
 ]
 KERNEL_KINDS = ["embed", "qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm",
@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
             "vsd_verify_step_profiled": ([p, p, c_int, p, p, p, p, p, c_int, p, p, ctypes.POINTER(c_int)],
                                          c_int),
             "vsd_draft_step": ([p, p, c_int, p, c_int, p, p], c_int),
+            "vsd_verify_step_sampled": ([p, p, c_int, p, p, p, p, p, p, p, ctypes.c_float, p, p], c_int),
             "vsd_draft_step_debug": ([p, p, c_int, p, c_int, p, p, p, p, p], c_int),
             "vsd_kv_get_anchor": ([p, c_int, p, p], c_int),
             "vsd_spec_loop": ([p, p, p, c_int, c_int, p, p, p, p, p, p, p, p, p, p, c_int, c_int, c_int, p], c_int),
@@ -271,6 +272,18 @@ def vsd_verify_step_debug(model: Model, kv: KV, batch: int, seq_lens, pending, d
                                        _dev(out_tokens, I32, "out_tokens", batch * 17),
                                        _dev(logits, F32, "logits"), _dev(hidden, F32, "hidden"),
                                        _stream(stream)))
+
+
+def vsd_verify_step_sampled(model: Model, kv: KV, batch: int, seq_lens, pending, drafts, accepted, out_tokens,
+                            u_accept, u_sample, temperature: float, logits=None, stream=None) -> None:
+    _check(lib().vsd_verify_step_sampled(model.handle, kv.handle, batch,
+                                         _dev(seq_lens, I32, "seq_lens", batch), _dev(pending, I32, "pending", batch),
+                                         _dev(drafts, I32, "drafts", batch * 16),
+                                         _dev(accepted, I32, "accepted", batch),
+                                         _dev(out_tokens, I32, "out_tokens", batch * 17),
+                                         _dev(u_accept, F32, "u_accept", batch * 16),
+                                         _dev(u_sample, F32, "u_sample", batch * 17), float(temperature),
+                                         _dev(logits, F32, "logits"), _stream(stream)))
 
 
 def vsd_draft_step(drafter: Model, kv: KV, batch: int, seq_lens, mask_token: int, drafts, stream=None) -> None:

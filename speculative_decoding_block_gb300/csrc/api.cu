@@ -141,6 +141,9 @@ struct vsd_kv {
   int* zeros = nullptr;     // [max_batch] zero context lengths (the draft pass reads no cache)
   // slot state of the device-resident loop: lengths, pending, drafts, accepted [max_batch], outputs [max_batch][17]
   int *loop_seq = nullptr, *loop_pend = nullptr, *loop_drafts = nullptr, *loop_acc = nullptr, *loop_out = nullptr;
+  // stochastic verification: per (row, vocabulary tile) sums, the drafts' logits, the decisions [max_batch][18]
+  float *tile_sum = nullptr, *draft_logit = nullptr;
+  int* decided = nullptr;
   int* status = nullptr;
   unsigned long long* trace = nullptr;  // optional phase timestamps [launch][CTA][tag]
   int trace_launches = 0;
@@ -300,8 +303,8 @@ struct Plan {
 // grows with the columns exchanged.  Clusters beyond what can be resident
 // at once run in further waves.
 Plan plan_gemm(const vsd_model* m, const Linear& w, int M, int epi, bool lo) {
-  const bool no_split = epi == EPI_ARGMAX;
-  const double t_group = epi == EPI_QKV ? 1.5 : (epi == EPI_ARGMAX || epi == EPI_STORE ? 0.3 : 0.5);
+  const bool no_split = epi == EPI_ARGMAX || epi == EPI_SAMPLE;  // the epilogue needs the finished dot products
+  const double t_group = epi == EPI_QKV ? 1.5 : (epi == EPI_ARGMAX || epi == EPI_SAMPLE || epi == EPI_STORE ? 0.3 : 0.5);
   Plan best{};
   double best_cost = 1e30;
   const int max_t = std::max(1, ceil_div(M, 16));
@@ -657,6 +660,9 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
       (s = dalloc(&kv->loop_seq, max_batch)) || (s = dalloc(&kv->loop_pend, max_batch)) ||
       (s = dalloc(&kv->loop_drafts, static_cast<size_t>(max_batch) * kBlock)) ||
       (s = dalloc(&kv->loop_acc, max_batch)) || (s = dalloc(&kv->loop_out, static_cast<size_t>(max_batch) * kRows)) ||
+      (s = dalloc(&kv->tile_sum, static_cast<size_t>(kv->m_alloc) * m->lm.n_tiles)) ||
+      (s = dalloc(&kv->draft_logit, kv->m_alloc)) ||
+      (s = dalloc(&kv->decided, static_cast<size_t>(max_batch) * (kRows + 1))) ||
       (s = dalloc(&kv->status, 1)))
     return cleanup(s);
   if ((s = dalloc(&kv->ssq, static_cast<size_t>(ceil_div(H, kTileN)) * kv->m_alloc))) return cleanup(s);
@@ -689,7 +695,8 @@ void vsd_kv_destroy(vsd_kv* kv) {
   void* ptrs[] = {kv->k_pool, kv->v_pool, kv->page_table, kv->x, kv->u, kv->act_o, kv->act_a, kv->q_tile,
                   kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->req_ok, kv->ssq, kv->attn_o,
                   kv->attn_ml, kv->attn_counters, kv->anchor, kv->zeros, kv->loop_seq, kv->loop_pend,
-                  kv->loop_drafts, kv->loop_acc, kv->loop_out, kv->status, kv->trace};
+                  kv->loop_drafts, kv->loop_acc, kv->loop_out, kv->tile_sum, kv->draft_logit, kv->decided,
+                  kv->status, kv->trace};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete kv;
@@ -851,21 +858,37 @@ static vsd_status run_layers(const vsd_model* m, vsd_kv* kv, int B, const int* a
   return VSD_OK;
 }
 
-// Final RMSNorm + lm_head + per-row argmax keys (kv->keys), logits optional.
-static vsd_status run_head(const vsd_model* m, vsd_kv* kv, int M, float* logits, cudaStream_t st, LaunchTimer* timer) {
+// Stochastic verification inputs of one step (nullptr: greedy).
+struct SampleIn {
+  float inv_temp;
+  const float* u_accept;  // [B][16]
+  const float* u_sample;  // [B][17]
+};
+
+// Final RMSNorm + lm_head: per-row argmax keys (kv->keys; greedy) or, with
+// `smp`, the per-tile exp sums and the drafts' logits; logits optional.
+static vsd_status run_head(const vsd_model* m, vsd_kv* kv, int M, float* logits, cudaStream_t st, LaunchTimer* timer,
+                           const int* drafts = nullptr, const SampleIn* smp = nullptr) {
   vsd_status s;
   GemmArgs a{};
   set_norm_input(a, kv);
   a.keys = kv->keys;
   a.logits = logits;
   a.act_lo_rows = kv->m_alloc;
-  TIMED(VSD_K_LM_HEAD, if ((s = run_gemm(m, m->lm, EPI_ARGMAX, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
+  if (smp) {
+    a.inv_temp = smp->inv_temp;
+    a.drafts = drafts;
+    a.tile_sum = kv->tile_sum;
+    a.draft_logit = kv->draft_logit;
+  }
+  TIMED(VSD_K_LM_HEAD, if ((s = run_gemm(m, m->lm, smp ? EPI_SAMPLE : EPI_ARGMAX, kv->tm_u, M, a, kv->status, st,
+                                         next_trace(kv)))) return s);
   return VSD_OK;
 }
 
 static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_lens, int* pending, const int* drafts,
                               int* accepted, int* out_tokens, float* logits, float* hidden, cudaStream_t st,
-                              LaunchTimer* timer = nullptr) {
+                              LaunchTimer* timer = nullptr, const SampleIn* smp = nullptr) {
   if (!m || !kv || !seq_lens || !pending || !drafts || !accepted || !out_tokens)
     return fail(VSD_ERR_ARG, "NULL pointer");
   if (kv->m != m) return fail(VSD_ERR_ARG, "the cache was created for another model");
@@ -896,8 +919,30 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), false, e)));
   }
   if ((s = run_layers(m, kv, B, seq_lens, hidden, st, timer))) return s;
-  if ((s = run_head(m, kv, M, logits, st, timer))) return s;
+  if ((s = run_head(m, kv, M, logits, st, timer, drafts, smp))) return s;
+  if (smp) {
+    SampleArgs sa{};
+    sa.vocab = c.vocab;
+    sa.hidden = H;
+    sa.n_tiles = m->lm.n_tiles;
+    sa.m_alloc = kv->m_alloc;
+    sa.ssq_slices = ceil_div(H, kTileN);
+    sa.inv_temp = smp->inv_temp;
+    sa.inv_hidden = 1.0f / static_cast<float>(H);
+    sa.eps = c.eps;
+    sa.tile_sum = kv->tile_sum;
+    sa.draft_logit = kv->draft_logit;
+    sa.drafts = drafts;
+    sa.u_accept = smp->u_accept;
+    sa.u_sample = smp->u_sample;
+    sa.head = static_cast<const __half*>(m->lm.data);
+    sa.x16 = kv->u;
+    sa.ssq = kv->ssq;
+    sa.decided = kv->decided;
+    TIMED(VSD_K_COMMIT, CK(launch_ex(sample_decide_kernel, dim3(B), dim3(256), 0, st, use_pdl(st), false, sa)));
+  }
   CommitArgs ca = commit_args(kv, drafts, seq_lens, pending, accepted, out_tokens);
+  if (smp) ca.decided = kv->decided;
   ca.x = kv->x;  // the drafter's next conditioning row
   ca.anchor = kv->anchor;
   ca.hidden = H;
@@ -986,6 +1031,19 @@ vsd_status vsd_verify_step_debug(const vsd_model* m, vsd_kv* kv, int32_t batch, 
                                  float* hidden, vsd_stream stream) {
   return verify_impl(m, kv, batch, seq_lens, pending, drafts, accepted, out_tokens, logits, hidden,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+vsd_status vsd_verify_step_sampled(const vsd_model* m, vsd_kv* kv, int32_t batch, int32_t* seq_lens, int32_t* pending,
+                                   const int32_t* drafts, int32_t* accepted, int32_t* out_tokens,
+                                   const float* u_accept, const float* u_sample, float temperature, float* logits,
+                                   vsd_stream stream) {
+  if (!u_accept || !u_sample) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return fail(VSD_ERR_ARG, "temperature must be > 0");
+  if (m && m->lm.fmt != VSD_FMT_BF16) return fail(VSD_ERR_UNSUPPORTED, "sampling needs a 16-bit head");
+  if (m && (m->cfg.hidden % 16)) return fail(VSD_ERR_UNSUPPORTED, "sampling needs hidden %% 16 == 0");
+  SampleIn smp{1.0f / temperature, u_accept, u_sample};
+  return verify_impl(m, kv, batch, seq_lens, pending, drafts, accepted, out_tokens, logits, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), nullptr, &smp);
 }
 
 vsd_status vsd_draft_step(const vsd_model* drafter, vsd_kv* kv, int32_t batch, const int32_t* seq_lens,

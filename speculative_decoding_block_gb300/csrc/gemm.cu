@@ -47,6 +47,9 @@ static cudaError_t launch_fmt(int epi, const CUtensorMap& tm_act, const CUtensor
     case EPI_QKV: return launch_one<WF, EPI_QKV>(tm_act, tm_w, a, grid, st, pdl);
     case EPI_SILU: return launch_one<WF, EPI_SILU>(tm_act, tm_w, a, grid, st, pdl);
     case EPI_ARGMAX: return launch_one<WF, EPI_ARGMAX>(tm_act, tm_w, a, grid, st, pdl);
+    case EPI_SAMPLE:
+      if constexpr (WF == W_BF16) return launch_one<WF, EPI_SAMPLE>(tm_act, tm_w, a, grid, st, pdl);
+      return cudaErrorInvalidValue;  // the head is a 16-bit matrix
   }
   return cudaErrorInvalidValue;
 }

@@ -49,7 +49,7 @@
 namespace vsd {
 
 enum WFmt { W_BF16 = 0, W_FP8 = 1, W_NVFP4 = 2 };
-enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SILU = 3, EPI_ARGMAX = 4 };
+enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SILU = 3, EPI_ARGMAX = 4, EPI_SAMPLE = 5 };
 
 constexpr int kGemmThreads = 320;
 constexpr int kTileN = 128;   // weight rows per tile (MMA M)
@@ -105,7 +105,13 @@ struct GemmArgs {
   int ffn;
   // ARGMAX
   unsigned long long* keys;  // [M]
-  float* logits;             // optional [M][vocab]
+  float* logits;             // optional [M][vocab] (ARGMAX, SAMPLE)
+  // SAMPLE: per (token row, 128-row vocabulary tile) the sum of exp(min(logit / T, 80)),
+  // and the logit of each row's draft token (rows j < 16 of a request)
+  float inv_temp;
+  const int* drafts;         // [B][16]
+  float* tile_sum;           // [M][n_tiles]
+  float* draft_logit;        // [M]
   int* status;
   Trace trace;
 };
@@ -408,6 +414,20 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
         if (a.out_lo) a.act_out[o + a.out_lo] = __float2half_rn(y - __half2float(hi));
       }
     }
+  } else if constexpr (EPI == EPI_SAMPLE) {
+    // exp of the tempered logits, summed over the warp's 32 vocabulary rows
+    // per column (reduce-scatter); the caller folds the four warps
+    float e[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int tok = tok0 + i;
+      const bool ok = row_ok && tok < a.m_tokens;
+      if (a.logits && ok) a.logits[static_cast<size_t>(tok) * a.n_rows + prow] = x[i];
+      if (ok && prow == pos[c0 + i]) a.draft_logit[tok] = x[i];
+      e[i] = ok ? __expf(fminf(x[i] * a.inv_temp, 80.0f)) : 0.0f;
+    }
+    const float tot = warp_reduce_scatter16(e, lane, [](float p, float q) { return p + q; });
+    if ((lane & 1) == 0) reinterpret_cast<float*>(wbest)[warp_e * 16 + scatter16_element(lane)] = tot;
   } else if constexpr (EPI == EPI_ARGMAX) {
     unsigned long long key[16];
 #pragma unroll
@@ -535,6 +555,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int off = 0; off < (a.head_dim >> 1) * 8; off += 128) prefetch_l2(row_p + off);
         }
         pos_s[c] = p;
+      }
+      if constexpr (EPI == EPI_SAMPLE) {  // the column's draft token (-1: the bonus row, padding)
+        const int j = tok % kRows;
+        pos_s[c] = (tok < a.m_tokens && j < kBlock) ? a.drafts[(tok / kRows) * kBlock + j] : -1;
       }
     }
   };
@@ -868,6 +892,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               }
             }
             if (et2 == 0 && acc == 0 && g == rank) trace_point(a.trace, 15);
+          }
+          if constexpr (EPI == EPI_SAMPLE) {
+            named_bar_sync(4 + half, 128);  // this set's four warps only
+            if (et < 16) {  // the tile's sum for column c0 + et, warps in fixed order (deterministic)
+              const float* ws = reinterpret_cast<const float*>(wb);
+              const float sum = ((ws[et] + ws[16 + et]) + ws[32 + et]) + ws[48 + et];
+              const int col = tt * a.n_tok + c0 + et;
+              if (col < a.m_tokens) a.tile_sum[static_cast<size_t>(col) * a.n_tiles + tile] = sum;
+            }
           }
         }
         if (cs == 1) {

@@ -125,6 +125,7 @@ __global__ void validate_requests_kernel(const int* seq_lens, const int* pending
 struct CommitArgs {
   int vocab, layers, n_kv, hd, batch_cap, num_pages, pages_per_req;
   const unsigned long long* keys;  // [B*17]
+  const int* decided;             // optional [B][18] (stochastic verification): a, then out tokens -- used instead of keys
   const int* drafts;              // [B][16]
   const int* ctx_len;             // [B] validated committed length
   const int* req_ok;              // [B]
@@ -165,9 +166,16 @@ __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) 
     int gt = -1, dt = -1;
     bool bad = false;
     if (t < kRows) {
-      const unsigned long long k = a.keys[b * kRows + t];
-      gt = k ? static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull)) : -1;
-      if (gt < 0 || gt >= a.vocab) bad = true;
+      if (a.decided) {
+        const int dacc = a.decided[b * (kRows + 1)];
+        gt = a.decided[b * (kRows + 1) + 1 + t];
+        if (t <= dacc && (gt < 0 || gt >= a.vocab)) bad = true;
+        if (t > dacc) gt = -1;
+      } else {
+        const unsigned long long k = a.keys[b * kRows + t];
+        gt = k ? static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull)) : -1;
+        if (gt < 0 || gt >= a.vocab) bad = true;
+      }
       g[t] = gt;
     }
     int pg = 0;
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) 
     const unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
     const unsigned pbad = __ballot_sync(0xFFFFFFFFu, t < kRows && (pg < 0 || pg >= a.num_pages));
     if (t == 0) {
-      const int acc0 = mism ? (__ffs(mism) - 1) : kBlock;
+      const int acc0 = a.decided ? a.decided[b * (kRows + 1)] : (mism ? (__ffs(mism) - 1) : kBlock);
       const bool pages_ok = (pbad & ((2u << acc0) - 1u)) == 0;  // only the committed rows need pages
       if (!pages_ok && l == 0) atomicOr(a.status, VSD_DEV_BAD_PAGE);
       s_valid = (badm == 0 && a.req_ok[b] && pages_ok) ? 1 : 0;
@@ -320,6 +328,161 @@ __global__ void loop_collect_kernel(const LoopArgs a) {
     }
   }
   if (b == 0 && t == 0) *a.iter += 1;
+}
+
+// ------------------------------------------------------------------ stochastic verification
+struct SampleArgs {
+  int vocab, hidden, n_tiles, m_alloc, ssq_slices;
+  float inv_temp, inv_hidden, eps;
+  const float* tile_sum;     // [M][n_tiles] sums of exp(min(logit / T, 80)) per vocabulary tile
+  const float* draft_logit;  // [M]
+  const int* drafts;         // [B][16]
+  const float* u_accept;     // [B][16]
+  const float* u_sample;     // [B][17]
+  const __half* head;        // [vocab][hidden] the head's f16 rows (as the GEMM reads them)
+  const __half* x16;         // [M][hidden] hi, lo copy m_alloc rows later: the head's input rows
+  const float* ssq;          // [slices][m_alloc] sums of squares of the final residual rows
+  int* decided;              // [B][18]: accepted count a, then out tokens 0..16 (-1 beyond a)
+};
+
+__device__ __forceinline__ float tempered_weight(float logit, float inv_temp) {
+  return __expf(fminf(logit * inv_temp, 80.0f));
+}
+
+// One CTA (256 threads) per request: accept draft j while u_accept[j] < p_j(d_j),
+// p_j = w(d_j) / Z_j with w = exp(min(logit / T, 80)) and Z_j the row's total
+// over the vocabulary; at the first rejection (or after 16 acceptances) sample
+// row a by inverse CDF over token ids in increasing order, without the
+// rejected draft: the vocabulary tile holding the target mass comes from the
+// GEMM's per-tile sums, its 128 logits are recomputed from the head rows.
+__global__ void __launch_bounds__(256) sample_decide_kernel(const SampleArgs a) {
+  __shared__ float red[256];
+  __shared__ float z_row[kRows];
+  __shared__ float w_tile[128];
+  __shared__ int s_acc, s_tile, s_excl;
+  __shared__ float s_base, s_target, s_we;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x, t = threadIdx.x;
+  // Z_j: strided partial sums, then a fixed tree (deterministic)
+  for (int j = 0; j < kRows; ++j) {
+    const float* ts = a.tile_sum + static_cast<size_t>(b * kRows + j) * a.n_tiles;
+    float sum = 0.0f;
+    for (int i = t; i < a.n_tiles; i += 256) sum += ts[i];
+    red[t] = sum;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+      if (t < w) red[t] += red[t + w];
+      __syncthreads();
+    }
+    if (t == 0) z_row[j] = red[0];
+    __syncthreads();
+  }
+  if (t == 0) {
+    int acc = kBlock;
+    for (int j = 0; j < kBlock; ++j) {
+      const int d = a.drafts[b * kBlock + j];
+      const float p = (d >= 0 && d < a.vocab) ? tempered_weight(a.draft_logit[b * kRows + j], a.inv_temp) / z_row[j] : 0.0f;
+      if (!(a.u_accept[b * kBlock + j] < p)) {
+        acc = j;
+        break;
+      }
+    }
+    const int d = acc < kBlock ? a.drafts[b * kBlock + acc] : -1;
+    const bool excl = d >= 0 && d < a.vocab;
+    const float we = excl ? tempered_weight(a.draft_logit[b * kRows + acc], a.inv_temp) : 0.0f;
+    s_acc = acc;
+    s_excl = excl ? d : -1;
+    s_we = we;
+    s_target = a.u_sample[b * kRows + acc] * fmaxf(z_row[acc] - we, 0.0f);
+  }
+  __syncthreads();
+  const int acc = s_acc, r = b * kRows + acc;
+  // the tile holding the target mass: chunk sums of consecutive tiles (the
+  // draft's weight taken out of its tile), a scan of the 256 chunk sums,
+  // then a scan inside the chunk
+  const float* ts = a.tile_sum + static_cast<size_t>(r) * a.n_tiles;
+  const int per = (a.n_tiles + 255) / 256;
+  auto tile_w = [&](int i) { return ts[i] - ((s_excl >= 0 && i == s_excl / 128) ? s_we : 0.0f); };
+  {
+    float sum = 0.0f;
+    for (int i = t * per; i < min(a.n_tiles, (t + 1) * per); ++i) sum += tile_w(i);
+    red[t] = sum;
+  }
+  __syncthreads();
+  if (t == 0) {
+    float run = 0.0f;
+    int c = 255;
+    for (int i = 0; i < 256; ++i) {
+      if (run + red[i] >= s_target && red[i] > 0.0f) {
+        c = i;
+        break;
+      }
+      run += red[i];
+    }
+    int tile = min(a.n_tiles - 1, c * per + per - 1);
+    for (int i = c * per; i < min(a.n_tiles, (c + 1) * per); ++i) {
+      const float wi = tile_w(i);
+      if (run + wi >= s_target && wi > 0.0f) {
+        tile = i;
+        break;
+      }
+      run += wi;
+    }
+    s_tile = tile;
+    s_base = run;
+  }
+  __syncthreads();
+  const int tile = s_tile;
+  // the tile's 128 logits: two threads per head row, halves of the hidden size, 8 values per load
+  float ss = 0.0f;
+  for (int k = 0; k < a.ssq_slices; ++k) ss += a.ssq[static_cast<size_t>(k) * a.m_alloc + r];
+  const float rs = 1.0f / sqrtf(ss * a.inv_hidden + a.eps);
+  {
+    const int i = t >> 1, half = t & 1;
+    const int v = tile * 128 + i;
+    float dot = 0.0f;
+    if (v < a.vocab) {
+      const __half* wrow = a.head + static_cast<size_t>(v) * a.hidden;
+      const __half* xh = a.x16 + static_cast<size_t>(r) * a.hidden;
+      const __half* xl = xh + static_cast<size_t>(a.m_alloc) * a.hidden;
+      const int n8 = a.hidden / 8, h8 = n8 / 2;
+      for (int q = half ? h8 : 0; q < (half ? n8 : h8); ++q) {
+        const uint4 w4 = reinterpret_cast<const uint4*>(wrow)[q];
+        const uint4 h4 = reinterpret_cast<const uint4*>(xh)[q];
+        const uint4 l4 = reinterpret_cast<const uint4*>(xl)[q];
+        const __half2* w2 = reinterpret_cast<const __half2*>(&w4);
+        const __half2* hh = reinterpret_cast<const __half2*>(&h4);
+        const __half2* ll = reinterpret_cast<const __half2*>(&l4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 wf = __half22float2(w2[e]), hf = __half22float2(hh[e]), lf = __half22float2(ll[e]);
+          dot += wf.x * (hf.x + lf.x) + wf.y * (hf.y + lf.y);
+        }
+      }
+    }
+    dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 1);
+    if (half == 0) w_tile[i] = (v < a.vocab && v != s_excl) ? tempered_weight(dot * rs, a.inv_temp) : 0.0f;
+  }
+  __syncthreads();
+  if (t == 0) {
+    float run = s_base;
+    int tok = -1, last = -1;
+    for (int i = 0; i < 128; ++i) {
+      if (w_tile[i] <= 0.0f) continue;
+      last = tile * 128 + i;
+      run += w_tile[i];
+      if (run >= s_target) {
+        tok = last;
+        break;
+      }
+    }
+    if (tok < 0) tok = last;  // rounding: the mass ran out inside the tile
+    int* dec = a.decided + b * (kRows + 1);
+    dec[0] = acc;
+    for (int j = 0; j < kRows; ++j)
+      dec[1 + j] = j < acc ? a.drafts[b * kBlock + j] : (j == acc ? tok : -1);
+  }
 }
 
 // Drafts from the argmax keys of a draft pass: drafts[b][j] = token of row
