@@ -471,6 +471,7 @@ def run_gpu(args, rank: int, world: int):
         "gpu_launches": len(prof),
         "clocks": clk.summary(t_region0, t_region1),
     }
+    result["sampled"] = time_sampled(B, model, kv, Bn, seq, pen, drafts, acc, out, seq0, pend0, flush, stream, args)
     if drafter is not None:
         result["draft"] = time_draft(B, model, drafter, kv, shape, Bn, seq, pen, drafts, acc, out, seq0, pend0, g,
                                      flush, stream, args)
@@ -488,6 +489,39 @@ def run_gpu(args, rank: int, world: int):
                                       "error": (r or {}).get("error", "no result")}
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def time_sampled(B, model, kv, Bn, seq, pen, drafts, acc, out, seq0, pend0, flush, stream, args, temperature=0.7):
+    """The stochastic verification step at temperature 0.7 on the same inputs (graph replay, L2 flushed);
+    uniforms from a fixed generator (they are inputs of the step)."""
+    import torch
+    rng = np.random.default_rng(7)
+    ua = torch.tensor(rng.random((Bn, 16)), dtype=torch.float32, device="cuda")
+    us = torch.tensor(rng.random((Bn, 17)), dtype=torch.float32, device="cuda")
+    gs = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gs, stream=stream):
+        B.vsd_verify_step_sampled(model, kv, Bn, seq, pen, drafts, acc, out, ua, us, temperature, stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        with torch.cuda.stream(stream):
+            seq.copy_(seq0)
+            pen.copy_(pend0)
+            flush.fill_(1.0)
+            if i >= args.warmup:
+                ev[i - args.warmup][0].record(stream)
+            gs.replay()
+            if i >= args.warmup:
+                ev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    if B.vsd_get_device_status(kv) != 0:
+        raise RuntimeError("sampled step reported a device error")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    tokens = int((acc + 1).sum().item())
+    return {"temperature": temperature, "ms_per_step": round(ms, 4), "tokens_per_step": tokens,
+            "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+            "accepted": [int(x) for x in acc.cpu().numpy()],
+            "note": "random-init target: at T = 0.7 a planted draft has p(d) ~ 1e-4, so almost every step emits "
+                    "one sampled token per request; ms_per_step is the cost of the sampled step"}
 
 
 def time_draft(B, model, drafter, kv, shape, Bn, seq, pen, drafts, acc, out, seq0, pend0, g_verify, flush, stream,
