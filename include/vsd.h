@@ -203,7 +203,14 @@ vsd_status vsd_get_device_status(vsd_kv* kv, vsd_stream stream, int32_t* status_
  * Rows [pending, d_0..d_15] run at positions L_b..L_b+16.  Rows 0..a_b (the
  * pending token and the accepted drafts) have their K (after RoPE) and V
  * committed at positions L_b..L_b+a_b; no other cache row changes.  argmax
- * ties go to the lowest token id.  Needs L_b + 17 <= max_tokens_per_req. */
+ * ties go to the lowest token id.  Needs L_b + 17 <= max_tokens_per_req.
+ * The step's kernel launches (about five per layer) are recorded once into a CUDA graph for
+ * each new (model, batch, five device pointers) combination (up to four kept
+ * per cache, oldest replaced; the first call of a combination captures on a
+ * library-owned stream, costing some milliseconds) and replayed on `stream`
+ * afterwards, so reuse the same device buffers across steps.  Launches go
+ * straight to `stream` instead while that stream is itself being captured,
+ * while phase tracing is on, or when the environment sets VSD_NO_STEP_GRAPH. */
 vsd_status vsd_verify_step(const vsd_model* m, vsd_kv* kv, int32_t batch,
                            int32_t* seq_lens_dev, int32_t* pending_dev,
                            const int32_t* drafts_dev, int32_t* accepted_dev,

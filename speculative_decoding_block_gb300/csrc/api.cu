@@ -4,9 +4,11 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -120,6 +122,7 @@ struct vsd_model {
   float2* rope = nullptr;
   int sms = 1;
   int max_clusters[4] = {1, 1, 1, 1};  // resident GEMM clusters of 1, 2, 4, 8 CTAs
+  uint64_t uid = 0;                     // distinct per created model (keys the cached step graphs)
 };
 
 struct vsd_kv {
@@ -144,6 +147,16 @@ struct vsd_kv {
   // stochastic verification: per (row, vocabulary tile) sums, the drafts' logits, the decisions [max_batch][18]
   float *tile_sum = nullptr, *draft_logit = nullptr;
   int* decided = nullptr;
+  // vsd_verify_step replays a graph of the step captured on its first call
+  // with the same arguments (a few kept, oldest replaced)
+  struct StepGraph {
+    uint64_t model_uid;
+    int batch;
+    const void* args[5];
+    cudaGraphExec_t exec;
+  };
+  std::vector<StepGraph> graphs;
+  cudaStream_t capture_stream = nullptr;
   int* status = nullptr;
   unsigned long long* trace = nullptr;  // optional phase timestamps [launch][CTA][tag]
   int trace_launches = 0;
@@ -546,6 +559,8 @@ vsd_status vsd_model_create(const vsd_model_config* cfg, const vsd_weights* w, v
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const vsd_model_config& c = *cfg;
   vsd_model* m = new vsd_model();
+  static std::atomic<uint64_t> next_uid{1};
+  m->uid = next_uid++;
   m->cfg = c;
   m->sms = sm_count();
   for (int i = 0; i < 4; ++i) m->max_clusters[i] = gemm_max_clusters(1 << i);
@@ -692,6 +707,8 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
 
 void vsd_kv_destroy(vsd_kv* kv) {
   if (!kv) return;
+  for (auto& g : kv->graphs) cudaGraphExecDestroy(g.exec);
+  if (kv->capture_stream) cudaStreamDestroy(kv->capture_stream);
   void* ptrs[] = {kv->k_pool, kv->v_pool, kv->page_table, kv->x, kv->u, kv->act_o, kv->act_a, kv->q_tile,
                   kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->req_ok, kv->ssq, kv->attn_o,
                   kv->attn_ml, kv->attn_counters, kv->anchor, kv->zeros, kv->loop_seq, kv->loop_pend,
@@ -1020,10 +1037,52 @@ vsd_status vsd_verify_step_profiled(const vsd_model* m, vsd_kv* kv, int32_t batc
   return VSD_OK;
 }
 
+// The step as one graph launch: its ~5 launches per layer cost more host time
+// than the GPU takes for the step.  Captured on a library stream the first
+// time these arguments are seen, replayed on the caller's stream after.  Not
+// while the caller's stream is itself being captured (its graph then holds
+// the launches), nor with phase tracing on, nor with VSD_NO_STEP_GRAPH set.
+static bool step_graphs_enabled() {
+  static const bool on = getenv("VSD_NO_STEP_GRAPH") == nullptr;
+  return on;
+}
+
 vsd_status vsd_verify_step(const vsd_model* m, vsd_kv* kv, int32_t batch, int32_t* seq_lens, int32_t* pending,
                            const int32_t* drafts, int32_t* accepted, int32_t* out_tokens, vsd_stream stream) {
-  return verify_impl(m, kv, batch, seq_lens, pending, drafts, accepted, out_tokens, nullptr, nullptr,
-                     reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (!m || !kv || kv->trace || !step_graphs_enabled() || cudaStreamIsCapturing(st, &cap) != cudaSuccess ||
+      cap != cudaStreamCaptureStatusNone)
+    return verify_impl(m, kv, batch, seq_lens, pending, drafts, accepted, out_tokens, nullptr, nullptr, st);
+  const void* args[5] = {seq_lens, pending, drafts, accepted, out_tokens};
+  cudaGraphExec_t exec = nullptr;
+  for (auto& g : kv->graphs)
+    if (g.model_uid == m->uid && g.batch == batch && std::equal(args, args + 5, g.args)) exec = g.exec;
+  if (!exec) {
+    if (!kv->capture_stream) CK(cudaStreamCreateWithFlags(&kv->capture_stream, cudaStreamNonBlocking));
+    CK(cudaStreamBeginCapture(kv->capture_stream, cudaStreamCaptureModeThreadLocal));
+    const vsd_status s = verify_impl(m, kv, batch, seq_lens, pending, drafts, accepted, out_tokens, nullptr, nullptr,
+                                     kv->capture_stream);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(kv->capture_stream, &graph);
+    if (s) {
+      if (graph) cudaGraphDestroy(graph);
+      return s;
+    }
+    if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "step capture: %s", cudaGetErrorString(e));
+    const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) return fail(VSD_ERR_CUDA, "step graph: %s", cudaGetErrorString(ei));
+    if (kv->graphs.size() >= 4) {
+      cudaGraphExecDestroy(kv->graphs.front().exec);
+      kv->graphs.erase(kv->graphs.begin());
+    }
+    vsd_kv::StepGraph g{m->uid, batch, {}, exec};
+    std::copy(args, args + 5, g.args);
+    kv->graphs.push_back(g);
+  }
+  CK(cudaGraphLaunch(exec, st));
+  return VSD_OK;
 }
 
 vsd_status vsd_verify_step_debug(const vsd_model* m, vsd_kv* kv, int32_t batch, int32_t* seq_lens, int32_t* pending,
