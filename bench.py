@@ -261,6 +261,19 @@ def finish_oracle(handle, timeout=900):
 
 
 # ------------------------------------------------------------------ GPU arm
+def job_totals(seconds: float, units: float, world: int, device: str = "cpu"):
+    """Whole-job figures of a replicated run: the slowest rank's time and the
+    units all ranks processed (the replicas exchange nothing else)."""
+    if world == 1:
+        return seconds, units
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def run_gpu(args, rank: int, world: int):
     import torch
     from speculative_decoding_block_gb300 import binding as B
@@ -369,11 +382,7 @@ def run_gpu(args, rank: int, world: int):
     if world > 1:
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s, job_tokens = job_totals(sum(step_ms) / 1e3, tokens_per_step * args.steps, world, dev)
 
     # per-kernel times of the same step (events around every launch)
     prof = []
@@ -426,12 +435,13 @@ def run_gpu(args, rank: int, world: int):
             e2e_tokens += int(np.sum(h_acc.numpy() + 1))
     h2d = 4 * Bn + 4 * Bn + 4 * Bn * 16
     d2h = 4 * Bn + 4 * Bn * ROWS + 8 * Bn
-    e2e_value = e2e_tokens * world / sum(e2e_times)
+    e2e_s, e2e_job_tokens = job_totals(sum(e2e_times), e2e_tokens, world, dev)
+    e2e_value = e2e_job_tokens / e2e_s
 
     hbm, tf_burst, tf_sust, peak_src = peaks()
     sb = step_bytes(shape, lens, accepted)
     ms_per_step = total_s * 1e3 / args.steps
-    value = tokens_per_step * args.steps * world / total_s
+    value = job_tokens / total_s
     dk = kernels[dominant]
     achieved = dk["bytes_per_launch"] / (dk["us_avg"] * 1e-6) / 1e9
     result = {
