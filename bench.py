@@ -405,36 +405,31 @@ def run_gpu(args, rank: int, world: int):
         k["share"] = round(k["ms_total"] / tot_prof, 4)
     dominant = max(kernels, key=lambda k: kernels[k]["ms_total"])
 
-    # end to end through the public call: pinned host inputs -> device, step, outputs -> host
-    h_seq = torch.tensor(lens, dtype=torch.int32).pin_memory()
-    h_pen = torch.tensor(pend, dtype=torch.int32).pin_memory()
-    h_dr = torch.tensor(planted, dtype=torch.int32).pin_memory()
-    h_acc = torch.empty(Bn, dtype=torch.int32).pin_memory()
-    h_out = torch.empty((Bn, ROWS), dtype=torch.int32).pin_memory()
-    h_seq_out = torch.empty(Bn, dtype=torch.int32).pin_memory()
-    h_pen_out = torch.empty(Bn, dtype=torch.int32).pin_memory()
+    # end to end through the public host-buffer call: inputs up, the step,
+    # outputs down, all inside vsd_verify_step_host
+    h_seq0 = np.asarray(lens, dtype=np.int32)
+    h_pen0 = np.asarray(pend, dtype=np.int32)
+    h_dr = np.ascontiguousarray(np.asarray(planted, dtype=np.int32))
+    h_seq, h_pen = h_seq0.copy(), h_pen0.copy()
+    h_acc = np.empty(Bn, dtype=np.int32)
+    h_out = np.empty((Bn, ROWS), dtype=np.int32)
     e2e_times = []
     e2e_tokens = 0
     for i in range(args.warmup + args.steps):
         with torch.cuda.stream(stream):
             flush.fill_(1.0)
         stream.synchronize()
+        h_seq[:] = h_seq0
+        h_pen[:] = h_pen0
         t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            seq.copy_(h_seq, non_blocking=True)
-            pen.copy_(h_pen, non_blocking=True)
-            drafts.copy_(h_dr, non_blocking=True)
-            B.vsd_verify_step(model, kv, Bn, seq, pen, drafts, acc, out, stream=stream)
-            h_acc.copy_(acc, non_blocking=True)
-            h_out.copy_(out, non_blocking=True)
-            h_seq_out.copy_(seq, non_blocking=True)
-            h_pen_out.copy_(pen, non_blocking=True)
-        stream.synchronize()
+        B.vsd_verify_step_host(model, kv, Bn, h_seq, h_pen, h_dr, h_acc, h_out, stream=stream)
         if i >= args.warmup:
             e2e_times.append(time.perf_counter() - t0)
-            e2e_tokens += int(np.sum(h_acc.numpy() + 1))
-    h2d = 4 * Bn + 4 * Bn + 4 * Bn * 16
-    d2h = 4 * Bn + 4 * Bn * ROWS + 8 * Bn
+            e2e_tokens += int(np.sum(h_acc + 1))
+    if not np.array_equal(h_acc, accepted):
+        raise RuntimeError("the host-buffer step gave different accepted lengths than the device step")
+    h2d = 4 * Bn * (16 + 2)
+    d2h = 4 * Bn * (3 + ROWS)
     e2e_s, e2e_job_tokens = job_totals(sum(e2e_times), e2e_tokens, world, dev)
     e2e_value = e2e_job_tokens / e2e_s
 
@@ -477,7 +472,7 @@ def run_gpu(args, rank: int, world: int):
         "kernels": kernels,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * statistics.mean(e2e_times), 4),
-                "call": "vsd_verify_step (replays the step graph the library captured on its first call)"},
+                "call": "vsd_verify_step_host (one packed copy each way; replays the step graph the library captured on its first call)"},
         "gpu_launches": len(prof),
         "clocks": clk.summary(t_region0, t_region1),
     }

@@ -216,6 +216,20 @@ vsd_status vsd_verify_step(const vsd_model* m, vsd_kv* kv, int32_t batch,
                            const int32_t* drafts_dev, int32_t* accepted_dev,
                            int32_t* out_tokens_dev, vsd_stream stream);
 
+/* The same step for a caller holding its state in host memory (any host
+ * buffers, pageable or pinned; same shapes and meanings as above).  The
+ * inputs travel to the device as one copy through library-owned staging
+ * (device and pinned host, max_batch * 37 words each, allocated on the first
+ * call and freed with the cache), the step runs as above (the staging
+ * addresses are fixed, so its graph is reused), and lengths, pending tokens,
+ * accepted counts and output rows come back as one copy.  Synchronous: it
+ * returns after the outputs are in the caller's buffers.  VSD_ERR_OOM if the
+ * staging cannot be allocated. */
+vsd_status vsd_verify_step_host(const vsd_model* m, vsd_kv* kv, int32_t batch,
+                                int32_t* seq_lens_host, int32_t* pending_host,
+                                const int32_t* drafts_host, int32_t* accepted_host,
+                                int32_t* out_tokens_host, vsd_stream stream);
+
 /* The same step, also writing float32 logits [B*17, vocab] and the residual
  * stream hidden [layers+1, B*17, hidden] (entry 0 = embeddings, entry l+1 =
  * after layer l); either pointer may be NULL.  Row index = b*17 + j. */

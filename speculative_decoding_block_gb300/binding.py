@@ -27,6 +27,7 @@ EXPORTS = [
     "vsd_kv_read", "vsd_get_device_status", "vsd_verify_step", "vsd_verify_step_debug",
     "vsd_linear", "vsd_block_attention", "vsd_block_attention_static", "vsd_accept_commit",
     "vsd_verify_step_profiled", "vsd_draft_step", "vsd_draft_step_debug", "vsd_kv_get_anchor", "vsd_spec_loop", "vsd_verify_step_sampled",
+    "vsd_verify_step_host",
     "vsd_trace_enable", "vsd_trace_read",
 ]
 KERNEL_KINDS = ["embed", "qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm",
@@ -86,6 +87,7 @@ def lib() -> ctypes.CDLL:
             "vsd_kv_read": ([p, c_int, c_int, c_int, p, p, p], c_int),
             "vsd_get_device_status": ([p, p, ctypes.POINTER(c_int)], c_int),
             "vsd_verify_step": ([p, p, c_int, p, p, p, p, p, p], c_int),
+            "vsd_verify_step_host": ([p, p, c_int, p, p, p, p, p, p], c_int),
             "vsd_verify_step_debug": ([p, p, c_int, p, p, p, p, p, p, p, p], c_int),
             "vsd_verify_step_profiled": ([p, p, c_int, p, p, p, p, p, c_int, p, p, ctypes.POINTER(c_int)],
                                          c_int),
@@ -117,6 +119,22 @@ def _check(status: int) -> None:
 def _stream(stream=None) -> ctypes.c_void_p:
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _host(t, name: str, numel: int):
+    """Address of a contiguous int32 host array (numpy array or CPU tensor) of at least numel elements."""
+    if isinstance(t, torch.Tensor):
+        if t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous int32 CPU tensor")
+        n, ptr = t.numel(), t.data_ptr()
+    else:
+        import numpy as np
+        if not isinstance(t, np.ndarray) or t.dtype != np.int32 or not t.flags.c_contiguous or not t.flags.writeable:
+            raise TypeError(f"{name} must be a writeable contiguous int32 numpy array")
+        n, ptr = t.size, t.ctypes.data
+    if n < numel:
+        raise ValueError(f"{name} holds {n} elements, needs {numel}")
+    return ctypes.c_void_p(ptr)
 
 
 def _dev(t: torch.Tensor | None, dtypes, name: str, numel: int | None = None):
@@ -260,6 +278,15 @@ def vsd_verify_step(model: Model, kv: KV, batch: int, seq_lens, pending, drafts,
                                  _dev(pending, I32, "pending", batch), _dev(drafts, I32, "drafts", batch * 16),
                                  _dev(accepted, I32, "accepted", batch),
                                  _dev(out_tokens, I32, "out_tokens", batch * 17), _stream(stream)))
+
+
+def vsd_verify_step_host(model: Model, kv: KV, batch: int, seq_lens, pending, drafts, accepted, out_tokens,
+                         stream=None) -> None:
+    """The step on host arrays (int32 numpy arrays or CPU tensors); synchronous."""
+    _check(lib().vsd_verify_step_host(model.handle, kv.handle, batch, _host(seq_lens, "seq_lens", batch),
+                                      _host(pending, "pending", batch), _host(drafts, "drafts", batch * 16),
+                                      _host(accepted, "accepted", batch),
+                                      _host(out_tokens, "out_tokens", batch * 17), _stream(stream)))
 
 
 def vsd_verify_step_debug(model: Model, kv: KV, batch: int, seq_lens, pending, drafts, accepted,

@@ -157,6 +157,10 @@ struct vsd_kv {
   };
   std::vector<StepGraph> graphs;
   cudaStream_t capture_stream = nullptr;
+  // host-buffer step: [drafts 16B | seq B | pending B | accepted B | out 17B]
+  // on the device and in pinned host memory (allocated on first use)
+  int* io_dev = nullptr;
+  int* io_host = nullptr;
   int* status = nullptr;
   unsigned long long* trace = nullptr;  // optional phase timestamps [launch][CTA][tag]
   int trace_launches = 0;
@@ -709,6 +713,8 @@ void vsd_kv_destroy(vsd_kv* kv) {
   if (!kv) return;
   for (auto& g : kv->graphs) cudaGraphExecDestroy(g.exec);
   if (kv->capture_stream) cudaStreamDestroy(kv->capture_stream);
+  if (kv->io_dev) cudaFree(kv->io_dev);
+  if (kv->io_host) cudaFreeHost(kv->io_host);
   void* ptrs[] = {kv->k_pool, kv->v_pool, kv->page_table, kv->x, kv->u, kv->act_o, kv->act_a, kv->q_tile,
                   kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->req_ok, kv->ssq, kv->attn_o,
                   kv->attn_ml, kv->attn_counters, kv->anchor, kv->zeros, kv->loop_seq, kv->loop_pend,
@@ -1082,6 +1088,45 @@ vsd_status vsd_verify_step(const vsd_model* m, vsd_kv* kv, int32_t batch, int32_
     kv->graphs.push_back(g);
   }
   CK(cudaGraphLaunch(exec, st));
+  return VSD_OK;
+}
+
+// One packed copy each way through library-owned staging: the step's inputs
+// go up as one block, its outputs (lengths, pending tokens, accepted counts,
+// output rows, laid out contiguously) come back as one block.
+vsd_status vsd_verify_step_host(const vsd_model* m, vsd_kv* kv, int32_t batch, int32_t* seq_lens, int32_t* pending,
+                                const int32_t* drafts, int32_t* accepted, int32_t* out_tokens, vsd_stream stream) {
+  if (!m || !kv || !seq_lens || !pending || !drafts || !accepted || !out_tokens || batch < 1 ||
+      batch > kv->max_batch)
+    return fail(VSD_ERR_ARG, "bad arguments");
+  const size_t cap = static_cast<size_t>(kv->max_batch) * (kBlock + 3 + kRows);
+  if (!kv->io_dev) {
+    vsd_status s;
+    if ((s = dalloc(&kv->io_dev, cap))) return s;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&kv->io_host), cap * sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+      kv->io_host = nullptr;
+      return fail(VSD_ERR_OOM, "pinned staging of %zu bytes", cap * sizeof(int));
+    }
+  }
+  // the layout depends on the batch; the step graph is keyed by the pointers, so each batch size gets its own
+  const size_t B = static_cast<size_t>(batch);
+  int* h = kv->io_host;
+  int* d = kv->io_dev;
+  memcpy(h, drafts, B * kBlock * sizeof(int));
+  memcpy(h + B * kBlock, seq_lens, B * sizeof(int));
+  memcpy(h + B * (kBlock + 1), pending, B * sizeof(int));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t n_in = B * (kBlock + 2), n_out = B * (3 + kRows);
+  CK(cudaMemcpyAsync(d, h, n_in * sizeof(int), cudaMemcpyHostToDevice, st));
+  const vsd_status s = vsd_verify_step(m, kv, batch, d + B * kBlock, d + B * (kBlock + 1), d, d + B * (kBlock + 2),
+                                       d + B * (kBlock + 3), stream);
+  if (s) return s;
+  CK(cudaMemcpyAsync(h + B * kBlock, d + B * kBlock, n_out * sizeof(int), cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  memcpy(seq_lens, h + B * kBlock, B * sizeof(int));
+  memcpy(pending, h + B * (kBlock + 1), B * sizeof(int));
+  memcpy(accepted, h + B * (kBlock + 2), B * sizeof(int));
+  memcpy(out_tokens, h + B * (kBlock + 3), B * kRows * sizeof(int));
   return VSD_OK;
 }
 

@@ -35,6 +35,7 @@ def test_host_side_errors_without_gpu():
     assert L.vsd_quantize_fp8_rowwise(None, 4, 4, None, None, None) == binding.VSD_ERR_ARG
     assert b"NULL" in L.vsd_last_error()
     assert L.vsd_verify_step(None, None, 1, None, None, None, None, None, None) == binding.VSD_ERR_ARG
+    assert L.vsd_verify_step_host(None, None, 1, None, None, None, None, None, None) == binding.VSD_ERR_ARG
     cfg = binding.ModelConfig(2, 256, 4, 2, 96, 688, 4096, 1e4, 1e-6, 1, 0, 0, 256)
     h = ctypes.c_void_p()
     assert L.vsd_model_create(ctypes.byref(cfg), None, None, ctypes.byref(h)) == binding.VSD_ERR_UNSUPPORTED

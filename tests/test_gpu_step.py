@@ -106,3 +106,34 @@ def test_tiny_consecutive_steps_match_oracle(tiny_setup):
         for l in range(TINY.layers):
             assert rel_rows(k_all[l], st.k[l]).max() < KV_TOL
             assert rel_rows(v_all[l], st.v[l]).max() < KV_TOL
+
+
+def test_tiny_host_buffer_steps_match_oracle(tiny_setup):
+    """vsd_verify_step_host on numpy arrays: consecutive steps at batch 3,
+    then a step of the first two requests alone (a different staging
+    layout), each against the oracle."""
+    B, om, model = tiny_setup
+    states = [OM.prefill(om, gen.prompt_ids(TINY.vocab, 40 + 25 * b, 93, b)) for b in range(3)]
+    kv = B.vsd_kv_create(model, 3, 400)
+    for b, st in enumerate(states):
+        load_state(B, kv, b, st)
+    for step, Bn in enumerate([3, 3, 3, 2]):
+        drafts = []
+        for b in range(Bn):
+            k = (step * 7 + b * 5) % 17
+            g = OM.ar_greedy(om, states[b].copy(), min(k + 1, 17))
+            drafts.append(gen.plant_drafts(g, k, TINY.vocab, "host", step, b))
+        seq = np.array([s.length for s in states[:Bn]], dtype=np.int32)
+        pend = np.array([s.pending for s in states[:Bn]], dtype=np.int32)
+        dr = np.ascontiguousarray(np.stack(drafts).astype(np.int32))
+        acc = np.full(Bn, -7, dtype=np.int32)
+        out = np.full((Bn, 17), -7, dtype=np.int32)
+        B.vsd_verify_step_host(model, kv, Bn, seq, pend, dr, acc, out)
+        assert B.vsd_get_device_status(kv) == 0
+        for b in range(Bn):
+            ref = OM.verify_step(om, states[b], drafts[b])   # advances the oracle state
+            ok, tie = near_tie_check(ref, int(acc[b]), out[b])
+            assert ok and tie is None, (step, b)
+            assert int(seq[b]) == states[b].length and int(pend[b]) == states[b].pending
+    with pytest.raises(TypeError):
+        B.vsd_verify_step_host(model, kv, 1, seq.astype(np.int64), pend, dr, acc, out)
