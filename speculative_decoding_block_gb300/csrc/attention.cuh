@@ -119,6 +119,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* cps_s = reinterpret_cast<volatile int*>(tmem_p + 4);
   volatile int* sum_s = reinterpret_cast<volatile int*>(tmem_p + 5);
   auto chunks_of = [&](int b) { return (valid_len(a, b) + 127) / 128 + 1; };
+  // the caller's lengths are read first, so that the loads overlap the set-up
+  int mine = 0;
+  for (int b = threadIdx.x; b < a.batch; b += blockDim.x) mine += chunks_of(b);
 
   if (threadIdx.x == 0) {
     trace_start(a.trace);
@@ -153,8 +156,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // walks about one item.  seq_lens is the caller's input and does not
   // change during the step, so every CTA derives the same split.
   {
-    int mine = 0;
-    for (int b = threadIdx.x; b < a.batch; b += blockDim.x) mine += chunks_of(b);
     if (mine) atomicAdd(const_cast<int*>(sum_s), mine);
     __syncthreads();
     const int total_chunks = *sum_s * a.n_kv;
@@ -169,16 +170,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       __syncthreads();
       if (*sum_s * a.n_kv <= static_cast<int>(gridDim.x) || *sum_s == a.batch) break;
     }
-    if (threadIdx.x == 0) {
-      *cps_s = c;
-      // item list: request-major, then KV head, then split
-      int acc = 0;
-      for (int b = 0; b < a.batch; ++b) {
-        item_off[b] = acc;
-        acc += a.n_kv * ((chunks_of(b) + c - 1) / c);
+    if (warp == 0) {
+      // item list: request-major, then KV head, then split; each request's
+      // first item by an exclusive prefix sum, 32 requests at a time
+      int base = 0;
+      for (int b0 = 0; b0 < a.batch; b0 += 32) {
+        const int b = b0 + lane;
+        const int cnt = b < a.batch ? a.n_kv * ((chunks_of(b) + c - 1) / c) : 0;
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (b < a.batch) item_off[b] = base + incl - cnt;
+        base += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
-      item_off[a.batch] = acc;
-      *n_items = acc;
+      if (lane == 0) {
+        item_off[a.batch] = base;
+        *n_items = base;
+        *cps_s = c;
+      }
     }
     __syncthreads();
   }
@@ -258,17 +270,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         return true;
       };
-      // context pages of the first item: committed by earlier steps, safe before the dependency wait
-      int pre = 0;
+      // The page-table entries of the first item's first chunks, in one round
+      // trip before the dependency wait (lane 8 i + p: page p of chunk i; the
+      // table is the caller's).  Their copies are issued after the wait,
+      // behind the q tile: the cooperative grid starts only once the previous
+      // kernel has left, so copies issued earlier would only queue ahead of q.
+      int npre = 0, pg = -1;
       if (static_cast<int>(blockIdx.x) < total) {
         const Item x = decode(blockIdx.x);
-        int npre = 0;
         while (npre < min(x.n, NS) && x.c_begin + npre < x.n_ctx) ++npre;
-        // the page-table entries of all of these chunks in one round trip (lane 8 i + p: page p of chunk i)
-        int pg = -1;
         if (lane < 8 * npre)
           pg = a.page_table[x.b * a.pages_per_req + min((x.c_begin + lane / 8) * 8 + lane % 8, a.pages_per_req - 1)];
-        for (; pre < npre; ++pre) issue(x, pre, pre, __shfl_sync(0xFFFFFFFFu, pg, (pre * 8 + lane) & 31));  // g < NS: no slot waits
       }
       pdl_wait();  // q tiles and the block's K/V come from the QKV kernel
       if (lane == 0) trace_point(a.trace, 2);
@@ -289,8 +301,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
         for (int i = 0; i < x.n; ++i, ++g) {
-          if (g < pre) continue;  // fetched before the dependency wait
-          if (!issue(x, i, g, -1)) {
+          const int page_pre = (ic == 0 && i < npre) ? __shfl_sync(0xFFFFFFFFu, pg, (i * 8 + lane) & 31) : -1;
+          if (!issue(x, i, g, page_pre)) {
             ok = false;
             break;
           }
