@@ -472,6 +472,8 @@ def run_gpu(args, rank: int, world: int):
         "kernels": kernels,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * statistics.mean(e2e_times), 4),
+                "ms_per_step_median": round(1e3 * statistics.median(e2e_times), 4),
+                "ms_per_step_max": round(1e3 * max(e2e_times), 4),
                 "call": "vsd_verify_step_host (one packed copy each way; replays the step graph the library captured on its first call)"},
         "gpu_launches": len(prof),
         "clocks": clk.summary(t_region0, t_region1),
