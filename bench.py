@@ -24,6 +24,7 @@ import hashlib
 import json
 import multiprocessing as mp
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -100,12 +101,22 @@ def step_flops(shape, lens) -> float:
     return 2.0 * M * params + attn
 
 
+_CODE_TOKENS = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'', re.S)
+
+
+def code_only(src: str) -> str:
+    """C++ source without comments and blank lines (string and char literals kept)."""
+    src = _CODE_TOKENS.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", src)
+    return "\n".join(l.rstrip() for l in src.splitlines() if l.strip())
+
+
 def kernel_source_sha() -> str:
+    """Hash of the library's code (comments and blank lines excluded), naming the build an ncu capture was taken on."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "speculative_decoding_block_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(f.encode() + code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,9 +18,11 @@
 //   O_c = P V     P written as bf16 to shared memory, V read MN-major
 // and the per-chunk O_c is folded into registers with the running rescale.
 // Context pages do not depend on the preceding kernels of the step, so the
-// first stages are fetched before the grid-dependency wait.  Split partials
-// (unnormalised O, max, sum) go to a workspace; the last CTA to finish a
-// (request, head) merges them in split order and writes the f16 output rows.
+// page-table entries of the first chunks are read before the grid-dependency
+// wait (their copies follow the q tile after it).  Split partials
+// (unnormalised O, max, sum) go to a workspace; once all of a (request, head)
+// pair's partials are in, each of its splits merges a slice of the pair's
+// rows in split order and writes those f16 output rows.
 #pragma once
 
 #include "vsd_common.cuh"
