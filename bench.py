@@ -490,6 +490,9 @@ def run_gpu(args, rank: int, world: int):
         "clocks": clk.summary(t_region0, t_region1),
     }
     result["sampled"] = time_sampled(B, model, kv, Bn, seq, pen, drafts, acc, out, seq0, pend0, flush, stream, args)
+    if w.steps > 1:
+        result["consecutive"] = time_consecutive(B, model, kv, shape, w, Bn, seq, pen, seq0, pend0, max_tok, flush,
+                                                 stream)
     if drafter is not None:
         result["draft"] = time_draft(B, model, drafter, kv, shape, Bn, seq, pen, drafts, acc, out, seq0, pend0, g,
                                      flush, stream, args)
@@ -507,6 +510,85 @@ def run_gpu(args, rank: int, world: int):
                                       "error": (r or {}).get("error", "no result")}
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def time_consecutive(B, model, kv, shape, w, Bn, seq, pen, seq0, pend0, max_tok, flush, stream, runs=3):
+    """The workload's consecutive committing steps as one timed unit.  Drafts
+    are planted per step and request (prefix lengths drawn per step) from the
+    library's own greedy trace, taken by a pre-pass from the same start with
+    random drafts (every such step emits the target's greedy tokens, at least
+    one per request).  All steps run as one CUDA graph; lengths and pending
+    tokens are restored before each replay, which recommits identical rows."""
+    import torch
+    S = w.steps
+    ks = np.stack([gen.prefix_lengths(w, s) for s in range(S)])      # [S, B]
+    need = (ks + 1).sum(axis=0) + ROWS                                  # trace tokens per request
+    acc1 = torch.empty(Bn, dtype=torch.int32, device="cuda")
+    out1 = torch.empty((Bn, ROWS), dtype=torch.int32, device="cuda")
+    dr1 = torch.empty((Bn, 16), dtype=torch.int32, device="cuda")
+    seq.copy_(seq0)
+    pen.copy_(pend0)
+    torch.cuda.synchronize()
+    L0 = seq0.cpu().numpy()
+    trace = [[] for _ in range(Bn)]
+    rnd = np.random.default_rng(54321)
+    while any(len(t) < n for t, n in zip(trace, need)):
+        if max(int(L0[b]) + len(trace[b]) for b in range(Bn)) + ROWS > max_tok:
+            raise RuntimeError("greedy trace would outgrow the cache")
+        dr1.copy_(torch.tensor(rnd.integers(0, shape.vocab, (Bn, 16)), dtype=torch.int32))
+        B.vsd_verify_step(model, kv, Bn, seq, pen, dr1, acc1, out1)
+        o = out1.cpu().numpy()
+        for b in range(Bn):
+            trace[b].extend(int(x) for x in o[b] if x >= 0)
+    planted = np.zeros((S, Bn, 16), np.int32)
+    pos = np.zeros(Bn, np.int64)
+    for st in range(S):
+        for b in range(Bn):
+            t = np.asarray(trace[b][pos[b]:pos[b] + ROWS])
+            planted[st, b] = gen.plant_drafts(t, int(ks[st, b]), shape.vocab, "consecutive", w.seed, st, b)
+            pos[b] += int(ks[st, b]) + 1
+    drafts_all = torch.tensor(planted, device="cuda")
+    acc_all = torch.full((S, Bn), -1, dtype=torch.int32, device="cuda")
+    out_all = torch.empty((S, Bn, ROWS), dtype=torch.int32, device="cuda")
+    seq.copy_(seq0)
+    pen.copy_(pend0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for st in range(S):
+            B.vsd_verify_step(model, kv, Bn, seq, pen, drafts_all[st], acc_all[st], out_all[st], stream=stream)
+
+    def replay(ev=None):
+        with torch.cuda.stream(stream):
+            seq.copy_(seq0)
+            pen.copy_(pend0)
+            flush.fill_(1.0)
+            if ev:
+                ev[0].record(stream)
+            g.replay()
+            if ev:
+                ev[1].record(stream)
+
+    replay()
+    torch.cuda.synchronize()
+    if B.vsd_get_device_status(kv) != 0:
+        raise RuntimeError("consecutive steps reported a device error")
+    accs = acc_all.cpu().numpy()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+    for ev in evs:
+        replay(ev)
+    torch.cuda.synchronize()
+    if not np.array_equal(acc_all.cpu().numpy(), accs):
+        raise RuntimeError("consecutive replays disagree")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    tokens = int((accs + 1).sum())
+    return {"steps": S, "replays": runs, "ms_total": round(ms, 3), "ms_per_step": round(ms / S, 4),
+            "tokens": tokens, "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+            "mean_accepted_plus_1": round(float((accs + 1).mean()), 3),
+            "planted_mean_k_plus_1": round(float((ks + 1).mean()), 3),
+            "steps_as_planted": round(float((accs == ks).mean()), 4),
+            "kv_tokens_first_last": [int(L0.sum()), int(L0.sum() + (accs[:-1] + 1).sum())],
+            "graph": f"{S} committing steps in one CUDA graph, L2 flushed before each replay"}
 
 
 def time_sampled(B, model, kv, Bn, seq, pen, drafts, acc, out, seq0, pend0, flush, stream, args, temperature=0.7):
