@@ -541,7 +541,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         atomicAdd(arrived, 1);
         const long long t0 = cycles();
         while (ld_acquire_gpu(arrived) < x.n_splits) {
-          __nanosleep(64);
           if (cycles() - t0 > kWaitLimitCycles) {
             atomicOr(a.status, VSD_DEV_TIMEOUT);
             break;

@@ -176,7 +176,6 @@ constexpr uint32_t kCtrlT = 1024, kCtrlBest = kCtrlT + 2048, kCtrlSq = kCtrlBest
                    kCtrlPos = kCtrlRs + 1024;
 constexpr int kBestCap = 1024;  // token columns whose running argmax fits in shared memory
 constexpr int kMaxRd = 32, kMaxDb = 16, kMaxDa = 4;
-constexpr uint32_t kSleepLongWaitNs = 128;  // back-off of the epilogue's wait for the accumulator
 __host__ __device__ inline uint32_t gemm_ctrl_bytes() { return kCtrlPos + 1024u; }
 __host__ __device__ inline uint32_t gemm_smem_bytes(int wf, int n_tok, int rd, int da, int db, int cs, bool lo,
                                                     bool r_alias) {
@@ -667,9 +666,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           t_last = cycles();
           continue;
         }
-        // nothing to issue: back off briefly, so that this thread does not
-        // take shared-memory and issue slots from the expansion warps
-        __nanosleep(64);
+        // nothing to issue: poll again (a 64 ns back-off here measured
+        // slower, as did one in the epilogue's wait for the accumulator)
         if (*abort_flag || cycles() - t_last > kWaitLimitCycles) {
           if (!*abort_flag) atomicOr(a.status, VSD_DEV_TIMEOUT);
           *abort_flag = 1;
@@ -798,7 +796,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         named_bar_sync(1, ep_n);
         if (et2 == 0 && acc == 0) trace_point(a.trace, 8);
         if (cs > 1 && acc > 0 && !mbar_wait_cluster(rfree, (acc - 1) & 1, abort_flag, a.status)) break;
-        if (!mbar_wait(&tfull[ab], (acc >> 1) & 1, abort_flag, a.status, kSleepLongWaitNs)) break;
+        if (!mbar_wait(&tfull[ab], (acc >> 1) & 1, abort_flag, a.status)) break;
         if (et2 == 0 && acc == 0) trace_point(a.trace, 6);
         if constexpr (EPI == EPI_RESID) {
           // the residual rows this thread updates: into L1 now, read after the reduction

@@ -119,12 +119,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // every warp role, and keeping only the first probe inline keeps those loops
 // short.
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                   int* status, uint32_t sleep_ns) {
+                                                   int* status) {
   const long long t0 = cycles();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i) {
-      if (sleep_ns) __nanosleep(sleep_ns);
       if (mbar_test_wait(bar, parity)) return true;
     }
     if (*abort_flag) return false;
@@ -138,16 +137,16 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 
 // Bounded wait for the phase of `parity` to complete.  Polls with the
 // non-suspending test_wait (a suspended try_wait was seen to miss wake-ups
-// from TMA and MMA completions by microseconds); `sleep_ns` > 0 backs off
-// between probes, for long waits whose polling would otherwise take shared
-// memory and issue slots from the warps doing the work.  Returns false when
+// from TMA and MMA completions by microseconds), without back-off between
+// probes (a 128 ns back-off in the GEMM epilogue's long wait for its
+// accumulator measured 14 us per step slower).  Returns false when
 // another thread of the CTA has raised the abort flag, or after
 // kWaitLimitCycles (then it raises the flag and records VSD_DEV_TIMEOUT in
 // *status).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, uint32_t sleep_ns = 0) {
+                                          int* status) {
   if (mbar_test_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, status, sleep_ns);
+  return mbar_wait_slow(bar, parity, abort_flag, status);
 }
 
 // ------------------------------------------------------------------ clusters
