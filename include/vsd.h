@@ -219,7 +219,7 @@ vsd_status vsd_verify_step(const vsd_model* m, vsd_kv* kv, int32_t batch,
 /* The same step for a caller holding its state in host memory (any host
  * buffers, pageable or pinned; same shapes and meanings as above).  The
  * inputs travel to the device as one copy through library-owned staging
- * (device and pinned host, max_batch * 37 words each, allocated on the first
+ * (device and pinned host, max_batch * 36 words each, allocated on the first
  * call and freed with the cache), the step runs as above (the staging
  * addresses are fixed, so its graph is reused), and lengths, pending tokens,
  * accepted counts and output rows come back as one copy.  Synchronous: it
