@@ -1,4 +1,5 @@
-"""The bench's whole-job figures over two replica ranks (gloo on CPU).
+"""bench.py host logic: whole-job figures over replica ranks (gloo on CPU),
+and the hash naming the build an ncu capture was taken on.
 
 A multi-GPU run is replicas only: each rank runs the same step on its own
 requests and nothing crosses ranks on the data path.  The job's time is the
@@ -51,3 +52,16 @@ def test_job_totals_take_slowest_rank_and_all_units(world):
 
 def test_job_totals_single_rank_is_identity():
     assert bench.job_totals(0.3, 42.0, 1) == (0.3, 42.0)
+
+
+def test_kernel_hash_ignores_comments_and_blank_lines():
+    """The hash that names the build an ncu capture was taken on changes with
+    the code, not with its comments (string literals count as code)."""
+    a = 'int f() {  // one\n  return 1; /* two\n three */\n\n}\nconst char* s = "x // y";\n'
+    b = 'int f() {\n  return 1;\n}\nconst char* s = "x // y";  // other words\n'
+    c = 'int f() {\n  return 2;\n}\nconst char* s = "x // y";\n'
+    d = 'int f() {\n  return 1;\n}\nconst char* s = "x // z";\n'
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
+    assert bench.code_only(a) != bench.code_only(d)
+    assert len(bench.kernel_source_sha()) == 16
