@@ -464,9 +464,11 @@ def run_gpu(args, rank: int, world: int):
         "dtype": "f16",
         "data": "synthetic (seeded random-init weights, random KV context, planted draft prefixes)",
         "config": {
-            "workload": w.name, "model": shape.name, "layers": shape.layers, "hidden": shape.hidden,
-            "heads": f"{shape.n_q}q/{shape.n_kv}kv/{shape.head_dim}", "ffn": shape.ffn, "vocab": shape.vocab,
-            "weights": f"attn {shape.attn_fmt}, mlp {shape.mlp_fmt}, embed/lm_head bf16",
+            "workload": w.name,
+            "shape": {"name": shape.name, "layers": shape.layers, "hidden": shape.hidden,
+                      "heads": f"{shape.n_q}q/{shape.n_kv}kv/{shape.head_dim}", "ffn": shape.ffn,
+                      "vocab": shape.vocab,
+                      "weights": f"attn {shape.attn_fmt}, mlp {shape.mlp_fmt}, embed/lm_head bf16"},
             "batch": Bn, "rows_per_request": ROWS, "ctx_lens": [int(x) for x in lens],
             "paged": w.paged, "accepted": [int(a) for a in accepted],
             "tokens_per_step": tokens_per_step, "mean_accepted_plus_1": round(tokens_per_step / Bn, 3),
@@ -762,7 +764,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded random-init weights, random KV context, planted draft prefixes)",
-        "config": {"workload": w.name, "model": shape.name, "batch_sample": "one request per step, requests 0-1",
+        "config": {"workload": w.name, "batch_sample": "one request per step, requests 0-1",
                    "parallelism": "none (host cores)"},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} float64 verify steps (one request each), {dt:.1f} s"},
