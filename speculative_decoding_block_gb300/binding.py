@@ -121,16 +121,19 @@ def _stream(stream=None) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _host(t, name: str, numel: int):
-    """Address of a contiguous int32 host array (numpy array or CPU tensor) of at least numel elements."""
+def _host(t, name: str, numel: int, writable: bool = True):
+    """Address of a contiguous int32 host array (numpy array or CPU tensor) of at least numel elements;
+    writable for the arrays the call writes."""
     if isinstance(t, torch.Tensor):
         if t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
             raise TypeError(f"{name} must be a contiguous int32 CPU tensor")
         n, ptr = t.numel(), t.data_ptr()
     else:
         import numpy as np
-        if not isinstance(t, np.ndarray) or t.dtype != np.int32 or not t.flags.c_contiguous or not t.flags.writeable:
-            raise TypeError(f"{name} must be a writeable contiguous int32 numpy array")
+        if not isinstance(t, np.ndarray) or t.dtype != np.int32 or not t.flags.c_contiguous:
+            raise TypeError(f"{name} must be a contiguous int32 numpy array")
+        if writable and not t.flags.writeable:
+            raise TypeError(f"{name} is written by the call and must be writeable")
         n, ptr = t.size, t.ctypes.data
     if n < numel:
         raise ValueError(f"{name} holds {n} elements, needs {numel}")
@@ -284,7 +287,7 @@ def vsd_verify_step_host(model: Model, kv: KV, batch: int, seq_lens, pending, dr
                          stream=None) -> None:
     """The step on host arrays (int32 numpy arrays or CPU tensors); synchronous."""
     _check(lib().vsd_verify_step_host(model.handle, kv.handle, batch, _host(seq_lens, "seq_lens", batch),
-                                      _host(pending, "pending", batch), _host(drafts, "drafts", batch * 16),
+                                      _host(pending, "pending", batch), _host(drafts, "drafts", batch * 16, writable=False),
                                       _host(accepted, "accepted", batch),
                                       _host(out_tokens, "out_tokens", batch * 17), _stream(stream)))
 

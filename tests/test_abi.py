@@ -42,3 +42,23 @@ def test_host_side_errors_without_gpu():
     assert b"head_dim" in L.vsd_last_error()
     cfg.head_dim, cfg.n_q = 64, 3
     assert L.vsd_model_create(ctypes.byref(cfg), None, None, ctypes.byref(h)) == binding.VSD_ERR_ARG
+
+
+def test_host_array_checks():
+    """The host-buffer step's argument marshalling: int32, contiguous, long
+    enough, writeable where the call writes."""
+    import numpy as np
+    import pytest
+    ok = np.zeros(34, dtype=np.int32)
+    assert binding._host(ok, "a", 34).value == ok.ctypes.data
+    with pytest.raises(TypeError):
+        binding._host(ok.astype(np.int64), "a", 34)
+    with pytest.raises(TypeError):
+        binding._host(np.zeros((4, 9), np.int32)[:, :8], "a", 32)
+    with pytest.raises(ValueError):
+        binding._host(ok, "a", 35)
+    ro = np.zeros(16, dtype=np.int32)
+    ro.flags.writeable = False
+    assert binding._host(ro, "drafts", 16, writable=False).value == ro.ctypes.data
+    with pytest.raises(TypeError):
+        binding._host(ro, "seq_lens", 16)
