@@ -60,7 +60,7 @@ def kernel_bytes(shape, lens, accepted):
     H = shape.hidden
     kv_row = 2 * shape.n_kv * shape.head_dim * 2            # K + V of one token, one layer
     act = lambda k: M * k * 2
-    return {
+    d = {
         "embed": M * H * 2 + M * H * 6 + M * 4,
         "qkv_gemm": sum(weight_bytes(shape, n) for n in ("wq", "wk", "wv")) + act(H),
         "attention": int(np.sum(lens)) * kv_row + M * shape.n_q * shape.head_dim * 2 * 2,
@@ -70,6 +70,10 @@ def kernel_bytes(shape, lens, accepted):
         "lm_head_gemm": shape.vocab * H * 2 + act(H),
         "accept_commit": int(np.sum(np.asarray(accepted) + 1)) * kv_row * shape.layers + B * 4 * 60,
     }
+    # the persistent launch: every layer's GEMMs and attention, then the head
+    per_layer = sum(d[k] for k in ("qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm"))
+    d["step"] = per_layer * shape.layers + d["lm_head_gemm"]
+    return d
 
 
 def step_bytes(shape, lens, accepted) -> int:

@@ -249,8 +249,10 @@ vsd_status vsd_verify_step_debug(const vsd_model* m, vsd_kv* kv, int32_t batch,
  * rejected row a gives out[a] = a sample of p_a without d_a; after 16
  * acceptances out[16] = a sample of p_16.  Samples are drawn by inverse CDF
  * over token ids in increasing order at u_sample[b][a] (the smallest id whose
- * cumulative mass reaches u times the total).  Weights exp(min(logit / T, 80))
- * in float32.  Commits as the greedy step.
+ * cumulative mass reaches u times the total).  Weights are float32 and taken
+ * relative to each row's largest logit, exp((logit - max) / T), so any logit
+ * magnitude and any T > 0 give the softmax (no overflow, no clamp).  Commits
+ * as the greedy step.
  *   u_accept_dev float32 [B, 16], u_sample_dev float32 [B, 17]: uniforms in
  *                (0, 1), the caller's random numbers
  *   logits_dev   optional float32 [B*17, vocab]
@@ -271,6 +273,7 @@ vsd_status vsd_verify_step_sampled(const vsd_model* m, vsd_kv* kv, int32_t batch
 #define VSD_K_DOWN       5  /* down GEMM + residual */
 #define VSD_K_LM_HEAD    6  /* lm_head GEMM + RMSNorm scale + argmax */
 #define VSD_K_COMMIT     7  /* accept + KV commit */
+#define VSD_K_STEP       8  /* the decoder layers and the head in one persistent launch */
 
 /* The same step with a CUDA event recorded before and after every kernel
  * launch (which keeps each launch from overlapping its neighbours).  Writes,

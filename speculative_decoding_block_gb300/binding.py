@@ -31,7 +31,7 @@ EXPORTS = [
     "vsd_trace_enable", "vsd_trace_read",
 ]
 KERNEL_KINDS = ["embed", "qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm",
-                "lm_head_gemm", "accept_commit"]
+                "lm_head_gemm", "accept_commit", "step"]
 
 
 class VsdError(RuntimeError):

@@ -99,10 +99,9 @@ struct Linear {
   int n_rows = 0;   // packed rows with data (tile rows beyond are zero)
   int k = 0;
   int n_tiles = 0, k_tiles = 0;
-  void* data = nullptr;        // BF16 [n_rows][k] | FP8 / NVFP4 tiles
+  void* data = nullptr;        // tiles [n_tiles][k_tiles]: f16 (BF16 weights, MMA layout) | FP8 | NVFP4
   float* row_scale = nullptr;  // FP8 / NVFP4
   bool owns = true;
-  CUtensorMap tm{};            // BF16 only
 };
 
 void free_linear(Linear& l) {
@@ -123,6 +122,7 @@ struct vsd_model {
   int sms = 1;
   int max_clusters[4] = {1, 1, 1, 1};  // resident GEMM clusters of 1, 2, 4, 8 CTAs
   uint64_t uid = 0;                     // distinct per created model (keys the cached step graphs)
+  MkLayerW* mk_layers = nullptr;        // device [layers]: tile and scale pointers of every layer
 };
 
 struct vsd_kv {
@@ -145,7 +145,7 @@ struct vsd_kv {
   // slot state of the device-resident loop: lengths, pending, drafts, accepted [max_batch], outputs [max_batch][17]
   int *loop_seq = nullptr, *loop_pend = nullptr, *loop_drafts = nullptr, *loop_acc = nullptr, *loop_out = nullptr;
   // stochastic verification: per (row, vocabulary tile) sums, the drafts' logits, the decisions [max_batch][18]
-  float *tile_sum = nullptr, *draft_logit = nullptr;
+  float *tile_max = nullptr, *tile_sum = nullptr, *draft_logit = nullptr;
   int* decided = nullptr;
   // vsd_verify_step replays a graph of the step captured on its first call
   // with the same arguments (a few kept, oldest replaced)
@@ -162,6 +162,10 @@ struct vsd_kv {
   int* io_dev = nullptr;
   int* io_host = nullptr;
   int* status = nullptr;
+  // persistent step kernel: phase counters (+ exit counter, abort flag), split-k partial sums, per-item counters
+  int* mk_sync = nullptr;
+  float* mk_part = nullptr;
+  int* mk_item_cnt = nullptr;
   unsigned long long* trace = nullptr;  // optional phase timestamps [launch][CTA][tag]
   int trace_launches = 0;
   int trace_seq = 0;
@@ -218,13 +222,12 @@ vsd_status build_linear(const vsd_weight* const* parts, const int* part_rows, in
       off += static_cast<size_t>(part_rows[i]) * K;
     }
     uint16_t* packed = nullptr;
-    if ((s = dalloc(&packed, static_cast<size_t>(np) * K, false))) return s;
-    pack_bf16_kernel<<<1024, 256, 0, st>>>(stacked, perm_d, np, K, packed);
+    if ((s = dalloc(&packed, static_cast<size_t>(L.n_tiles) * L.k_tiles * 8192, false))) return s;
+    pack_bf16_tiles_kernel<<<dim3(L.k_tiles, L.n_tiles), 256, 0, st>>>(stacked, perm_d, np, K, L.k_tiles, packed);
     CK(cudaGetLastError());
     CK(cudaStreamSynchronize(st));
     cudaFree(stacked);
     L.data = packed;
-    if ((s = tmap_2d(&L.tm, packed, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, np, 64, 128))) return s;
   } else {
     const size_t vbytes_row = fmt == VSD_FMT_FP8 ? K : K / 2;
     uint8_t* stacked = nullptr;
@@ -421,7 +424,7 @@ vsd_status run_gemm(const vsd_model* m, const Linear& w, int epi, const CUtensor
   a.r_alias = p.r_alias ? 1 : 0;
   if (gemm_smem_bytes(w.fmt, p.n_tok, p.rd, p.da, p.db, p.cs, lo, p.r_alias) > 232448)
     return fail(VSD_ERR_UNSUPPORTED, "GEMM tile does not fit in shared memory");
-  const cudaError_t e = launch_gemm(w.fmt, epi, tm_acts[p.n_tok / 16 - 1], w.tm, a, p.grid, st, use_pdl(st));
+  const cudaError_t e = launch_gemm(w.fmt, epi, tm_acts[p.n_tok / 16 - 1], a, p.grid, st, use_pdl(st));
   if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
   return VSD_OK;
 }
@@ -605,6 +608,19 @@ vsd_status vsd_model_create(const vsd_model_config* cfg, const vsd_weights* w, v
     if ((s = build_linear(&dp, &orows, 1, F, identity_perm(H), st, &lin))) return cleanup(s);
     m->down.push_back(lin);
   }
+  {
+    std::vector<MkLayerW> tab(c.layers);
+    for (int l = 0; l < c.layers; ++l) {
+      const Linear* ls[4] = {&m->qkv[l], &m->o[l], &m->gu[l], &m->down[l]};
+      for (int k = 0; k < 4; ++k) {
+        tab[l].w[k] = static_cast<const uint8_t*>(ls[k]->data);
+        tab[l].s[k] = ls[k]->row_scale;
+      }
+    }
+    if ((s = dalloc(&m->mk_layers, tab.size(), false))) return cleanup(s);
+    if (cudaMemcpy(m->mk_layers, tab.data(), tab.size() * sizeof(MkLayerW), cudaMemcpyHostToDevice))
+      return cleanup(fail(VSD_ERR_CUDA, "layer table copy failed"));
+  }
   // RoPE table: angle = pos * theta^(-2i/hd), evaluated in double, stored as fp32 (cos, sin)
   {
     const int half = hd / 2;
@@ -630,6 +646,7 @@ void vsd_model_destroy(vsd_model* m) {
     for (auto& l : *v) free_linear(l);
   if (m->embed) cudaFree(m->embed);
   if (m->rope) cudaFree(m->rope);
+  if (m->mk_layers) cudaFree(m->mk_layers);
   delete m;
 }
 
@@ -679,12 +696,18 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
       (s = dalloc(&kv->loop_seq, max_batch)) || (s = dalloc(&kv->loop_pend, max_batch)) ||
       (s = dalloc(&kv->loop_drafts, static_cast<size_t>(max_batch) * kBlock)) ||
       (s = dalloc(&kv->loop_acc, max_batch)) || (s = dalloc(&kv->loop_out, static_cast<size_t>(max_batch) * kRows)) ||
+      (s = dalloc(&kv->tile_max, static_cast<size_t>(kv->m_alloc) * m->lm.n_tiles)) ||
       (s = dalloc(&kv->tile_sum, static_cast<size_t>(kv->m_alloc) * m->lm.n_tiles)) ||
       (s = dalloc(&kv->draft_logit, kv->m_alloc)) ||
       (s = dalloc(&kv->decided, static_cast<size_t>(max_batch) * (kRows + 1))) ||
       (s = dalloc(&kv->status, 1)))
     return cleanup(s);
   if ((s = dalloc(&kv->ssq, static_cast<size_t>(ceil_div(H, kTileN)) * kv->m_alloc))) return cleanup(s);
+  // persistent step kernel: counters zero between launches (the kernel resets them on exit)
+  if ((s = dalloc(&kv->mk_sync, static_cast<size_t>(5) * c.layers + 3)) ||
+      (s = dalloc(&kv->mk_item_cnt, static_cast<size_t>(2) * kMaxSplitItems)) ||
+      (s = dalloc(&kv->mk_part, static_cast<size_t>(m->sms) * kMkMaxTok * kTileN, false)))
+    return cleanup(s);
   kv->attn_items_cap = static_cast<size_t>(4) * m->sms + static_cast<size_t>(2) * max_batch * c.n_kv;
   if ((s = dalloc(&kv->attn_o, kv->attn_items_cap * 128 * hd, false)) ||
       (s = dalloc(&kv->attn_ml, kv->attn_items_cap * 128 * 2, false)) ||
@@ -718,8 +741,8 @@ void vsd_kv_destroy(vsd_kv* kv) {
   void* ptrs[] = {kv->k_pool, kv->v_pool, kv->page_table, kv->x, kv->u, kv->act_o, kv->act_a, kv->q_tile,
                   kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->req_ok, kv->ssq, kv->attn_o,
                   kv->attn_ml, kv->attn_counters, kv->anchor, kv->zeros, kv->loop_seq, kv->loop_pend,
-                  kv->loop_drafts, kv->loop_acc, kv->loop_out, kv->tile_sum, kv->draft_logit, kv->decided,
-                  kv->status, kv->trace};
+                  kv->loop_drafts, kv->loop_acc, kv->loop_out, kv->tile_max, kv->tile_sum, kv->draft_logit, kv->decided,
+                  kv->status, kv->trace, kv->mk_sync, kv->mk_part, kv->mk_item_cnt};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete kv;
@@ -836,51 +859,6 @@ struct LaunchTimer {
     if (timer) timer->after();    \
   } while (0)
 
-// The decoder layers of model m over the M = 17 B rows already in the
-// residual scratch; attention reads attn_lens[b] cached rows per request.
-static vsd_status run_layers(const vsd_model* m, vsd_kv* kv, int B, const int* attn_lens, float* hidden,
-                             cudaStream_t st, LaunchTimer* timer) {
-  const vsd_model_config& c = m->cfg;
-  const int M = kRows * B, H = c.hidden;
-  vsd_status s;
-  const size_t layer_scratch = static_cast<size_t>(kv->max_batch) * c.n_kv * 32 * c.head_dim;
-  for (int l = 0; l < c.layers; ++l) {
-    GemmArgs a{};
-    set_norm_input(a, kv);
-    a.q_tile = kv->q_tile;
-    a.act_lo_rows = kv->m_alloc;
-    a.out_lo = static_cast<size_t>(kv->max_batch) * c.n_kv * 128 * c.head_dim;
-    a.k_new = kv->k_new + l * layer_scratch;
-    a.v_new = kv->v_new + l * layer_scratch;
-    a.ctx_len = kv->ctx_len;
-    a.rope = m->rope;
-    a.n_q = c.n_q;
-    a.n_kv = c.n_kv;
-    a.head_dim = c.head_dim;
-    TIMED(VSD_K_QKV, if ((s = run_gemm(m, m->qkv[l], EPI_QKV, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
-    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, attn_lens, st, true))) return s);
-    GemmArgs r{};
-    r.out_f32 = kv->x;
-    r.ld_out = H;
-    r.x16_out = kv->u;
-    r.act_lo_rows = kv->m_alloc;
-    r.out_lo = static_cast<size_t>(kv->m_alloc) * H;
-    r.ssq_out = kv->ssq;
-    r.ssq_ld = kv->m_alloc;
-    TIMED(VSD_K_O_PROJ, if ((s = run_gemm(m, m->o[l], EPI_RESID, kv->tm_o, M, r, kv->status, st, next_trace(kv)))) return s);
-    GemmArgs g{};
-    set_norm_input(g, kv);
-    g.act_out = kv->act_a;
-    g.act_lo_rows = kv->m_alloc;
-    g.out_lo = static_cast<size_t>(kv->m_alloc) * c.ffn;
-    g.ffn = c.ffn;
-    TIMED(VSD_K_GATE_UP, if ((s = run_gemm(m, m->gu[l], EPI_SILU, kv->tm_u, M, g, kv->status, st, next_trace(kv)))) return s);
-    r.hidden_out = hidden ? hidden + static_cast<size_t>(l + 1) * M * H : nullptr;
-    TIMED(VSD_K_DOWN, if ((s = run_gemm(m, m->down[l], EPI_RESID, kv->tm_a, M, r, kv->status, st, next_trace(kv)))) return s);
-  }
-  return VSD_OK;
-}
-
 // Stochastic verification inputs of one step (nullptr: greedy).
 struct SampleIn {
   float inv_temp;
@@ -888,24 +866,148 @@ struct SampleIn {
   const float* u_sample;  // [B][17]
 };
 
-// Final RMSNorm + lm_head: per-row argmax keys (kv->keys; greedy) or, with
-// `smp`, the per-tile exp sums and the drafts' logits; logits optional.
-static vsd_status run_head(const vsd_model* m, vsd_kv* kv, int M, float* logits, cudaStream_t st, LaunchTimer* timer,
-                           const int* drafts = nullptr, const SampleIn* smp = nullptr) {
-  vsd_status s;
-  GemmArgs a{};
-  set_norm_input(a, kv);
-  a.keys = kv->keys;
-  a.logits = logits;
-  a.act_lo_rows = kv->m_alloc;
-  if (smp) {
-    a.inv_temp = smp->inv_temp;
-    a.drafts = drafts;
-    a.tile_sum = kv->tile_sum;
-    a.draft_logit = kv->draft_logit;
+// The decoder layers of model m over the M = 17 B rows already in the
+// residual scratch, then the final RMSNorm + head: per-row argmax keys
+// (kv->keys; greedy) or, with `smp`, the per-tile exp sums and the drafts'
+// logits; logits and hidden rows optional.  Attention reads attn_lens[b]
+// cached rows per request.  One persistent launch (persistent.cuh).
+static vsd_status run_persistent(const vsd_model* m, vsd_kv* kv, int B, const int* attn_lens, float* hidden,
+                                 float* logits, const int* drafts, const SampleIn* smp, cudaStream_t st) {
+  const vsd_model_config& c = m->cfg;
+  const int M = kRows * B, H = c.hidden, G = m->sms;
+  if (B > kMaxReqs) return fail(VSD_ERR_UNSUPPORTED, "at most %d requests per step", kMaxReqs);
+  if (c.layers > kv->m->cfg.layers) return fail(VSD_ERR_ARG, "model deeper than the cache's target");
+  MkParams p{};
+  const int tok_tiles = ceil_div(M, kMkMaxTok);
+  const int n_tok = round_up(ceil_div(M, tok_tiles), 16);
+  p.tm_act[0] = kv->tm_u[n_tok / 16 - 1];
+  p.tm_act[1] = kv->tm_o[n_tok / 16 - 1];
+  p.tm_act[2] = kv->tm_a[n_tok / 16 - 1];
+  p.tm_q = kv->tm_q;
+  p.tm_kc = kv->tm_kc;
+  p.tm_vc = kv->tm_vc;
+  p.tm_kn = kv->tm_kn;
+  p.tm_vn = kv->tm_vn;
+  const Linear* lin[kMkKinds] = {&m->qkv[0], &m->o[0], &m->gu[0], &m->down[0], &m->lm};
+  const int act_of[kMkKinds] = {0, 1, 0, 2, 0};
+  for (int k = 0; k < kMkKinds; ++k) {
+    GemmArgs& a = p.g[k];
+    const Linear& w = *lin[k];
+    a.n_rows = w.n_rows;
+    a.n_tiles = w.n_tiles;
+    a.k_tiles = w.k_tiles;
+    a.tok_tiles = tok_tiles;
+    a.n_tok = n_tok;
+    a.m_tokens = M;
+    // k split over consecutive CTAs when the output tiles alone leave most
+    // SMs idle: as many members as fit the grid in one round, each with at
+    // least one k tile and one 16-column group to finish
+    const int items = w.n_tiles * tok_tiles;
+    a.cs = 1;
+    a.kps = w.k_tiles;
+    if (k != 4 && 2 * items <= G) {
+      const int cs_max = std::min({G / items, w.k_tiles, n_tok / 16});
+      a.kps = ceil_div(w.k_tiles, cs_max);
+      a.cs = ceil_div(w.k_tiles, a.kps);
+    }
+    if (a.cs > 1 && (items > kMaxSplitItems || static_cast<size_t>(items) * a.cs > static_cast<size_t>(G)))
+      return fail(VSD_ERR_UNSUPPORTED, "split-k plan outside the workspace");
+    a.act_lo_rows = kv->m_alloc;
+    a.status = kv->status;
+    p.wf[k] = w.fmt;
+    p.act_of[k] = act_of[k];
   }
-  TIMED(VSD_K_LM_HEAD, if ((s = run_gemm(m, m->lm, smp ? EPI_SAMPLE : EPI_ARGMAX, kv->tm_u, M, a, kv->status, st,
-                                         next_trace(kv)))) return s);
+  {  // QKV: RoPE, q tile, block K / V scratch
+    GemmArgs& a = p.g[0];
+    set_norm_input(a, kv);
+    a.q_tile = kv->q_tile;
+    a.out_lo = static_cast<size_t>(kv->max_batch) * c.n_kv * 128 * c.head_dim;
+    a.k_new = kv->k_new;
+    a.v_new = kv->v_new;
+    a.kv_layer_stride = static_cast<size_t>(kv->max_batch) * c.n_kv * 32 * c.head_dim;
+    a.ctx_len = kv->ctx_len;
+    a.rope = m->rope;
+    a.n_q = c.n_q;
+    a.n_kv = c.n_kv;
+    a.head_dim = c.head_dim;
+  }
+  for (int k : {1, 3}) {  // O and down: residual update, f16 copy, sums of squares
+    GemmArgs& a = p.g[k];
+    a.out_f32 = kv->x;
+    a.ld_out = H;
+    a.x16_out = kv->u;
+    a.out_lo = static_cast<size_t>(kv->m_alloc) * H;
+    a.ssq_out = kv->ssq;
+    a.ssq_ld = kv->m_alloc;
+  }
+  if (hidden) {  // layer l's output rows at hidden + (l + 1) M H
+    p.g[3].hidden_out = hidden + static_cast<size_t>(M) * H;
+    p.g[3].hidden_layer_stride = static_cast<size_t>(M) * H;
+  }
+  {  // gate/up: SiLU(gate) * up
+    GemmArgs& a = p.g[2];
+    set_norm_input(a, kv);
+    a.act_out = kv->act_a;
+    a.out_lo = static_cast<size_t>(kv->m_alloc) * c.ffn;
+    a.ffn = c.ffn;
+  }
+  {  // head
+    GemmArgs& a = p.g[4];
+    set_norm_input(a, kv);
+    a.w_tiles = static_cast<const uint8_t*>(m->lm.data);
+    a.row_scale = m->lm.row_scale;
+    a.logits = logits;
+    if (smp) {
+      a.inv_temp = smp->inv_temp;
+      a.drafts = drafts;
+      a.tile_max = kv->tile_max;
+      a.tile_sum = kv->tile_sum;
+      a.draft_logit = kv->draft_logit;
+    } else {
+      a.keys = kv->keys;
+    }
+  }
+  {  // attention (every layer; the layer is the phase's)
+    AttnArgs& a = p.at;
+    const int max_chunks = ceil_div(kv->max_tokens, 128) + 1;
+    const int cps = std::max(1, ceil_div(B * c.n_kv * max_chunks, 2 * G));
+    const int max_splits = ceil_div(max_chunks, cps);
+    if (static_cast<size_t>(B) * c.n_kv * max_splits > kv->attn_items_cap)
+      return fail(VSD_ERR_UNSUPPORTED, "attention workspace too small");
+    a.batch = B;
+    a.batch_cap = kv->max_batch;
+    a.n_q = c.n_q;
+    a.n_kv = c.n_kv;
+    a.hd = c.head_dim;
+    a.group = c.n_q / c.n_kv;
+    a.rows_valid = kRows * a.group;
+    a.chunks_per_split = cps;
+    a.max_splits = max_splits;
+    a.num_pages = kv->num_pages;
+    a.pages_per_req = kv->ppr;
+    a.max_tokens = kv->max_tokens;
+    a.seq_lens = attn_lens;
+    a.page_table = kv->page_table;
+    a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
+    a.part_o = kv->attn_o;
+    a.part_ml = kv->attn_ml;
+    a.counters = kv->attn_counters;
+    a.out = kv->act_o;
+    a.out_lo = static_cast<size_t>(kv->m_alloc) * c.n_q * c.head_dim;
+    a.q_lo_rows = kv->max_batch * c.n_kv * 128;
+    a.status = kv->status;
+  }
+  p.layers = m->mk_layers;
+  p.n_layers = c.layers;
+  p.sync = kv->mk_sync;
+  p.part = kv->mk_part;
+  p.item_cnt = kv->mk_item_cnt;
+  p.status = kv->status;
+  // launch ids: one per phase, one more for the kernel's start / end stamps
+  p.trace = next_trace(kv);
+  if (kv->trace) kv->trace_seq += 5 * c.layers + 1;
+  const cudaError_t e = launch_step(c.head_dim, p, G, st);
+  if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "step launch: %s", cudaGetErrorString(e));
   return VSD_OK;
 }
 
@@ -941,8 +1043,7 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     e.trace = next_trace(kv);
     TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), false, e)));
   }
-  if ((s = run_layers(m, kv, B, seq_lens, hidden, st, timer))) return s;
-  if ((s = run_head(m, kv, M, logits, st, timer, drafts, smp))) return s;
+  TIMED(VSD_K_STEP, if ((s = run_persistent(m, kv, B, seq_lens, hidden, logits, drafts, smp, st))) return s);
   if (smp) {
     SampleArgs sa{};
     sa.vocab = c.vocab;
@@ -953,12 +1054,14 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     sa.inv_temp = smp->inv_temp;
     sa.inv_hidden = 1.0f / static_cast<float>(H);
     sa.eps = c.eps;
+    sa.tile_max = kv->tile_max;
     sa.tile_sum = kv->tile_sum;
     sa.draft_logit = kv->draft_logit;
     sa.drafts = drafts;
     sa.u_accept = smp->u_accept;
     sa.u_sample = smp->u_sample;
     sa.head = static_cast<const __half*>(m->lm.data);
+    sa.head_k_tiles = m->lm.k_tiles;
     sa.x16 = kv->u;
     sa.ssq = kv->ssq;
     sa.decided = kv->decided;
@@ -1014,8 +1117,7 @@ static vsd_status draft_impl(const vsd_model* d, vsd_kv* kv, int B, const int* s
     e.trace = next_trace(kv);
     TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), false, e)));
   }
-  if ((s = run_layers(d, kv, B, kv->zeros, hidden, st, timer))) return s;
-  if ((s = run_head(d, kv, M, logits, st, timer))) return s;
+  TIMED(VSD_K_STEP, if ((s = run_persistent(d, kv, B, kv->zeros, hidden, logits, nullptr, nullptr, st))) return s);
   TIMED(VSD_K_COMMIT, CK(launch_ex(draft_pick_kernel, dim3(ceil_div(B * kBlock, 128)), dim3(128), 0, st, use_pdl(st),
                                    false, static_cast<const unsigned long long*>(kv->keys), B, c.vocab, drafts,
                                    kv->status)));
@@ -1099,14 +1201,23 @@ vsd_status vsd_verify_step_host(const vsd_model* m, vsd_kv* kv, int32_t batch, i
   if (!m || !kv || !seq_lens || !pending || !drafts || !accepted || !out_tokens || batch < 1 ||
       batch > kv->max_batch)
     return fail(VSD_ERR_ARG, "bad arguments");
+  // every check the step itself makes on the host comes before the input copy is queued
+  if (kv->m != m) return fail(VSD_ERR_ARG, "the cache was created for another model");
   const size_t cap = static_cast<size_t>(kv->max_batch) * (kBlock + 3 + kRows);
-  if (!kv->io_dev) {
+  if (!kv->io_dev || !kv->io_host) {
+    // both staging buffers are published together or not at all
+    int* dev = nullptr;
+    int* host = nullptr;
     vsd_status s;
-    if ((s = dalloc(&kv->io_dev, cap))) return s;
-    if (cudaHostAlloc(reinterpret_cast<void**>(&kv->io_host), cap * sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
-      kv->io_host = nullptr;
+    if ((s = dalloc(&dev, cap))) return s;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&host), cap * sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+      cudaFree(dev);
       return fail(VSD_ERR_OOM, "pinned staging of %zu bytes", cap * sizeof(int));
     }
+    if (kv->io_dev) cudaFree(kv->io_dev);
+    if (kv->io_host) cudaFreeHost(kv->io_host);
+    kv->io_dev = dev;
+    kv->io_host = host;
   }
   // the layout depends on the batch; the step graph is keyed by the pointers, so each batch size gets its own
   const size_t B = static_cast<size_t>(batch);
@@ -1120,7 +1231,12 @@ vsd_status vsd_verify_step_host(const vsd_model* m, vsd_kv* kv, int32_t batch, i
   CK(cudaMemcpyAsync(d, h, n_in * sizeof(int), cudaMemcpyHostToDevice, st));
   const vsd_status s = vsd_verify_step(m, kv, batch, d + B * kBlock, d + B * (kBlock + 1), d, d + B * (kBlock + 2),
                                        d + B * (kBlock + 3), stream);
-  if (s) return s;
+  if (s) {
+    // the queued copy still reads the pinned staging: let it finish before
+    // the next call may overwrite it (the step's own error message stands)
+    cudaStreamSynchronize(st);
+    return s;
+  }
   CK(cudaMemcpyAsync(h + B * kBlock, d + B * kBlock, n_out * sizeof(int), cudaMemcpyDeviceToHost, st));
   CK(cudaStreamSynchronize(st));
   memcpy(seq_lens, h + B * kBlock, B * sizeof(int));

@@ -9,13 +9,9 @@ template <int HD>
 static cudaError_t launch_hd(const CUtensorMap& tm_q, const CUtensorMap& tm_kc, const CUtensorMap& tm_vc,
                              const CUtensorMap& tm_kn, const CUtensorMap& tm_vn, const AttnArgs& a, dim3 grid,
                              cudaStream_t st, bool pdl) {
-  static bool configured = false;
   const uint32_t smem = attn_smem_bytes(HD);
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const cudaError_t e = ensure_smem_opt_in(reinterpret_cast<const void*>(attn_kernel<HD>), static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   // cooperative: the splits of a request wait for one another before merging
   return launch_ex(attn_kernel<HD>, grid, dim3(kAttnThreads), smem, st, pdl, true, tm_q, tm_kc, tm_vc, tm_kn, tm_vn,
                    a);

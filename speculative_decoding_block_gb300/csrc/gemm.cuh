@@ -93,6 +93,9 @@ struct GemmArgs {
   __half* x16_out;         // RESID: f16 copy of the updated rows (next GEMM's input)
   float* ssq_out;          // RESID: [tile][ssq_ld] sum of squares of the updated rows per 128-feature tile
   float* hidden_out;       // RESID (optional): copy of the updated rows
+  // layer l of a multi-layer launch writes its block K / V and its hidden
+  // rows this many elements after layer 0's (0: single-layer launches)
+  size_t kv_layer_stride, hidden_layer_stride;
   // QKV
   __nv_bfloat16* q_tile;   // [B][n_kv][128][hd]
   __nv_bfloat16* k_new;    // [B][n_kv][32][hd] (this layer)
@@ -106,10 +109,12 @@ struct GemmArgs {
   // ARGMAX
   unsigned long long* keys;  // [M]
   float* logits;             // optional [M][vocab] (ARGMAX, SAMPLE)
-  // SAMPLE: per (token row, 128-row vocabulary tile) the sum of exp(min(logit / T, 80)),
-  // and the logit of each row's draft token (rows j < 16 of a request)
+  // SAMPLE: per (token row, 128-row vocabulary tile) the maximum m of
+  // y = logit / T * log2(e) and the sum of 2^(y - m), and the logit of each
+  // row's draft token (rows j < 16 of a request)
   float inv_temp;
   const int* drafts;         // [B][16]
+  float* tile_max;           // [M][n_tiles]
   float* tile_sum;           // [M][n_tiles]
   float* draft_logit;        // [M]
   int* status;
@@ -305,7 +310,8 @@ __device__ __forceinline__ int scatter16_element(int lane) {
 template <int EPI, int WF>
 __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int tt, int row, int c0, float* v,
                                               float scale, const float* rs, const int* pos,
-                                              unsigned long long* wbest, float* sq_red, int warp_e, int lane) {
+                                              unsigned long long* wbest, float* sq_red, int warp_e, int lane,
+                                              int layer = 0) {
   const int prow = tile * kTileN + row;  // packed row
   const bool row_ok = prow < a.n_rows;
   const int tok0 = tt * a.n_tok + c0;
@@ -324,7 +330,8 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int tok = tok0 + i;
-      old[i] = (row_ok && tok < a.m_tokens) ? a.out_f32[static_cast<size_t>(tok) * a.ld_out + prow] : 0.0f;
+      // (read at L2: in a multi-phase launch other SMs wrote these rows)
+      old[i] = (row_ok && tok < a.m_tokens) ? __ldcg(a.out_f32 + static_cast<size_t>(tok) * a.ld_out + prow) : 0.0f;
     }
     float sq[16];
 #pragma unroll
@@ -339,7 +346,7 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
         const __half hi = __float2half_rn(r);
         a.x16_out[o] = hi;
         if (a.out_lo) a.x16_out[o + a.out_lo] = __float2half_rn(r - __half2float(hi));
-        if (a.hidden_out) a.hidden_out[o] = r;
+        if (a.hidden_out) a.hidden_out[o + layer * a.hidden_layer_stride] = r;
       }
     }
     const float tot = warp_reduce_scatter16(sq, lane, [](float p, float q) { return p + q; });
@@ -369,7 +376,7 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
       roff = head - kvh * group;  // + j * group
     } else {
       kvh = rotate ? head - a.n_q : head - a.n_q - a.n_kv;
-      dst = rotate ? a.k_new : a.v_new;
+      dst = (rotate ? a.k_new : a.v_new) + layer * a.kv_layer_stride;
       rstride = 32;
       roff = 0;
     }
@@ -414,19 +421,23 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
       }
     }
   } else if constexpr (EPI == EPI_SAMPLE) {
-    // exp of the tempered logits, summed over the warp's 32 vocabulary rows
-    // per column (reduce-scatter); the caller folds the four warps
-    float e[16];
+    // tempered logits y = logit / T in log2 units; per column, the maximum
+    // over the warp's 32 vocabulary rows and the sum of 2^(y - max), merged
+    // pairwise (reduce-scatter); the caller folds the four warps
+    const float c2 = a.inv_temp * kLog2e;
+    unsigned long long e[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int tok = tok0 + i;
       const bool ok = row_ok && tok < a.m_tokens;
       if (a.logits && ok) a.logits[static_cast<size_t>(tok) * a.n_rows + prow] = x[i];
       if (ok && prow == pos[c0 + i]) a.draft_logit[tok] = x[i];
-      e[i] = ok ? __expf(fminf(x[i] * a.inv_temp, 80.0f)) : 0.0f;
+      e[i] = ok ? ms_pack(x[i] * c2, 1.0f) : ms_pack(-INFINITY, 0.0f);
     }
-    const float tot = warp_reduce_scatter16(e, lane, [](float p, float q) { return p + q; });
-    if ((lane & 1) == 0) reinterpret_cast<float*>(wbest)[warp_e * 16 + scatter16_element(lane)] = tot;
+    const unsigned long long tot = warp_reduce_scatter16(e, lane, [](unsigned long long p, unsigned long long q) {
+      return ms_merge(p, q);
+    });
+    if ((lane & 1) == 0) wbest[warp_e * 16 + scatter16_element(lane)] = tot;
   } else if constexpr (EPI == EPI_ARGMAX) {
     unsigned long long key[16];
 #pragma unroll
@@ -443,8 +454,7 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, int tile, int t
 
 template <int WF, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
-                const GemmArgs a) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const bool act_lo = a.act_lo_rows > 0;
@@ -612,12 +622,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       auto issue_w = [&](int r, const ItemIter& it) {
         uint8_t* dst = smem + L.w_off + r * L.w_bytes;
         mbar_expect_tx(&wfull[r], L.w_bytes);
-        if constexpr (WF == W_BF16) {
-          tma_load_2d_hint(dst, &tm_w, &wfull[r], it.kt * kTileK, it.tile() * kTileN, pol_w);
-        } else {
-          const uint8_t* src = a.w_tiles + (static_cast<size_t>(it.tile()) * a.k_tiles + it.kt) * L.w_bytes;
-          bulk_load(dst, src, L.w_bytes, &wfull[r], pol_w);
-        }
+        // every format is pre-packed in tiles (16-bit ones already in the MMA's swizzled layout)
+        const uint8_t* src = a.w_tiles + (static_cast<size_t>(it.tile()) * a.k_tiles + it.kt) * L.w_bytes;
+        bulk_load(dst, src, L.w_bytes, &wfull[r], pol_w);
       };
       auto issue_b = [&](int b, const ItemIter& it) {
         uint8_t* dst = smem + L.b_off + b * L.b_bytes;
@@ -893,11 +900,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           if constexpr (EPI == EPI_SAMPLE) {
             named_bar_sync(4 + half, 128);  // this set's four warps only
-            if (et < 16) {  // the tile's sum for column c0 + et, warps in fixed order (deterministic)
-              const float* ws = reinterpret_cast<const float*>(wb);
-              const float sum = ((ws[et] + ws[16 + et]) + ws[32 + et]) + ws[48 + et];
+            if (et < 16) {  // the tile's (max, sum) for column c0 + et, warps in fixed order (deterministic)
+              const unsigned long long r = ms_merge(ms_merge(ms_merge(wb[et], wb[16 + et]), wb[32 + et]), wb[48 + et]);
               const int col = tt * a.n_tok + c0 + et;
-              if (col < a.m_tokens) a.tile_sum[static_cast<size_t>(col) * a.n_tiles + tile] = sum;
+              if (col < a.m_tokens) {
+                a.tile_max[static_cast<size_t>(col) * a.n_tiles + tile] = ms_max(r);
+                a.tile_sum[static_cast<size_t>(col) * a.n_tiles + tile] = ms_sum(r);
+              }
             }
           }
         }

@@ -2,10 +2,32 @@
 // unit per kernel family keeps the build parallel).
 #pragma once
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "attention.cuh"
 #include "gemm.cuh"
+#include "persistent.cuh"
 
 namespace vsd {
+
+// Opts kernel `k` in to `bytes` of dynamic shared memory on the current
+// device.  The attribute is per device, so it is set once per (kernel,
+// device, size); thread-safe.
+inline cudaError_t ensure_smem_opt_in(const void* k, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<std::pair<const void*, int>, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(std::make_pair(k, dev), bytes);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
+}
 
 // Launches gemm_kernel<wf, epi> on `grid` persistent CTAs; programmatic
 // dependent launch when pdl is set.
@@ -13,11 +35,14 @@ namespace vsd {
 // a.cs and is clamped to the clusters that can be resident at once.
 // Clusters of `cs` GEMM CTAs (full shared memory each) that can be resident at once.
 int gemm_max_clusters(int cs);
-cudaError_t launch_gemm(int wf, int epi, const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
-                        int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_gemm(int wf, int epi, const CUtensorMap& tm_act, const GemmArgs& a, int grid, cudaStream_t st,
+                        bool pdl);
 cudaError_t launch_attn(int hd, const CUtensorMap& tm_q, const CUtensorMap& tm_kc, const CUtensorMap& tm_vc,
                         const CUtensorMap& tm_kn, const CUtensorMap& tm_vn, const AttnArgs& a, dim3 grid,
                         cudaStream_t st, bool pdl);
+
+// Launches the persistent step kernel (head_dim 64 or 128) on `grid` CTAs, one per SM.
+cudaError_t launch_step(int hd, const MkParams& p, int grid, cudaStream_t st);
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_ex_cluster(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, int cluster, cudaStream_t st,

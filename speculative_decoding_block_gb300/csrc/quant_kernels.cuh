@@ -148,16 +148,22 @@ __global__ void pack_row_scale_kernel(const float* src_scale, const int* perm, i
   if (p < n_packed) row_scale[p] = perm[p] >= 0 ? src_scale[perm[p]] : 0.0f;
 }
 
-// BF16 -> f16 row gather [n_packed][K] (the GEMM consumes 16-bit weights as
-// f16: exact for magnitudes in [2^-14, 65504], nearest f16 below 2^-14).
-__global__ void pack_bf16_kernel(const uint16_t* w, const int* perm, int n_packed, int K, uint16_t* out) {
-  const size_t n = static_cast<size_t>(n_packed) * K;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int p = static_cast<int>(i / K), k = static_cast<int>(i % K);
-    const int src = perm[p];
-    const float v = src >= 0 ? __uint_as_float(static_cast<uint32_t>(w[static_cast<size_t>(src) * K + k]) << 16) : 0.0f;
-    out[i] = __half_as_ushort(__float2half_rn(v));
+// BF16 -> f16 tiles [n_tiles][k_tiles][128 rows x 64 k] laid out exactly as
+// the MMA reads them from shared memory (128-byte swizzle: 16-byte chunk c of
+// tile row r at r * 128 + ((c ^ (r & 7)) << 4)), so one 1-D bulk copy moves a
+// tile; k beyond K and padding rows are zero.  The GEMM consumes 16-bit
+// weights as f16: exact for magnitudes in [2^-14, 65504], nearest f16 below.
+__global__ void pack_bf16_tiles_kernel(const uint16_t* w, const int* perm, int n_packed, int K, int k_tiles,
+                                       uint16_t* tiles) {
+  const int tile = blockIdx.y, kt = blockIdx.x;
+  uint16_t* dst = tiles + (static_cast<size_t>(tile) * k_tiles + kt) * 8192;
+  for (int i = threadIdx.x; i < 8192; i += blockDim.x) {
+    const int r = i >> 6, col = i & 63;
+    const int p = tile * 128 + r, k = kt * 64 + col;
+    const int src = p < n_packed ? perm[p] : -1;
+    const float v =
+        (src >= 0 && k < K) ? __uint_as_float(static_cast<uint32_t>(w[static_cast<size_t>(src) * K + k]) << 16) : 0.0f;
+    dst[sw128_off(r, col >> 3) / 2 + (col & 7)] = __half_as_ushort(__float2half_rn(v));
   }
 }
 

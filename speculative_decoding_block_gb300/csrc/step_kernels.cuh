@@ -334,55 +334,73 @@ __global__ void loop_collect_kernel(const LoopArgs a) {
 struct SampleArgs {
   int vocab, hidden, n_tiles, m_alloc, ssq_slices;
   float inv_temp, inv_hidden, eps;
-  const float* tile_sum;     // [M][n_tiles] sums of exp(min(logit / T, 80)) per vocabulary tile
+  // per (row, 128-row vocabulary tile): maximum m of y = logit / T * log2(e)
+  // and sum of 2^(y - m)
+  const float* tile_max;     // [M][n_tiles]
+  const float* tile_sum;     // [M][n_tiles]
   const float* draft_logit;  // [M]
   const int* drafts;         // [B][16]
   const float* u_accept;     // [B][16]
   const float* u_sample;     // [B][17]
-  const __half* head;        // [vocab][hidden] the head's f16 rows (as the GEMM reads them)
+  const __half* head;        // the head's f16 tiles [vocab/128][hidden/64][128 x 64], MMA layout (as the GEMM reads them)
+  int head_k_tiles;
   const __half* x16;         // [M][hidden] hi, lo copy m_alloc rows later: the head's input rows
   const float* ssq;          // [slices][m_alloc] sums of squares of the final residual rows
   int* decided;              // [B][18]: accepted count a, then out tokens 0..16 (-1 beyond a)
 };
 
-__device__ __forceinline__ float tempered_weight(float logit, float inv_temp) {
-  return __expf(fminf(logit * inv_temp, 80.0f));
-}
-
-// One CTA (256 threads) per request: accept draft j while u_accept[j] < p_j(d_j),
-// p_j = w(d_j) / Z_j with w = exp(min(logit / T, 80)) and Z_j the row's total
-// over the vocabulary; at the first rejection (or after 16 acceptances) sample
-// row a by inverse CDF over token ids in increasing order, without the
-// rejected draft: the vocabulary tile holding the target mass comes from the
-// GEMM's per-tile sums, its 128 logits are recomputed from the head rows.
+// One CTA (256 threads) per request.  Every weight is taken relative to its
+// row's maximum, w(v) = 2^(y_v - M_j) with y = logit / T * log2(e) and M_j the
+// row's largest y, so that no logit overflows or saturates the exponential:
+// accept draft j while u_accept[j] < p_j(d_j) = w(d_j) / Z_j, Z_j = sum of
+// w over the vocabulary (from the per-tile (max, sum) pairs); at the first
+// rejection (or after 16 acceptances) sample row a by inverse CDF over
+// token ids in increasing order, without the rejected draft: the vocabulary
+// tile holding the target mass comes from the per-tile sums, its 128 logits
+// are recomputed from the head rows.
 __global__ void __launch_bounds__(256) sample_decide_kernel(const SampleArgs a) {
   __shared__ float red[256];
-  __shared__ float z_row[kRows];
+  __shared__ float z_row[kRows], m_row[kRows];
   __shared__ float w_tile[128];
   __shared__ int s_acc, s_tile, s_excl;
   __shared__ float s_base, s_target, s_we;
   pdl_wait();
   pdl_launch_dependents();
   const int b = blockIdx.x, t = threadIdx.x;
-  // Z_j: strided partial sums, then a fixed tree (deterministic)
+  const float c2 = a.inv_temp * kLog2e;
+  // M_j, then Z_j: strided partials, then a fixed tree (deterministic)
   for (int j = 0; j < kRows; ++j) {
-    const float* ts = a.tile_sum + static_cast<size_t>(b * kRows + j) * a.n_tiles;
+    const size_t r0 = static_cast<size_t>(b * kRows + j) * a.n_tiles;
+    float mx = -INFINITY;
+    for (int i = t; i < a.n_tiles; i += 256) mx = fmaxf(mx, a.tile_max[r0 + i]);
+    red[t] = mx;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+      if (t < w) red[t] = fmaxf(red[t], red[t + w]);
+      __syncthreads();
+    }
+    const float M = red[0];
+    __syncthreads();
     float sum = 0.0f;
-    for (int i = t; i < a.n_tiles; i += 256) sum += ts[i];
+    for (int i = t; i < a.n_tiles; i += 256) sum += a.tile_sum[r0 + i] * ex2(a.tile_max[r0 + i] - M);
     red[t] = sum;
     __syncthreads();
     for (int w = 128; w > 0; w >>= 1) {
       if (t < w) red[t] += red[t + w];
       __syncthreads();
     }
-    if (t == 0) z_row[j] = red[0];
+    if (t == 0) {
+      z_row[j] = red[0];
+      m_row[j] = M;
+    }
     __syncthreads();
   }
   if (t == 0) {
     int acc = kBlock;
     for (int j = 0; j < kBlock; ++j) {
       const int d = a.drafts[b * kBlock + j];
-      const float p = (d >= 0 && d < a.vocab) ? tempered_weight(a.draft_logit[b * kRows + j], a.inv_temp) / z_row[j] : 0.0f;
+      const float p =
+          (d >= 0 && d < a.vocab) ? ex2(a.draft_logit[b * kRows + j] * c2 - m_row[j]) / z_row[j] : 0.0f;
       if (!(a.u_accept[b * kBlock + j] < p)) {
         acc = j;
         break;
@@ -390,7 +408,7 @@ __global__ void __launch_bounds__(256) sample_decide_kernel(const SampleArgs a) 
     }
     const int d = acc < kBlock ? a.drafts[b * kBlock + acc] : -1;
     const bool excl = d >= 0 && d < a.vocab;
-    const float we = excl ? tempered_weight(a.draft_logit[b * kRows + acc], a.inv_temp) : 0.0f;
+    const float we = excl ? ex2(a.draft_logit[b * kRows + acc] * c2 - m_row[acc]) : 0.0f;
     s_acc = acc;
     s_excl = excl ? d : -1;
     s_we = we;
@@ -398,12 +416,16 @@ __global__ void __launch_bounds__(256) sample_decide_kernel(const SampleArgs a) 
   }
   __syncthreads();
   const int acc = s_acc, r = b * kRows + acc;
+  const float M = m_row[acc];
   // the tile holding the target mass: chunk sums of consecutive tiles (the
   // draft's weight taken out of its tile), a scan of the 256 chunk sums,
   // then a scan inside the chunk
+  const float* tm = a.tile_max + static_cast<size_t>(r) * a.n_tiles;
   const float* ts = a.tile_sum + static_cast<size_t>(r) * a.n_tiles;
   const int per = (a.n_tiles + 255) / 256;
-  auto tile_w = [&](int i) { return ts[i] - ((s_excl >= 0 && i == s_excl / 128) ? s_we : 0.0f); };
+  auto tile_w = [&](int i) {
+    return ts[i] * ex2(tm[i] - M) - ((s_excl >= 0 && i == s_excl / 128) ? s_we : 0.0f);
+  };
   {
     float sum = 0.0f;
     for (int i = t * per; i < min(a.n_tiles, (t + 1) * per); ++i) sum += tile_w(i);
@@ -443,12 +465,15 @@ __global__ void __launch_bounds__(256) sample_decide_kernel(const SampleArgs a) 
     const int v = tile * 128 + i;
     float dot = 0.0f;
     if (v < a.vocab) {
-      const __half* wrow = a.head + static_cast<size_t>(v) * a.hidden;
+      // 16-byte chunk q of head row v: tile (v / 128, q / 8), swizzled chunk (q % 8) of tile row v % 128
+      const __half* wtiles = a.head + static_cast<size_t>(v >> 7) * a.head_k_tiles * 8192;
+      const uint32_t wr = static_cast<uint32_t>(v & 127);
       const __half* xh = a.x16 + static_cast<size_t>(r) * a.hidden;
       const __half* xl = xh + static_cast<size_t>(a.m_alloc) * a.hidden;
       const int n8 = a.hidden / 8, h8 = n8 / 2;
       for (int q = half ? h8 : 0; q < (half ? n8 : h8); ++q) {
-        const uint4 w4 = reinterpret_cast<const uint4*>(wrow)[q];
+        const uint4 w4 =
+            *reinterpret_cast<const uint4*>(wtiles + static_cast<size_t>(q >> 3) * 8192 + sw128_off(wr, q & 7) / 2);
         const uint4 h4 = reinterpret_cast<const uint4*>(xh)[q];
         const uint4 l4 = reinterpret_cast<const uint4*>(xl)[q];
         const __half2* w2 = reinterpret_cast<const __half2*>(&w4);
@@ -462,7 +487,7 @@ __global__ void __launch_bounds__(256) sample_decide_kernel(const SampleArgs a) 
       }
     }
     dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 1);
-    if (half == 0) w_tile[i] = (v < a.vocab && v != s_excl) ? tempered_weight(dot * rs, a.inv_temp) : 0.0f;
+    if (half == 0) w_tile[i] = (v < a.vocab && v != s_excl) ? ex2(dot * rs * c2 - M) : 0.0f;
   }
   __syncthreads();
   if (t == 0) {

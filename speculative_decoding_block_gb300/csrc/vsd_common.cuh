@@ -413,6 +413,28 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
 }
 
+__device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation (ex2(-inf) = 0)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Softmax partials as (maximum m, sum s of 2^(y - m)) pairs packed in 64
+// bits (m low, s high).  Merging two pairs rescales both sums to the larger
+// maximum, so partial sums over any split of a row combine without ever
+// forming 2^y of a large y ("online" softmax normaliser).
+__device__ __forceinline__ unsigned long long ms_pack(float m, float s) {
+  return (static_cast<unsigned long long>(__float_as_uint(s)) << 32) | __float_as_uint(m);
+}
+__device__ __forceinline__ float ms_max(unsigned long long v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float ms_sum(unsigned long long v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ unsigned long long ms_merge(unsigned long long a, unsigned long long b) {
+  const float ma = ms_max(a), mb = ms_max(b), m = fmaxf(ma, mb);
+  if (m == -INFINITY) return ms_pack(-INFINITY, 0.0f);
+  return ms_pack(m, ms_sum(a) * ex2(ma - m) + ms_sum(b) * ex2(mb - m));
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
 // Orderable key of a float for an unsigned max: larger float -> larger key.
 __device__ __forceinline__ uint32_t float_order_key(float f) {
   const uint32_t u = __float_as_uint(f);

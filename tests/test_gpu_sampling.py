@@ -10,8 +10,10 @@ about 7e-6 of it.
 Covered: accepted prefixes of every length 0..16 (u_accept tiny on planted
 rows, 0.5 where the draft should be rejected), the correction sample
 without the rejected draft, the bonus sample after 16 acceptances; the
-tiny shape and the benchmarked 0.5B mixed workload (four requests checked
-against the oracle, all requests' outputs valid).
+tiny shape at T = 0.7 and at temperatures low enough that logit / T far
+exceeds the range of a float32 exponential (the weights must be taken
+relative to the row maximum), and the benchmarked 0.5B mixed workload
+(four requests checked against the oracle, all requests' outputs valid).
 """
 import numpy as np
 import pytest
@@ -48,7 +50,8 @@ def _check(ref, acc, out, report, b):
     assert np.all(out[a + 1:] == -1)
 
 
-def test_tiny_sampled_every_prefix():
+@pytest.mark.parametrize("temp", [T, 0.01, 0.004])
+def test_tiny_sampled_every_prefix(temp):
     B = require_gpu()
     from speculative_decoding_block_gb300.target import build_target
     master = gen.master_weights(TINY, seed=61)
@@ -68,20 +71,24 @@ def test_tiny_sampled_every_prefix():
     ua, us = _uniforms(ks, 63)
     io = StepIO(len(ks), [s.length for s in states], [s.pending for s in states], np.stack(drafts))
     B.vsd_verify_step_sampled(model, kv, len(ks), io.seq, io.pending, io.drafts, io.acc, io.out,
-                              torch.tensor(ua).cuda(), torch.tensor(us).cuda(), T)
+                              torch.tensor(ua).cuda(), torch.tensor(us).cuda(), temp)
     torch.cuda.synchronize()
     assert B.vsd_get_device_status(kv) == 0
     ties = []
+    top = []
     for b, st in enumerate(states):
         before = st.copy()
-        ref = S.verify_step_sampled(om, st, drafts[b], T, ua[b].astype(np.float64), us[b].astype(np.float64))
+        ref = S.verify_step_sampled(om, st, drafts[b], temp, ua[b].astype(np.float64), us[b].astype(np.float64))
+        top.append(float(ref["logits"].max()) / temp)
         _check(ref, int(io.acc[b]), io.out[b].cpu().numpy(), ties, b)
         if b not in ties:
             assert int(io.seq[b]) == before.length + ref["accepted"] + 1
             assert int(io.pending[b]) == int(ref["out"][ref["accepted"]])
-    print("near ties", ties)
+    print("near ties", ties, "largest logit / T", max(top))
     # the planted full block with tiny u_accept reaches the bonus row
     assert int(io.acc[3]) == 16 or 3 in ties
+    if temp < 0.1:  # the case is meant to exceed what exp() of a raw logit / T holds in float32
+        assert max(top) > 88.0
 
 
 def test_half_b_mixed_sampled_bench_workload():
