@@ -530,6 +530,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
                 ++bn;
                 ib.next();
                 progress = true;
+                if (ib.done()) trace_point(tq, 11);
               }
             }
             if (try_w()) progress = true;
@@ -721,6 +722,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
             } while (!last);
             if (!ok) break;
             umma_commit(&bar[MB_TFULL + ab]);
+            trace_point(tq, 10);
             ++acc;
           }
         }
@@ -873,6 +875,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
               mbar_arrive(&bar[MB_WEMPTY + sw]);
             }
           }
+          if (t == 0) trace_point(tq, 9);
         }
         if (ok && (!half || ep8)) {
           // -------------------------------------------------------------- epilogue
@@ -919,10 +922,12 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
               }
             }
             named_bar_sync(NB_EPI, ep_n);
+            if (et2 == 0 && acc == acc_pos) trace_point(tq, 4);
             if (!mwait(&bar[MB_TFULL + ab], static_cast<uint32_t>((acc >> 1) & 1))) {
               ok = false;
               break;
             }
+            if (et2 == 0 && acc == acc_pos) trace_point(tq, 5);
             tc_fence_after();
             const bool act_lo = a.act_lo_rows > 0;
             const bool stacked = act_lo && 2 * a.n_tok <= 256;
@@ -953,6 +958,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
               __threadfence();
               named_bar_sync(NB_EPI, ep_n);
               if (et2 == 0) {
+                trace_point(tq, 6);
                 mbar_arrive(&bar[MB_TEMPTY + ab]);
                 int* arrived = p.item_cnt + item;
                 red_release_add(arrived, 1);
@@ -970,6 +976,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
                   }
                 }
                 *flag_s = okw;
+                trace_point(tq, 7);
               }
               named_bar_sync(NB_EPI, ep_n);
               if (!*flag_s) {
@@ -1051,6 +1058,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
             } else {
               named_bar_sync(NB_EPI, ep_n);
             }
+            if (et2 == 0 && acc == acc_pos) trace_point(tq, 8);
             if (kind == 1 || kind == 3) {  // RESID: sums of squares of the updated rows, per token
               for (int c = et2; c < a.n_tok; c += ep_n) {
                 const int tok = tt * a.n_tok + c;
