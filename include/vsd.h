@@ -43,7 +43,10 @@
  *     device can see (a token id >= vocab, a sequence length beyond the
  *     cache, a page id outside the pool, a bounded wait that ran out) set a
  *     bit in the cache's device status word (vsd_get_device_status); an
- *     affected request is left unchanged (no commit, accepted = -1).
+ *     affected request is left unchanged (no commit, accepted = -1).  A
+ *     page outside the pool anywhere in a request's rows [0, L + 17)
+ *     rejects that request; a wait that ran out (VSD_DEV_TIMEOUT, sticky
+ *     until the status word is read) rejects every request of the step.
  *   - Token ids, lengths and counts are int32.  BF16 is raw 16-bit storage
  *     (uint16_t bit patterns); FP8 is E4M3 ("fn": max 448, no infinities);
  *     FP4 is E2M1, two per byte with the even element in the low nibble.
@@ -188,6 +191,15 @@ vsd_status vsd_trace_read(vsd_kv* kv, uint64_t* slots_host, int32_t max_launches
 /* Reads and clears the device status word (VSD_DEV_* bits).  Synchronises
  * the stream. */
 vsd_status vsd_get_device_status(vsd_kv* kv, vsd_stream stream, int32_t* status_host);
+
+/* Test-only; the method has no counterpart.  Enqueues one CTA that waits,
+ * with the same bounded-wait pattern as the step's kernels, on a device flag
+ * that nothing sets and on a shared-memory mbarrier that nothing completes.
+ * Each wait gives up after limit_cycles SM cycles (1 .. 2e9), sets
+ * VSD_DEV_TIMEOUT in kv's device status word and the kernel returns; the
+ * context stays usable.  Returns VSD_ERR_ARG for a NULL cache or a limit out
+ * of range.  Asynchronous. */
+vsd_status vsd_debug_wait_probe(vsd_kv* kv, int64_t limit_cycles, vsd_stream stream);
 
 /* ---------------------------------------------------------------- the step
  * Greedy block verification of B requests (slots 0..B-1), 1 <= B <= max_batch.

@@ -28,7 +28,7 @@ EXPORTS = [
     "vsd_linear", "vsd_block_attention", "vsd_block_attention_static", "vsd_accept_commit",
     "vsd_verify_step_profiled", "vsd_draft_step", "vsd_draft_step_debug", "vsd_kv_get_anchor", "vsd_spec_loop", "vsd_verify_step_sampled",
     "vsd_verify_step_host",
-    "vsd_trace_enable", "vsd_trace_read",
+    "vsd_trace_enable", "vsd_trace_read", "vsd_debug_wait_probe",
 ]
 KERNEL_KINDS = ["embed", "qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm",
                 "lm_head_gemm", "accept_commit", "step"]
@@ -98,6 +98,7 @@ def lib() -> ctypes.CDLL:
             "vsd_spec_loop": ([p, p, p, c_int, c_int, p, p, p, p, p, p, p, p, p, p, c_int, c_int, c_int, p], c_int),
             "vsd_linear": ([ctypes.POINTER(Weight), c_int, c_int, p, c_int, p, p], c_int),
             "vsd_trace_enable": ([p, c_int], c_int),
+            "vsd_debug_wait_probe": ([p, ctypes.c_int64, p], c_int),
             "vsd_trace_read": ([p, p, c_int, ctypes.POINTER(c_int), p], c_int),
             "vsd_block_attention": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
             "vsd_block_attention_static": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
@@ -267,6 +268,12 @@ def vsd_trace_read(kv: KV, max_launches: int = 256, stream=None):
     _check(lib().vsd_trace_read(kv.handle, ctypes.c_void_p(buf.ctypes.data), max_launches, ctypes.byref(n),
                                 _stream(stream)))
     return buf[: n.value]
+
+
+def vsd_debug_wait_probe(kv: KV, limit_cycles: int, stream=None) -> None:
+    """Test-only: a kernel whose bounded waits can never succeed gives up after
+    limit_cycles and sets VSD_DEV_TIMEOUT in the cache's status word."""
+    _check(lib().vsd_debug_wait_probe(kv.handle, ctypes.c_int64(limit_cycles), _stream(stream)))
 
 
 def vsd_get_device_status(kv: KV, stream=None) -> int:

@@ -142,6 +142,8 @@ struct vsd_kv {
   size_t attn_items_cap = 0;
   float* anchor = nullptr;  // [max_batch][H] residual row of the last accepted position (drafter input)
   int* zeros = nullptr;     // [max_batch] zero context lengths (the draft pass reads no cache)
+  int* probe_flag = nullptr;  // one int nothing ever sets (the wait probe's flag)
+  long long wait_limit = kWaitLimitCycles;  // SM cycles a persistent-kernel wait may take
   // slot state of the device-resident loop: lengths, pending, drafts, accepted [max_batch], outputs [max_batch][17]
   int *loop_seq = nullptr, *loop_pend = nullptr, *loop_drafts = nullptr, *loop_acc = nullptr, *loop_out = nullptr;
   // stochastic verification: per (row, vocabulary tile) sums, the drafts' logits, the decisions [max_batch][18]
@@ -693,6 +695,7 @@ vsd_status vsd_kv_create(const vsd_model* m, int32_t max_batch, int32_t max_toke
       (s = dalloc(&kv->v_new, static_cast<size_t>(c.layers) * max_batch * c.n_kv * 32 * hd)) ||
       (s = dalloc(&kv->keys, M)) || (s = dalloc(&kv->ctx_len, max_batch)) || (s = dalloc(&kv->req_ok, max_batch)) ||
       (s = dalloc(&kv->anchor, static_cast<size_t>(max_batch) * H)) || (s = dalloc(&kv->zeros, max_batch)) ||
+      (s = dalloc(&kv->probe_flag, 1)) ||
       (s = dalloc(&kv->loop_seq, max_batch)) || (s = dalloc(&kv->loop_pend, max_batch)) ||
       (s = dalloc(&kv->loop_drafts, static_cast<size_t>(max_batch) * kBlock)) ||
       (s = dalloc(&kv->loop_acc, max_batch)) || (s = dalloc(&kv->loop_out, static_cast<size_t>(max_batch) * kRows)) ||
@@ -740,7 +743,7 @@ void vsd_kv_destroy(vsd_kv* kv) {
   if (kv->io_host) cudaFreeHost(kv->io_host);
   void* ptrs[] = {kv->k_pool, kv->v_pool, kv->page_table, kv->x, kv->u, kv->act_o, kv->act_a, kv->q_tile,
                   kv->k_new, kv->v_new, kv->keys, kv->ctx_len, kv->req_ok, kv->ssq, kv->attn_o,
-                  kv->attn_ml, kv->attn_counters, kv->anchor, kv->zeros, kv->loop_seq, kv->loop_pend,
+                  kv->attn_ml, kv->attn_counters, kv->anchor, kv->zeros, kv->probe_flag, kv->loop_seq, kv->loop_pend,
                   kv->loop_drafts, kv->loop_acc, kv->loop_out, kv->tile_max, kv->tile_sum, kv->draft_logit, kv->decided,
                   kv->status, kv->trace, kv->mk_sync, kv->mk_part, kv->mk_item_cnt};
   for (void* p : ptrs)
@@ -817,6 +820,14 @@ vsd_status vsd_trace_read(vsd_kv* kv, uint64_t* slots_host, int32_t max_launches
   CK(cudaMemset(kv->trace, 0, static_cast<size_t>(kv->trace_launches) * kTraceCtas * kTraceTags * 8));
   kv->trace_seq = 0;
   *n_launches = n;
+  return VSD_OK;
+}
+
+vsd_status vsd_debug_wait_probe(vsd_kv* kv, int64_t limit_cycles, vsd_stream stream) {
+  if (!kv) return fail(VSD_ERR_ARG, "NULL pointer");
+  if (limit_cycles < 1 || limit_cycles > kWaitLimitCycles) return fail(VSD_ERR_ARG, "limit out of range");
+  wait_probe_kernel<<<1, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(kv->probe_flag, limit_cycles, kv->status);
+  CK(cudaGetLastError());
   return VSD_OK;
 }
 
@@ -999,6 +1010,7 @@ static vsd_status run_persistent(const vsd_model* m, vsd_kv* kv, int B, const in
   }
   p.layers = m->mk_layers;
   p.n_layers = c.layers;
+  p.wait_limit = kv->wait_limit;
   p.sync = kv->mk_sync;
   p.part = kv->mk_part;
   p.item_cnt = kv->mk_item_cnt;

@@ -101,6 +101,7 @@ struct MkParams {
   float* part;            // split-k partials [item][member][n_tok][128]
   int* item_cnt;          // [2][kMaxSplitItems] arrivals / departures per item
   int* status;
+  long long wait_limit;   // SM cycles after which a wait gives up (VSD_DEV_TIMEOUT)
   Trace trace;            // launch id = trace.id + phase; trace.id + n_phases: kernel start / end
 };
 
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
         *abort_flag = 1;
         return false;
       }
-      if (cycles() - t0 > kWaitLimitCycles) {
+      if (cycles() - t0 > p.wait_limit) {
         give_up(true);
         return false;
       }
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
         *abort_flag = 1;
         return false;
       }
-      if (cycles() - t0 > kWaitLimitCycles) {
+      if (cycles() - t0 > p.wait_limit) {
         give_up(true);
         return false;
       }
@@ -449,7 +450,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
             okw = 0;
             break;
           }
-          if (cycles() - t0 > kWaitLimitCycles) {
+          if (cycles() - t0 > p.wait_limit) {
             give_up(true);
             okw = 0;
             break;
@@ -466,7 +467,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
           *abort_flag = 1;
           return false;
         }
-        if (cycles() - t0 > kWaitLimitCycles) {
+        if (cycles() - t0 > p.wait_limit) {
           give_up(true);
           return false;
         }
@@ -543,7 +544,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
               ok = false;
               break;
             }
-            if (cycles() - t_last > kWaitLimitCycles) {
+            if (cycles() - t_last > p.wait_limit) {
               give_up(true);
               ok = false;
               break;
@@ -969,7 +970,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
                     okw = 0;
                     break;
                   }
-                  if (cycles() - t0 > kWaitLimitCycles) {
+                  if (cycles() - t0 > p.wait_limit) {
                     give_up(true);
                     okw = 0;
                     break;
@@ -1233,7 +1234,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) step_kernel(const __grid_consta
                 okw = 0;
                 break;
               }
-              if (cycles() - t0 > kWaitLimitCycles) {
+              if (cycles() - t0 > p.wait_limit) {
                 give_up(true);
                 okw = 0;
                 break;

@@ -122,6 +122,30 @@ __global__ void validate_requests_kernel(const int* seq_lens, const int* pending
   req_ok[b] = (ok && p >= 0 && p < vocab) ? 1 : 0;
 }
 
+// Test-only: one CTA waits, with the kernels' bounded-wait pattern, on a
+// global flag and on a shared-memory mbarrier that nothing ever completes;
+// after `limit` SM cycles each gives up, records VSD_DEV_TIMEOUT and the
+// kernel returns (no copy or MMA is in flight, so it exits cleanly).
+__global__ void wait_probe_kernel(const int* flag, long long limit, int* status) {
+  __shared__ uint64_t never_full;
+  if (threadIdx.x == 0) {
+    mbar_init(&never_full, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  bool gave_up = false;
+  if (threadIdx.x == 0 || threadIdx.x == 32) {
+    const long long t0 = clock64();
+    while (threadIdx.x == 0 ? ld_acquire_gpu(flag) == 0 : !mbar_test_wait(&never_full, 0)) {
+      if (clock64() - t0 > limit) {
+        gave_up = true;
+        break;
+      }
+    }
+  }
+  if (gave_up) atomicOr(status, VSD_DEV_TIMEOUT);
+}
+
 struct CommitArgs {
   int vocab, layers, n_kv, hd, batch_cap, num_pages, pages_per_req;
   const unsigned long long* keys;  // [B*17]
@@ -152,7 +176,11 @@ struct CommitArgs {
 // scratch into request b's cache pages at positions L..L+a; CTA (b, 0) also
 // writes the outputs and then seq_len = L + a + 1, pending = g_a.  All CTAs
 // read L from the step's validated copy, so the in-place update races with
-// nothing.
+// nothing.  A request is rejected (accepted = -1, outputs -1, cache and
+// lengths untouched) when its length or a token was out of range, when a
+// page of its rows [0, L + 17) lies outside the pool (the attention read its
+// context through them), or when the step's kernel gave up on a wait (its
+// outputs are then incomplete): then every request of the step is rejected.
 __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) {
   __shared__ int g[kRows];
   __shared__ int page[kRows];
@@ -162,6 +190,13 @@ __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) 
   const int b = blockIdx.x, l = blockIdx.y, t = threadIdx.x;
   if (t == 0 && l == 0) trace_start(a.trace);
   const int L = a.ctx_len[b];
+  const bool timed_out = (*reinterpret_cast<volatile int*>(a.status) & VSD_DEV_TIMEOUT) != 0;
+  int bad_page = 0;
+  for (int i = t; i < (L + kRows + kPage - 1) / kPage; i += blockDim.x) {
+    const int pg = a.page_table[b * a.pages_per_req + i];
+    bad_page |= (pg < 0 || pg >= a.num_pages) ? 1 : 0;
+  }
+  bad_page = __syncthreads_or(bad_page);
   if (t < 32) {
     int gt = -1, dt = -1;
     bool bad = false;
@@ -178,23 +213,17 @@ __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) 
       }
       g[t] = gt;
     }
-    int pg = 0;
-    if (t < kRows) {
-      pg = a.page_table[b * a.pages_per_req + (L + t) / kPage];
-      page[t] = pg;
-    }
+    if (t < kRows) page[t] = a.page_table[b * a.pages_per_req + (L + t) / kPage];
     if (t < kBlock) {
       dt = a.drafts[b * kBlock + t];
       if (dt < 0 || dt >= a.vocab) bad = true;
     }
     const unsigned mism = __ballot_sync(0xFFFFFFFFu, t < kBlock && dt != gt);
     const unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
-    const unsigned pbad = __ballot_sync(0xFFFFFFFFu, t < kRows && (pg < 0 || pg >= a.num_pages));
     if (t == 0) {
       const int acc0 = a.decided ? a.decided[b * (kRows + 1)] : (mism ? (__ffs(mism) - 1) : kBlock);
-      const bool pages_ok = (pbad & ((2u << acc0) - 1u)) == 0;  // only the committed rows need pages
-      if (!pages_ok && l == 0) atomicOr(a.status, VSD_DEV_BAD_PAGE);
-      s_valid = (badm == 0 && a.req_ok[b] && pages_ok) ? 1 : 0;
+      if (bad_page && l == 0) atomicOr(a.status, VSD_DEV_BAD_PAGE);
+      s_valid = (badm == 0 && a.req_ok[b] && !bad_page && !timed_out) ? 1 : 0;
       s_acc = acc0;
     }
   }
