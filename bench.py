@@ -148,7 +148,7 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples every 50 ms from before the warm-up; the summary keeps
+    """nvidia-smi samples every 10 ms from before the warm-up; the summary keeps
     the samples whose timestamps fall inside the timed region (or, when the
     region is shorter than the sampling interval, the two nearest)."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -164,7 +164,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -289,6 +289,127 @@ def job_totals(seconds: float, units: float, world: int, device: str = "cpu"):
     return float(t.item()), float(u.item())
 
 
+class Step:
+    """One workload's cache, inputs and planted drafts on the device, and the
+    one-step CUDA graph on a side stream (inputs reset and L2 flushed before
+    every replay)."""
+
+    def __init__(self, B, w, model, flush, stream):
+        import torch
+        self.B, self.w, self.shape, self.model, self.flush, self.stream = B, w, w.shape, model, flush, stream
+        dev = "cuda"
+        self.max_tok = w.max_tokens_per_req()
+        Bn = self.Bn = w.batch
+        kv = self.kv = B.vsd_kv_create(model, Bn, self.max_tok)
+        if w.paged:
+            pt = gen.page_table(w, kv.pages_per_req)
+            B.vsd_kv_set_page_table(kv, torch.tensor(pt, device=dev).contiguous())
+        self.lens = gen.context_lengths(w)
+        self.pend = gen.pending_tokens(w)
+        for b in range(Bn):
+            kk, vv = gen.synthetic_kv(self.shape, int(self.lens[b]), w.seed, b)
+            B.vsd_kv_write(kv, b, 0, kk.to(dev).contiguous(), vv.to(dev).contiguous())
+            del kk, vv
+        torch.cuda.synchronize()
+        self.seq0 = torch.tensor(self.lens, dtype=torch.int32, device=dev)
+        self.pend0 = torch.tensor(self.pend, dtype=torch.int32, device=dev)
+        self.seq, self.pen = self.seq0.clone(), self.pend0.clone()
+        self.acc = torch.empty(Bn, dtype=torch.int32, device=dev)
+        self.out = torch.empty((Bn, ROWS), dtype=torch.int32, device=dev)
+        self.drafts = torch.zeros((Bn, 16), dtype=torch.int32, device=dev)
+        # greedy trace of every request from the library itself (verify steps with
+        # arbitrary drafts advance the greedy continuation by a+1 >= 1 tokens)
+        trace = [[] for _ in range(Bn)]
+        rnd = np.random.default_rng(12345)
+        while min(len(t) for t in trace) < ROWS:
+            self.drafts.copy_(torch.tensor(rnd.integers(0, self.shape.vocab, (Bn, 16)), dtype=torch.int32))
+            B.vsd_verify_step(model, kv, Bn, self.seq, self.pen, self.drafts, self.acc, self.out)
+            o = self.out.cpu().numpy()
+            for b in range(Bn):
+                trace[b].extend(int(x) for x in o[b] if x >= 0)
+        ks = gen.prefix_lengths(w)
+        self.planted = np.stack([gen.plant_drafts(np.array(trace[b]), int(ks[b]), self.shape.vocab, "bench", w.seed, b)
+                                 for b in range(Bn)])
+        self.drafts.copy_(torch.tensor(self.planted, dtype=torch.int32))
+        self.reset()
+        B.vsd_verify_step(model, kv, Bn, self.seq, self.pen, self.drafts, self.acc, self.out)
+        torch.cuda.synchronize()
+        assert B.vsd_get_device_status(kv) == 0
+        self.accepted = self.acc.cpu().numpy()
+        self.tokens_per_step = int(np.sum(self.accepted + 1))
+        self.reset()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            B.vsd_verify_step(model, kv, Bn, self.seq, self.pen, self.drafts, self.acc, self.out, stream=stream)
+
+    def reset(self):
+        self.seq.copy_(self.seq0)
+        self.pen.copy_(self.pend0)
+
+    def replay(self, ev=None):
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.reset()
+            self.flush.fill_(1.0)
+            if ev:
+                ev[0].record(self.stream)
+            self.graph.replay()
+            if ev:
+                ev[1].record(self.stream)
+
+    def timed(self, warmup, steps):
+        """Per-step device times (ms) of `steps` replays after `warmup`."""
+        import torch
+        for _ in range(warmup):
+            self.replay()
+        torch.cuda.synchronize()
+        if not np.array_equal(self.acc.cpu().numpy(), self.accepted):
+            raise RuntimeError("graph replay gave different accepted lengths than the direct call")
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for ev in evs:
+            self.replay(ev)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def direct(self):
+        """One step launched directly on the side stream (inputs reset, L2 flushed)."""
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.reset()
+            self.flush.fill_(1.0)
+        self.B.vsd_verify_step(self.model, self.kv, self.Bn, self.seq, self.pen, self.drafts, self.acc, self.out,
+                               stream=self.stream)
+
+    def profiled(self, reps=3):
+        """Per-kernel device times (us) of one step: each launch bracketed by CUDA
+        events on the side stream (inputs reset, L2 flushed); medians over reps."""
+        import torch
+        per = {}
+        for _ in range(reps):
+            with torch.cuda.stream(self.stream):
+                self.reset()
+                self.flush.fill_(1.0)
+            for kind, ms in self.B.vsd_verify_step_profiled(self.model, self.kv, self.Bn, self.seq, self.pen,
+                                                            self.drafts, self.acc, self.out, stream=self.stream):
+                per.setdefault(kind, []).append(ms * 1e3)
+        return {k: float(np.median(v)) for k, v in per.items()}
+
+
+def kernel_report(shape, lens, accepted, kern, ms_per_step):
+    """`kernels` key of the bench line: per launch its share of the step, that
+    share of the event-timed step, and its algorithmic bytes."""
+    kb = kernel_bytes(shape, lens, accepted)
+    tot = sum(kern.values())
+    kernels = {}
+    for k, us in kern.items():
+        us_ev = ms_per_step * 1e3 * us / tot
+        kernels[k] = {"launches": 1, "us_bracketed": round(us, 2), "us_avg": round(us_ev, 2),
+                      "ms_total": round(us_ev / 1e3, 4), "share": round(us / tot, 4),
+                      "bytes_per_launch": kb[k], "gbs": round(kb[k] / (us_ev * 1e-6) / 1e9, 1)}
+    return kernels
+
+
 def run_gpu(args, rank: int, world: int):
     import torch
     from speculative_decoding_block_gb300 import binding as B
@@ -297,134 +418,53 @@ def run_gpu(args, rank: int, world: int):
 
     w = WORKLOADS[args.workload]
     shape = w.shape
-    oracle_handle = None
-    if rank == 0 and not args.no_cpu_baseline:
-        oracle_handle = start_oracle(args.workload, n_requests=2, budget_s=args.cpu_budget)
-
     build()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     dev = "cuda"
     max_tok = w.max_tokens_per_req()
+    # the RoPE table also covers the other configurations of the same shape, which reuse this target
+    max_pos = max([max_tok] + [x.max_tokens_per_req() for x in WORKLOADS.values() if x.shape == shape])
     master = gen.master_weights(shape, w.seed)
-    model, _ = build_target(shape, master, max_positions=max_tok)
+    model, _ = build_target(shape, master, max_positions=max_pos)
     drafter = None
     if not args.no_draft:
         ds = drafter_shape(shape)
         drafter, _ = build_target(ds, gen.drafter_master(master, shape.layers, ds.layers), max_positions=max_tok)
     del master
-    Bn = w.batch
-    kv = B.vsd_kv_create(model, Bn, max_tok)
-    if w.paged:
-        pt = gen.page_table(w, kv.pages_per_req)
-        B.vsd_kv_set_page_table(kv, torch.tensor(pt, device=dev).contiguous())
-    lens = gen.context_lengths(w)
-    pend = gen.pending_tokens(w)
-    for b in range(Bn):
-        kk, vv = gen.synthetic_kv(shape, int(lens[b]), w.seed, b)
-        B.vsd_kv_write(kv, b, 0, kk.to(dev).contiguous(), vv.to(dev).contiguous())
-        del kk, vv
-    torch.cuda.synchronize()
-
-    seq0 = torch.tensor(lens, dtype=torch.int32, device=dev)
-    pend0 = torch.tensor(pend, dtype=torch.int32, device=dev)
-    seq = seq0.clone()
-    pen = pend0.clone()
-    acc = torch.empty(Bn, dtype=torch.int32, device=dev)
-    out = torch.empty((Bn, ROWS), dtype=torch.int32, device=dev)
-    drafts = torch.zeros((Bn, 16), dtype=torch.int32, device=dev)
-
-    # greedy trace of every request from the library itself (verify steps with
-    # arbitrary drafts advance the greedy continuation by a+1 >= 1 tokens)
-    trace = [[] for _ in range(Bn)]
-    rnd = np.random.default_rng(12345)
-    while min(len(t) for t in trace) < ROWS:
-        drafts.copy_(torch.tensor(rnd.integers(0, shape.vocab, (Bn, 16)), dtype=torch.int32))
-        B.vsd_verify_step(model, kv, Bn, seq, pen, drafts, acc, out)
-        o = out.cpu().numpy()
-        for b in range(Bn):
-            trace[b].extend(int(x) for x in o[b] if x >= 0)
-    ks = gen.prefix_lengths(w)
-    planted = np.stack([gen.plant_drafts(np.array(trace[b]), int(ks[b]), shape.vocab, "bench", w.seed, b)
-                        for b in range(Bn)])
-    drafts.copy_(torch.tensor(planted, dtype=torch.int32))
-    seq.copy_(seq0)
-    pen.copy_(pend0)
-    B.vsd_verify_step(model, kv, Bn, seq, pen, drafts, acc, out)
-    torch.cuda.synchronize()
-    assert B.vsd_get_device_status(kv) == 0
-    accepted = acc.cpu().numpy()
-    tokens_per_step = int(np.sum(accepted + 1))
-
-    # CUDA graph of one step on a side stream
     stream = torch.cuda.Stream()
-    g = torch.cuda.CUDAGraph()
-    seq.copy_(seq0)
-    pen.copy_(pend0)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g, stream=stream):
-        B.vsd_verify_step(model, kv, Bn, seq, pen, drafts, acc, out, stream=stream)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-
-    def one_step(timed_events=None):
-        with torch.cuda.stream(stream):
-            seq.copy_(seq0)
-            pen.copy_(pend0)
-            flush.fill_(1.0)
-            if timed_events:
-                timed_events[0].record(stream)
-            g.replay()
-            if timed_events:
-                timed_events[1].record(stream)
+    S = Step(B, w, model, flush, stream)
+    Bn, kv, lens, pend, accepted = S.Bn, S.kv, S.lens, S.pend, S.accepted
+    seq, pen, acc, out, drafts, seq0, pend0 = S.seq, S.pen, S.acc, S.out, S.drafts, S.seq0, S.pend0
+    tokens_per_step = S.tokens_per_step
 
     clk = ClockSampler(torch.cuda.current_device()).start()
     atexit.register(clk.stop)  # never leave the sampler running
     for _ in range(args.warmup):
-        one_step()
+        S.replay()
     torch.cuda.synchronize()
-    if not np.array_equal(acc.cpu().numpy(), accepted):
-        raise RuntimeError("graph replay gave different accepted lengths than the direct call")
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_region0 = time.time()
-    for i in range(args.steps):
-        one_step(evs[i])
-    torch.cuda.synchronize()
+    step_ms = S.timed(0, args.steps)
     t_region1 = time.time()
     clk.stop()
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
     total_s, job_tokens = job_totals(sum(step_ms) / 1e3, tokens_per_step * args.steps, world, dev)
+    ms_per_step = total_s * 1e3 / args.steps
 
-    # per-kernel times of the same step (events around every launch)
-    prof = []
-    for _ in range(3):
-        seq.copy_(seq0)
-        pen.copy_(pend0)
-        flush.fill_(1.0)
-        prof = B.vsd_verify_step_profiled(model, kv, Bn, seq, pen, drafts, acc, out, stream=stream)
-    per_kind = {}
-    for kind, ms in prof:
-        per_kind.setdefault(kind, []).append(ms)
-    kb = kernel_bytes(shape, lens, accepted)
-    kernels = {}
-    for kind, v in per_kind.items():
-        avg = sum(v) / len(v)
-        kernels[kind] = {"launches": len(v), "ms_total": round(sum(v), 4), "us_avg": round(avg * 1e3, 2),
-                         "bytes_per_launch": kb[kind], "gbs": round(kb[kind] / (avg * 1e-3) / 1e9, 1)}
-    tot_prof = sum(k["ms_total"] for k in kernels.values())
-    for k in kernels.values():
-        k["share"] = round(k["ms_total"] / tot_prof, 4)
-    dominant = max(kernels, key=lambda k: kernels[k]["ms_total"])
+    # per-kernel times of the same step (event-bracketed launches)
+    kern = S.profiled()
+    kernels = kernel_report(shape, lens, accepted, kern, ms_per_step)
+    dominant = max(kernels, key=lambda k: kernels[k]["us_avg"])
 
     # end to end through the public host-buffer call: inputs up, the step,
     # outputs down, all inside vsd_verify_step_host
     h_seq0 = np.asarray(lens, dtype=np.int32)
     h_pen0 = np.asarray(pend, dtype=np.int32)
-    h_dr = np.ascontiguousarray(np.asarray(planted, dtype=np.int32))
+    h_dr = np.ascontiguousarray(np.asarray(S.planted, dtype=np.int32))
     h_seq, h_pen = h_seq0.copy(), h_pen0.copy()
     h_acc = np.empty(Bn, dtype=np.int32)
     h_out = np.empty((Bn, ROWS), dtype=np.int32)
@@ -450,7 +490,6 @@ def run_gpu(args, rank: int, world: int):
 
     hbm, tf_burst, tf_sust, peak_src = peaks()
     sb = step_bytes(shape, lens, accepted)
-    ms_per_step = total_s * 1e3 / args.steps
     value = job_tokens / total_s
     dk = kernels[dominant]
     achieved = dk["bytes_per_launch"] / (dk["us_avg"] * 1e-6) / 1e9
@@ -485,14 +524,17 @@ def run_gpu(args, rank: int, world: int):
         "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": recorded_traffic(dominant, w.name),
-                     "bytes_per_launch": dk["bytes_per_launch"], "us_avg": dk["us_avg"]},
+                     "bytes_per_launch": dk["bytes_per_launch"], "us_avg": dk["us_avg"],
+                     "time": "event-timed step x the kernel's share of the event-bracketed launches"},
         "kernels": kernels,
+        "kernel_times": "each launch of one step bracketed by CUDA events (median of 3, L2 flushed); us_avg is "
+                        "the event-timed step x the launch's share of those times",
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * statistics.mean(e2e_times), 4),
                 "ms_per_step_median": round(1e3 * statistics.median(e2e_times), 4),
                 "ms_per_step_max": round(1e3 * max(e2e_times), 4),
                 "call": "vsd_verify_step_host (one packed copy each way; replays the step graph the library captured on its first call)"},
-        "gpu_launches": len(prof),
+        "gpu_launches": len(kern),
         "clocks": clk.summary(t_region0, t_region1),
     }
     result["sampled"] = time_sampled(B, model, kv, Bn, seq, pen, drafts, acc, out, seq0, pend0, flush, stream, args)
@@ -500,11 +542,23 @@ def run_gpu(args, rank: int, world: int):
         result["consecutive"] = time_consecutive(B, model, kv, shape, w, Bn, seq, pen, seq0, pend0, max_tok, flush,
                                                  stream)
     if drafter is not None:
-        result["draft"] = time_draft(B, model, drafter, kv, shape, Bn, seq, pen, drafts, acc, out, seq0, pend0, g,
-                                     flush, stream, args)
+        result["draft"] = time_draft(B, model, drafter, kv, shape, Bn, seq, pen, drafts, acc, out, seq0, pend0,
+                                     S.graph, flush, stream, args)
         result["loop"] = time_loop(B, model, drafter, shape, w, max_tok, flush, stream)
-    if oracle_handle is not None:
-        r = finish_oracle(oracle_handle)
+    del S, kv, drafter
+    # the other configurations' own units, measured in the same run
+    for key, name in (("config4", "0.5b_mixed_b32_ctx1024-8192_paged16_64steps"), ("config5", "7b_mixed_b16_ctx4096")):
+        if args.no_extra or name == w.name or name not in WORKLOADS:
+            continue
+        try:
+            result[key] = measure_extra(B, WORKLOADS[name], model if WORKLOADS[name].shape == shape else None,
+                                        flush, stream, args)
+        except Exception as e:  # report, keep the main line
+            result[key] = {"workload": name, "error": repr(e)[:300]}
+        torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle's set-up and its timed sample start after the GPU arm
+        r = finish_oracle(start_oracle(args.workload, n_requests=2, budget_s=args.cpu_budget))
         if r and "tokens" in r:
             result["cpu_baseline"] = {
                 "value": round(r["tokens"] / r["seconds"], 3), "unit": "tokens/s", "cores": r["cores"],
@@ -516,6 +570,40 @@ def run_gpu(args, rank: int, world: int):
                                       "error": (r or {}).get("error", "no result")}
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def measure_extra(B, w, model, flush, stream, args):
+    """Another configuration's unit on the same GPU: its step (graph replays,
+    L2 flushed), the per-kernel split and, for a multi-step workload, its
+    consecutive committing steps as one graph.  `model`: the already built
+    target when the shape is the same (random-init weights either way)."""
+    import torch
+    from speculative_decoding_block_gb300.target import build_target
+    t_setup = time.time()
+    shape = w.shape
+    if model is None:
+        master = gen.master_weights(shape, w.seed)
+        model, _ = build_target(shape, master, max_positions=w.max_tokens_per_req())
+        del master
+    S = Step(B, w, model, flush, stream)
+    setup_s = time.time() - t_setup
+    steps = max(10, min(args.steps, 50))
+    ms = S.timed(args.warmup, steps)
+    ms_step = statistics.mean(ms)
+    kernels = kernel_report(shape, S.lens, S.accepted, S.profiled(), ms_step)
+    hbm = peaks()[0]
+    sb = step_bytes(shape, S.lens, S.accepted)
+    r = {"workload": w.name, "batch": S.Bn, "steps": steps, "warmup": args.warmup,
+         "ms_per_step": round(ms_step, 4), "tokens_per_step": S.tokens_per_step,
+         "tokens_per_s": round(S.tokens_per_step / (ms_step * 1e-3), 1),
+         "verify_steps_per_s": round(1e3 / ms_step, 2), "step_bytes": sb,
+         "step_hbm_frac": round(sb / (ms_step * 1e-3) / 1e9 / hbm, 4),
+         "accepted": [int(a) for a in S.accepted], "kernels": kernels,
+         "setup_s": round(setup_s, 1)}
+    if w.steps > 1:
+        r["consecutive"] = time_consecutive(B, model, S.kv, shape, w, S.Bn, S.seq, S.pen, S.seq0, S.pend0,
+                                            S.max_tok, flush, stream)
+    return r
 
 
 def time_consecutive(B, model, kv, shape, w, Bn, seq, pen, seq0, pend0, max_tok, flush, stream, runs=3):
@@ -785,6 +873,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-draft", action="store_true", help="skip the drafter-pass measurement")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other configurations' keys")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of timed oracle work")
     args = ap.parse_args()
     if args.warmup < 3:

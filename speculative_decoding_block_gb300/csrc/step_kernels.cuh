@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(128) embed_kernel(const EmbedArgs a) {
   __syncthreads();
   if (t < slices)
     a.ssq[static_cast<size_t>(t) * a.ssq_ld + row] = part[t][0] + part[t][1] + part[t][2] + part[t][3];
+  if (t == 0) trace_end(a.trace, 1);
 }
 
 // Validation of the caller's per-request state (component entry points that
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) 
       if (t < kRows) a.out_tokens[b * kRows + t] = -1;
       if (t == 0) a.accepted[b] = -1;
     }
+    if (t == 0) trace_end(a.trace, 1);
     return;
   }
   // KV commit of layer l: rows 0..acc, K and V, every head, 16-byte pieces
@@ -269,6 +271,7 @@ __global__ void __launch_bounds__(256) accept_commit_kernel(const CommitArgs a) 
       for (int i = t; i < a.hidden; i += blockDim.x) a.anchor[static_cast<size_t>(b) * a.hidden + i] = src[i];
     }
   }
+  if (t == 0) trace_end(a.trace, 1);
 }
 
 // ------------------------------------------------------------------ device-resident loop

@@ -61,32 +61,24 @@ __device__ __forceinline__ unsigned long long* trace_slot(const Trace& t, int ta
   if (cta >= static_cast<unsigned>(kTraceCtas) || tag >= kTraceTags) return nullptr;
   return t.buf + (static_cast<size_t>(t.id) * kTraceCtas + cta) * kTraceTags + tag;
 }
-// The stores out of line: only the null test stays in the hot loops' code.
-static __device__ __noinline__ void trace_store(Trace t, int tag, unsigned long long clk) {
-  if (unsigned long long* p = trace_slot(t, tag)) *p = clk;
-}
+// The stores are inline: no function call (and no stack traffic) ever sits
+// between a warp's divergent stamp and its next warp-synchronous instruction.
 __device__ __forceinline__ void trace_point(const Trace& t, int tag) {
-  if (t.buf != nullptr) trace_store(t, tag, static_cast<unsigned long long>(clock64()));
+  if (unsigned long long* p = trace_slot(t, tag)) *p = static_cast<unsigned long long>(clock64());
 }
-static __device__ __noinline__ void trace_start_store(Trace t) {
+__device__ __forceinline__ void trace_start(const Trace& t) {
   if (unsigned long long* p = trace_slot(t, 0)) {
     p[kTraceTags - 1] = globaltimer();
     p[0] = static_cast<unsigned long long>(clock64());
   }
 }
-__device__ __forceinline__ void trace_start(const Trace& t) {
-  if (t.buf != nullptr) trace_start_store(t);
-}
 // Closing stamp: clock64 at `tag` and %globaltimer in the second-to-last
 // slot, which gives the SM clock rate over the CTA's lifetime.
-static __device__ __noinline__ void trace_end_store(Trace t, int tag) {
+__device__ __forceinline__ void trace_end(const Trace& t, int tag) {
   if (unsigned long long* p = trace_slot(t, tag)) {
     *p = static_cast<unsigned long long>(clock64());
     p[kTraceTags - 2 - tag] = globaltimer();
   }
-}
-__device__ __forceinline__ void trace_end(const Trace& t, int tag) {
-  if (t.buf != nullptr) trace_end_store(t, tag);
 }
 
 // ------------------------------------------------------------------ mbarrier
