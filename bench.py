@@ -382,30 +382,44 @@ class Step:
                                stream=self.stream)
 
     def profiled(self, reps=3):
-        """Per-kernel device times (us) of one step: each launch bracketed by CUDA
-        events on the side stream (inputs reset, L2 flushed); medians over reps."""
+        """Per-kind launch counts and device times (us, summed over the kind's
+        launches) of one step: each launch bracketed by CUDA events on the side
+        stream (inputs reset, L2 flushed); medians over reps."""
         import torch
-        per = {}
+        runs = []
         for _ in range(reps):
             with torch.cuda.stream(self.stream):
                 self.reset()
                 self.flush.fill_(1.0)
+            per = {}
             for kind, ms in self.B.vsd_verify_step_profiled(self.model, self.kv, self.Bn, self.seq, self.pen,
                                                             self.drafts, self.acc, self.out, stream=self.stream):
-                per.setdefault(kind, []).append(ms * 1e3)
-        return {k: float(np.median(v)) for k, v in per.items()}
+                n, t = per.get(kind, (0, 0.0))
+                per[kind] = (n + 1, t + ms * 1e3)
+            runs.append(per)
+        return {k: (runs[0][k][0], float(np.median([r[k][1] for r in runs]))) for k in runs[0]}
+
+    def recapture(self):
+        """Captures the step graph again (after a change of the cache's step kernel)."""
+        import torch
+        self.reset()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self.B.vsd_verify_step(self.model, self.kv, self.Bn, self.seq, self.pen, self.drafts, self.acc, self.out,
+                                   stream=self.stream)
 
 
 def kernel_report(shape, lens, accepted, kern, ms_per_step):
     """`kernels` key of the bench line: per launch its share of the step, that
     share of the event-timed step, and its algorithmic bytes."""
     kb = kernel_bytes(shape, lens, accepted)
-    tot = sum(kern.values())
+    tot = sum(us for _, us in kern.values())
     kernels = {}
-    for k, us in kern.items():
-        us_ev = ms_per_step * 1e3 * us / tot
-        kernels[k] = {"launches": 1, "us_bracketed": round(us, 2), "us_avg": round(us_ev, 2),
-                      "ms_total": round(us_ev / 1e3, 4), "share": round(us / tot, 4),
+    for k, (n, us) in kern.items():
+        us_ev = ms_per_step * 1e3 * us / tot / n  # per launch, scaled to the event-timed step
+        kernels[k] = {"launches": n, "us_bracketed": round(us / n, 2), "us_avg": round(us_ev, 2),
+                      "ms_total": round(us_ev * n / 1e3, 4), "share": round(us / tot, 4),
                       "bytes_per_launch": kb[k], "gbs": round(kb[k] / (us_ev * 1e-6) / 1e9, 1)}
     return kernels
 
@@ -458,7 +472,7 @@ def run_gpu(args, rank: int, world: int):
     # per-kernel times of the same step (event-bracketed launches)
     kern = S.profiled()
     kernels = kernel_report(shape, lens, accepted, kern, ms_per_step)
-    dominant = max(kernels, key=lambda k: kernels[k]["us_avg"])
+    dominant = max(kernels, key=lambda k: kernels[k]["ms_total"])
 
     # end to end through the public host-buffer call: inputs up, the step,
     # outputs down, all inside vsd_verify_step_host
@@ -534,9 +548,10 @@ def run_gpu(args, rank: int, world: int):
                 "ms_per_step_median": round(1e3 * statistics.median(e2e_times), 4),
                 "ms_per_step_max": round(1e3 * max(e2e_times), 4),
                 "call": "vsd_verify_step_host (one packed copy each way; replays the step graph the library captured on its first call)"},
-        "gpu_launches": len(kern),
+        "gpu_launches": sum(n for n, _ in kern.values()),
         "clocks": clk.summary(t_region0, t_region1),
     }
+    result["persistent"] = time_persistent(B, S, args)
     result["sampled"] = time_sampled(B, model, kv, Bn, seq, pen, drafts, acc, out, seq0, pend0, flush, stream, args)
     if w.steps > 1:
         result["consecutive"] = time_consecutive(B, model, kv, shape, w, Bn, seq, pen, seq0, pend0, max_tok, flush,
@@ -572,6 +587,25 @@ def run_gpu(args, rank: int, world: int):
         print(json.dumps(result), flush=True)
 
 
+def time_persistent(B, S, args):
+    """The same step with the single persistent launch (graph replays, L2
+    flushed), then the cache goes back to the default launches."""
+    B.vsd_kv_set_step_kernel(S.kv, B.STEP_PERSISTENT)
+    try:
+        S.recapture()
+        ms = S.timed(args.warmup, max(10, min(args.steps, 100)))
+        kern = S.profiled()
+    finally:
+        B.vsd_kv_set_step_kernel(S.kv, B.STEP_LAYERED)
+        S.recapture()
+    m = statistics.mean(ms)
+    kernels = kernel_report(S.shape, S.lens, S.accepted, kern, m)
+    return {"ms_per_step": round(m, 4), "tokens_per_s": round(S.tokens_per_step / (m * 1e-3), 1),
+            "step_hbm_frac": round(step_bytes(S.shape, S.lens, S.accepted) / (m * 1e-3) / 1e9 / peaks()[0], 4),
+            "kernels": kernels, "gpu_launches": sum(n for n, _ in kern.values()),
+            "note": "vsd_kv_set_step_kernel(VSD_STEP_PERSISTENT): the layers and the head in one cooperative launch"}
+
+
 def measure_extra(B, w, model, flush, stream, args):
     """Another configuration's unit on the same GPU: its step (graph replays,
     L2 flushed), the per-kernel split and, for a multi-step workload, its
@@ -590,7 +624,8 @@ def measure_extra(B, w, model, flush, stream, args):
     steps = max(10, min(args.steps, 50))
     ms = S.timed(args.warmup, steps)
     ms_step = statistics.mean(ms)
-    kernels = kernel_report(shape, S.lens, S.accepted, S.profiled(), ms_step)
+    kern = S.profiled()
+    kernels = kernel_report(shape, S.lens, S.accepted, kern, ms_step)
     hbm = peaks()[0]
     sb = step_bytes(shape, S.lens, S.accepted)
     r = {"workload": w.name, "batch": S.Bn, "steps": steps, "warmup": args.warmup,
@@ -599,7 +634,8 @@ def measure_extra(B, w, model, flush, stream, args):
          "verify_steps_per_s": round(1e3 / ms_step, 2), "step_bytes": sb,
          "step_hbm_frac": round(sb / (ms_step * 1e-3) / 1e9 / hbm, 4),
          "accepted": [int(a) for a in S.accepted], "kernels": kernels,
-         "setup_s": round(setup_s, 1)}
+         "gpu_launches": sum(n for n, _ in kern.values()), "setup_s": round(setup_s, 1)}
+    r["persistent"] = time_persistent(B, S, args)
     if w.steps > 1:
         r["consecutive"] = time_consecutive(B, model, S.kv, shape, w, S.Bn, S.seq, S.pen, S.seq0, S.pend0,
                                             S.max_tok, flush, stream)

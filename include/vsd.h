@@ -192,6 +192,21 @@ vsd_status vsd_trace_read(vsd_kv* kv, uint64_t* slots_host, int32_t max_launches
  * the stream. */
 vsd_status vsd_get_device_status(vsd_kv* kv, vsd_stream stream, int32_t* status_host);
 
+/* How a step launches the decoder layers and the head (per cache; the
+ * default is VSD_STEP_LAYERED):
+ *   VSD_STEP_LAYERED     one launch per GEMM and per attention of every
+ *                        layer, then the head (5 * layers + 1 launches,
+ *                        chained with programmatic dependent launch);
+ *   VSD_STEP_PERSISTENT  one cooperative launch of a persistent kernel (one
+ *                        CTA per SM) that runs the same phases in order,
+ *                        separated by grid-wide counters with bounded waits.
+ * Both compute the same step (same kernels' arithmetic, the same results up
+ * to the order of floating-point sums).  Changing the mode drops the step
+ * graphs the cache holds.  VSD_ERR_ARG for a NULL cache or an unknown mode. */
+#define VSD_STEP_LAYERED    0
+#define VSD_STEP_PERSISTENT 1
+vsd_status vsd_kv_set_step_kernel(vsd_kv* kv, int32_t mode);
+
 /* Test-only; the method has no counterpart.  Enqueues one CTA that waits,
  * with the same bounded-wait pattern as the step's kernels, on a device flag
  * that nothing sets and on a shared-memory mbarrier that nothing completes.

@@ -28,7 +28,7 @@ EXPORTS = [
     "vsd_linear", "vsd_block_attention", "vsd_block_attention_static", "vsd_accept_commit",
     "vsd_verify_step_profiled", "vsd_draft_step", "vsd_draft_step_debug", "vsd_kv_get_anchor", "vsd_spec_loop", "vsd_verify_step_sampled",
     "vsd_verify_step_host",
-    "vsd_trace_enable", "vsd_trace_read", "vsd_debug_wait_probe",
+    "vsd_trace_enable", "vsd_trace_read", "vsd_debug_wait_probe", "vsd_kv_set_step_kernel",
 ]
 KERNEL_KINDS = ["embed", "qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm",
                 "lm_head_gemm", "accept_commit", "step"]
@@ -99,6 +99,7 @@ def lib() -> ctypes.CDLL:
             "vsd_linear": ([ctypes.POINTER(Weight), c_int, c_int, p, c_int, p, p], c_int),
             "vsd_trace_enable": ([p, c_int], c_int),
             "vsd_debug_wait_probe": ([p, ctypes.c_int64, p], c_int),
+            "vsd_kv_set_step_kernel": ([p, c_int], c_int),
             "vsd_trace_read": ([p, p, c_int, ctypes.POINTER(c_int), p], c_int),
             "vsd_block_attention": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
             "vsd_block_attention_static": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
@@ -268,6 +269,16 @@ def vsd_trace_read(kv: KV, max_launches: int = 256, stream=None):
     _check(lib().vsd_trace_read(kv.handle, ctypes.c_void_p(buf.ctypes.data), max_launches, ctypes.byref(n),
                                 _stream(stream)))
     return buf[: n.value]
+
+
+STEP_LAYERED, STEP_PERSISTENT = 0, 1
+
+
+def vsd_kv_set_step_kernel(kv: KV, mode: int) -> None:
+    """How the cache's steps launch the layers and the head: STEP_LAYERED
+    (one launch per GEMM / attention, the default) or STEP_PERSISTENT (one
+    persistent launch)."""
+    _check(lib().vsd_kv_set_step_kernel(kv.handle, mode))
 
 
 def vsd_debug_wait_probe(kv: KV, limit_cycles: int, stream=None) -> None:

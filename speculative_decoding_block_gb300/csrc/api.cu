@@ -144,6 +144,7 @@ struct vsd_kv {
   int* zeros = nullptr;     // [max_batch] zero context lengths (the draft pass reads no cache)
   int* probe_flag = nullptr;  // one int nothing ever sets (the wait probe's flag)
   long long wait_limit = kWaitLimitCycles;  // SM cycles a persistent-kernel wait may take
+  int step_kernel = VSD_STEP_LAYERED;       // how the decoder layers and the head are launched
   // slot state of the device-resident loop: lengths, pending, drafts, accepted [max_batch], outputs [max_batch][17]
   int *loop_seq = nullptr, *loop_pend = nullptr, *loop_drafts = nullptr, *loop_acc = nullptr, *loop_out = nullptr;
   // stochastic verification: per (row, vocabulary tile) sums, the drafts' logits, the decisions [max_batch][18]
@@ -823,6 +824,17 @@ vsd_status vsd_trace_read(vsd_kv* kv, uint64_t* slots_host, int32_t max_launches
   return VSD_OK;
 }
 
+vsd_status vsd_kv_set_step_kernel(vsd_kv* kv, int32_t mode) {
+  if (!kv || (mode != VSD_STEP_LAYERED && mode != VSD_STEP_PERSISTENT)) return fail(VSD_ERR_ARG, "bad arguments");
+  if (kv->step_kernel != mode) {
+    // the cached step graphs hold the other mode's launches
+    for (auto& g : kv->graphs) cudaGraphExecDestroy(g.exec);
+    kv->graphs.clear();
+    kv->step_kernel = mode;
+  }
+  return VSD_OK;
+}
+
 vsd_status vsd_debug_wait_probe(vsd_kv* kv, int64_t limit_cycles, vsd_stream stream) {
   if (!kv) return fail(VSD_ERR_ARG, "NULL pointer");
   if (limit_cycles < 1 || limit_cycles > kWaitLimitCycles) return fail(VSD_ERR_ARG, "limit out of range");
@@ -1023,6 +1035,90 @@ static vsd_status run_persistent(const vsd_model* m, vsd_kv* kv, int B, const in
   return VSD_OK;
 }
 
+// The decoder layers of model m as separate launches: per layer the QKV
+// GEMM (+ RoPE, block K / V to scratch), attention, O GEMM (+ residual),
+// gate/up GEMM (+ SiLU), down GEMM (+ residual); programmatic dependent
+// launch lets each kernel's set-up overlap the previous one's tail, and a
+// CUDA graph of the step removes the host from the chain.  Attention reads
+// attn_lens[b] cached rows per request.
+static vsd_status run_layers(const vsd_model* m, vsd_kv* kv, int B, const int* attn_lens, float* hidden,
+                             cudaStream_t st, LaunchTimer* timer) {
+  const vsd_model_config& c = m->cfg;
+  const int M = kRows * B, H = c.hidden;
+  vsd_status s;
+  const size_t layer_scratch = static_cast<size_t>(kv->max_batch) * c.n_kv * 32 * c.head_dim;
+  for (int l = 0; l < c.layers; ++l) {
+    GemmArgs a{};
+    set_norm_input(a, kv);
+    a.q_tile = kv->q_tile;
+    a.act_lo_rows = kv->m_alloc;
+    a.out_lo = static_cast<size_t>(kv->max_batch) * c.n_kv * 128 * c.head_dim;
+    a.k_new = kv->k_new + l * layer_scratch;
+    a.v_new = kv->v_new + l * layer_scratch;
+    a.ctx_len = kv->ctx_len;
+    a.rope = m->rope;
+    a.n_q = c.n_q;
+    a.n_kv = c.n_kv;
+    a.head_dim = c.head_dim;
+    TIMED(VSD_K_QKV, if ((s = run_gemm(m, m->qkv[l], EPI_QKV, kv->tm_u, M, a, kv->status, st, next_trace(kv)))) return s);
+    TIMED(VSD_K_ATTENTION, if ((s = run_attention(kv, l, B, attn_lens, st, true))) return s);
+    GemmArgs r{};
+    r.out_f32 = kv->x;
+    r.ld_out = H;
+    r.x16_out = kv->u;
+    r.act_lo_rows = kv->m_alloc;
+    r.out_lo = static_cast<size_t>(kv->m_alloc) * H;
+    r.ssq_out = kv->ssq;
+    r.ssq_ld = kv->m_alloc;
+    TIMED(VSD_K_O_PROJ, if ((s = run_gemm(m, m->o[l], EPI_RESID, kv->tm_o, M, r, kv->status, st, next_trace(kv)))) return s);
+    GemmArgs g{};
+    set_norm_input(g, kv);
+    g.act_out = kv->act_a;
+    g.act_lo_rows = kv->m_alloc;
+    g.out_lo = static_cast<size_t>(kv->m_alloc) * c.ffn;
+    g.ffn = c.ffn;
+    TIMED(VSD_K_GATE_UP, if ((s = run_gemm(m, m->gu[l], EPI_SILU, kv->tm_u, M, g, kv->status, st, next_trace(kv)))) return s);
+    r.hidden_out = hidden ? hidden + static_cast<size_t>(l + 1) * M * H : nullptr;
+    TIMED(VSD_K_DOWN, if ((s = run_gemm(m, m->down[l], EPI_RESID, kv->tm_a, M, r, kv->status, st, next_trace(kv)))) return s);
+  }
+  return VSD_OK;
+}
+
+// Final RMSNorm + head as its own launch: per-row argmax keys (kv->keys;
+// greedy) or, with `smp`, the per-tile (max, sum) partials and the drafts'
+// logits; logits optional.
+static vsd_status run_head(const vsd_model* m, vsd_kv* kv, int M, float* logits, cudaStream_t st, LaunchTimer* timer,
+                           const int* drafts, const SampleIn* smp) {
+  vsd_status s;
+  GemmArgs a{};
+  set_norm_input(a, kv);
+  a.keys = smp ? nullptr : kv->keys;
+  a.logits = logits;
+  a.act_lo_rows = kv->m_alloc;
+  if (smp) {
+    a.inv_temp = smp->inv_temp;
+    a.drafts = drafts;
+    a.tile_max = kv->tile_max;
+    a.tile_sum = kv->tile_sum;
+    a.draft_logit = kv->draft_logit;
+  }
+  TIMED(VSD_K_LM_HEAD, if ((s = run_gemm(m, m->lm, smp ? EPI_SAMPLE : EPI_ARGMAX, kv->tm_u, M, a, kv->status, st,
+                                         next_trace(kv)))) return s);
+  return VSD_OK;
+}
+
+// The decoder layers and the head of one step, as the cache's mode says.
+static vsd_status run_body(const vsd_model* m, vsd_kv* kv, int B, const int* attn_lens, float* hidden, float* logits,
+                           const int* drafts, const SampleIn* smp, cudaStream_t st, LaunchTimer* timer) {
+  vsd_status s;
+  if (kv->step_kernel == VSD_STEP_PERSISTENT) {
+    TIMED(VSD_K_STEP, if ((s = run_persistent(m, kv, B, attn_lens, hidden, logits, drafts, smp, st))) return s);
+    return VSD_OK;
+  }
+  if ((s = run_layers(m, kv, B, attn_lens, hidden, st, timer))) return s;
+  return run_head(m, kv, kRows * B, logits, st, timer, drafts, smp);
+}
+
 static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_lens, int* pending, const int* drafts,
                               int* accepted, int* out_tokens, float* logits, float* hidden, cudaStream_t st,
                               LaunchTimer* timer = nullptr, const SampleIn* smp = nullptr) {
@@ -1055,7 +1151,7 @@ static vsd_status verify_impl(const vsd_model* m, vsd_kv* kv, int B, int* seq_le
     e.trace = next_trace(kv);
     TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), false, e)));
   }
-  TIMED(VSD_K_STEP, if ((s = run_persistent(m, kv, B, seq_lens, hidden, logits, drafts, smp, st))) return s);
+  if ((s = run_body(m, kv, B, seq_lens, hidden, logits, drafts, smp, st, timer))) return s;
   if (smp) {
     SampleArgs sa{};
     sa.vocab = c.vocab;
@@ -1129,7 +1225,7 @@ static vsd_status draft_impl(const vsd_model* d, vsd_kv* kv, int B, const int* s
     e.trace = next_trace(kv);
     TIMED(VSD_K_EMBED, CK(launch_ex(embed_kernel, dim3(M), dim3(128), 0, st, use_pdl(st), false, e)));
   }
-  TIMED(VSD_K_STEP, if ((s = run_persistent(d, kv, B, kv->zeros, hidden, logits, nullptr, nullptr, st))) return s);
+  if ((s = run_body(d, kv, B, kv->zeros, hidden, logits, nullptr, nullptr, st, timer))) return s;
   TIMED(VSD_K_COMMIT, CK(launch_ex(draft_pick_kernel, dim3(ceil_div(B * kBlock, 128)), dim3(128), 0, st, use_pdl(st),
                                    false, static_cast<const unsigned long long*>(kv->keys), B, c.vocab, drafts,
                                    kv->status)));
