@@ -77,6 +77,10 @@ __device__ __forceinline__ void f16_pairs8(const float* v, float scale, uint32_t
   }
 }
 
+// The maximum a row's softmax weights are taken against moves only when a
+// chunk exceeds it by more than this (log2 units): weights stay <= 2^8.
+constexpr float kRescaleLog2 = 8.0f;
+
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
@@ -105,7 +109,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* pfull = sfree + 2;
   uint64_t* ofull = pfull + 1;
   uint64_t* ofree = ofull + 1;
-  uint32_t* tmem_p = reinterpret_cast<uint32_t*>(ofree + 1);
+  uint64_t* pfree = ofree + 1;   // a chunk's PV product is done: its P tile may be rewritten
+  uint32_t* tmem_p = reinterpret_cast<uint32_t*>(pfree + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_p + 1);
   volatile int* n_items = reinterpret_cast<volatile int*>(tmem_p + 3);
   float* xstat = reinterpret_cast<float*>(p_s + 2 * 32768 + 256);  // [2 parity][2 halves][128] maxima; then [2][2][128] sums
@@ -136,6 +141,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(pfull, 256);
     mbar_init(ofull, 1);
     mbar_init(ofree, 256);
+    mbar_init(pfree, 1);
     *abort_flag = 0;
     *sum_s = 0;
     fence_mbar_init();
@@ -353,8 +359,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ok = false;
             break;
           }
+          // P of chunk i is in shared memory (and any rescale of O is done);
+          // the item's first product overwrites O once the previous item's O is read
           if (!mbar_wait(pfull, g & 1, abort_flag, a.status) ||
-              (g >= 1 && !mbar_wait(ofree, (g - 1) & 1, abort_flag, a.status))) {
+              (i == 0 && ic > 0 && !mbar_wait(ofree, (ic - 1) & 1, abort_flag, a.status))) {
             ok = false;
             break;
           }
@@ -370,10 +378,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
             const uint64_t vd = sw128_desc(va + kk * 2048, 16384, 1024);
-            umma_f16(tmem + 256, sw128_desc(pa + aoff, 16, 1024), vd, id_pv, kk > 0 ? 1u : 0u);
+            umma_f16(tmem + 256, sw128_desc(pa + aoff, 16, 1024), vd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
             umma_f16(tmem + 256, sw128_desc(pa + 32768 + aoff, 16, 1024), vd, id_pv, 1u);
           }
-          umma_commit(ofull);
+          umma_commit(pfree);
+          if (i + 1 == x.n) umma_commit(ofull);  // the item's O is complete
           umma_commit(&vempty[st]);
         }
         g0 += x.n;
@@ -392,9 +401,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int it = blockIdx.x; ok && it < total; it += gridDim.x, ++ic) {
       const Item x = decode(it);
       float o[HH];
-#pragma unroll
-      for (int d = 0; d < HH; ++d) o[d] = 0.0f;
+      // m: the maximum this row's P values are taken against (log2 units)
       float m = -INFINITY, l = 0.0f;
+      const uint32_t o_tmem = tmem + lane_base + 256 + hf * HH;  // this thread's O columns
       for (int i = 0; i < x.n; ++i) {
         const int g = g0 + i;
         if (!mbar_wait(&sfull[g & 1], (g >> 1) & 1, abort_flag, a.status)) {
@@ -429,9 +438,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         xs[hf * 128 + r] = cm;
         named_bar_sync(bar_id, 64);
         cm = fmaxf(xs[r], xs[128 + r]);
-        const float m_new = fmaxf(m, cm);
-        const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-        const float alpha = ex2(m - m_use);  // 0 on the first chunk (m = -inf)
+        // O accumulates over the item's chunks in TMEM.  The maximum moves up
+        // only when a chunk's maximum exceeds it by more than kRescaleLog2, so
+        // P <= 2^8 (exact in the BF16 pairs and f32 sums); then the rows of O
+        // accumulated so far are scaled by 2^(m_old - m_new) before this
+        // chunk's product is added.
+        float alpha = 1.0f;
+        bool rescale = false;
+        if (m == -INFINITY) {
+          m = cm;  // the first chunk with a visible key (O rows are still 0)
+        } else if (cm > m + kRescaleLog2) {
+          alpha = ex2(m - cm);
+          m = cm;
+          rescale = true;
+        }
+        const float m_use = (m == -INFINITY) ? 0.0f : m;
+        // the previous chunk's PV product must be done before its P tile is
+        // rewritten, and before O is read for a rescale
+        if (g >= 1 && !mbar_wait(pfree, (g - 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xFFFFFFFFu, rescale)) {
+          float v[16];
+#pragma unroll
+          for (int d0 = 0; d0 < HH; d0 += 16) {
+            tmem_ld16(o_tmem + d0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int t = 0; t < 16; ++t) v[t] *= alpha;
+            tmem_st16_wait(o_tmem + d0, v);
+          }
+        }
         float psum = 0.0f;
         // probabilities -> BF16 pairs P_hi, P_lo, one 16-byte chunk (8 keys) at a
         // time: keys [col0, col0 + ncol) of row r live in atom col0 / 64
@@ -458,25 +497,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         fence_proxy_async();
         mbar_arrive(pfull);
         l = l * alpha + psum;
-        m = m_new;
-        if (!mbar_wait(ofull, g & 1, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        float v[16];
-#pragma unroll
-        for (int d0 = 0; d0 < HH; d0 += 16) {
-          tmem_ld16(tmem + lane_base + 256 + hf * HH + d0, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int t = 0; t < 16; ++t) o[d0 + t] = o[d0 + t] * alpha + v[t];
-        }
-        tc_fence_before();
-        mbar_arrive(ofree);
       }
       g0 += x.n;
       if (!ok) break;
+      // the item's O once its last product is done
+      if (!mbar_wait(ofull, ic & 1, abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int d0 = 0; d0 < HH; d0 += 16) {
+        tmem_ld16(o_tmem + d0, o + d0);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(ofree);
       if (threadIdx.x == 0 && ic == 0) trace_point(a.trace, 6);
       // row sum over both halves
       float* xl = xstat + 512 + (ic & 1) * 256;
