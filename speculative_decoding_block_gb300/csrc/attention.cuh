@@ -56,9 +56,11 @@ struct AttnArgs {
 __host__ __device__ inline uint32_t attn_stages(int hd) { return hd == 64 ? 3u : 1u; }
 // q tile (hi, lo), K/V stages, P tile (hi, lo), then barriers (256 B), row
 // statistics (4 KB) and item offsets
+constexpr int kMaxItemPages = 1024;  // page-table entries of one item staged in shared memory (128 chunks)
 __host__ __device__ inline uint32_t attn_smem_bytes(int hd) {
   const uint32_t q = 128u * hd * 2u, kv = 2u * 128u * hd * 2u;
-  return 1024u + 2u * q + attn_stages(hd) * kv + 2u * 32768u + 256u + 4096u + 4u * (kMaxReqs + 1);
+  return 1024u + 2u * q + attn_stages(hd) * kv + 2u * 32768u + 256u + 4096u + 4u * (kMaxReqs + 1) +
+         4u * kMaxItemPages;
 }
 
 __device__ __forceinline__ int valid_len(const AttnArgs& a, int b) {
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* n_items = reinterpret_cast<volatile int*>(tmem_p + 3);
   float* xstat = reinterpret_cast<float*>(p_s + 2 * 32768 + 256);  // [2 parity][2 halves][128] maxima; then [2][2][128] sums
   int* item_off = reinterpret_cast<int*>(p_s + 2 * 32768 + 256 + 4096);  // [B + 1] first item of each request
+  int* item_pages = item_off + (kMaxReqs + 1);  // [kMaxItemPages] the producer's current item's pages
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* cps_s = reinterpret_cast<volatile int*>(tmem_p + 4);
@@ -233,9 +236,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // the q tile and the block's own rows.
     {
       const uint64_t pol = policy_evict_first();
+      // The page-table entries of an item's context chunks, read into shared
+      // memory in one pass (eight loads in flight per lane) before its first
+      // copy: no chunk's copies then wait for a page-table round trip.
+      // false when the item has more pages than the staging holds (the
+      // chunks then read their entries one by one).
+      auto stage_pages = [&](const Item& x) -> bool {
+        const int npg = max(0, min(x.n_ctx, x.c_begin + x.n) - x.c_begin) * 8;
+        if (npg > kMaxItemPages) return false;
+        for (int j0 = 0; j0 < npg; j0 += 256) {
+          int v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u * 32 + lane;
+            v[u] = j < npg ? a.page_table[x.b * a.pages_per_req + min(x.c_begin * 8 + j, a.pages_per_req - 1)] : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (j0 + u * 32 + lane < npg) item_pages[j0 + u * 32 + lane] = v[u];
+        }
+        __syncwarp();
+        return true;
+      };
       // chunk i of item x, global chunk number g: K then V, each once its slot is free
-      // (page_pre: lane p's page of the chunk when the caller has read it, else -1)
-      auto issue = [&](const Item& x, int i, int g, int page_pre) -> bool {
+      // (staged: the item's pages are in item_pages)
+      auto issue = [&](const Item& x, int i, int g, bool staged) -> bool {
         const int st = g % NS;
         uint8_t* ks = kv_s + st * KVB;
         uint8_t* vs = kv_s + (NS + st) * KVB;
@@ -244,7 +269,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         int row0 = 0;
         if (ctx && lane < 8) {  // lane p: page p of the chunk
           const int pi = min(c * 8 + lane, a.pages_per_req - 1);
-          int page = page_pre >= 0 ? page_pre : a.page_table[x.b * a.pages_per_req + pi];
+          int page = staged ? item_pages[i * 8 + lane] : a.page_table[x.b * a.pages_per_req + pi];
           if (page < 0 || page >= a.num_pages) {
             atomicOr(a.status, VSD_DEV_BAD_PAGE);
             page = 0;
@@ -272,18 +297,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         return true;
       };
-      // The page-table entries of the first item's first chunks, in one round
-      // trip before the dependency wait (lane 8 i + p: page p of chunk i; the
-      // table is the caller's).  Their copies are issued after the wait,
-      // behind the q tile: the cooperative grid starts only once the previous
-      // kernel has left, so copies issued earlier would only queue ahead of q.
-      int npre = 0, pg = -1;
-      if (static_cast<int>(blockIdx.x) < total) {
-        const Item x = decode(blockIdx.x);
-        while (npre < min(x.n, NS) && x.c_begin + npre < x.n_ctx) ++npre;
-        if (lane < 8 * npre)
-          pg = a.page_table[x.b * a.pages_per_req + min((x.c_begin + lane / 8) * 8 + lane % 8, a.pages_per_req - 1)];
-      }
+      // The first item's page-table entries are read before the dependency
+      // wait (the table is the caller's).  Its copies are issued after the
+      // wait, behind the q tile: the cooperative grid starts only once the
+      // previous kernel has left, so copies issued earlier would only queue
+      // ahead of q.
+      bool staged = false;
+      if (static_cast<int>(blockIdx.x) < total) staged = stage_pages(decode(blockIdx.x));
       pdl_wait();  // q tiles and the block's K/V come from the QKV kernel
       if (lane == 0) trace_point(a.trace, 2);
       int g = 0, ic = 0;
@@ -302,9 +322,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (a.q_lo_rows) tma_load_2d(q_s + QB + at * 16384, &tm_q, qfull, at * 64, a.q_lo_rows + q_row);
           }
         }
+        if (ic > 0) staged = stage_pages(x);
         for (int i = 0; i < x.n; ++i, ++g) {
-          const int page_pre = (ic == 0 && i < npre) ? __shfl_sync(0xFFFFFFFFu, pg, (i * 8 + lane) & 31) : -1;
-          if (!issue(x, i, g, page_pre)) {
+          if (!issue(x, i, g, staged)) {
             ok = false;
             break;
           }
