@@ -207,6 +207,45 @@ vsd_status vsd_get_device_status(vsd_kv* kv, vsd_stream stream, int32_t* status_
 #define VSD_STEP_PERSISTENT 1
 vsd_status vsd_kv_set_step_kernel(vsd_kv* kv, int32_t mode);
 
+/* ------------------------------------------------------ ReplaySSM rollback
+ * A recurrent (gated delta rule) layer's state under block speculative
+ * decoding, kept the ReplaySSM way ("The Inference Stack Behind OCRia",
+ * section "Make speculative verification cheaper"): per request and head a
+ * checkpoint S (d x d fp32) plus a buffer of up to `window` recent inputs
+ * (k, v: d floats each; alpha, beta); outputs come from the checkpoint
+ * replayed through the buffer; rejected drafts are dropped by moving the
+ * buffer pointer; the checkpoint is rewritten only at flushes.  The pages
+ * give no update rule; the gated delta rule is used, per token
+ *     S <- alpha S (I - beta k k^T) + beta v k^T,   o = S q.
+ * The library owns every state buffer; d is 64 or 128, 17 <= window <= 128.
+ * Errors as elsewhere: host-visible ones return before any launch; a commit
+ * count outside [-1, 16] (its block is then rejected) or a corrupted pointer
+ * sets VSD_DEV_BAD_SEQLEN in the object's own status word. */
+typedef struct vsd_ssm vsd_ssm;
+vsd_status vsd_ssm_create(int32_t max_batch, int32_t heads, int32_t d, int32_t window, vsd_ssm** out);
+void vsd_ssm_destroy(vsd_ssm* ssm);
+/* Request req's state := state_dev ([heads][d][d] fp32, device; row-major
+ * S[i][j] multiplies k[j]), with an empty buffer.  Asynchronous. */
+vsd_status vsd_ssm_set_state(vsd_ssm* ssm, int32_t req, const float* state_dev, vsd_stream stream);
+/* Request req's effective state (the checkpoint replayed through the
+ * retained buffer) into state_dev ([heads][d][d], device).  Asynchronous. */
+vsd_status vsd_ssm_get_state(vsd_ssm* ssm, int32_t req, float* state_dev, vsd_stream stream);
+/* One verify block for requests 0..B-1: inputs q, k, v [B][heads][17][d]
+ * and alpha, beta [B][heads][17] (device, fp32; k is used as given, the
+ * caller normalises it); out [B][heads][17][d] receives o for each row, the
+ * state after the retained buffer and rows 0..t applied to q_t.  The block's
+ * inputs are staged in the buffer after the pointer.  Asynchronous. */
+vsd_status vsd_ssm_verify(vsd_ssm* ssm, int32_t batch, const float* q, const float* k, const float* v,
+                          const float* alpha, const float* beta, float* out, vsd_stream stream);
+/* Commit of the last verify block: accepted_dev[B] (device int32) holds each
+ * request's accepted drafts a (rows 0..a stay in the buffer; -1 keeps none,
+ * as for a request the step rejected).  A request whose next block would
+ * not fit (pointer + 17 > window) folds its buffer into the checkpoint.
+ * Asynchronous. */
+vsd_status vsd_ssm_commit(vsd_ssm* ssm, int32_t batch, const int32_t* accepted_dev, vsd_stream stream);
+/* Reads and clears the object's device status word.  Synchronises. */
+vsd_status vsd_ssm_get_device_status(vsd_ssm* ssm, vsd_stream stream, int32_t* status_host);
+
 /* Test-only; the method has no counterpart.  Enqueues one CTA that waits,
  * with the same bounded-wait pattern as the step's kernels, on a device flag
  * that nothing sets and on a shared-memory mbarrier that nothing completes.

@@ -29,6 +29,8 @@ EXPORTS = [
     "vsd_verify_step_profiled", "vsd_draft_step", "vsd_draft_step_debug", "vsd_kv_get_anchor", "vsd_spec_loop", "vsd_verify_step_sampled",
     "vsd_verify_step_host",
     "vsd_trace_enable", "vsd_trace_read", "vsd_debug_wait_probe", "vsd_kv_set_step_kernel",
+    "vsd_ssm_create", "vsd_ssm_destroy", "vsd_ssm_set_state", "vsd_ssm_get_state", "vsd_ssm_verify",
+    "vsd_ssm_commit", "vsd_ssm_get_device_status",
 ]
 KERNEL_KINDS = ["embed", "qkv_gemm", "attention", "o_proj_gemm", "gate_up_gemm", "down_gemm",
                 "lm_head_gemm", "accept_commit", "step"]
@@ -100,6 +102,13 @@ def lib() -> ctypes.CDLL:
             "vsd_trace_enable": ([p, c_int], c_int),
             "vsd_debug_wait_probe": ([p, ctypes.c_int64, p], c_int),
             "vsd_kv_set_step_kernel": ([p, c_int], c_int),
+            "vsd_ssm_create": ([c_int, c_int, c_int, c_int, ctypes.POINTER(p)], c_int),
+            "vsd_ssm_destroy": ([p], None),
+            "vsd_ssm_set_state": ([p, c_int, p, p], c_int),
+            "vsd_ssm_get_state": ([p, c_int, p, p], c_int),
+            "vsd_ssm_verify": ([p, c_int, p, p, p, p, p, p, p], c_int),
+            "vsd_ssm_commit": ([p, c_int, p, p], c_int),
+            "vsd_ssm_get_device_status": ([p, p, ctypes.POINTER(c_int)], c_int),
             "vsd_trace_read": ([p, p, c_int, ctypes.POINTER(c_int), p], c_int),
             "vsd_block_attention": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
             "vsd_block_attention_static": ([p, p, c_int, c_int, p, p, p, p, p, p], c_int),
@@ -272,6 +281,42 @@ def vsd_trace_read(kv: KV, max_launches: int = 256, stream=None):
 
 
 STEP_LAYERED, STEP_PERSISTENT = 0, 1
+
+
+class SSM:
+    """A recurrent layer's ReplaySSM state (checkpoint + input buffer) for max_batch requests."""
+
+    def __init__(self, max_batch: int, heads: int, d: int, window: int):
+        h = ctypes.c_void_p()
+        _check(lib().vsd_ssm_create(max_batch, heads, d, window, ctypes.byref(h)))
+        self.handle, self.max_batch, self.heads, self.d, self.window = h, max_batch, heads, d, window
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.vsd_ssm_destroy(self.handle)
+
+    def set_state(self, req: int, state, stream=None) -> None:
+        """state: float32 device tensor [heads, d, d]."""
+        _check(lib().vsd_ssm_set_state(self.handle, req, _dev(state, F32, "state", self.heads * self.d * self.d),
+                                       _stream(stream)))
+
+    def get_state(self, req: int, state, stream=None) -> None:
+        _check(lib().vsd_ssm_get_state(self.handle, req, _dev(state, F32, "state", self.heads * self.d * self.d),
+                                       _stream(stream)))
+
+    def verify(self, batch: int, q, k, v, alpha, beta, out, stream=None) -> None:
+        n = batch * self.heads * 17
+        _check(lib().vsd_ssm_verify(self.handle, batch, _dev(q, F32, "q", n * self.d), _dev(k, F32, "k", n * self.d),
+                                    _dev(v, F32, "v", n * self.d), _dev(alpha, F32, "alpha", n),
+                                    _dev(beta, F32, "beta", n), _dev(out, F32, "out", n * self.d), _stream(stream)))
+
+    def commit(self, batch: int, accepted, stream=None) -> None:
+        _check(lib().vsd_ssm_commit(self.handle, batch, _dev(accepted, I32, "accepted", batch), _stream(stream)))
+
+    def device_status(self, stream=None) -> int:
+        out = ctypes.c_int32()
+        _check(lib().vsd_ssm_get_device_status(self.handle, _stream(stream), ctypes.byref(out)))
+        return out.value
 
 
 def vsd_kv_set_step_kernel(kv: KV, mode: int) -> None:
