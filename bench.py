@@ -552,6 +552,7 @@ def run_gpu(args, rank: int, world: int):
         "clocks": clk.summary(t_region0, t_region1),
     }
     result["persistent"] = time_persistent(B, S, args)
+    result["replay_ssm"] = time_replay_ssm(B, flush, stream)
     result["sampled"] = time_sampled(B, model, kv, Bn, seq, pen, drafts, acc, out, seq0, pend0, flush, stream, args)
     if w.steps > 1:
         result["consecutive"] = time_consecutive(B, model, kv, shape, w, Bn, seq, pen, seq0, pend0, max_tok, flush,
@@ -585,6 +586,62 @@ def run_gpu(args, rank: int, world: int):
                                       "error": (r or {}).get("error", "no result")}
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def time_replay_ssm(B, flush, stream, layers=24, batch=32, heads=16, d=128, window=64, steps=40):
+    """The ReplaySSM verify + commit of a recurrent layer stack at 32 requests
+    (the pages profile 24 GDN layers at 32 concurrent requests): each layer's
+    own state object, one CUDA graph of all layers' verify and commit, the
+    accepted counts of a planted-prefix mix (mean k + 1 about 9.9), L2
+    flushed before each replay.  The pointers advance from replay to replay,
+    so the flushes (about one commit in four) are in the mean."""
+    import torch
+    rng = np.random.default_rng(11)
+    objs = [B.SSM(batch, heads, d, window) for _ in range(layers)]
+    for o in objs:
+        for b in range(batch):
+            o.set_state(b, torch.tensor((rng.normal(size=(heads, d, d)) * 0.05).astype(np.float32), device="cuda"))
+    n = batch * heads * ROWS
+    q = torch.tensor(rng.normal(size=(n, d)).astype(np.float32), device="cuda")
+    k = rng.normal(size=(n, d))
+    k = torch.tensor((k / np.linalg.norm(k, axis=1, keepdims=True)).astype(np.float32), device="cuda")
+    v = torch.tensor(rng.normal(size=(n, d)).astype(np.float32), device="cuda")
+    alpha = torch.tensor(rng.uniform(0.9, 1.0, n).astype(np.float32), device="cuda")
+    beta = torch.tensor(rng.uniform(0.0, 1.0, n).astype(np.float32), device="cuda")
+    out = torch.empty((n, d), dtype=torch.float32, device="cuda")
+    acc = torch.tensor(np.minimum(rng.geometric(1.0 / 9.9, batch) - 1, 16).astype(np.int32), device="cuda")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for o in objs:
+            o.verify(batch, q, k, v, alpha, beta, out, stream=stream)
+            o.commit(batch, acc, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(5 + steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+            if i >= 5:
+                evs[i - 5][0].record(stream)
+            g.replay()
+            if i >= 5:
+                evs[i - 5][1].record(stream)
+    torch.cuda.synchronize()
+    if any(o.device_status() for o in objs):
+        raise RuntimeError("replay verify reported a device error")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    us = ms * 1e3 / layers
+    hb = batch * heads
+    mean_ptr = window / 2  # the retained buffer grows from 0 towards the window between flushes
+    per_layer = (hb * d * d * 4                            # checkpoint read
+                 + hb * mean_ptr * (2 * d + 2) * 4         # retained buffer read
+                 + hb * ROWS * (3 * d + 2) * 4              # block inputs read
+                 + hb * ROWS * d * 4                        # outputs written
+                 + hb * ROWS * (2 * d + 2) * 4)             # block inputs staged
+    return {"layers": layers, "requests": batch, "heads": heads, "d": d, "window": window,
+            "us_per_layer": round(us, 2), "ms_all_layers": round(ms, 4),
+            "bytes_per_layer_est": int(per_layer), "hbm_frac_est": round(per_layer / (us * 1e-6) / 1e9 / peaks()[0], 4),
+            "accepted_plus_1_mean": round(float((acc + 1).float().mean().item()), 2),
+            "note": "verify + commit (with its periodic flush) of every layer in one graph; bytes without flushes"}
 
 
 def time_persistent(B, S, args):

@@ -1742,8 +1742,9 @@ vsd_status vsd_ssm_get_state(vsd_ssm* s, int32_t req, float* state, vsd_stream s
   a.req = req;
   const uint32_t smem = ssm_smem_bytes(s->d, s->window);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (s->d == 64) ssm_state_kernel<64><<<s->heads, kSsmThreads, smem, st>>>(a);
-  else ssm_state_kernel<128><<<s->heads, kSsmThreads, smem, st>>>(a);
+  const dim3 grid(s->heads, 1, s->d / kSsmRowsPerCta);
+  if (s->d == 64) ssm_state_kernel<64><<<grid, kSsmThreads, smem, st>>>(a);
+  else ssm_state_kernel<128><<<grid, kSsmThreads, smem, st>>>(a);
   CK(cudaGetLastError());
   return VSD_OK;
 }
@@ -1761,7 +1762,7 @@ vsd_status vsd_ssm_verify(vsd_ssm* s, int32_t batch, const float* q, const float
   a.out = out;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const uint32_t smem = ssm_smem_bytes(s->d, s->window);
-  const dim3 grid(s->heads, batch);
+  const dim3 grid(s->heads, batch, s->d / kSsmRowsPerCta);
   const cudaError_t e = s->d == 64 ? launch_ex(ssm_verify_kernel<64>, grid, dim3(kSsmThreads), smem, st, use_pdl(st), false, a)
                                    : launch_ex(ssm_verify_kernel<128>, grid, dim3(kSsmThreads), smem, st, use_pdl(st), false, a);
   if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "replay verify launch: %s", cudaGetErrorString(e));
@@ -1775,7 +1776,7 @@ vsd_status vsd_ssm_commit(vsd_ssm* s, int32_t batch, const int32_t* accepted, vs
   a.accepted = accepted;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const uint32_t smem = ssm_smem_bytes(s->d, s->window);
-  const dim3 grid(s->heads, batch);
+  const dim3 grid(s->heads, batch, s->d / kSsmRowsPerCta);
   cudaError_t e = s->d == 64 ? launch_ex(ssm_flush_kernel<64>, grid, dim3(kSsmThreads), smem, st, use_pdl(st), false, a)
                              : launch_ex(ssm_flush_kernel<128>, grid, dim3(kSsmThreads), smem, st, use_pdl(st), false, a);
   if (e == cudaSuccess)

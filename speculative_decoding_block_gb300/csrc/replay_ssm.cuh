@@ -12,11 +12,12 @@
 // per request and head, S of d x d (d_k = d_v = d).  Computed per thread as
 // u = S k, S <- alpha S + beta (v - alpha u) k^T, o = S q.
 //
-// One CTA of 256 threads per (head, request): thread t owns row t / TPR of S
-// and d / TPR of its columns in registers (TPR = 256 / d threads per row);
-// every input of the replay is staged in shared memory first, so the token
+// The rows of S update independently (row i needs only S[i,:], k, v_i and the
+// gates), so a CTA of 256 threads takes 64 rows of one (head, request): four
+// adjacent lanes share a row, each holding d / 4 of its columns in registers.
+// Every input of the replay is staged in shared memory first, so the token
 // loop needs no block-wide barrier (a row's dot products reduce across its
-// TPR adjacent lanes).
+// four lanes).  grid (H, B, d / 64).
 #pragma once
 
 #include "vsd_common.cuh"
@@ -24,6 +25,8 @@
 namespace vsd {
 
 constexpr int kSsmThreads = 256;
+constexpr int kSsmTpr = 4;                          // lanes per state row
+constexpr int kSsmRowsPerCta = kSsmThreads / kSsmTpr;  // 64
 constexpr int kSsmMaxWindow = 128;
 
 struct SsmArgs {
@@ -44,41 +47,53 @@ __host__ __device__ inline uint32_t ssm_smem_bytes(int d, int window) {
   return static_cast<uint32_t>(window * (2 * d + 2) + kRows * d) * 4u;
 }
 
-// The thread's d / TPR columns of its row through `n` staged tokens; with q
+// The thread's d / TPR columns of its row (lane c0 of the row holds the
+// float4 chunks c0, c0 + TPR, c0 + 2 TPR, ...: the row's four lanes read
+// consecutive 16-byte pieces, free of bank conflicts) through `n` staged
+// tokens; with q
 // given, the outputs of tokens n_out_from.. are written to out (row t of out
 // for token n_out_from + t).
 template <int D>
 __device__ __forceinline__ void ssm_replay(float* S, const float* sk, const float* sv, const float* sab, int n,
                                            const float* sq, int n_out_from, float* out, int row, int c0) {
-  constexpr int TPR = kSsmThreads / D, CPT = D / TPR;
+  constexpr int TPR = kSsmTpr, CPT = D / TPR;
   for (int tau = 0; tau < n; ++tau) {
-    const float4* k4 = reinterpret_cast<const float4*>(sk + tau * D + c0);
-    float u = 0.0f;
+    const float4* k4 = reinterpret_cast<const float4*>(sk + tau * D) + c0;
+    // four independent partial sums: the dot product's dependent chain is d / 16 long
+    float u0 = 0.0f, u1 = 0.0f, u2 = 0.0f, u3 = 0.0f;
 #pragma unroll
     for (int c = 0; c < CPT / 4; ++c) {
-      const float4 kk = k4[c];
-      u += S[4 * c] * kk.x + S[4 * c + 1] * kk.y + S[4 * c + 2] * kk.z + S[4 * c + 3] * kk.w;
+      const float4 kk = k4[c * TPR];
+      u0 = fmaf(S[4 * c], kk.x, u0);
+      u1 = fmaf(S[4 * c + 1], kk.y, u1);
+      u2 = fmaf(S[4 * c + 2], kk.z, u2);
+      u3 = fmaf(S[4 * c + 3], kk.w, u3);
     }
+    float u = (u0 + u1) + (u2 + u3);
 #pragma unroll
     for (int o = 1; o < TPR; o <<= 1) u += __shfl_xor_sync(0xFFFFFFFFu, u, o);
     const float alpha = sab[2 * tau], beta = sab[2 * tau + 1];
     const float coef = beta * (sv[tau * D + row] - alpha * u);
 #pragma unroll
     for (int c = 0; c < CPT / 4; ++c) {
-      const float4 kk = k4[c];
+      const float4 kk = k4[c * TPR];
       S[4 * c] = alpha * S[4 * c] + coef * kk.x;
       S[4 * c + 1] = alpha * S[4 * c + 1] + coef * kk.y;
       S[4 * c + 2] = alpha * S[4 * c + 2] + coef * kk.z;
       S[4 * c + 3] = alpha * S[4 * c + 3] + coef * kk.w;
     }
     if (sq != nullptr && tau >= n_out_from) {
-      const float4* q4 = reinterpret_cast<const float4*>(sq + (tau - n_out_from) * D + c0);
-      float o = 0.0f;
+      const float4* q4 = reinterpret_cast<const float4*>(sq + (tau - n_out_from) * D) + c0;
+      float o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f;
 #pragma unroll
       for (int c = 0; c < CPT / 4; ++c) {
-        const float4 qq = q4[c];
-        o += S[4 * c] * qq.x + S[4 * c + 1] * qq.y + S[4 * c + 2] * qq.z + S[4 * c + 3] * qq.w;
+        const float4 qq = q4[c * TPR];
+        o0 = fmaf(S[4 * c], qq.x, o0);
+        o1 = fmaf(S[4 * c + 1], qq.y, o1);
+        o2 = fmaf(S[4 * c + 2], qq.z, o2);
+        o3 = fmaf(S[4 * c + 3], qq.w, o3);
       }
+      float o = (o0 + o1) + (o2 + o3);
 #pragma unroll
       for (int x = 1; x < TPR; x <<= 1) o += __shfl_xor_sync(0xFFFFFFFFu, o, x);
       if ((threadIdx.x % TPR) == 0) out[(tau - n_out_from) * D + row] = o;
@@ -88,11 +103,11 @@ __device__ __forceinline__ void ssm_replay(float* S, const float* sk, const floa
 
 template <int D>
 __device__ __forceinline__ void ssm_load_rows(float* S, const float* src, int row, int c0) {
-  constexpr int CPT = D / (kSsmThreads / D);
-  const float4* s4 = reinterpret_cast<const float4*>(src + row * D + c0);
+  constexpr int CPT = D / kSsmTpr;
+  const float4* s4 = reinterpret_cast<const float4*>(src + row * D) + c0;
 #pragma unroll
   for (int c = 0; c < CPT / 4; ++c) {
-    const float4 x = s4[c];
+    const float4 x = s4[c * kSsmTpr];
     S[4 * c] = x.x;
     S[4 * c + 1] = x.y;
     S[4 * c + 2] = x.z;
@@ -102,10 +117,10 @@ __device__ __forceinline__ void ssm_load_rows(float* S, const float* src, int ro
 
 template <int D>
 __device__ __forceinline__ void ssm_store_rows(const float* S, float* dst, int row, int c0) {
-  constexpr int CPT = D / (kSsmThreads / D);
-  float4* d4 = reinterpret_cast<float4*>(dst + row * D + c0);
+  constexpr int CPT = D / kSsmTpr;
+  float4* d4 = reinterpret_cast<float4*>(dst + row * D) + c0;
 #pragma unroll
-  for (int c = 0; c < CPT / 4; ++c) d4[c] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
+  for (int c = 0; c < CPT / 4; ++c) d4[c * kSsmTpr] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
 }
 
 // Buffered tokens 0..n-1 of (request b, head h) into shared memory.
@@ -123,18 +138,18 @@ __device__ __forceinline__ void ssm_stage_buffer(const SsmArgs& a, size_t hb, in
 
 // Verify: outputs of the 17 block rows from the checkpoint replayed through
 // the retained buffer and the block; the block's inputs are staged in the
-// buffer after the pointer (the commit decides how many stay).  grid (H, B).
+// buffer after the pointer (the commit decides how many stay).  grid (H, B, d / 64).
 template <int D>
-__global__ void __launch_bounds__(kSsmThreads) ssm_verify_kernel(const SsmArgs a) {
-  constexpr int TPR = kSsmThreads / D, CPT = D / TPR;
+__global__ void __launch_bounds__(kSsmThreads, 3) ssm_verify_kernel(const SsmArgs a) {
+  constexpr int TPR = kSsmTpr, CPT = D / TPR;
   extern __shared__ float4 ssm_smem4[];
   float* sm = reinterpret_cast<float*>(ssm_smem4);
   pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-  const int row = t / TPR, c0 = (t % TPR) * CPT;
+  const int row = blockIdx.z * kSsmRowsPerCta + t / TPR, c0 = t % TPR;
   const int n = a.ptr[b];
   if (n < 0 || n + kRows > a.window) {  // a pointer the commit never leaves: no output, nothing staged
-    if (t == 0 && h == 0) atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
+    if (t == 0 && h == 0 && blockIdx.z == 0) atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
     return;
   }
   const size_t hb = static_cast<size_t>(b) * a.heads + h;
@@ -158,7 +173,8 @@ __global__ void __launch_bounds__(kSsmThreads) ssm_verify_kernel(const SsmArgs a
   ssm_load_rows<D>(S, a.ckpt + hb * D * D, row, c0);
   __syncthreads();
   ssm_replay<D>(S, sk, sv, sab, nt, sq, n, a.out + blk * D, row, c0);
-  // the block's inputs after the pointer
+  // the block's inputs after the pointer (once per head: the first row slice)
+  if (blockIdx.z != 0) return;
   float4* bk = reinterpret_cast<float4*>(a.buf_k + (hb * a.window + n) * D);
   float4* bv = reinterpret_cast<float4*>(a.buf_v + (hb * a.window + n) * D);
   for (int x = t; x < kRows * D / 4; x += kSsmThreads) {
@@ -178,17 +194,17 @@ __device__ __forceinline__ int ssm_committed(const SsmArgs& a, int b, bool repor
 }
 
 // Commit, first part: a request whose next block would not fit the buffer
-// folds its retained tokens into the checkpoint.  grid (H, B).
+// folds its retained tokens into the checkpoint.  grid (H, B, d / 64).
 template <int D>
-__global__ void __launch_bounds__(kSsmThreads) ssm_flush_kernel(const SsmArgs a) {
-  constexpr int TPR = kSsmThreads / D, CPT = D / TPR;
+__global__ void __launch_bounds__(kSsmThreads, 3) ssm_flush_kernel(const SsmArgs a) {
+  constexpr int TPR = kSsmTpr, CPT = D / TPR;
   extern __shared__ float4 ssm_smem4[];
   float* sm = reinterpret_cast<float*>(ssm_smem4);
   pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-  const int n = ssm_committed(a, b, t == 0 && h == 0);
+  const int n = ssm_committed(a, b, t == 0 && h == 0 && blockIdx.z == 0);
   if (n + kRows <= a.window || n > a.window) return;  // no flush (n > window: never left by a verify)
-  const int row = t / TPR, c0 = (t % TPR) * CPT;
+  const int row = blockIdx.z * kSsmRowsPerCta + t / TPR, c0 = t % TPR;
   const size_t hb = static_cast<size_t>(b) * a.heads + h;
   float* sk = sm;
   float* sv = sk + n * D;
@@ -211,15 +227,16 @@ __global__ void ssm_pointer_kernel(const SsmArgs a) {
 }
 
 // The effective state of request a.req: its checkpoint replayed through the
-// retained buffer.  grid (H).
+// retained buffer.  grid (H, 1, d / 64).
 template <int D>
-__global__ void __launch_bounds__(kSsmThreads) ssm_state_kernel(const SsmArgs a) {
-  constexpr int TPR = kSsmThreads / D, CPT = D / TPR;
+__global__ void __launch_bounds__(kSsmThreads, 3) ssm_state_kernel(const SsmArgs a) {
+  constexpr int TPR = kSsmTpr, CPT = D / TPR;
   extern __shared__ float4 ssm_smem4[];
   float* sm = reinterpret_cast<float*>(ssm_smem4);
   const int h = blockIdx.x, t = threadIdx.x;
   const int n = min(max(a.ptr[a.req], 0), a.window);
-  const int row = t / TPR, c0 = (t % TPR) * CPT;
+  // (grid (H, 1, d / 64): blockIdx.z is the row slice)
+  const int row = blockIdx.z * kSsmRowsPerCta + t / TPR, c0 = t % TPR;
   const size_t hb = static_cast<size_t>(a.req) * a.heads + h;
   float* sk = sm;
   float* sv = sk + n * D;
