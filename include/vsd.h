@@ -211,12 +211,16 @@ vsd_status vsd_kv_set_step_kernel(vsd_kv* kv, int32_t mode);
  * A recurrent (gated delta rule) layer's state under block speculative
  * decoding, kept the ReplaySSM way ("The Inference Stack Behind OCRia",
  * section "Make speculative verification cheaper"): per request and head a
- * checkpoint S (d x d fp32) plus a buffer of up to `window` recent inputs
- * (k, v: d floats each; alpha, beta); outputs come from the checkpoint
- * replayed through the buffer; rejected drafts are dropped by moving the
- * buffer pointer; the checkpoint is rewritten only at flushes.  The pages
- * give no update rule; the gated delta rule is used, per token
+ * checkpoint S (d x d fp32) plus a buffer of up to `window` recent tokens;
+ * outputs come from the checkpoint and the buffered tokens; rejected drafts
+ * are dropped by moving the buffer pointer; the checkpoint is rewritten only
+ * at flushes.  The pages give no update rule; the gated delta rule is used,
+ * per token
  *     S <- alpha S (I - beta k k^T) + beta v k^T,   o = S q.
+ * The buffer holds per token its key, its corrected value
+ * u = beta (v - alpha S_prev k) and the sum of log alpha since the
+ * checkpoint, so that S = e^{L} S_ckpt + sum_s e^{L - L_s} u_s k_s^T in
+ * closed form (log alpha is floored at -200, where e^{L} underflows).
  * The library owns every state buffer; d is 64 or 128, 17 <= window <= 128.
  * Errors as elsewhere: host-visible ones return before any launch; a commit
  * count outside [-1, 16] (its block is then rejected) or a corrupted pointer
@@ -234,7 +238,8 @@ vsd_status vsd_ssm_get_state(vsd_ssm* ssm, int32_t req, float* state_dev, vsd_st
  * and alpha, beta [B][heads][17] (device, fp32; k is used as given, the
  * caller normalises it); out [B][heads][17][d] receives o for each row, the
  * state after the retained buffer and rows 0..t applied to q_t.  The block's
- * inputs are staged in the buffer after the pointer.  Asynchronous. */
+ * tokens are staged in the buffer after the pointer.  q, k, v and out must be
+ * 16-byte aligned (VSD_ERR_ARG otherwise).  Asynchronous. */
 vsd_status vsd_ssm_verify(vsd_ssm* ssm, int32_t batch, const float* q, const float* k, const float* v,
                           const float* alpha, const float* beta, float* out, vsd_stream stream);
 /* Commit of the last verify block: accepted_dev[B] (device int32) holds each

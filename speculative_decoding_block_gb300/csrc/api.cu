@@ -1656,19 +1656,19 @@ vsd_status vsd_accept_commit(const vsd_model* m, vsd_kv* kv, int32_t B, const fl
 
 // ------------------------------------------------------------------ ReplaySSM
 struct vsd_ssm {
-  int max_batch = 0, heads = 0, d = 0, window = 0;
-  float *ckpt = nullptr, *buf_k = nullptr, *buf_v = nullptr, *buf_ab = nullptr;
+  int max_batch = 0, heads = 0, d = 0, window = 0, sms = 1;
+  float *ckpt = nullptr, *buf_k = nullptr, *buf_u = nullptr, *buf_L = nullptr;
   int* ptr = nullptr;
   int* status = nullptr;
 };
 
 namespace {
 template <int D>
-vsd_status ssm_opt_in(uint32_t smem) {
+vsd_status ssm_opt_in(uint32_t verify_smem, uint32_t fold_smem) {
   cudaError_t e;
-  if ((e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_verify_kernel<D>), static_cast<int>(smem))) ||
-      (e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_flush_kernel<D>), static_cast<int>(smem))) ||
-      (e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_state_kernel<D>), static_cast<int>(smem))))
+  if ((e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_verify_kernel<D>), static_cast<int>(verify_smem))) ||
+      (e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_flush_kernel<D>), static_cast<int>(fold_smem))) ||
+      (e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_state_kernel<D>), static_cast<int>(fold_smem))))
     return fail(VSD_ERR_CUDA, "shared-memory opt-in: %s", cudaGetErrorString(e));
   return VSD_OK;
 }
@@ -1681,8 +1681,8 @@ SsmArgs ssm_args(const vsd_ssm* s, int batch) {
   a.batch = batch;
   a.ckpt = s->ckpt;
   a.buf_k = s->buf_k;
-  a.buf_v = s->buf_v;
-  a.buf_ab = s->buf_ab;
+  a.buf_u = s->buf_u;
+  a.buf_L = s->buf_L;
   a.ptr = s->ptr;
   a.status = s->status;
   return a;
@@ -1697,17 +1697,20 @@ vsd_status vsd_ssm_create(int32_t max_batch, int32_t heads, int32_t d, int32_t w
   if (d != 64 && d != 128) return fail(VSD_ERR_UNSUPPORTED, "state dimension d must be 64 or 128");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(VSD_ERR_CUDA, "no CUDA device");
-  const uint32_t smem = ssm_smem_bytes(d, window);
-  vsd_status st = d == 64 ? ssm_opt_in<64>(smem) : ssm_opt_in<128>(smem);
+  const uint32_t vsmem = ssm_verify_layout(d, window).total, fsmem = ssm_fold_smem_bytes(d, window);
+  vsd_status st = d == 64 ? ssm_opt_in<64>(vsmem, fsmem) : ssm_opt_in<128>(vsmem, fsmem);
   if (st) return st;
+  int sms = 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return fail(VSD_ERR_CUDA, "SM count");
   vsd_ssm* s = new vsd_ssm();
   s->max_batch = max_batch;
   s->heads = heads;
   s->d = d;
   s->window = window;
+  s->sms = sms;
   const size_t hb = static_cast<size_t>(max_batch) * heads;
   if ((st = dalloc(&s->ckpt, hb * d * d)) || (st = dalloc(&s->buf_k, hb * window * d)) ||
-      (st = dalloc(&s->buf_v, hb * window * d)) || (st = dalloc(&s->buf_ab, hb * window * 2)) ||
+      (st = dalloc(&s->buf_u, hb * window * d)) || (st = dalloc(&s->buf_L, hb * window)) ||
       (st = dalloc(&s->ptr, max_batch)) || (st = dalloc(&s->status, 1))) {
     vsd_ssm_destroy(s);
     return st;
@@ -1718,7 +1721,7 @@ vsd_status vsd_ssm_create(int32_t max_batch, int32_t heads, int32_t d, int32_t w
 
 void vsd_ssm_destroy(vsd_ssm* s) {
   if (!s) return;
-  void* ptrs[] = {s->ckpt, s->buf_k, s->buf_v, s->buf_ab, s->ptr, s->status};
+  void* ptrs[] = {s->ckpt, s->buf_k, s->buf_u, s->buf_L, s->ptr, s->status};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete s;
@@ -1740,11 +1743,10 @@ vsd_status vsd_ssm_get_state(vsd_ssm* s, int32_t req, float* state, vsd_stream s
   SsmArgs a = ssm_args(s, 0);
   a.state_out = state;
   a.req = req;
-  const uint32_t smem = ssm_smem_bytes(s->d, s->window);
+  const uint32_t smem = ssm_fold_smem_bytes(s->d, s->window);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid(s->heads, 1, s->d / kSsmRowsPerCta);
-  if (s->d == 64) ssm_state_kernel<64><<<grid, kSsmThreads, smem, st>>>(a);
-  else ssm_state_kernel<128><<<grid, kSsmThreads, smem, st>>>(a);
+  if (s->d == 64) ssm_state_kernel<64><<<s->heads, kSsmThreads, smem, st>>>(a);
+  else ssm_state_kernel<128><<<s->heads, kSsmThreads, smem, st>>>(a);
   CK(cudaGetLastError());
   return VSD_OK;
 }
@@ -1753,6 +1755,9 @@ vsd_status vsd_ssm_verify(vsd_ssm* s, int32_t batch, const float* q, const float
                           const float* alpha, const float* beta, float* out, vsd_stream stream) {
   if (!s || !q || !k || !v || !alpha || !beta || !out) return fail(VSD_ERR_ARG, "NULL pointer");
   if (batch < 1 || batch > s->max_batch) return fail(VSD_ERR_ARG, "batch %d outside [1, %d]", batch, s->max_batch);
+  for (const void* x : {static_cast<const void*>(q), static_cast<const void*>(k), static_cast<const void*>(v),
+                        static_cast<const void*>(out)})
+    if (reinterpret_cast<uintptr_t>(x) % 16) return fail(VSD_ERR_ARG, "q, k, v and out must be 16-byte aligned");
   SsmArgs a = ssm_args(s, batch);
   a.q = q;
   a.k = k;
@@ -1761,8 +1766,8 @@ vsd_status vsd_ssm_verify(vsd_ssm* s, int32_t batch, const float* q, const float
   a.beta = beta;
   a.out = out;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const uint32_t smem = ssm_smem_bytes(s->d, s->window);
-  const dim3 grid(s->heads, batch, s->d / kSsmRowsPerCta);
+  const uint32_t smem = ssm_verify_layout(s->d, s->window).total;
+  const dim3 grid(std::min(s->heads * batch, s->sms));  // persistent over the (request, head) items
   const cudaError_t e = s->d == 64 ? launch_ex(ssm_verify_kernel<64>, grid, dim3(kSsmThreads), smem, st, use_pdl(st), false, a)
                                    : launch_ex(ssm_verify_kernel<128>, grid, dim3(kSsmThreads), smem, st, use_pdl(st), false, a);
   if (e != cudaSuccess) return fail(VSD_ERR_CUDA, "replay verify launch: %s", cudaGetErrorString(e));
@@ -1775,8 +1780,8 @@ vsd_status vsd_ssm_commit(vsd_ssm* s, int32_t batch, const int32_t* accepted, vs
   SsmArgs a = ssm_args(s, batch);
   a.accepted = accepted;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const uint32_t smem = ssm_smem_bytes(s->d, s->window);
-  const dim3 grid(s->heads, batch, s->d / kSsmRowsPerCta);
+  const uint32_t smem = ssm_fold_smem_bytes(s->d, s->window);
+  const dim3 grid(s->heads, batch);
   cudaError_t e = s->d == 64 ? launch_ex(ssm_flush_kernel<64>, grid, dim3(kSsmThreads), smem, st, use_pdl(st), false, a)
                              : launch_ex(ssm_flush_kernel<128>, grid, dim3(kSsmThreads), smem, st, use_pdl(st), false, a);
   if (e == cudaSuccess)

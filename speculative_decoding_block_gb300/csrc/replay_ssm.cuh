@@ -3,21 +3,29 @@
 //
 // "The Inference Stack Behind OCRia", section "Make speculative verification
 // cheaper": a GDN layer's fixed-size state is kept as a checkpoint plus a
-// small buffer of recent inputs; outputs are computed from the checkpoint and
-// the buffered inputs, the checkpoint is rewritten only at periodic flushes,
+// small buffer of recent tokens; outputs are computed from the checkpoint and
+// the buffered tokens, the checkpoint is rewritten only at periodic flushes,
 // and rejected drafts are rolled back by moving the buffer pointer.  The
 // pages give no update rule; the gated delta rule of Gated DeltaNet is used:
 //     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
 //     o_t = S_t q_t,
-// per request and head, S of d x d (d_k = d_v = d).  Computed per thread as
-// u = S k, S <- alpha S + beta (v - alpha u) k^T, o = S q.
+// per request and head, S of d x d (d_k = d_v = d).
 //
-// The rows of S update independently (row i needs only S[i,:], k, v_i and the
-// gates), so a CTA of 256 threads takes 64 rows of one (head, request): four
-// adjacent lanes share a row, each holding d / 4 of its columns in registers.
-// Every input of the replay is staged in shared memory first, so the token
-// loop needs no block-wide barrier (a row's dot products reduce across its
-// four lanes).  grid (H, B, d / 64).
+// Form used here.  With u_t = beta_t (v_t - alpha_t S_{t-1} k_t) (the
+// token's corrected value) the update reads S_t = alpha_t S_{t-1} + u_t k_t^T,
+// so with L_t = sum of log alpha over the tokens since the checkpoint S_0,
+//     S_t = e^{L_t} S_0 + sum_{s<=t} e^{L_t - L_s} u_s k_s^T.
+// Hence, for a new token t after the retained ones,
+//     u_t = beta_t (v_t - e^{L_t} S_0 k_t - sum_{s<t} e^{L_t - L_s} (k_s.k_t) u_s),
+//     o_t = e^{L_t} S_0 q_t + sum_{s<=t} e^{L_t - L_s} (k_s.q_t) u_s.
+// The buffer keeps, per retained token, k_s, u_s and L_s (u_s depends only on
+// the checkpoint and the tokens before s, so rejected rows never touch it).
+// A verify block then costs two products with the checkpoint per block row
+// (S_0 k_t, S_0 q_t) plus dot products with the buffered keys -- dense
+// contractions, run on the tensor cores -- and a 17-step triangular solve
+// per state row, instead of a replay of the whole buffer through the d x d
+// state; a flush folds the buffer into the checkpoint with the closed form
+// above.
 #pragma once
 
 #include "vsd_common.cuh"
@@ -25,163 +33,489 @@
 namespace vsd {
 
 constexpr int kSsmThreads = 256;
-constexpr int kSsmTpr = 4;                          // lanes per state row
-constexpr int kSsmRowsPerCta = kSsmThreads / kSsmTpr;  // 64
 constexpr int kSsmMaxWindow = 128;
+constexpr int kSsmCoefLd = 20;             // 17 coefficients per key row, padded for float4 reads
+constexpr float kSsmMinLogGate = -200.0f;  // log alpha floor: e^-200 underflows to 0 in every product
 
 struct SsmArgs {
   int heads, d, window, batch;
   // a verify block [B][H][17][d] (q, k, v) and [B][H][17] (alpha, beta)
   const float *q, *k, *v, *alpha, *beta;
-  float* out;                        // [B][H][17][d]
-  float* ckpt;                       // [max_batch][H][d][d]
-  float *buf_k, *buf_v, *buf_ab;     // [max_batch][H][window][d], same, [..][window][2]
-  int* ptr;                          // [max_batch] retained buffered tokens
-  const int* accepted;               // [B] commit: accepted drafts a (-1: rejected)
-  float* state_out;                  // [H][d][d] effective state of one request
-  int req;                           // its request
+  float* out;                 // [B][H][17][d]
+  float* ckpt;                // [max_batch][H][d][d]
+  float *buf_k, *buf_u;       // [max_batch][H][window][d]: keys, corrected values
+  float* buf_L;               // [max_batch][H][window]: log gate sums since the checkpoint
+  int* ptr;                   // [max_batch] retained buffered tokens
+  const int* accepted;        // [B] commit: accepted drafts a (-1: rejected)
+  float* state_out;           // [H][d][d] effective state of one request
+  int req;                    // its request
   int* status;
 };
 
-__host__ __device__ inline uint32_t ssm_smem_bytes(int d, int window) {
-  return static_cast<uint32_t>(window * (2 * d + 2) + kRows * d) * 4u;
-}
-
-// The thread's d / TPR columns of its row (lane c0 of the row holds the
-// float4 chunks c0, c0 + TPR, c0 + 2 TPR, ...: the row's four lanes read
-// consecutive 16-byte pieces, free of bank conflicts) through `n` staged
-// tokens; with q
-// given, the outputs of tokens n_out_from.. are written to out (row t of out
-// for token n_out_from + t).
-template <int D>
-__device__ __forceinline__ void ssm_replay(float* S, const float* sk, const float* sv, const float* sab, int n,
-                                           const float* sq, int n_out_from, float* out, int row, int c0) {
-  constexpr int TPR = kSsmTpr, CPT = D / TPR;
-  for (int tau = 0; tau < n; ++tau) {
-    const float4* k4 = reinterpret_cast<const float4*>(sk + tau * D) + c0;
-    // four independent partial sums: the dot product's dependent chain is d / 16 long
-    float u0 = 0.0f, u1 = 0.0f, u2 = 0.0f, u3 = 0.0f;
+// Register slices for the fold: a row-pair group of kSsmLanes lanes holds two
+// state rows; lane p of the group holds float4 chunks p, p + 4, p + 8, ... of
+// both (the group's lanes read consecutive 16-byte pieces of a shared vector:
+// one wavefront, no bank conflict).
+constexpr int kSsmLanes = 4;
+template <int N>
+__device__ __forceinline__ void ssm_load_slice(float* x, const float* src, int p) {
+  const float4* s4 = reinterpret_cast<const float4*>(src) + p;
 #pragma unroll
-    for (int c = 0; c < CPT / 4; ++c) {
-      const float4 kk = k4[c * TPR];
-      u0 = fmaf(S[4 * c], kk.x, u0);
-      u1 = fmaf(S[4 * c + 1], kk.y, u1);
-      u2 = fmaf(S[4 * c + 2], kk.z, u2);
-      u3 = fmaf(S[4 * c + 3], kk.w, u3);
-    }
-    float u = (u0 + u1) + (u2 + u3);
-#pragma unroll
-    for (int o = 1; o < TPR; o <<= 1) u += __shfl_xor_sync(0xFFFFFFFFu, u, o);
-    const float alpha = sab[2 * tau], beta = sab[2 * tau + 1];
-    const float coef = beta * (sv[tau * D + row] - alpha * u);
-#pragma unroll
-    for (int c = 0; c < CPT / 4; ++c) {
-      const float4 kk = k4[c * TPR];
-      S[4 * c] = alpha * S[4 * c] + coef * kk.x;
-      S[4 * c + 1] = alpha * S[4 * c + 1] + coef * kk.y;
-      S[4 * c + 2] = alpha * S[4 * c + 2] + coef * kk.z;
-      S[4 * c + 3] = alpha * S[4 * c + 3] + coef * kk.w;
-    }
-    if (sq != nullptr && tau >= n_out_from) {
-      const float4* q4 = reinterpret_cast<const float4*>(sq + (tau - n_out_from) * D) + c0;
-      float o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f;
-#pragma unroll
-      for (int c = 0; c < CPT / 4; ++c) {
-        const float4 qq = q4[c * TPR];
-        o0 = fmaf(S[4 * c], qq.x, o0);
-        o1 = fmaf(S[4 * c + 1], qq.y, o1);
-        o2 = fmaf(S[4 * c + 2], qq.z, o2);
-        o3 = fmaf(S[4 * c + 3], qq.w, o3);
-      }
-      float o = (o0 + o1) + (o2 + o3);
-#pragma unroll
-      for (int x = 1; x < TPR; x <<= 1) o += __shfl_xor_sync(0xFFFFFFFFu, o, x);
-      if ((threadIdx.x % TPR) == 0) out[(tau - n_out_from) * D + row] = o;
-    }
+  for (int c = 0; c < N / 4; ++c) {
+    const float4 v = s4[c * kSsmLanes];
+    x[4 * c] = v.x;
+    x[4 * c + 1] = v.y;
+    x[4 * c + 2] = v.z;
+    x[4 * c + 3] = v.w;
   }
 }
 
+// ---------------------------------------------------------------- verify
+// The verify's two dense products run on the tensor cores (tcgen05.mma
+// kind::f16, fp32 accumulation in TMEM):
+//   P = S_0 X^T     (d state rows x 48 columns),
+//   G = K X^T       (the retained and block keys, up to 128 rows x 48),
+// with X the block's vectors in columns 0-15 k_0..k_15, 16-31 q_0..q_15,
+// 32 k_16, 33 q_16 (34-47 unused).  fp32 values enter as f16 pairs,
+// hi = f16(x 2^e), lo = f16(x 2^e - hi), with a power-of-2 scale 2^e per
+// row that puts the row's largest magnitude in [2^14, 2^15); the products
+// hi.hi + hi.lo + lo.hi carry about 22 significant bits, and the scales are
+// divided out exactly afterwards.
+constexpr int kSsmN = 48;              // MMA N (block vectors, padded)
+constexpr int kSsmTmemCols = 128;      // P at columns 0-47, G at 64-111
+constexpr uint32_t kSsmAtomA = 16384;  // one 64-wide K atom of a 128-row A tile (128-byte rows, swizzled)
+constexpr uint32_t kSsmAtomB = kSsmN * 128;
+
+struct SsmVerifyLayout {
+  uint32_t a, b, x, v, u, coefA, coefB, L, eL, beta, expS, expK, expB, bar, total;
+};
+__host__ __device__ inline SsmVerifyLayout ssm_verify_layout(int d, int window) {
+  SsmVerifyLayout l{};
+  const uint32_t na = static_cast<uint32_t>(d / 64);
+  uint32_t o = 0;
+  l.a = o;  o += 2u * na * kSsmAtomA;  // A hi, then A lo
+  l.b = o;  o += 2u * na * kSsmAtomB;  // B hi, then B lo
+  l.x = o;  o += 4u * 2u * kRows * d;  // block k_t, q_t fp32, [2t] = k_t, [2t + 1] = q_t
+  l.v = o;  o += 4u * kRows * d;
+  l.u = o;  o += 4u * window * d;     // corrected values: retained, then the block's
+  l.coefA = o;  o += 4u * window * kSsmCoefLd;
+  l.coefB = o;  o += 4u * window * kSsmCoefLd;
+  l.L = o;  o += 4u * window;
+  l.eL = o;  o += 4u * kRows;
+  l.beta = o;  o += 4u * kRows;
+  l.expS = o;  o += 4u * 128u;
+  l.expK = o;  o += 4u * 128u;
+  l.expB = o;  o += 4u * kSsmN;
+  o = (o + 7u) & ~7u;
+  l.bar = o;  o += 16u;               // mbarrier, then the TMEM base and the abort flag
+  l.total = o + 1024u;                // + alignment of the dynamic shared memory base
+  return l;
+}
+
+__host__ __device__ inline uint32_t ssm_fold_smem_bytes(int d, int window) {
+  return static_cast<uint32_t>(2 * window * d + window) * 4u;
+}
+
+// Exponent e with max * 2^e in [2^14, 2^15) (127 for m = 0: no bound),
+// clamped so that 2^e and 2^-e are normal floats.
+__device__ __forceinline__ int ssm_scale_exp(float m) {
+  if (!(m > 0.0f)) return 127;
+  int ex;
+  frexpf(m, &ex);  // m = f 2^ex, f in [0.5, 1)
+  return max(-120, min(120, 15 - ex));
+}
+__device__ __forceinline__ float ssm_pow2(int e) { return __int_as_float((127 + e) << 23); }
+
+// Tiles are filled a whole row per warp instruction (d = 128; two rows for
+// d = 64), lane l holding the row's values 4l..4l+3, so that every global
+// load is one contiguous run of whole lines.  Slot i of a thread is row
+// (8 i + warp) RPI + lane / LPR.
 template <int D>
-__device__ __forceinline__ void ssm_load_rows(float* S, const float* src, int row, int c0) {
-  constexpr int CPT = D / kSsmTpr;
-  const float4* s4 = reinterpret_cast<const float4*>(src + row * D) + c0;
+struct SsmTile {
+  static constexpr int LPR = D / 4;     // lanes per row
+  static constexpr int RPI = 32 / LPR;  // rows per warp instruction
+  static constexpr int RPP = 8 * RPI;   // rows per pass of the 8 warps
+};
+template <int D>
+__device__ __forceinline__ int ssm_tile_row(int i) {
+  return (8 * i + static_cast<int>(threadIdx.x >> 5)) * SsmTile<D>::RPI +
+         static_cast<int>(threadIdx.x & 31) / SsmTile<D>::LPR;
+}
+// Loads slots 0..N-1 (row r from src(r); zero for r >= rows or a null src).
+template <int D, int N, typename Src>
+__device__ __forceinline__ void ssm_tile_load(float4* x, int rows, Src src) {
+  const int l4 = static_cast<int>(threadIdx.x & 31) % SsmTile<D>::LPR;
 #pragma unroll
-  for (int c = 0; c < CPT / 4; ++c) {
-    const float4 x = s4[c * kSsmTpr];
-    S[4 * c] = x.x;
-    S[4 * c + 1] = x.y;
-    S[4 * c + 2] = x.z;
-    S[4 * c + 3] = x.w;
+  for (int i = 0; i < N; ++i) {
+    const int r = ssm_tile_row<D>(i);
+    const float* s = r < rows ? src(r) : nullptr;
+    x[i] = s ? reinterpret_cast<const float4*>(s)[l4] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
-
-template <int D>
-__device__ __forceinline__ void ssm_store_rows(const float* S, float* dst, int row, int c0) {
-  constexpr int CPT = D / kSsmTpr;
-  float4* d4 = reinterpret_cast<float4*>(dst + row * D) + c0;
+// Stores slots 0..N-1 with r < rows into a swizzled f16 tile (hi at tile, lo
+// at tile + lo_off; atom_bytes per 64-wide K atom), each row scaled by 2^e
+// for its own e (a min-reduction over the row's lanes), e into expo[r].
+template <int D, int N>
+__device__ __forceinline__ void ssm_tile_store(uint8_t* tile, uint32_t atom_bytes, uint32_t lo_off, const float4* x,
+                                               int* expo, int rows) {
+  constexpr int LPR = SsmTile<D>::LPR;
+  const int lane = static_cast<int>(threadIdx.x & 31), l4 = lane % LPR;
+  const unsigned mask = LPR == 32 ? 0xFFFFFFFFu : (0xFFFFu << (lane & 16));
+  const int k0 = 4 * l4;
+  const uint32_t col_off = static_cast<uint32_t>(k0 >> 6) * atom_bytes + static_cast<uint32_t>((k0 >> 2) & 1) * 8u;
 #pragma unroll
-  for (int c = 0; c < CPT / 4; ++c) d4[c * kSsmTpr] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
+  for (int i = 0; i < N; ++i) {
+    const int r = ssm_tile_row<D>(i);
+    if (r >= rows) continue;  // the row's lanes agree
+    const float4 v = x[i];
+    const float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    int e = __reduce_min_sync(mask, ssm_scale_exp(m));
+    if (e == 127) e = 0;  // a zero row
+    const float sc = ssm_pow2(e);
+    const float y0 = v.x * sc, y1 = v.y * sc, y2 = v.z * sc, y3 = v.w * sc;
+    const uint32_t h01 = f32x2_to_f16x2(y0, y1), h23 = f32x2_to_f16x2(y2, y3);
+    const __half2 a01 = *reinterpret_cast<const __half2*>(&h01), a23 = *reinterpret_cast<const __half2*>(&h23);
+    const uint32_t l01 = f32x2_to_f16x2(y0 - __low2float(a01), y1 - __high2float(a01));
+    const uint32_t l23 = f32x2_to_f16x2(y2 - __low2float(a23), y3 - __high2float(a23));
+    const uint32_t off = col_off + sw128_off(static_cast<uint32_t>(r), (k0 & 63) >> 3);
+    *reinterpret_cast<uint2*>(tile + off) = make_uint2(h01, h23);
+    *reinterpret_cast<uint2*>(tile + lo_off + off) = make_uint2(l01, l23);
+    if (l4 == 0) expo[r] = e;
+  }
 }
 
-// Buffered tokens 0..n-1 of (request b, head h) into shared memory.
+// One product tile issue: (A hi, B hi), (A hi, B lo), (A lo, B hi)
+// over the K atoms, into TMEM columns d_col..d_col + 47; commit on bar.
 template <int D>
-__device__ __forceinline__ void ssm_stage_buffer(const SsmArgs& a, size_t hb, int n, float* sk, float* sv, float* sab) {
-  const float4* bk = reinterpret_cast<const float4*>(a.buf_k + hb * a.window * D);
-  const float4* bv = reinterpret_cast<const float4*>(a.buf_v + hb * a.window * D);
-  for (int x = threadIdx.x; x < n * D / 4; x += kSsmThreads) {
-    reinterpret_cast<float4*>(sk)[x] = bk[x];
-    reinterpret_cast<float4*>(sv)[x] = bv[x];
-  }
-  const float* bab = a.buf_ab + hb * a.window * 2;
-  for (int x = threadIdx.x; x < 2 * n; x += kSsmThreads) sab[x] = bab[x];
+__device__ __forceinline__ void ssm_issue(uint32_t d_tmem, const uint8_t* a_tile, const uint8_t* b_tile,
+                                          uint64_t* bar) {
+  constexpr uint32_t NA = D / 64;
+  const uint32_t idesc = idesc_f16(128, kSsmN, false, false, false);
+  const uint64_t ah = sw128_desc(smem_u32(a_tile), 16, 1024), al = sw128_desc(smem_u32(a_tile + NA * kSsmAtomA), 16, 1024);
+  const uint64_t bh = sw128_desc(smem_u32(b_tile), 16, 1024), bl = sw128_desc(smem_u32(b_tile + NA * kSsmAtomB), 16, 1024);
+  const uint64_t ad[3] = {ah, ah, al}, bd[3] = {bh, bl, bh};
+#pragma unroll
+  for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+    for (uint32_t at = 0; at < NA; ++at)
+#pragma unroll
+      for (uint32_t kk = 0; kk < 4; ++kk)  // 16-element K steps inside the 128-byte atom
+        umma_f16(d_tmem, ad[pr] + at * (kSsmAtomA >> 4) + 2 * kk, bd[pr] + at * (kSsmAtomB >> 4) + 2 * kk, idesc,
+                 (pr | at | kk) != 0 ? 1u : 0u);
+  umma_commit(bar);
 }
 
-// Verify: outputs of the 17 block rows from the checkpoint replayed through
-// the retained buffer and the block; the block's inputs are staged in the
-// buffer after the pointer (the commit decides how many stay).  grid (H, B, d / 64).
+// This warp's 17 values of one TMEM product row: lane quarter q's row, k
+// columns (kind 0: 0-15 and 32) or q columns (kind 1: 16-31 and 33), each
+// divided by 2^(row exponent + column exponent).
+__device__ __forceinline__ void ssm_tmem_row(uint32_t taddr, int kind, int row_exp, const int* expB, float* out) {
+  float v0[16], v1[16];
+  tmem_ld16(taddr + 16u * kind, v0);
+  tmem_ld16(taddr + 32u, v1);
+  tmem_ld_wait();
+  const float rs = ssm_pow2(-row_exp);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) out[j] = v0[j] * rs * ssm_pow2(-expB[16 * kind + j]);
+  out[16] = (kind ? v1[1] : v1[0]) * rs * ssm_pow2(-expB[32 + kind]);
+}
+
+// Verify: outputs of the 17 block rows, and the block's keys, corrected
+// values and log gates staged in the buffer after the pointer (the commit
+// decides how many stay).  Persistent: grid min(H B, SMs), 256 threads, one
+// (request, head) item at a time, the next item's checkpoint and buffer
+// pulled into L2 first.  Per item:
+//   1. stage the block's k, q, v, the retained corrected values and logs;
+//      the checkpoint rows into the A tile, the block vectors into the B tile;
+//   2. P = S_0 X^T on the tensor cores; then the key rows into the A tile and
+//      G = K X^T;
+//   3. from TMEM: warps 0-3 take the k columns of their lane quarter's rows,
+//      warps 4-7 the q columns (P), then the coefficients
+//      e^{L_t - L_s} (k_s.k_t) and e^{L_t - L_s} (k_s.q_t) from G;
+//   4. per state row: warps 0-3 solve the block's corrected values in token
+//      order, warps 4-7 then form the outputs; both first sum the retained
+//      tokens' terms.
 template <int D>
-__global__ void __launch_bounds__(kSsmThreads, 3) ssm_verify_kernel(const SsmArgs a) {
-  constexpr int TPR = kSsmTpr, CPT = D / TPR;
-  extern __shared__ float4 ssm_smem4[];
-  float* sm = reinterpret_cast<float*>(ssm_smem4);
-  pdl_wait();
-  const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-  const int row = blockIdx.z * kSsmRowsPerCta + t / TPR, c0 = t % TPR;
-  const int n = a.ptr[b];
-  if (n < 0 || n + kRows > a.window) {  // a pointer the commit never leaves: no output, nothing staged
-    if (t == 0 && h == 0 && blockIdx.z == 0) atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
-    return;
+__global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArgs a) {
+  constexpr uint32_t NA = D / 64;
+  extern __shared__ uint8_t ssm_smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ssm_smem_raw) + 1023) & ~uintptr_t(1023));
+  const SsmVerifyLayout l = ssm_verify_layout(D, a.window);
+  uint8_t* tA = base + l.a;
+  uint8_t* tB = base + l.b;
+  float* sx = reinterpret_cast<float*>(base + l.x);
+  float* sv = reinterpret_cast<float*>(base + l.v);
+  float* su = reinterpret_cast<float*>(base + l.u);
+  float* sA = reinterpret_cast<float*>(base + l.coefA);
+  float* sB = reinterpret_cast<float*>(base + l.coefB);
+  float* sL = reinterpret_cast<float*>(base + l.L);
+  float* seL = reinterpret_cast<float*>(base + l.eL);
+  float* sbeta = reinterpret_cast<float*>(base + l.beta);
+  int* expS = reinterpret_cast<int*>(base + l.expS);
+  int* expK = reinterpret_cast<int*>(base + l.expK);
+  int* expB = reinterpret_cast<int*>(base + l.expB);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + l.bar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + l.bar + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + l.bar + 12);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int quarter = warp & 3, kind = warp >> 2;
+  const int row = 32 * quarter + lane;  // TMEM lane of this thread
+  if (t == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  const size_t hb = static_cast<size_t>(b) * a.heads + h;
-  const int nt = n + kRows;
-  float* sk = sm;           // [nt][D]
-  float* sv = sk + nt * D;  // [nt][D]
-  float* sq = sv + nt * D;  // [17][D]
-  float* sab = sq + kRows * D;  // [nt][2]
-  ssm_stage_buffer<D>(a, hb, n, sk, sv, sab);
-  const size_t blk = hb * kRows;
-  for (int x = t; x < kRows * D / 4; x += kSsmThreads) {
-    reinterpret_cast<float4*>(sk + n * D)[x] = reinterpret_cast<const float4*>(a.k + blk * D)[x];
-    reinterpret_cast<float4*>(sv + n * D)[x] = reinterpret_cast<const float4*>(a.v + blk * D)[x];
-    reinterpret_cast<float4*>(sq)[x] = reinterpret_cast<const float4*>(a.q + blk * D)[x];
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kSsmTmemCols);
+    tmem_relinquish();
   }
-  if (t < kRows) {
-    sab[2 * (n + t)] = a.alpha[blk + t];
-    sab[2 * (n + t) + 1] = a.beta[blk + t];
-  }
-  float S[CPT];
-  ssm_load_rows<D>(S, a.ckpt + hb * D * D, row, c0);
+  tc_fence_before();
   __syncthreads();
-  ssm_replay<D>(S, sk, sv, sab, nt, sq, n, a.out + blk * D, row, c0);
-  // the block's inputs after the pointer (once per head: the first row slice)
-  if (blockIdx.z != 0) return;
-  float4* bk = reinterpret_cast<float4*>(a.buf_k + (hb * a.window + n) * D);
-  float4* bv = reinterpret_cast<float4*>(a.buf_v + (hb * a.window + n) * D);
-  for (int x = t; x < kRows * D / 4; x += kSsmThreads) {
-    bk[x] = reinterpret_cast<const float4*>(sk + n * D)[x];
-    bv[x] = reinterpret_cast<const float4*>(sv + n * D)[x];
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+  pdl_wait();
+  const int items = a.heads * a.batch;
+  constexpr int NS0 = D / SsmTile<D>::RPP;    // checkpoint rows per thread
+  constexpr int NKR = 128 / SsmTile<D>::RPP;  // key rows per thread (up to 128)
+  constexpr int NXB = kSsmN / SsmTile<D>::RPP;  // block vector rows per thread
+  uint32_t phase = 0;  // completions of bar so far
+  int nb_next = blockIdx.x < items ? a.ptr[blockIdx.x / a.heads] : 0;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int b = item / a.heads, h = item % a.heads;
+    const int nb = nb_next;
+    const size_t hb = static_cast<size_t>(b) * a.heads + h;
+    const size_t blk = hb * kRows, brow = hb * a.window;
+    const int nx = item + gridDim.x;
+    if (nx < items) {
+      nb_next = a.ptr[nx / a.heads];  // used by the next item: its latency hides behind this one
+      // the next item's checkpoint, retained buffer and block inputs into L2
+      if (t == kSsmThreads - 32) {
+        const size_t hbn = static_cast<size_t>(nx / a.heads) * a.heads + nx % a.heads;
+        bulk_prefetch_l2(a.ckpt + hbn * D * D, D * D * 4u);
+        bulk_prefetch_l2(a.k + hbn * kRows * D, kRows * D * 4u);
+        bulk_prefetch_l2(a.q + hbn * kRows * D, kRows * D * 4u);
+        bulk_prefetch_l2(a.v + hbn * kRows * D, kRows * D * 4u);
+        const int nbn = min(max(nb_next, 0), a.window);
+        if (nbn > 0) {
+          bulk_prefetch_l2(a.buf_k + hbn * a.window * D, nbn * D * 4u);
+          bulk_prefetch_l2(a.buf_u + hbn * a.window * D, nbn * D * 4u);
+        }
+      }
+    }
+    if (nb < 0 || nb + kRows > a.window) {  // a pointer the commit never leaves: no output, nothing staged
+      if (t == 0) atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
+      continue;  // uniform over the CTA
+    }
+    const int nt = nb + kRows;
+    // ---- 1. staging: the checkpoint rows and block vectors into registers,
+    // the rest by asynchronous copies
+    const float* ck = a.ckpt + hb * D * D;
+    float4 xr[NKR];  // checkpoint rows now, key rows later
+    ssm_tile_load<D, NS0>(xr, D, [&](int r) { return ck + static_cast<size_t>(r) * D; });
+    float4 xb[NXB];
+    ssm_tile_load<D, NXB>(xb, kSsmN, [&](int r) -> const float* {
+      // B rows: 0-15 k_0..k_15, 16-31 q_0..q_15, 32 k_16, 33 q_16, then zero
+      if (r < 16 || r == 32) return a.k + (blk + (r < 16 ? r : 16)) * D;
+      if (r < 34) return a.q + (blk + (r < 32 ? r - 16 : 16)) * D;
+      return nullptr;
+    });
+    {
+      constexpr int R4 = D / 4;
+      for (int x = t; x < kRows * R4; x += kSsmThreads) {
+        const int tok = x / R4, c = x % R4;
+        cp_async16(sx + (2 * tok) * D + 4 * c, a.k + blk * D + 4 * x);
+        cp_async16(sx + (2 * tok + 1) * D + 4 * c, a.q + blk * D + 4 * x);
+        cp_async16(sv + 4 * x, a.v + blk * D + 4 * x);
+      }
+      for (int x = t; x < nb * R4; x += kSsmThreads) cp_async16(su + 4 * x, a.buf_u + brow * D + 4 * x);
+      for (int x = t; x < nb; x += kSsmThreads) cp_async4(sL + x, a.buf_L + brow + x);
+    }
+    if (warp == 0) {  // the block's log gate sums, continuing the last retained token's
+      const float base_L = nb > 0 ? a.buf_L[brow + nb - 1] : 0.0f;
+      float la = 0.0f, beta = 0.0f;
+      if (lane < kRows) {
+        la = fmaxf(logf(a.alpha[blk + lane]), kSsmMinLogGate);
+        beta = a.beta[blk + lane];
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, la, o);
+        if (lane >= o) la += y;
+      }
+      if (lane < kRows) {
+        sL[nb + lane] = base_L + la;
+        seL[lane] = expf(base_L + la);
+        sbeta[lane] = beta;
+      }
+    }
+    // checkpoint rows -> A (rows >= d of the tile are never read back), block vectors -> B
+    ssm_tile_store<D, NS0>(tA, kSsmAtomA, NA * kSsmAtomA, xr, expS, D);
+    ssm_tile_store<D, NXB>(tB, kSsmAtomB, NA * kSsmAtomB, xb, expB, kSsmN);
+    cp_async_wait_all();
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    // ---- 2. P = S_0 X^T
+    if (t == 0) {
+      tc_fence_after();
+      ssm_issue<D>(tmem, tA, tB, bar);
+    }
+    // key rows: loaded before the wait, stored into A once the P product has
+    // read the checkpoint tile
+    ssm_tile_load<D, NKR>(xr, nt, [&](int r) { return r < nb ? a.buf_k + (brow + r) * D : sx + 2 * (r - nb) * D; });
+    mbar_wait(bar, phase & 1u, abort_flag, a.status);
+    ++phase;
+    tc_fence_after();
+    ssm_tile_store<D, NKR>(tA, kSsmAtomA, NA * kSsmAtomA, xr, expK, nt);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) break;
+    if (t == 0) {
+      tc_fence_after();
+      ssm_issue<D>(tmem + 64u, tA, tB, bar);
+    }
+    // ---- 3. P rows while G is computed
+    float P[kRows];
+    if (row < D) ssm_tmem_row(taddr, kind, expS[row], expB, P);
+    mbar_wait(bar, phase & 1u, abort_flag, a.status);
+    ++phase;
+    tc_fence_after();
+    if (32 * quarter < nt) {  // warp-uniform (the TMEM load is warp-wide); rows >= nt write nothing
+      // coefficients of key row s = row against the block's tokens (kind 0: k_t, 1: q_t)
+      float g[kRows];
+      ssm_tmem_row(taddr + 64u, kind, expK[row], expB, g);
+      if (row < nt) {
+        const float Ls = sL[row];
+        float* dst = (kind ? sB : sA) + row * kSsmCoefLd;
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+          // a: strictly earlier tokens (s < nb + t); b: up to the token itself
+          const bool used = row < nb + j + kind;
+          dst[j] = used ? expf(sL[nb + j] - Ls) * g[j] : 0.0f;
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) break;
+    // ---- 4. per state row
+    float X[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) X[j] = 0.0f;
+    const float* C = kind ? sB : sA;
+    if (row < D) {
+#pragma unroll 4
+      for (int s = 0; s < nb; ++s) {
+        const float u = su[s * D + row];
+        const float4* c4 = reinterpret_cast<const float4*>(C + s * kSsmCoefLd);
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+          const float4 cc = c4[j];
+          X[4 * j] = fmaf(cc.x, u, X[4 * j]);
+          if (4 * j + 1 < kRows) X[4 * j + 1] = fmaf(cc.y, u, X[4 * j + 1]);
+          if (4 * j + 2 < kRows) X[4 * j + 2] = fmaf(cc.z, u, X[4 * j + 2]);
+          if (4 * j + 3 < kRows) X[4 * j + 3] = fmaf(cc.w, u, X[4 * j + 3]);
+        }
+      }
+      if (kind == 0) {  // the block's corrected values, in token order
+        float U[kRows];
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+          float acc = X[j];
+#pragma unroll
+          for (int i = 0; i < j; ++i) acc = fmaf(C[(nb + i) * kSsmCoefLd + j], U[i], acc);
+          U[j] = sbeta[j] * (sv[j * D + row] - fmaf(seL[j], P[j], acc));
+          su[(nb + j) * D + row] = U[j];
+          a.buf_u[(brow + nb + j) * D + row] = U[j];
+        }
+      }
+    }
+    __syncthreads();
+    if (row < D && kind == 1) {  // outputs
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) {
+        float acc = fmaf(seL[j], P[j], X[j]);
+#pragma unroll
+        for (int i = 0; i <= j; ++i) acc = fmaf(C[(nb + i) * kSsmCoefLd + j], su[(nb + i) * D + row], acc);
+        a.out[(blk + j) * D + row] = acc;
+      }
+    }
+    // the block's keys and log sums after the pointer
+    {
+      constexpr int R4 = D / 4;
+      float4* bk = reinterpret_cast<float4*>(a.buf_k + (brow + nb) * D);
+      for (int x = t; x < kRows * R4; x += kSsmThreads)
+        bk[x] = reinterpret_cast<const float4*>(sx)[(2 * (x / R4)) * R4 + x % R4];
+      if (t < kRows) a.buf_L[brow + nb + t] = sL[nb + t];
+    }
+    __syncthreads();  // the shared buffers are reused by the next item
   }
-  if (t < 2 * kRows) a.buf_ab[(hb * a.window + n) * 2 + t] = sab[2 * n + t];
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kSsmTmemCols);
+  }
+}
+
+// S = e^{L_{n-1}} S_0 + sum_{s<n} e^{L_{n-1} - L_s} u_s k_s^T for (request,
+// head) hb with n retained tokens, into dst (may be the checkpoint itself:
+// each thread reads its rows before writing them).  256 threads; two rows
+// per 4-lane group as in the verify.
+template <int D>
+__device__ __forceinline__ void ssm_fold(const SsmArgs& a, size_t hb, int n, float* dst, float* sm) {
+  constexpr int CPT = D / kSsmLanes;
+  const int t = threadIdx.x, g = t / kSsmLanes, p = t % kSsmLanes;
+  const size_t brow = hb * a.window;
+  float* sk = sm;               // [n][D]
+  float* su = sk + n * D;       // [n][D]
+  float* sc = su + n * D;       // [n] e^{L_{n-1} - L_s}
+  const float4* k4 = reinterpret_cast<const float4*>(a.buf_k + brow * D);
+  const float4* u4 = reinterpret_cast<const float4*>(a.buf_u + brow * D);
+  for (int x = t; x < n * D / 4; x += kSsmThreads) {
+    reinterpret_cast<float4*>(sk)[x] = k4[x];
+    reinterpret_cast<float4*>(su)[x] = u4[x];
+  }
+  const float Ln = n > 0 ? a.buf_L[brow + n - 1] : 0.0f;
+  for (int x = t; x < n; x += kSsmThreads) sc[x] = expf(Ln - a.buf_L[brow + x]);
+  const bool has_rows = 2 * g < D;
+  float S[2 * CPT];
+  if (has_rows) {
+    const float* src = a.ckpt + hb * D * D + static_cast<size_t>(2 * g) * D;
+    ssm_load_slice<CPT>(S, src, p);
+    ssm_load_slice<CPT>(S + CPT, src + D, p);
+    const float e = expf(Ln);
+#pragma unroll
+    for (int j = 0; j < 2 * CPT; ++j) S[j] *= e;
+  }
+  __syncthreads();
+  if (!has_rows) return;
+  for (int s = 0; s < n; ++s) {
+    const float2 uu = *reinterpret_cast<const float2*>(su + s * D + 2 * g);
+    const float c0 = sc[s] * uu.x, c1 = sc[s] * uu.y;
+    const float4* kk4 = reinterpret_cast<const float4*>(sk + s * D) + p;
+#pragma unroll
+    for (int c = 0; c < CPT / 4; ++c) {
+      const float4 kk = kk4[c * kSsmLanes];
+      S[4 * c] = fmaf(c0, kk.x, S[4 * c]);
+      S[4 * c + 1] = fmaf(c0, kk.y, S[4 * c + 1]);
+      S[4 * c + 2] = fmaf(c0, kk.z, S[4 * c + 2]);
+      S[4 * c + 3] = fmaf(c0, kk.w, S[4 * c + 3]);
+      S[CPT + 4 * c] = fmaf(c1, kk.x, S[CPT + 4 * c]);
+      S[CPT + 4 * c + 1] = fmaf(c1, kk.y, S[CPT + 4 * c + 1]);
+      S[CPT + 4 * c + 2] = fmaf(c1, kk.z, S[CPT + 4 * c + 2]);
+      S[CPT + 4 * c + 3] = fmaf(c1, kk.w, S[CPT + 4 * c + 3]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    float4* d4 = reinterpret_cast<float4*>(dst + static_cast<size_t>(2 * g + r) * D) + p;
+#pragma unroll
+    for (int c = 0; c < CPT / 4; ++c)
+      d4[c * kSsmLanes] = make_float4(S[r * CPT + 4 * c], S[r * CPT + 4 * c + 1], S[r * CPT + 4 * c + 2],
+                                      S[r * CPT + 4 * c + 3]);
+  }
 }
 
 // The number of buffered tokens after the commit of request b (accepted
@@ -194,27 +528,16 @@ __device__ __forceinline__ int ssm_committed(const SsmArgs& a, int b, bool repor
 }
 
 // Commit, first part: a request whose next block would not fit the buffer
-// folds its retained tokens into the checkpoint.  grid (H, B, d / 64).
+// folds its retained tokens into the checkpoint.  grid (H, B).
 template <int D>
-__global__ void __launch_bounds__(kSsmThreads, 3) ssm_flush_kernel(const SsmArgs a) {
-  constexpr int TPR = kSsmTpr, CPT = D / TPR;
+__global__ void __launch_bounds__(kSsmThreads, 2) ssm_flush_kernel(const SsmArgs a) {
   extern __shared__ float4 ssm_smem4[];
-  float* sm = reinterpret_cast<float*>(ssm_smem4);
   pdl_wait();
-  const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-  const int n = ssm_committed(a, b, t == 0 && h == 0 && blockIdx.z == 0);
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int n = ssm_committed(a, b, threadIdx.x == 0 && h == 0);
   if (n + kRows <= a.window || n > a.window) return;  // no flush (n > window: never left by a verify)
-  const int row = blockIdx.z * kSsmRowsPerCta + t / TPR, c0 = t % TPR;
   const size_t hb = static_cast<size_t>(b) * a.heads + h;
-  float* sk = sm;
-  float* sv = sk + n * D;
-  float* sab = sv + n * D;
-  ssm_stage_buffer<D>(a, hb, n, sk, sv, sab);
-  float S[CPT];
-  ssm_load_rows<D>(S, a.ckpt + hb * D * D, row, c0);
-  __syncthreads();
-  ssm_replay<D>(S, sk, sv, sab, n, nullptr, 0, nullptr, row, c0);
-  ssm_store_rows<D>(S, a.ckpt + hb * D * D, row, c0);
+  ssm_fold<D>(a, hb, n, a.ckpt + hb * D * D, reinterpret_cast<float*>(ssm_smem4));
 }
 
 // Commit, second part: the pointers (0 after a flush).  One thread per request.
@@ -226,27 +549,15 @@ __global__ void ssm_pointer_kernel(const SsmArgs a) {
   a.ptr[b] = (n + kRows > a.window) ? 0 : n;
 }
 
-// The effective state of request a.req: its checkpoint replayed through the
-// retained buffer.  grid (H, 1, d / 64).
+// The effective state of request a.req: the closed form of its checkpoint
+// and retained buffer.  grid (H).
 template <int D>
-__global__ void __launch_bounds__(kSsmThreads, 3) ssm_state_kernel(const SsmArgs a) {
-  constexpr int TPR = kSsmTpr, CPT = D / TPR;
+__global__ void __launch_bounds__(kSsmThreads, 2) ssm_state_kernel(const SsmArgs a) {
   extern __shared__ float4 ssm_smem4[];
-  float* sm = reinterpret_cast<float*>(ssm_smem4);
-  const int h = blockIdx.x, t = threadIdx.x;
+  const int h = blockIdx.x;
   const int n = min(max(a.ptr[a.req], 0), a.window);
-  // (grid (H, 1, d / 64): blockIdx.z is the row slice)
-  const int row = blockIdx.z * kSsmRowsPerCta + t / TPR, c0 = t % TPR;
   const size_t hb = static_cast<size_t>(a.req) * a.heads + h;
-  float* sk = sm;
-  float* sv = sk + n * D;
-  float* sab = sv + n * D;
-  ssm_stage_buffer<D>(a, hb, n, sk, sv, sab);
-  float S[CPT];
-  ssm_load_rows<D>(S, a.ckpt + hb * D * D, row, c0);
-  __syncthreads();
-  ssm_replay<D>(S, sk, sv, sab, n, nullptr, 0, nullptr, row, c0);
-  ssm_store_rows<D>(S, a.state_out + static_cast<size_t>(h) * D * D, row, c0);
+  ssm_fold<D>(a, hb, n, a.state_out + static_cast<size_t>(h) * D * D, reinterpret_cast<float*>(ssm_smem4));
 }
 
 }  // namespace vsd
