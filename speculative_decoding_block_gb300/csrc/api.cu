@@ -1657,7 +1657,8 @@ vsd_status vsd_accept_commit(const vsd_model* m, vsd_kv* kv, int32_t B, const fl
 // ------------------------------------------------------------------ ReplaySSM
 struct vsd_ssm {
   int max_batch = 0, heads = 0, d = 0, window = 0, sms = 1;
-  float *ckpt = nullptr, *buf_k = nullptr, *buf_u = nullptr, *buf_L = nullptr;
+  float *ckpt = nullptr, *buf_k = nullptr, *buf_u = nullptr;
+  double* buf_L = nullptr;
   int* ptr = nullptr;
   int* status = nullptr;
 };

@@ -2,8 +2,8 @@
 // unit per kernel family keeps the build parallel).
 #pragma once
 
+#include <map>
 #include <mutex>
-#include <set>
 #include <utility>
 
 #include "attention.cuh"
@@ -12,20 +12,22 @@
 
 namespace vsd {
 
-// Opts kernel `k` in to `bytes` of dynamic shared memory on the current
-// device.  The attribute is per device, so it is set once per (kernel,
-// device, size); thread-safe.
+// Opts kernel `k` in to at least `bytes` of dynamic shared memory on the
+// current device.  The attribute is one value per (kernel, device) that
+// every later launch is checked against, so it only ever grows: a smaller
+// request after a larger one keeps the larger limit.  Thread-safe.
 inline cudaError_t ensure_smem_opt_in(const void* k, int bytes) {
   static std::mutex mu;
-  static std::set<std::pair<std::pair<const void*, int>, int>> done;
+  static std::map<std::pair<const void*, int>, int> limit;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_pair(std::make_pair(k, dev), bytes);
-  if (done.count(key)) return cudaSuccess;
+  const auto key = std::make_pair(k, dev);
+  const auto it = limit.find(key);
+  if (it != limit.end() && it->second >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.insert(key);
+  if (e == cudaSuccess) limit[key] = bytes;
   return e;
 }
 

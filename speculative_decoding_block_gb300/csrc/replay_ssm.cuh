@@ -44,7 +44,8 @@ struct SsmArgs {
   float* out;                 // [B][H][17][d]
   float* ckpt;                // [max_batch][H][d][d]
   float *buf_k, *buf_u;       // [max_batch][H][window][d]: keys, corrected values
-  float* buf_L;               // [max_batch][H][window]: log gate sums since the checkpoint
+  double* buf_L;              // [max_batch][H][window]: log gate sums since the checkpoint (double: the
+                              // coefficients use differences of nearby sums, which stay exact)
   int* ptr;                   // [max_batch] retained buffered tokens
   const int* accepted;        // [B] commit: accepted drafts a (-1: rejected)
   float* state_out;           // [H][d][d] effective state of one request
@@ -87,7 +88,7 @@ constexpr uint32_t kSsmAtomA = 16384;  // one 64-wide K atom of a 128-row A tile
 constexpr uint32_t kSsmAtomB = kSsmN * 128;
 
 struct SsmVerifyLayout {
-  uint32_t a, b, x, v, u, coefA, coefB, L, eL, beta, expS, expK, expB, bar, total;
+  uint32_t a, b, x, v, u, coefA, coefB, L, eL, Lrel, beta, expS, expK, expB, bar, total;
 };
 __host__ __device__ inline SsmVerifyLayout ssm_verify_layout(int d, int window) {
   SsmVerifyLayout l{};
@@ -100,8 +101,9 @@ __host__ __device__ inline SsmVerifyLayout ssm_verify_layout(int d, int window) 
   l.u = o;  o += 4u * window * d;     // corrected values: retained, then the block's
   l.coefA = o;  o += 4u * window * kSsmCoefLd;
   l.coefB = o;  o += 4u * window * kSsmCoefLd;
-  l.L = o;  o += 4u * window;
+  l.L = o;  o += 8u * window;         // (8-byte aligned: every region before is a multiple of 16 bytes)
   l.eL = o;  o += 4u * kRows;
+  l.Lrel = o;  o += 4u * kRows;
   l.beta = o;  o += 4u * kRows;
   l.expS = o;  o += 4u * 128u;
   l.expK = o;  o += 4u * 128u;
@@ -247,8 +249,9 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
   float* su = reinterpret_cast<float*>(base + l.u);
   float* sA = reinterpret_cast<float*>(base + l.coefA);
   float* sB = reinterpret_cast<float*>(base + l.coefB);
-  float* sL = reinterpret_cast<float*>(base + l.L);
+  double* sL = reinterpret_cast<double*>(base + l.L);
   float* seL = reinterpret_cast<float*>(base + l.eL);
+  float* sLrel = reinterpret_cast<float*>(base + l.Lrel);  // [17] L_t - L_ref of the block rows
   float* sbeta = reinterpret_cast<float*>(base + l.beta);
   int* expS = reinterpret_cast<int*>(base + l.expS);
   int* expK = reinterpret_cast<int*>(base + l.expK);
@@ -328,23 +331,25 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
         cp_async16(sv + 4 * x, a.v + blk * D + 4 * x);
       }
       for (int x = t; x < nb * R4; x += kSsmThreads) cp_async16(su + 4 * x, a.buf_u + brow * D + 4 * x);
-      for (int x = t; x < nb; x += kSsmThreads) cp_async4(sL + x, a.buf_L + brow + x);
+      for (int x = t; x < nb; x += kSsmThreads) cp_async8(sL + x, a.buf_L + brow + x);
     }
     if (warp == 0) {  // the block's log gate sums, continuing the last retained token's
-      const float base_L = nb > 0 ? a.buf_L[brow + nb - 1] : 0.0f;
-      float la = 0.0f, beta = 0.0f;
+      const double base_L = nb > 0 ? a.buf_L[brow + nb - 1] : 0.0;
+      double la = 0.0;
+      float beta = 0.0f;
       if (lane < kRows) {
         la = fmaxf(logf(a.alpha[blk + lane]), kSsmMinLogGate);
         beta = a.beta[blk + lane];
       }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xFFFFFFFFu, la, o);
+        const double y = __shfl_up_sync(0xFFFFFFFFu, la, o);
         if (lane >= o) la += y;
       }
       if (lane < kRows) {
         sL[nb + lane] = base_L + la;
-        seL[lane] = expf(base_L + la);
+        seL[lane] = expf(static_cast<float>(base_L + la));
+        sLrel[lane] = static_cast<float>(la);  // relative to L_ref = the last retained token's sum
         sbeta[lane] = beta;
       }
     }
@@ -386,13 +391,15 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
       float g[kRows];
       ssm_tmem_row(taddr + 64u, kind, expK[row], expB, g);
       if (row < nt) {
-        const float Ls = sL[row];
+        // L_s - L_ref once in double, then float differences: the terms that
+        // matter (nearby tokens) have small exponents, far ones underflow
+        const float Ls = static_cast<float>(sL[row] - (nb > 0 ? sL[nb - 1] : 0.0));
         float* dst = (kind ? sB : sA) + row * kSsmCoefLd;
 #pragma unroll
         for (int j = 0; j < kRows; ++j) {
           // a: strictly earlier tokens (s < nb + t); b: up to the token itself
           const bool used = row < nb + j + kind;
-          dst[j] = used ? expf(sL[nb + j] - Ls) * g[j] : 0.0f;
+          dst[j] = used ? expf(sLrel[j] - Ls) * g[j] : 0.0f;
         }
       }
     }
@@ -477,15 +484,15 @@ __device__ __forceinline__ void ssm_fold(const SsmArgs& a, size_t hb, int n, flo
     reinterpret_cast<float4*>(sk)[x] = k4[x];
     reinterpret_cast<float4*>(su)[x] = u4[x];
   }
-  const float Ln = n > 0 ? a.buf_L[brow + n - 1] : 0.0f;
-  for (int x = t; x < n; x += kSsmThreads) sc[x] = expf(Ln - a.buf_L[brow + x]);
+  const double Ln = n > 0 ? a.buf_L[brow + n - 1] : 0.0;
+  for (int x = t; x < n; x += kSsmThreads) sc[x] = expf(static_cast<float>(Ln - a.buf_L[brow + x]));
   const bool has_rows = 2 * g < D;
   float S[2 * CPT];
   if (has_rows) {
     const float* src = a.ckpt + hb * D * D + static_cast<size_t>(2 * g) * D;
     ssm_load_slice<CPT>(S, src, p);
     ssm_load_slice<CPT>(S + CPT, src + D, p);
-    const float e = expf(Ln);
+    const float e = expf(static_cast<float>(Ln));
 #pragma unroll
     for (int j = 0; j < 2 * CPT; ++j) S[j] *= e;
   }

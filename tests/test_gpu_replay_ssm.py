@@ -87,3 +87,45 @@ def test_bad_commit_count_rejects_the_block():
     r0.commit(5)
     ssm.get_state(0, after)
     assert rel_rows(after.cpu().numpy()[0], r0.state()).max() < TOL
+
+
+@pytest.mark.parametrize("d,window", [(64, 40), (128, 64)])
+def test_extreme_gates_and_scales(d, window):
+    """Gates of exactly 0 (the state is forgotten) and near 0 next to gates of
+    1, a write strength of 0, and state, keys and values at very different
+    magnitudes (the per-row power-of-2 operand scales), over enough steps to
+    flush."""
+    B_ = require_gpu()
+    rng = np.random.default_rng(100 + d)
+    B, H = 2, 2
+    ssm = B_.SSM(B, H, d, window)
+    S0 = (rng.normal(size=(B, H, d, d)) * 1e3).astype(np.float32)
+    S0[0, 0, :3] = 0.0  # zero rows
+    ref = [[ReplayState(S0[b, h].astype(np.float64), window) for h in range(H)] for b in range(B)]
+    for b in range(B):
+        ssm.set_state(b, torch.tensor(S0[b], device="cuda"))
+    for step in range(8):
+        q, k, v, alpha, beta = _inputs(rng, B, H, d)
+        q *= 1e-3
+        v *= 1e2
+        alpha = rng.choice(np.array([0.0, 1e-6, 0.5, 1.0], np.float32), size=alpha.shape).astype(np.float32)
+        beta[:, :, ::5] = 0.0
+        out = torch.empty((B, H, ROWS, d), dtype=torch.float32, device="cuda")
+        ssm.verify(B, *[torch.tensor(x, device="cuda") for x in (q, k, v, alpha, beta)], out)
+        got = out.cpu().numpy()
+        for b in range(B):
+            for h in range(H):
+                want = ref[b][h].verify(q[b, h], k[b, h], v[b, h], alpha[b, h], beta[b, h])
+                assert rel_rows(got[b, h], want).max() < TOL, (step, b, h)
+        acc = rng.integers(-1, ROWS, size=B).astype(np.int32)
+        ssm.commit(B, torch.tensor(acc, device="cuda"))
+        for b in range(B):
+            for h in range(H):
+                ref[b][h].commit(int(acc[b]))
+        st = torch.empty((H, d, d), dtype=torch.float32, device="cuda")
+        for b in range(B):
+            ssm.get_state(b, st)
+            s = st.cpu().numpy()
+            for h in range(H):
+                assert rel_rows(s[h], ref[b][h].state()).max() < TOL, (step, b, h)
+    assert ssm.device_status() == 0
