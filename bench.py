@@ -633,10 +633,10 @@ def time_replay_ssm(B, flush, stream, layers=24, batch=32, heads=16, d=128, wind
     hb = batch * heads
     mean_ptr = (window - ROWS) / 2  # the retained buffer grows from 0 to at most window - 17 between flushes
     per_layer = (hb * d * d * 4                            # checkpoint read
-                 + hb * mean_ptr * (2 * d + 1) * 4         # retained keys, corrected values, log gates read
+                 + hb * mean_ptr * (8 * d + 8)             # retained keys, corrected values (fp32), log sums (f64)
                  + hb * ROWS * (3 * d + 2) * 4              # block inputs read
                  + hb * ROWS * d * 4                        # outputs written
-                 + hb * ROWS * (2 * d + 1) * 4)             # the block's keys, corrected values, logs staged
+                 + hb * ROWS * (8 * d + 8))                 # the block's keys, corrected values, log sums staged
     return {"layers": layers, "requests": batch, "heads": heads, "d": d, "window": window,
             "us_per_layer": round(us, 2), "ms_all_layers": round(ms, 4),
             "bytes_per_layer_est": int(per_layer), "hbm_frac_est": round(per_layer / (us * 1e-6) / 1e9 / peaks()[0], 4),

@@ -2,6 +2,7 @@
 target for an external profiler (ncu) or a plain timing run.
 
     python -m speculative_decoding_block_gb300.profile_target WORKLOAD [layered|persistent] [STEPS]
+    python -m speculative_decoding_block_gb300.profile_target replay_ssm [LAYERS] [STEPS]
 
 Builds the seeded random-init target of the workload's shape, loads its
 synthetic contexts, and runs STEPS steps (default 3) from the same inputs
@@ -22,7 +23,38 @@ from speculative_decoding_block_gb300 import binding as B  # noqa: E402
 from speculative_decoding_block_gb300.target import build_target  # noqa: E402
 
 
+def replay_ssm(argv):
+    """STEPS verify + commit rounds of LAYERS recurrent-state rollback objects
+    at 32 requests, 16 heads, d = 128, window 64 (17 rows accepted per
+    request and step, so every third commit flushes)."""
+    layers = int(argv[0]) if argv else 2
+    steps = int(argv[1]) if len(argv) > 1 else 3
+    batch, heads, d, window = 32, 16, 128, 64
+    rng = np.random.default_rng(11)
+    objs = [B.SSM(batch, heads, d, window) for _ in range(layers)]
+    for o in objs:
+        for b in range(batch):
+            o.set_state(b, torch.tensor((rng.normal(size=(heads, d, d)) * 0.05).astype(np.float32), device="cuda"))
+    n = batch * heads * ROWS
+    q, k, v = (torch.tensor(rng.normal(size=(n, d)).astype(np.float32), device="cuda") for _ in range(3))
+    k = k / k.norm(dim=1, keepdim=True)
+    alpha = torch.tensor(rng.uniform(0.9, 1.0, n).astype(np.float32), device="cuda")
+    beta = torch.tensor(rng.uniform(0.0, 1.0, n).astype(np.float32), device="cuda")
+    out = torch.empty((n, d), dtype=torch.float32, device="cuda")
+    acc = torch.full((batch,), 16, dtype=torch.int32, device="cuda")
+    for _ in range(steps):
+        for o in objs:
+            o.verify(batch, q, k, v, alpha, beta, out)
+            o.commit(batch, acc)
+    torch.cuda.synchronize()
+    if any(o.device_status() for o in objs):
+        raise SystemExit("device status set")
+    print("ok replay_ssm", layers, steps)
+
+
 def main(argv):
+    if argv[0] == "replay_ssm":
+        return replay_ssm(argv[1:])
     w = WORKLOADS[argv[0]]
     mode = argv[1] if len(argv) > 1 else "layered"
     steps = int(argv[2]) if len(argv) > 2 else 3
