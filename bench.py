@@ -114,11 +114,18 @@ def code_only(src: str) -> str:
     return "\n".join(l.rstrip() for l in src.splitlines() if l.strip())
 
 
-def kernel_source_sha() -> str:
-    """Hash of the library's code (comments and blank lines excluded), naming the build an ncu capture was taken on."""
+SSM_SOURCES = ("replay_ssm.cuh",)  # the recurrent-state rollback kernels, outside the verify step
+
+
+def kernel_source_sha(ssm: bool = False) -> str:
+    """Hash of the library's code (comments and blank lines excluded), naming
+    the build an ncu capture was taken on: the verify step's sources, or
+    (ssm) the recurrent-state rollback kernels' own."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "speculative_decoding_block_gb300", "csrc")
     for f in sorted(os.listdir(d)):
+        if (f in SSM_SOURCES) != ssm:
+            continue
         with open(os.path.join(d, f), encoding="utf-8") as fh:
             h.update(f.encode() + code_only(fh.read()).encode())
     return h.hexdigest()[:16]
