@@ -298,8 +298,11 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
         bulk_prefetch_l2(a.k + hbn * kRows * D, kRows * D * 4u);
         bulk_prefetch_l2(a.q + hbn * kRows * D, kRows * D * 4u);
         bulk_prefetch_l2(a.v + hbn * kRows * D, kRows * D * 4u);
+        prefetch_l2(a.alpha + hbn * kRows);
+        prefetch_l2(a.beta + hbn * kRows);
         const int nbn = min(max(nb_next, 0), a.window);
         if (nbn > 0) {
+          prefetch_l2(a.buf_L + hbn * a.window + nbn - 1);
           bulk_prefetch_l2(a.buf_k + hbn * a.window * D, nbn * D * 4u);
           bulk_prefetch_l2(a.buf_u + hbn * a.window * D, nbn * D * 4u);
         }
@@ -335,20 +338,19 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
     }
     if (warp == 0) {  // the block's log gate sums, continuing the last retained token's
       const double base_L = nb > 0 ? a.buf_L[brow + nb - 1] : 0.0;
-      double la = 0.0;
-      float beta = 0.0f;
+      float la = 0.0f, beta = 0.0f;
       if (lane < kRows) {
         la = fmaxf(logf(a.alpha[blk + lane]), kSsmMinLogGate);
         beta = a.beta[blk + lane];
       }
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xFFFFFFFFu, la, o);
+      for (int o = 1; o < 32; o <<= 1) {  // the block's own sums stay small: float suffices
+        const float y = __shfl_up_sync(0xFFFFFFFFu, la, o);
         if (lane >= o) la += y;
       }
       if (lane < kRows) {
-        sL[nb + lane] = base_L + la;
-        seL[lane] = expf(static_cast<float>(base_L + la));
+        sL[nb + lane] = base_L + static_cast<double>(la);
+        seL[lane] = expf(static_cast<float>(base_L + static_cast<double>(la)));
         sLrel[lane] = static_cast<float>(la);  // relative to L_ref = the last retained token's sum
         sbeta[lane] = beta;
       }
@@ -412,29 +414,44 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
     for (int j = 0; j < kRows; ++j) X[j] = 0.0f;
     const float* C = kind ? sB : sA;
     if (row < D) {
-#pragma unroll 4
-      for (int s = 0; s < nb; ++s) {
-        const float u = su[s * D + row];
-        const float4* c4 = reinterpret_cast<const float4*>(C + s * kSsmCoefLd);
+      // the retained tokens' terms, two tokens' loads ahead of their FMAs
+      auto add_rows = [&](int s0, int cnt) {
+        float u[2];
+        float4 cc[2][5];
 #pragma unroll
-        for (int j = 0; j < 5; ++j) {
-          const float4 cc = c4[j];
-          X[4 * j] = fmaf(cc.x, u, X[4 * j]);
-          if (4 * j + 1 < kRows) X[4 * j + 1] = fmaf(cc.y, u, X[4 * j + 1]);
-          if (4 * j + 2 < kRows) X[4 * j + 2] = fmaf(cc.z, u, X[4 * j + 2]);
-          if (4 * j + 3 < kRows) X[4 * j + 3] = fmaf(cc.w, u, X[4 * j + 3]);
-        }
-      }
-      if (kind == 0) {  // the block's corrected values, in token order
-        float U[kRows];
+        for (int q = 0; q < 2; ++q)
+          if (q < cnt) {
+            u[q] = su[(s0 + q) * D + row];
 #pragma unroll
-        for (int j = 0; j < kRows; ++j) {
-          float acc = X[j];
+            for (int j = 0; j < 5; ++j) cc[q][j] = reinterpret_cast<const float4*>(C + (s0 + q) * kSsmCoefLd)[j];
+          }
 #pragma unroll
-          for (int i = 0; i < j; ++i) acc = fmaf(C[(nb + i) * kSsmCoefLd + j], U[i], acc);
-          U[j] = sbeta[j] * (sv[j * D + row] - fmaf(seL[j], P[j], acc));
-          su[(nb + j) * D + row] = U[j];
-          a.buf_u[(brow + nb + j) * D + row] = U[j];
+        for (int q = 0; q < 2; ++q)
+          if (q < cnt) {
+#pragma unroll
+            for (int j = 0; j < 5; ++j) {
+              X[4 * j] = fmaf(cc[q][j].x, u[q], X[4 * j]);
+              if (4 * j + 1 < kRows) X[4 * j + 1] = fmaf(cc[q][j].y, u[q], X[4 * j + 1]);
+              if (4 * j + 2 < kRows) X[4 * j + 2] = fmaf(cc[q][j].z, u[q], X[4 * j + 2]);
+              if (4 * j + 3 < kRows) X[4 * j + 3] = fmaf(cc[q][j].w, u[q], X[4 * j + 3]);
+            }
+          }
+      };
+      int s0 = 0;
+      for (; s0 + 2 <= nb; s0 += 2) add_rows(s0, 2);
+      if (s0 < nb) add_rows(s0, nb - s0);
+      if (kind == 0) {
+        // the block's corrected values in token order; each one's terms go
+        // into the later tokens' sums at once (the dependent chain per
+        // token is then one product, not a dot product)
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+          const float ui = sbeta[i] * (sv[i * D + row] - fmaf(seL[i], P[i], X[i]));
+          su[(nb + i) * D + row] = ui;
+          a.buf_u[(brow + nb + i) * D + row] = ui;
+          const float* ci = C + (nb + i) * kSsmCoefLd;
+#pragma unroll
+          for (int j = i + 1; j < kRows; ++j) X[j] = fmaf(ci[j], ui, X[j]);
         }
       }
     }
