@@ -221,7 +221,12 @@ vsd_status vsd_kv_set_step_kernel(vsd_kv* kv, int32_t mode);
  * u = beta (v - alpha S_prev k) and the sum of log alpha since the
  * checkpoint, so that S = e^{L} S_ckpt + sum_s e^{L - L_s} u_s k_s^T in
  * closed form (log alpha is floored at -200, where e^{L} underflows).
- * The library owns every state buffer; d is 64 or 128, 17 <= window <= 128.
+ * The checkpoint and the retained keys are kept as f16 hi / lo pairs with a
+ * power-of-2 scale per row (about 22 significant bits of each row's
+ * largest value), the form the tensor cores read.
+ * The library owns every state buffer; d is 64 or 128, 17 <= window <= 128
+ * for d = 64 and <= 64 for d = 128 (VSD_ERR_UNSUPPORTED above: shared
+ * memory).
  * Errors as elsewhere: host-visible ones return before any launch; a commit
  * count outside [-1, 16] (its block is then rejected) or a corrupted pointer
  * sets VSD_DEV_BAD_SEQLEN in the object's own status word. */

@@ -1657,7 +1657,9 @@ vsd_status vsd_accept_commit(const vsd_model* m, vsd_kv* kv, int32_t B, const fl
 // ------------------------------------------------------------------ ReplaySSM
 struct vsd_ssm {
   int max_batch = 0, heads = 0, d = 0, window = 0, sms = 1;
-  float *ckpt = nullptr, *buf_k = nullptr, *buf_u = nullptr;
+  uint8_t *ckpt = nullptr, *buf_k = nullptr;  // row images (replay_ssm.cuh)
+  int *ckpt_exp = nullptr, *buf_kexp = nullptr;
+  float* buf_u = nullptr;
   double* buf_L = nullptr;
   int* ptr = nullptr;
   int* status = nullptr;
@@ -1669,7 +1671,8 @@ vsd_status ssm_opt_in(uint32_t verify_smem, uint32_t fold_smem) {
   cudaError_t e;
   if ((e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_verify_kernel<D>), static_cast<int>(verify_smem))) ||
       (e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_flush_kernel<D>), static_cast<int>(fold_smem))) ||
-      (e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_state_kernel<D>), static_cast<int>(fold_smem))))
+      (e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_state_kernel<D>), static_cast<int>(fold_smem))) ||
+      (e = ensure_smem_opt_in(reinterpret_cast<const void*>(ssm_set_kernel<D>), static_cast<int>(fold_smem))))
     return fail(VSD_ERR_CUDA, "shared-memory opt-in: %s", cudaGetErrorString(e));
   return VSD_OK;
 }
@@ -1681,7 +1684,9 @@ SsmArgs ssm_args(const vsd_ssm* s, int batch) {
   a.window = s->window;
   a.batch = batch;
   a.ckpt = s->ckpt;
+  a.ckpt_exp = s->ckpt_exp;
   a.buf_k = s->buf_k;
+  a.buf_kexp = s->buf_kexp;
   a.buf_u = s->buf_u;
   a.buf_L = s->buf_L;
   a.ptr = s->ptr;
@@ -1696,6 +1701,8 @@ vsd_status vsd_ssm_create(int32_t max_batch, int32_t heads, int32_t d, int32_t w
   if (max_batch < 1 || heads < 1 || window < kRows || window > kSsmMaxWindow)
     return fail(VSD_ERR_ARG, "max_batch, heads >= 1 and window in [17, %d]", kSsmMaxWindow);
   if (d != 64 && d != 128) return fail(VSD_ERR_UNSUPPORTED, "state dimension d must be 64 or 128");
+  if (window > ssm_max_window(d))
+    return fail(VSD_ERR_UNSUPPORTED, "window %d above %d for d = %d (shared memory)", window, ssm_max_window(d), d);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(VSD_ERR_CUDA, "no CUDA device");
   const uint32_t vsmem = ssm_verify_layout(d, window).total, fsmem = ssm_fold_smem_bytes(d, window);
@@ -1710,7 +1717,8 @@ vsd_status vsd_ssm_create(int32_t max_batch, int32_t heads, int32_t d, int32_t w
   s->window = window;
   s->sms = sms;
   const size_t hb = static_cast<size_t>(max_batch) * heads;
-  if ((st = dalloc(&s->ckpt, hb * d * d)) || (st = dalloc(&s->buf_k, hb * window * d)) ||
+  if ((st = dalloc(&s->ckpt, hb * d * d * 4)) || (st = dalloc(&s->ckpt_exp, hb * d)) ||
+      (st = dalloc(&s->buf_k, hb * window * d * 4)) || (st = dalloc(&s->buf_kexp, hb * ssm_exp_stride(window))) ||
       (st = dalloc(&s->buf_u, hb * window * d)) || (st = dalloc(&s->buf_L, hb * window)) ||
       (st = dalloc(&s->ptr, max_batch)) || (st = dalloc(&s->status, 1))) {
     vsd_ssm_destroy(s);
@@ -1722,7 +1730,7 @@ vsd_status vsd_ssm_create(int32_t max_batch, int32_t heads, int32_t d, int32_t w
 
 void vsd_ssm_destroy(vsd_ssm* s) {
   if (!s) return;
-  void* ptrs[] = {s->ckpt, s->buf_k, s->buf_u, s->buf_L, s->ptr, s->status};
+  void* ptrs[] = {s->ckpt, s->ckpt_exp, s->buf_k, s->buf_kexp, s->buf_u, s->buf_L, s->ptr, s->status};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete s;
@@ -1732,8 +1740,13 @@ vsd_status vsd_ssm_set_state(vsd_ssm* s, int32_t req, const float* state, vsd_st
   if (!s || !state) return fail(VSD_ERR_ARG, "NULL pointer");
   if (req < 0 || req >= s->max_batch) return fail(VSD_ERR_ARG, "request %d outside [0, %d)", req, s->max_batch);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const size_t n = static_cast<size_t>(s->heads) * s->d * s->d;
-  CK(cudaMemcpyAsync(s->ckpt + req * n, state, n * sizeof(float), cudaMemcpyDeviceToDevice, st));
+  SsmArgs a = ssm_args(s, 0);
+  a.state_in = state;
+  a.req = req;
+  const uint32_t smem = ssm_fold_smem_bytes(s->d, s->window);
+  if (s->d == 64) ssm_set_kernel<64><<<s->heads, kSsmThreads, smem, st>>>(a);
+  else ssm_set_kernel<128><<<s->heads, kSsmThreads, smem, st>>>(a);
+  CK(cudaGetLastError());
   CK(cudaMemsetAsync(s->ptr + req, 0, sizeof(int), st));
   return VSD_OK;
 }

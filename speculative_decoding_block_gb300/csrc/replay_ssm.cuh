@@ -20,6 +20,10 @@
 //     o_t = e^{L_t} S_0 q_t + sum_{s<=t} e^{L_t - L_s} (k_s.q_t) u_s.
 // The buffer keeps, per retained token, k_s, u_s and L_s (u_s depends only on
 // the checkpoint and the tokens before s, so rejected rows never touch it).
+// The checkpoint and the retained keys are stored as the tensor cores read
+// them: f16 hi / lo images with a power-of-2 scale per row (about 22
+// significant bits), so that the verify copies them into shared memory
+// with bulk copies, the next item's while the current one computes.
 // A verify block then costs two products with the checkpoint per block row
 // (S_0 k_t, S_0 q_t) plus dot products with the buffered keys -- dense
 // contractions, run on the tensor cores -- and a 17-step triangular solve
@@ -33,89 +37,77 @@
 namespace vsd {
 
 constexpr int kSsmThreads = 256;
-constexpr int kSsmMaxWindow = 128;
+constexpr int kSsmMaxWindow = 128;         // d = 64; d = 128 allows up to 64 (shared memory)
 constexpr int kSsmCoefLd = 20;             // 17 coefficients per key row, padded for float4 reads
 constexpr float kSsmMinLogGate = -200.0f;  // log alpha floor: e^-200 underflows to 0 in every product
+constexpr int kSsmN = 48;                  // MMA N: the block vectors, padded
+constexpr int kSsmTmemCols = 128;          // P at columns 0-47, G at 64-111
+constexpr uint32_t kSsmAtomA = 16384;      // one 64-wide K atom of a 128-row tile in shared memory
+constexpr uint32_t kSsmAtomB = kSsmN * 128;
+
+__host__ __device__ inline int ssm_max_window(int d) { return d == 128 ? 64 : kSsmMaxWindow; }
+__host__ __device__ inline int ssm_exp_stride(int window) { return (window + 3) & ~3; }  // 16-byte rows
 
 struct SsmArgs {
   int heads, d, window, batch;
   // a verify block [B][H][17][d] (q, k, v) and [B][H][17] (alpha, beta)
   const float *q, *k, *v, *alpha, *beta;
-  float* out;                 // [B][H][17][d]
-  float* ckpt;                // [max_batch][H][d][d]
-  float *buf_k, *buf_u;       // [max_batch][H][window][d]: keys, corrected values
-  double* buf_L;              // [max_batch][H][window]: log gate sums since the checkpoint (double: the
-                              // coefficients use differences of nearby sums, which stay exact)
-  int* ptr;                   // [max_batch] retained buffered tokens
-  const int* accepted;        // [B] commit: accepted drafts a (-1: rejected)
-  float* state_out;           // [H][d][d] effective state of one request
-  int req;                    // its request
+  float* out;             // [B][H][17][d]
+  uint8_t* ckpt;          // [max_batch][H] checkpoint images, 4 d^2 bytes each
+  int* ckpt_exp;          // [max_batch][H][d] their row exponents
+  uint8_t* buf_k;         // [max_batch][H] retained-key images, 4 window d bytes each
+  int* buf_kexp;          // [max_batch][H][exp_stride(window)] their row exponents
+  float* buf_u;           // [max_batch][H][window][d] corrected values
+  double* buf_L;          // [max_batch][H][window] log gate sums since the checkpoint (double: the
+                          // coefficients use differences of nearby sums, which stay exact)
+  int* ptr;               // [max_batch] retained buffered tokens
+  const int* accepted;    // [B] commit: accepted drafts a (-1: rejected)
+  const float* state_in;  // [H][d][d] a request's new state (set)
+  float* state_out;       // [H][d][d] a request's effective state (get)
+  int req;                // that request
   int* status;
 };
 
-// Register slices for the fold: a row-pair group of kSsmLanes lanes holds two
-// state rows; lane p of the group holds float4 chunks p, p + 4, p + 8, ... of
-// both (the group's lanes read consecutive 16-byte pieces of a shared vector:
-// one wavefront, no bank conflict).
-constexpr int kSsmLanes = 4;
-template <int N>
-__device__ __forceinline__ void ssm_load_slice(float* x, const float* src, int p) {
-  const float4* s4 = reinterpret_cast<const float4*>(src) + p;
-#pragma unroll
-  for (int c = 0; c < N / 4; ++c) {
-    const float4 v = s4[c * kSsmLanes];
-    x[4 * c] = v.x;
-    x[4 * c + 1] = v.y;
-    x[4 * c + 2] = v.z;
-    x[4 * c + 3] = v.w;
-  }
-}
-
-// ---------------------------------------------------------------- verify
-// The verify's two dense products run on the tensor cores (tcgen05.mma
-// kind::f16, fp32 accumulation in TMEM):
-//   P = S_0 X^T     (d state rows x 48 columns),
-//   G = K X^T       (the retained and block keys, up to 128 rows x 48),
-// with X the block's vectors in columns 0-15 k_0..k_15, 16-31 q_0..q_15,
-// 32 k_16, 33 q_16 (34-47 unused).  fp32 values enter as f16 pairs,
-// hi = f16(x 2^e), lo = f16(x 2^e - hi), with a power-of-2 scale 2^e per
-// row that puts the row's largest magnitude in [2^14, 2^15); the products
-// hi.hi + hi.lo + lo.hi carry about 22 significant bits, and the scales are
-// divided out exactly afterwards.
-constexpr int kSsmN = 48;              // MMA N (block vectors, padded)
-constexpr int kSsmTmemCols = 128;      // P at columns 0-47, G at 64-111
-constexpr uint32_t kSsmAtomA = 16384;  // one 64-wide K atom of a 128-row A tile (128-byte rows, swizzled)
-constexpr uint32_t kSsmAtomB = kSsmN * 128;
-
-struct SsmVerifyLayout {
-  uint32_t a, b, x, v, u, coefA, coefB, L, eL, Lrel, beta, expS, expK, expB, bar, total;
+// ---------------------------------------------------------------- images
+// An image of R rows x d columns: the f16 hi values, then the f16 lo
+// values, each as d / 64 atoms of R rows x 128 bytes with the 128-byte
+// swizzle: element (r, k) in atom k / 64, row r, 16-byte chunk (k % 64) / 8
+// (swizzled by r % 8), half-word k % 8.  Row r stands for x = (hi + lo) 2^-e_r.
+struct SsmImage {
+  uint32_t atom, lo;  // bytes per atom, offset of the lo half
 };
-__host__ __device__ inline SsmVerifyLayout ssm_verify_layout(int d, int window) {
-  SsmVerifyLayout l{};
-  const uint32_t na = static_cast<uint32_t>(d / 64);
-  uint32_t o = 0;
-  l.a = o;  o += 2u * na * kSsmAtomA;  // A hi, then A lo
-  l.b = o;  o += 2u * na * kSsmAtomB;  // B hi, then B lo
-  l.x = o;  o += 4u * 2u * kRows * d;  // block k_t, q_t fp32, [2t] = k_t, [2t + 1] = q_t
-  l.v = o;  o += 4u * kRows * d;
-  l.u = o;  o += 4u * window * d;     // corrected values: retained, then the block's
-  l.coefA = o;  o += 4u * window * kSsmCoefLd;
-  l.coefB = o;  o += 4u * window * kSsmCoefLd;
-  l.L = o;  o += 8u * window;         // (8-byte aligned: every region before is a multiple of 16 bytes)
-  l.eL = o;  o += 4u * kRows;
-  l.Lrel = o;  o += 4u * kRows;
-  l.beta = o;  o += 4u * kRows;
-  l.expS = o;  o += 4u * 128u;
-  l.expK = o;  o += 4u * 128u;
-  l.expB = o;  o += 4u * kSsmN;
-  o = (o + 7u) & ~7u;
-  l.bar = o;  o += 16u;               // mbarrier, then the TMEM base and the abort flag
-  l.total = o + 1024u;                // + alignment of the dynamic shared memory base
-  return l;
+__host__ __device__ inline SsmImage ssm_image(int rows, int d) {
+  SsmImage g;
+  g.atom = static_cast<uint32_t>(rows) * 128u;
+  g.lo = static_cast<uint32_t>(d / 64) * g.atom;
+  return g;
 }
+__device__ __forceinline__ uint32_t ssm_img_off(const SsmImage& g, int r, int k0) {
+  return static_cast<uint32_t>(k0 >> 6) * g.atom + sw128_off(static_cast<uint32_t>(r), (k0 & 63) >> 3) +
+         static_cast<uint32_t>((k0 >> 2) & 1) * 8u;
+}
+__device__ __forceinline__ float ssm_pow2(int e) { return __int_as_float((127 + e) << 23); }
 
-__host__ __device__ inline uint32_t ssm_fold_smem_bytes(int d, int window) {
-  return static_cast<uint32_t>(2 * window * d + window) * 4u;
+// Values k0..k0+3 of row r (k0 % 4 == 0), times 2^-e.
+__device__ __forceinline__ float4 ssm_img_get4(const uint8_t* img, const SsmImage& g, int r, int k0, int e) {
+  const uint32_t off = ssm_img_off(g, r, k0);
+  const uint2 h = *reinterpret_cast<const uint2*>(img + off);
+  const uint2 l = *reinterpret_cast<const uint2*>(img + g.lo + off);
+  const __half2 h01 = *reinterpret_cast<const __half2*>(&h.x), h23 = *reinterpret_cast<const __half2*>(&h.y);
+  const __half2 l01 = *reinterpret_cast<const __half2*>(&l.x), l23 = *reinterpret_cast<const __half2*>(&l.y);
+  const float s = ssm_pow2(-e);
+  return make_float4((__low2float(h01) + __low2float(l01)) * s, (__high2float(h01) + __high2float(l01)) * s,
+                     (__low2float(h23) + __low2float(l23)) * s, (__high2float(h23) + __high2float(l23)) * s);
+}
+// Stores y (already scaled by 2^e) at k0..k0+3 of row r as hi / lo.
+__device__ __forceinline__ void ssm_img_put4(uint8_t* img, const SsmImage& g, int r, int k0, float4 y) {
+  const uint32_t off = ssm_img_off(g, r, k0);
+  const uint32_t h01 = f32x2_to_f16x2(y.x, y.y), h23 = f32x2_to_f16x2(y.z, y.w);
+  const __half2 a01 = *reinterpret_cast<const __half2*>(&h01), a23 = *reinterpret_cast<const __half2*>(&h23);
+  const uint32_t l01 = f32x2_to_f16x2(y.x - __low2float(a01), y.y - __high2float(a01));
+  const uint32_t l23 = f32x2_to_f16x2(y.z - __low2float(a23), y.w - __high2float(a23));
+  *reinterpret_cast<uint2*>(img + off) = make_uint2(h01, h23);
+  *reinterpret_cast<uint2*>(img + g.lo + off) = make_uint2(l01, l23);
 }
 
 // Exponent e with max * 2^e in [2^14, 2^15) (127 for m = 0: no bound),
@@ -126,12 +118,11 @@ __device__ __forceinline__ int ssm_scale_exp(float m) {
   frexpf(m, &ex);  // m = f 2^ex, f in [0.5, 1)
   return max(-120, min(120, 15 - ex));
 }
-__device__ __forceinline__ float ssm_pow2(int e) { return __int_as_float((127 + e) << 23); }
 
-// Tiles are filled a whole row per warp instruction (d = 128; two rows for
-// d = 64), lane l holding the row's values 4l..4l+3, so that every global
-// load is one contiguous run of whole lines.  Slot i of a thread is row
-// (8 i + warp) RPI + lane / LPR.
+// Rows are converted a whole row per warp instruction (d = 128; two rows
+// for d = 64), lane l holding the row's values 4l..4l+3, so that every
+// global load is one contiguous run of whole lines.  Slot i of a thread is
+// row r0 + (8 i + warp) RPI + lane / LPR.
 template <int D>
 struct SsmTile {
   static constexpr int LPR = D / 4;     // lanes per row
@@ -145,45 +136,81 @@ __device__ __forceinline__ int ssm_tile_row(int i) {
 }
 // Loads slots 0..N-1 (row r from src(r); zero for r >= rows or a null src).
 template <int D, int N, typename Src>
-__device__ __forceinline__ void ssm_tile_load(float4* x, int rows, Src src) {
+__device__ __forceinline__ void ssm_tile_load(float4* x, int r0, int rows, Src src) {
   const int l4 = static_cast<int>(threadIdx.x & 31) % SsmTile<D>::LPR;
 #pragma unroll
   for (int i = 0; i < N; ++i) {
-    const int r = ssm_tile_row<D>(i);
+    const int r = r0 + ssm_tile_row<D>(i);
     const float* s = r < rows ? src(r) : nullptr;
     x[i] = s ? reinterpret_cast<const float4*>(s)[l4] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
-// Stores slots 0..N-1 with r < rows into a swizzled f16 tile (hi at tile, lo
-// at tile + lo_off; atom_bytes per 64-wide K atom), each row scaled by 2^e
-// for its own e (a min-reduction over the row's lanes), e into expo[r].
+// Stores slots 0..N-1 with r < rows as row images (each row scaled by its
+// own 2^e, a min-reduction over the row's lanes; e into expo[r]), into
+// `img` and, when img2 is set, into img2 / expo2 too.
 template <int D, int N>
-__device__ __forceinline__ void ssm_tile_store(uint8_t* tile, uint32_t atom_bytes, uint32_t lo_off, const float4* x,
-                                               int* expo, int rows) {
+__device__ __forceinline__ void ssm_tile_store(const float4* x, int r0, int rows, uint8_t* img, const SsmImage& g,
+                                               int* expo, uint8_t* img2 = nullptr, SsmImage g2 = SsmImage{},
+                                               int* expo2 = nullptr) {
   constexpr int LPR = SsmTile<D>::LPR;
   const int lane = static_cast<int>(threadIdx.x & 31), l4 = lane % LPR;
   const unsigned mask = LPR == 32 ? 0xFFFFFFFFu : (0xFFFFu << (lane & 16));
-  const int k0 = 4 * l4;
-  const uint32_t col_off = static_cast<uint32_t>(k0 >> 6) * atom_bytes + static_cast<uint32_t>((k0 >> 2) & 1) * 8u;
 #pragma unroll
   for (int i = 0; i < N; ++i) {
-    const int r = ssm_tile_row<D>(i);
+    const int r = r0 + ssm_tile_row<D>(i);
     if (r >= rows) continue;  // the row's lanes agree
     const float4 v = x[i];
     const float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     int e = __reduce_min_sync(mask, ssm_scale_exp(m));
     if (e == 127) e = 0;  // a zero row
     const float sc = ssm_pow2(e);
-    const float y0 = v.x * sc, y1 = v.y * sc, y2 = v.z * sc, y3 = v.w * sc;
-    const uint32_t h01 = f32x2_to_f16x2(y0, y1), h23 = f32x2_to_f16x2(y2, y3);
-    const __half2 a01 = *reinterpret_cast<const __half2*>(&h01), a23 = *reinterpret_cast<const __half2*>(&h23);
-    const uint32_t l01 = f32x2_to_f16x2(y0 - __low2float(a01), y1 - __high2float(a01));
-    const uint32_t l23 = f32x2_to_f16x2(y2 - __low2float(a23), y3 - __high2float(a23));
-    const uint32_t off = col_off + sw128_off(static_cast<uint32_t>(r), (k0 & 63) >> 3);
-    *reinterpret_cast<uint2*>(tile + off) = make_uint2(h01, h23);
-    *reinterpret_cast<uint2*>(tile + lo_off + off) = make_uint2(l01, l23);
+    const float4 y = make_float4(v.x * sc, v.y * sc, v.z * sc, v.w * sc);
+    ssm_img_put4(img, g, r, 4 * l4, y);
     if (l4 == 0) expo[r] = e;
+    if (img2 != nullptr) {
+      ssm_img_put4(img2, g2, r, 4 * l4, y);
+      if (l4 == 0) expo2[r] = e;
+    }
   }
+}
+
+// ---------------------------------------------------------------- verify
+// The verify's two dense products run on the tensor cores (tcgen05.mma
+// kind::f16, fp32 accumulation in TMEM):
+//   P = S_0 X^T     (d state rows x 48 columns),
+//   G = K X^T       (the retained and block keys, up to 128 rows x 48),
+// with X the block's vectors in columns 0-15 k_0..k_15, 16-31 q_0..q_15,
+// 32 k_16, 33 q_16 (34-47 zero); the operands are row images (above).
+struct SsmVerifyLayout {
+  uint32_t a, k, b, u, v, coefA, coefB, L, eL, Lrel, beta, expS, expK, expKb, expB, bar, total;
+};
+__host__ __device__ inline SsmVerifyLayout ssm_verify_layout(int d, int window) {
+  SsmVerifyLayout l{};
+  const uint32_t na = static_cast<uint32_t>(d / 64);
+  uint32_t o = 0;
+  l.a = o;  o += 2u * na * kSsmAtomA;  // checkpoint tile: hi atoms, then lo atoms (128 rows each)
+  l.k = o;  o += 2u * na * kSsmAtomA;  // key tile
+  l.b = o;  o += 2u * na * kSsmAtomB;  // block-vector tile
+  l.u = o;  o += 4u * window * d;      // corrected values: retained, then the block's
+  l.v = o;  o += 4u * kRows * d;
+  l.coefA = o;  o += 4u * window * kSsmCoefLd;
+  l.coefB = o;  o += 4u * window * kSsmCoefLd;
+  l.L = o;  o += 8u * window;          // (every region before is a multiple of 16 bytes)
+  l.eL = o;  o += 4u * kRows;
+  l.Lrel = o;  o += 4u * kRows;
+  l.beta = o;  o += 4u * kRows;
+  o = (o + 15u) & ~15u;
+  l.expS = o;  o += 2u * 4u * 128u;    // two items' checkpoint row exponents (bulk-copied)
+  l.expK = o;  o += 2u * 4u * 128u;    // two items' retained-key row exponents (bulk-copied)
+  l.expKb = o;  o += 4u * 32u;         // the block keys' exponents (apart: a copy may round up over them)
+  l.expB = o;  o += 4u * kSsmN;
+  o = (o + 15u) & ~15u;
+  l.bar = o;  o += 48u;               // four mbarriers, the TMEM base, the abort flag
+  l.total = o + 1024u;                // + alignment of the dynamic shared memory base
+  return l;
+}
+__host__ __device__ inline uint32_t ssm_fold_smem_bytes(int d, int window) {
+  return static_cast<uint32_t>(2 * window * d + window) * 4u;
 }
 
 // One product tile issue: (A hi, B hi), (A hi, B lo), (A lo, B hi)
@@ -224,12 +251,15 @@ __device__ __forceinline__ void ssm_tmem_row(uint32_t taddr, int kind, int row_e
 // Verify: outputs of the 17 block rows, and the block's keys, corrected
 // values and log gates staged in the buffer after the pointer (the commit
 // decides how many stay).  Persistent: grid min(H B, SMs), 256 threads, one
-// (request, head) item at a time, the next item's checkpoint and buffer
-// pulled into L2 first.  Per item:
-//   1. stage the block's k, q, v, the retained corrected values and logs;
-//      the checkpoint rows into the A tile, the block vectors into the B tile;
-//   2. P = S_0 X^T on the tensor cores; then the key rows into the A tile and
-//      G = K X^T;
+// (request, head) item at a time.  Per item:
+//   1. the block vectors into the B tile, the block's keys into the key
+//      tile after the retained rows (and into the buffer's key image); the
+//      retained corrected values, v and the log sums by cp.async; the block's
+//      log sums;
+//   2. wait for the item's checkpoint and retained-key images (bulk copies
+//      issued during the previous item); P = S_0 X^T and G = K X^T on the
+//      tensor cores; as soon as each product has read its tile, the next
+//      item's images are copied in;
 //   3. from TMEM: warps 0-3 take the k columns of their lane quarter's rows,
 //      warps 4-7 the q columns (P), then the coefficients
 //      e^{L_t - L_s} (k_s.k_t) and e^{L_t - L_s} (k_s.q_t) from G;
@@ -239,31 +269,36 @@ __device__ __forceinline__ void ssm_tmem_row(uint32_t taddr, int kind, int row_e
 template <int D>
 __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArgs a) {
   constexpr uint32_t NA = D / 64;
+  constexpr int NXB = kSsmN / SsmTile<D>::RPP;                  // block-vector rows per thread
+  constexpr int NBK = (kRows + SsmTile<D>::RPP - 1) / SsmTile<D>::RPP;  // block-key rows per thread
   extern __shared__ uint8_t ssm_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ssm_smem_raw) + 1023) & ~uintptr_t(1023));
   const SsmVerifyLayout l = ssm_verify_layout(D, a.window);
   uint8_t* tA = base + l.a;
+  uint8_t* tK = base + l.k;
   uint8_t* tB = base + l.b;
-  float* sx = reinterpret_cast<float*>(base + l.x);
-  float* sv = reinterpret_cast<float*>(base + l.v);
   float* su = reinterpret_cast<float*>(base + l.u);
+  float* sv = reinterpret_cast<float*>(base + l.v);
   float* sA = reinterpret_cast<float*>(base + l.coefA);
   float* sB = reinterpret_cast<float*>(base + l.coefB);
   double* sL = reinterpret_cast<double*>(base + l.L);
   float* seL = reinterpret_cast<float*>(base + l.eL);
   float* sLrel = reinterpret_cast<float*>(base + l.Lrel);  // [17] L_t - L_ref of the block rows
   float* sbeta = reinterpret_cast<float*>(base + l.beta);
-  int* expS = reinterpret_cast<int*>(base + l.expS);
-  int* expK = reinterpret_cast<int*>(base + l.expK);
+  int* expS = reinterpret_cast<int*>(base + l.expS);  // [2][128]
+  int* expK = reinterpret_cast<int*>(base + l.expK);  // [2][128]
+  int* expKb = reinterpret_cast<int*>(base + l.expKb);  // [17], row nb + j
   int* expB = reinterpret_cast<int*>(base + l.expB);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(base + l.bar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + l.bar + 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + l.bar + 12);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + l.bar);  // checkpoint in, keys in, P done, G done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + l.bar + 32);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + l.bar + 36);
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int quarter = warp & 3, kind = warp >> 2;
   const int row = 32 * quarter + lane;  // TMEM lane of this thread
+  const SsmImage gS = ssm_image(D, D), gKb = ssm_image(a.window, D), gT = ssm_image(128, D);
+  const SsmImage gB = ssm_image(kSsmN, D);
   if (t == 0) {
-    mbar_init(bar, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -278,12 +313,46 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
   const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
   pdl_wait();
   const int items = a.heads * a.batch;
-  constexpr int NS0 = D / SsmTile<D>::RPP;    // checkpoint rows per thread
-  constexpr int NKR = 128 / SsmTile<D>::RPP;  // key rows per thread (up to 128)
-  constexpr int NXB = kSsmN / SsmTile<D>::RPP;  // block vector rows per thread
-  uint32_t phase = 0;  // completions of bar so far
+  const int kstride = ssm_exp_stride(a.window);
+  const uint64_t pol = policy_evict_first();
+  // bulk copies (one thread): an item's checkpoint image and exponents into
+  // the checkpoint tile / expS[slot], its first nb key rows into the key tile
+  auto issue_ckpt = [&](int it_, int slot) {
+    const size_t hbi = static_cast<size_t>(it_ / a.heads) * a.heads + it_ % a.heads;
+    const uint8_t* img = a.ckpt + hbi * D * D * 4;
+    mbar_expect_tx(&bars[0], 2u * NA * gS.atom + D * 4u);
+#pragma unroll
+    for (uint32_t h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+      for (uint32_t at = 0; at < NA; ++at)
+        bulk_load(tA + (h2 * NA + at) * kSsmAtomA, img + (h2 * NA + at) * gS.atom, gS.atom, &bars[0], pol);
+    bulk_load(expS + slot * 128, a.ckpt_exp + hbi * D, D * 4u, &bars[0], pol);
+  };
+  auto issue_keys = [&](int it_, int nbi, int slot) {
+    nbi = min(max(nbi, 0), a.window - kRows);
+    const size_t hbi = static_cast<size_t>(it_ / a.heads) * a.heads + it_ % a.heads;
+    const uint8_t* img = a.buf_k + hbi * a.window * D * 4;
+    const uint32_t rows_b = static_cast<uint32_t>(nbi) * 128u, eb = static_cast<uint32_t>(ssm_exp_stride(nbi)) * 4u;
+    if (nbi == 0) {
+      mbar_arrive(&bars[1]);
+      return;
+    }
+    mbar_expect_tx(&bars[1], 2u * NA * rows_b + eb);
+#pragma unroll
+    for (uint32_t h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+      for (uint32_t at = 0; at < NA; ++at)
+        bulk_load(tK + (h2 * NA + at) * kSsmAtomA, img + (h2 * NA + at) * gKb.atom, rows_b, &bars[1], pol);
+    bulk_load(expK + slot * 128, a.buf_kexp + hbi * kstride, eb, &bars[1], pol);
+  };
   int nb_next = blockIdx.x < items ? a.ptr[blockIdx.x / a.heads] : 0;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+  if (t == 0 && static_cast<int>(blockIdx.x) < items) {
+    issue_ckpt(blockIdx.x, 0);
+    issue_keys(blockIdx.x, nb_next, 0);
+  }
+  uint32_t it = 0, mma_ph = 0;  // items walked, products completed
+  for (int item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+    const int slot = static_cast<int>(it & 1u);
     const int b = item / a.heads, h = item % a.heads;
     const int nb = nb_next;
     const size_t hb = static_cast<size_t>(b) * a.heads + h;
@@ -291,10 +360,8 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
     const int nx = item + gridDim.x;
     if (nx < items) {
       nb_next = a.ptr[nx / a.heads];  // used by the next item: its latency hides behind this one
-      // the next item's checkpoint, retained buffer and block inputs into L2
-      if (t == kSsmThreads - 32) {
+      if (t == kSsmThreads - 32) {    // the next item's block inputs and retained buffer into L2
         const size_t hbn = static_cast<size_t>(nx / a.heads) * a.heads + nx % a.heads;
-        bulk_prefetch_l2(a.ckpt + hbn * D * D, D * D * 4u);
         bulk_prefetch_l2(a.k + hbn * kRows * D, kRows * D * 4u);
         bulk_prefetch_l2(a.q + hbn * kRows * D, kRows * D * 4u);
         bulk_prefetch_l2(a.v + hbn * kRows * D, kRows * D * 4u);
@@ -303,95 +370,88 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
         const int nbn = min(max(nb_next, 0), a.window);
         if (nbn > 0) {
           prefetch_l2(a.buf_L + hbn * a.window + nbn - 1);
-          bulk_prefetch_l2(a.buf_k + hbn * a.window * D, nbn * D * 4u);
           bulk_prefetch_l2(a.buf_u + hbn * a.window * D, nbn * D * 4u);
         }
       }
     }
-    if (nb < 0 || nb + kRows > a.window) {  // a pointer the commit never leaves: no output, nothing staged
-      if (t == 0) atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
-      continue;  // uniform over the CTA
-    }
+    const bool bad = nb < 0 || nb + kRows > a.window;  // a pointer the commit never leaves
     const int nt = nb + kRows;
-    // ---- 1. staging: the checkpoint rows and block vectors into registers,
-    // the rest by asynchronous copies
-    const float* ck = a.ckpt + hb * D * D;
-    float4 xr[NKR];  // checkpoint rows now, key rows later
-    ssm_tile_load<D, NS0>(xr, D, [&](int r) { return ck + static_cast<size_t>(r) * D; });
-    float4 xb[NXB];
-    ssm_tile_load<D, NXB>(xb, kSsmN, [&](int r) -> const float* {
-      // B rows: 0-15 k_0..k_15, 16-31 q_0..q_15, 32 k_16, 33 q_16, then zero
-      if (r < 16 || r == 32) return a.k + (blk + (r < 16 ? r : 16)) * D;
-      if (r < 34) return a.q + (blk + (r < 32 ? r - 16 : 16)) * D;
-      return nullptr;
-    });
-    {
+    // ---- 1. the block's operands and the staging copies
+    if (!bad) {
       constexpr int R4 = D / 4;
-      for (int x = t; x < kRows * R4; x += kSsmThreads) {
-        const int tok = x / R4, c = x % R4;
-        cp_async16(sx + (2 * tok) * D + 4 * c, a.k + blk * D + 4 * x);
-        cp_async16(sx + (2 * tok + 1) * D + 4 * c, a.q + blk * D + 4 * x);
-        cp_async16(sv + 4 * x, a.v + blk * D + 4 * x);
-      }
+      for (int x = t; x < kRows * R4; x += kSsmThreads) cp_async16(sv + 4 * x, a.v + blk * D + 4 * x);
       for (int x = t; x < nb * R4; x += kSsmThreads) cp_async16(su + 4 * x, a.buf_u + brow * D + 4 * x);
       for (int x = t; x < nb; x += kSsmThreads) cp_async8(sL + x, a.buf_L + brow + x);
-    }
-    if (warp == 0) {  // the block's log gate sums, continuing the last retained token's
-      const double base_L = nb > 0 ? a.buf_L[brow + nb - 1] : 0.0;
-      float la = 0.0f, beta = 0.0f;
-      if (lane < kRows) {
-        la = fmaxf(logf(a.alpha[blk + lane]), kSsmMinLogGate);
-        beta = a.beta[blk + lane];
-      }
+      float4 xb[NXB];
+      ssm_tile_load<D, NXB>(xb, 0, kSsmN, [&](int r) -> const float* {
+        // B rows: 0-15 k_0..k_15, 16-31 q_0..q_15, 32 k_16, 33 q_16, then zero
+        if (r < 16 || r == 32) return a.k + (blk + (r < 16 ? r : 16)) * D;
+        if (r < 34) return a.q + (blk + (r < 32 ? r - 16 : 16)) * D;
+        return nullptr;
+      });
+      float4 xk[NBK];
+      ssm_tile_load<D, NBK>(xk, nb, nt, [&](int r) { return a.k + (blk + r - nb) * D; });
+      if (warp == 0) {  // the block's log gate sums, continuing the last retained token's
+        const double base_L = nb > 0 ? a.buf_L[brow + nb - 1] : 0.0;
+        float la = 0.0f, beta = 0.0f;
+        if (lane < kRows) {
+          la = fmaxf(logf(a.alpha[blk + lane]), kSsmMinLogGate);
+          beta = a.beta[blk + lane];
+        }
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {  // the block's own sums stay small: float suffices
-        const float y = __shfl_up_sync(0xFFFFFFFFu, la, o);
-        if (lane >= o) la += y;
+        for (int o = 1; o < 32; o <<= 1) {  // the block's own sums stay small: float suffices
+          const float y = __shfl_up_sync(0xFFFFFFFFu, la, o);
+          if (lane >= o) la += y;
+        }
+        if (lane < kRows) {
+          sL[nb + lane] = base_L + static_cast<double>(la);
+          seL[lane] = expf(static_cast<float>(base_L + static_cast<double>(la)));
+          sLrel[lane] = la;  // relative to L_ref = the last retained token's sum
+          sbeta[lane] = beta;
+        }
       }
-      if (lane < kRows) {
-        sL[nb + lane] = base_L + static_cast<double>(la);
-        seL[lane] = expf(static_cast<float>(base_L + static_cast<double>(la)));
-        sLrel[lane] = static_cast<float>(la);  // relative to L_ref = the last retained token's sum
-        sbeta[lane] = beta;
-      }
+      ssm_tile_store<D, NXB>(xb, 0, kSsmN, tB, gB, expB);
+      // the block's keys after the retained rows: key tile and the buffer's image
+      ssm_tile_store<D, NBK>(xk, nb, nt, tK, gT, expKb - nb, a.buf_k + hb * a.window * D * 4, gKb,
+                             a.buf_kexp + hb * kstride);
     }
-    // checkpoint rows -> A (rows >= d of the tile are never read back), block vectors -> B
-    ssm_tile_store<D, NS0>(tA, kSsmAtomA, NA * kSsmAtomA, xr, expS, D);
-    ssm_tile_store<D, NXB>(tB, kSsmAtomB, NA * kSsmAtomB, xb, expB, kSsmN);
+    // ---- 2. the item's images
+    mbar_wait(&bars[0], it & 1u, abort_flag, a.status);
+    mbar_wait(&bars[1], it & 1u, abort_flag, a.status);
     cp_async_wait_all();
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-    // ---- 2. P = S_0 X^T
-    if (t == 0) {
-      tc_fence_after();
-      ssm_issue<D>(tmem, tA, tB, bar);
-    }
-    // key rows: loaded before the wait, stored into A once the P product has
-    // read the checkpoint tile
-    ssm_tile_load<D, NKR>(xr, nt, [&](int r) { return r < nb ? a.buf_k + (brow + r) * D : sx + 2 * (r - nb) * D; });
-    mbar_wait(bar, phase & 1u, abort_flag, a.status);
-    ++phase;
-    tc_fence_after();
-    ssm_tile_store<D, NKR>(tA, kSsmAtomA, NA * kSsmAtomA, xr, expK, nt);
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
     if (*abort_flag) break;
+    if (bad) {
+      if (t == 0) {
+        atomicOr(a.status, VSD_DEV_BAD_SEQLEN);
+        if (nx < items) {
+          issue_ckpt(nx, slot ^ 1);
+          issue_keys(nx, nb_next, slot ^ 1);
+        }
+      }
+      continue;  // uniform over the CTA
+    }
     if (t == 0) {
       tc_fence_after();
-      ssm_issue<D>(tmem + 64u, tA, tB, bar);
+      ssm_issue<D>(tmem, tA, tB, &bars[2]);
+      ssm_issue<D>(tmem + 64u, tK, tB, &bars[3]);
     }
-    // ---- 3. P rows while G is computed
-    float P[kRows];
-    if (row < D) ssm_tmem_row(taddr, kind, expS[row], expB, P);
-    mbar_wait(bar, phase & 1u, abort_flag, a.status);
-    ++phase;
+    // ---- 3. P rows, then the coefficients from G
+    mbar_wait(&bars[2], mma_ph & 1u, abort_flag, a.status);
     tc_fence_after();
+    if (t == 0 && nx < items) issue_ckpt(nx, slot ^ 1);  // the checkpoint tile is free
+    float P[kRows];
+    if (row < D) ssm_tmem_row(taddr, kind, expS[slot * 128 + row], expB, P);
+    mbar_wait(&bars[3], mma_ph & 1u, abort_flag, a.status);
+    ++mma_ph;
+    tc_fence_after();
+    if (t == 0 && nx < items) issue_keys(nx, nb_next, slot ^ 1);  // the key tile is free
     if (32 * quarter < nt) {  // warp-uniform (the TMEM load is warp-wide); rows >= nt write nothing
       // coefficients of key row s = row against the block's tokens (kind 0: k_t, 1: q_t)
       float g[kRows];
-      ssm_tmem_row(taddr + 64u, kind, expK[row], expB, g);
+      ssm_tmem_row(taddr + 64u, kind, row < nb ? expK[slot * 128 + row] : expKb[min(row - nb, kRows - 1)], expB, g);
       if (row < nt) {
         // L_s - L_ref once in double, then float differences: the terms that
         // matter (nearby tokens) have small exponents, far ones underflow
@@ -465,14 +525,7 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
         a.out[(blk + j) * D + row] = acc;
       }
     }
-    // the block's keys and log sums after the pointer
-    {
-      constexpr int R4 = D / 4;
-      float4* bk = reinterpret_cast<float4*>(a.buf_k + (brow + nb) * D);
-      for (int x = t; x < kRows * R4; x += kSsmThreads)
-        bk[x] = reinterpret_cast<const float4*>(sx)[(2 * (x / R4)) * R4 + x % R4];
-      if (t < kRows) a.buf_L[brow + nb + t] = sL[nb + t];
-    }
+    if (t < kRows) a.buf_L[brow + nb + t] = sL[nb + t];  // the block's log sums after the pointer
     __syncthreads();  // the shared buffers are reused by the next item
   }
   tc_fence_before();
@@ -483,35 +536,52 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
   }
 }
 
+// ---------------------------------------------------------------- fold
 // S = e^{L_{n-1}} S_0 + sum_{s<n} e^{L_{n-1} - L_s} u_s k_s^T for (request,
-// head) hb with n retained tokens, into dst (may be the checkpoint itself:
-// each thread reads its rows before writing them).  256 threads; two rows
-// per 4-lane group as in the verify.
+// head) hb with n retained tokens; S_0 is the checkpoint image, or the fp32
+// rows src (set).  The result goes to dst (fp32 rows, get) or, when dst is
+// null, back into the checkpoint image (each thread rewrites what it read).
+// 256 threads; a 4-lane group holds two rows, lane p float4 chunks p, p + 4,
+// ... of both (the group's lanes read consecutive 16-byte pieces of a shared
+// key: one wavefront, no bank conflict).
 template <int D>
-__device__ __forceinline__ void ssm_fold(const SsmArgs& a, size_t hb, int n, float* dst, float* sm) {
-  constexpr int CPT = D / kSsmLanes;
-  const int t = threadIdx.x, g = t / kSsmLanes, p = t % kSsmLanes;
+__device__ __forceinline__ void ssm_fold(const SsmArgs& a, size_t hb, int n, const float* src, float* dst, float* sm) {
+  constexpr int CPT = D / 4;
+  const int t = threadIdx.x, g = t / 4, p = t % 4;
   const size_t brow = hb * a.window;
-  float* sk = sm;               // [n][D]
-  float* su = sk + n * D;       // [n][D]
-  float* sc = su + n * D;       // [n] e^{L_{n-1} - L_s}
-  const float4* k4 = reinterpret_cast<const float4*>(a.buf_k + brow * D);
-  const float4* u4 = reinterpret_cast<const float4*>(a.buf_u + brow * D);
+  const SsmImage gK = ssm_image(a.window, D), gS = ssm_image(D, D);
+  const uint8_t* kimg = a.buf_k + brow * D * 4;
+  const int* kexp = a.buf_kexp + hb * ssm_exp_stride(a.window);
+  uint8_t* cimg = a.ckpt + hb * D * D * 4;
+  int* cexp = a.ckpt_exp + hb * D;
+  float* sk = sm;          // [n][D]
+  float* su = sk + n * D;  // [n][D]
+  float* sc = su + n * D;  // [n] e^{L_{n-1} - L_s}
   for (int x = t; x < n * D / 4; x += kSsmThreads) {
-    reinterpret_cast<float4*>(sk)[x] = k4[x];
-    reinterpret_cast<float4*>(su)[x] = u4[x];
+    const int r = x / (D / 4), k0 = 4 * (x % (D / 4));
+    reinterpret_cast<float4*>(sk)[x] = ssm_img_get4(kimg, gK, r, k0, kexp[r]);
+    reinterpret_cast<float4*>(su)[x] = reinterpret_cast<const float4*>(a.buf_u + brow * D)[x];
   }
   const double Ln = n > 0 ? a.buf_L[brow + n - 1] : 0.0;
   for (int x = t; x < n; x += kSsmThreads) sc[x] = expf(static_cast<float>(Ln - a.buf_L[brow + x]));
-  const bool has_rows = 2 * g < D;
+  const bool has_rows = 2 * g < D;  // warp-uniform (d = 64 leaves warps 4-7 idle)
   float S[2 * CPT];
   if (has_rows) {
-    const float* src = a.ckpt + hb * D * D + static_cast<size_t>(2 * g) * D;
-    ssm_load_slice<CPT>(S, src, p);
-    ssm_load_slice<CPT>(S + CPT, src + D, p);
     const float e = expf(static_cast<float>(Ln));
 #pragma unroll
-    for (int j = 0; j < 2 * CPT; ++j) S[j] *= e;
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = 2 * g + rr;
+#pragma unroll
+      for (int c = 0; c < CPT / 4; ++c) {
+        const int k0 = 4 * (p + 4 * c);
+        const float4 v = src ? *reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * D + k0)
+                             : ssm_img_get4(cimg, gS, r, k0, cexp[r]);
+        S[rr * CPT + 4 * c] = v.x * e;
+        S[rr * CPT + 4 * c + 1] = v.y * e;
+        S[rr * CPT + 4 * c + 2] = v.z * e;
+        S[rr * CPT + 4 * c + 3] = v.w * e;
+      }
+    }
   }
   __syncthreads();
   if (!has_rows) return;
@@ -521,7 +591,7 @@ __device__ __forceinline__ void ssm_fold(const SsmArgs& a, size_t hb, int n, flo
     const float4* kk4 = reinterpret_cast<const float4*>(sk + s * D) + p;
 #pragma unroll
     for (int c = 0; c < CPT / 4; ++c) {
-      const float4 kk = kk4[c * kSsmLanes];
+      const float4 kk = kk4[c * 4];
       S[4 * c] = fmaf(c0, kk.x, S[4 * c]);
       S[4 * c + 1] = fmaf(c0, kk.y, S[4 * c + 1]);
       S[4 * c + 2] = fmaf(c0, kk.z, S[4 * c + 2]);
@@ -533,12 +603,30 @@ __device__ __forceinline__ void ssm_fold(const SsmArgs& a, size_t hb, int n, flo
     }
   }
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    float4* d4 = reinterpret_cast<float4*>(dst + static_cast<size_t>(2 * g + r) * D) + p;
+  for (int rr = 0; rr < 2; ++rr) {
+    const int r = 2 * g + rr;
+    if (dst != nullptr) {
+      float4* d4 = reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * D) + p;
 #pragma unroll
-    for (int c = 0; c < CPT / 4; ++c)
-      d4[c * kSsmLanes] = make_float4(S[r * CPT + 4 * c], S[r * CPT + 4 * c + 1], S[r * CPT + 4 * c + 2],
-                                      S[r * CPT + 4 * c + 3]);
+      for (int c = 0; c < CPT / 4; ++c)
+        d4[c * 4] = make_float4(S[rr * CPT + 4 * c], S[rr * CPT + 4 * c + 1], S[rr * CPT + 4 * c + 2],
+                                S[rr * CPT + 4 * c + 3]);
+    } else {
+      float m = 0.0f;
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) m = fmaxf(m, fabsf(S[rr * CPT + j]));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      int e = ssm_scale_exp(m);
+      if (e == 127) e = 0;
+      const float sc2 = ssm_pow2(e);
+#pragma unroll
+      for (int c = 0; c < CPT / 4; ++c)
+        ssm_img_put4(cimg, gS, r, 4 * (p + 4 * c),
+                     make_float4(S[rr * CPT + 4 * c] * sc2, S[rr * CPT + 4 * c + 1] * sc2,
+                                 S[rr * CPT + 4 * c + 2] * sc2, S[rr * CPT + 4 * c + 3] * sc2));
+      if (p == 0) cexp[r] = e;
+    }
   }
 }
 
@@ -560,8 +648,7 @@ __global__ void __launch_bounds__(kSsmThreads, 2) ssm_flush_kernel(const SsmArgs
   const int h = blockIdx.x, b = blockIdx.y;
   const int n = ssm_committed(a, b, threadIdx.x == 0 && h == 0);
   if (n + kRows <= a.window || n > a.window) return;  // no flush (n > window: never left by a verify)
-  const size_t hb = static_cast<size_t>(b) * a.heads + h;
-  ssm_fold<D>(a, hb, n, a.ckpt + hb * D * D, reinterpret_cast<float*>(ssm_smem4));
+  ssm_fold<D>(a, static_cast<size_t>(b) * a.heads + h, n, nullptr, nullptr, reinterpret_cast<float*>(ssm_smem4));
 }
 
 // Commit, second part: the pointers (0 after a flush).  One thread per request.
@@ -573,15 +660,25 @@ __global__ void ssm_pointer_kernel(const SsmArgs a) {
   a.ptr[b] = (n + kRows > a.window) ? 0 : n;
 }
 
-// The effective state of request a.req: the closed form of its checkpoint
-// and retained buffer.  grid (H).
+// The effective state of request a.req (the closed form of its checkpoint
+// and retained buffer) into a.state_out.  grid (H).
 template <int D>
 __global__ void __launch_bounds__(kSsmThreads, 2) ssm_state_kernel(const SsmArgs a) {
   extern __shared__ float4 ssm_smem4[];
   const int h = blockIdx.x;
   const int n = min(max(a.ptr[a.req], 0), a.window);
-  const size_t hb = static_cast<size_t>(a.req) * a.heads + h;
-  ssm_fold<D>(a, hb, n, a.state_out + static_cast<size_t>(h) * D * D, reinterpret_cast<float*>(ssm_smem4));
+  ssm_fold<D>(a, static_cast<size_t>(a.req) * a.heads + h, n, nullptr,
+              a.state_out + static_cast<size_t>(h) * D * D, reinterpret_cast<float*>(ssm_smem4));
+}
+
+// Request a.req's checkpoint := a.state_in (fp32 rows), as an image; the
+// caller empties its buffer.  grid (H).
+template <int D>
+__global__ void __launch_bounds__(kSsmThreads, 2) ssm_set_kernel(const SsmArgs a) {
+  extern __shared__ float4 ssm_smem4[];
+  const int h = blockIdx.x;
+  ssm_fold<D>(a, static_cast<size_t>(a.req) * a.heads + h, 0, a.state_in + static_cast<size_t>(h) * D * D,
+              nullptr, reinterpret_cast<float*>(ssm_smem4));
 }
 
 }  // namespace vsd
