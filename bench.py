@@ -114,7 +114,7 @@ def code_only(src: str) -> str:
     return "\n".join(l.rstrip() for l in src.splitlines() if l.strip())
 
 
-SSM_SOURCES = ("replay_ssm.cuh",)  # the recurrent-state rollback kernels, outside the verify step
+SSM_SOURCES = ("replay_ssm.cuh", "replay_ssm.cu")  # the recurrent-state rollback, outside the verify step
 
 
 def kernel_source_sha(ssm: bool = False) -> str:

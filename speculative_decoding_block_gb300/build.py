@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libvsd.so")
 BUILD = os.path.join(HERE, "_build")
-UNITS = ["api.cu", "gemm.cu", "attention.cu", "step.cu"]
+UNITS = ["api.cu", "gemm.cu", "attention.cu", "step.cu", "replay_ssm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 
