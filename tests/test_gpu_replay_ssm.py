@@ -129,3 +129,40 @@ def test_extreme_gates_and_scales(d, window):
             for h in range(H):
                 assert rel_rows(s[h], ref[b][h].state()).max() < TOL, (step, b, h)
     assert ssm.device_status() == 0
+
+
+@pytest.mark.parametrize("d,window,B,H", [(64, 40, 16, 12), (128, 64, 10, 16)])
+def test_more_items_than_sms(d, window, B, H):
+    """More (request, head) items than SMs, so that persistent CTAs walk
+    several items and each item's checkpoint and key images are the bulk
+    copies its CTA issued during the previous one; requests keep different
+    pointers (random accepted lengths), so consecutive items copy different
+    numbers of retained rows."""
+    B_ = require_gpu()
+    rng = np.random.default_rng(1000 + d)
+    ssm = B_.SSM(B, H, d, window)
+    S0 = (rng.normal(size=(B, H, d, d)) * 0.1).astype(np.float32)
+    ref = [[ReplayState(S0[b, h].astype(np.float64), window) for h in range(H)] for b in range(B)]
+    for b in range(B):
+        ssm.set_state(b, torch.tensor(S0[b], device="cuda"))
+    for step in range(5):
+        q, k, v, alpha, beta = _inputs(rng, B, H, d)
+        out = torch.empty((B, H, ROWS, d), dtype=torch.float32, device="cuda")
+        ssm.verify(B, *[torch.tensor(x, device="cuda") for x in (q, k, v, alpha, beta)], out)
+        got = out.cpu().numpy()
+        for b in range(B):
+            for h in range(H):
+                want = ref[b][h].verify(q[b, h], k[b, h], v[b, h], alpha[b, h], beta[b, h])
+                assert rel_rows(got[b, h], want).max() < TOL, (step, b, h)
+        acc = rng.integers(-1, ROWS, size=B).astype(np.int32)
+        ssm.commit(B, torch.tensor(acc, device="cuda"))
+        for b in range(B):
+            for h in range(H):
+                ref[b][h].commit(int(acc[b]))
+    st = torch.empty((H, d, d), dtype=torch.float32, device="cuda")
+    for b in (0, B // 2, B - 1):
+        ssm.get_state(b, st)
+        s = st.cpu().numpy()
+        for h in range(H):
+            assert rel_rows(s[h], ref[b][h].state()).max() < TOL, (b, h)
+    assert ssm.device_status() == 0
