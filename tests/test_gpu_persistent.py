@@ -14,7 +14,7 @@ from tests.test_gpu_sampling import test_tiny_sampled_every_prefix  # noqa: F401
 from tests.test_gpu_step import tiny_setup  # noqa: F401
 from tests.test_gpu_step import test_tiny_batch_every_prefix_length, test_tiny_consecutive_steps_match_oracle  # noqa: F401
 from tests.test_gpu_workloads import test_half_b_bf16_one_request_full  # noqa: F401
-from tests.test_gpu_workloads import test_half_b_mixed_bench_workload_sampled  # noqa: F401
+from tests.test_gpu_workloads import test_half_b_mixed_bench_workload_all_requests  # noqa: F401
 from tests.test_gpu_workloads import test_seven_b_shape_one_layer_full  # noqa: F401
 
 pytestmark = gpu
