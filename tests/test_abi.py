@@ -62,3 +62,20 @@ def test_host_array_checks():
     assert binding._host(ro, "drafts", 16, writable=False).value == ro.ctypes.data
     with pytest.raises(TypeError):
         binding._host(ro, "seq_lens", 16)
+
+
+def test_rollback_object_argument_checks_without_gpu():
+    """vsd_ssm_create rejects bad shapes on the host, before any device call."""
+    L = binding.lib()
+    h = ctypes.c_void_p()
+    assert L.vsd_ssm_create(4, 2, 128, 64, None) == binding.VSD_ERR_ARG           # NULL out
+    assert L.vsd_ssm_create(0, 2, 128, 64, ctypes.byref(h)) == binding.VSD_ERR_ARG  # no requests
+    assert L.vsd_ssm_create(4, 2, 128, 16, ctypes.byref(h)) == binding.VSD_ERR_ARG  # window below one block
+    assert L.vsd_ssm_create(4, 2, 64, 129, ctypes.byref(h)) == binding.VSD_ERR_ARG  # window above the buffer's cap
+    assert L.vsd_ssm_create(4, 2, 96, 64, ctypes.byref(h)) == binding.VSD_ERR_UNSUPPORTED
+    assert b"64 or 128" in L.vsd_last_error()
+    assert L.vsd_ssm_create(4, 2, 128, 65, ctypes.byref(h)) == binding.VSD_ERR_UNSUPPORTED  # shared memory
+    assert b"window 65" in L.vsd_last_error()
+    assert not h.value
+    assert L.vsd_ssm_verify(None, 1, None, None, None, None, None, None, None) == binding.VSD_ERR_ARG
+    assert L.vsd_ssm_commit(None, 1, None, None) == binding.VSD_ERR_ARG
