@@ -445,15 +445,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_ld_wait();
         // visible keys of this row form a prefix [0, lim) of the thread's columns:
         // block keys 0..j (causal), context keys below L, nothing for padding rows
-        int lim = ncol;
-        if (need_mask) lim = !row_ok ? 0 : min(ncol, blk ? jr + 1 - col0 : x.L - c * 128 - col0);
+        // (the scale is applied once to the maximum and fused into the
+        // exponent's argument below: it is positive, so it commutes with max)
         const float sl = a.scale_log2;
         float cm = -INFINITY;
+        if (!need_mask) {  // a full context chunk: 64 columns, all visible
 #pragma unroll
-        for (int t = 0; t < 64; ++t) {
-          s[t] = t < lim ? s[t] * sl : -INFINITY;
-          cm = fmaxf(cm, s[t]);
+          for (int t = 0; t < 64; ++t) cm = fmaxf(cm, s[t]);
+        } else {
+          const int lim = !row_ok ? 0 : min(ncol, blk ? jr + 1 - col0 : x.L - c * 128 - col0);
+#pragma unroll
+          for (int t = 0; t < 64; ++t) {
+            s[t] = t < lim ? s[t] : -INFINITY;
+            cm = fmaxf(cm, s[t]);
+          }
         }
+        cm *= sl;
         float* xs = xstat + (g & 1) * 256;
         xs[hf * 128 + r] = cm;
         named_bar_sync(bar_id, 64);
@@ -500,7 +507,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             uint32_t w[4], wl[4];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-              const float p0 = ex2(s[t + e] - m_use), p1 = ex2(s[t + e + 1] - m_use);
+              const float p0 = ex2(fmaf(s[t + e], sl, -m_use)), p1 = ex2(fmaf(s[t + e + 1], sl, -m_use));
               w[e >> 1] = f32x2_to_bf16x2(p0, p1);
               const float h0 = __uint_as_float(w[e >> 1] << 16), h1 = __uint_as_float(w[e >> 1] & 0xFFFF0000u);
               wl[e >> 1] = f32x2_to_bf16x2(p0 - h0, p1 - h1);
