@@ -102,3 +102,28 @@ def test_rejected_block_leaves_the_state():
     assert rs.ptr == 0 and np.array_equal(rs.state(), before)
     with pytest.raises(ValueError):
         rs.commit(17)
+
+
+def test_flush_changes_no_result():
+    """The same blocks and accepted lengths through buffers of different
+    windows (so the flushes fall at different steps, or never) give the
+    same outputs and states."""
+    rng = np.random.default_rng(21)
+    d_k, d_v = 5, 4
+    S0 = rng.normal(size=(d_v, d_k))
+    blocks = [_block(rng, d_k, d_v) for _ in range(12)]
+    accs = [int(a) for a in rng.integers(-1, ROWS, size=12)]
+    runs = []
+    for window in (17, 30, 1000):
+        rs = ReplayState(S0, window)
+        outs, states = [], []
+        for blk, acc in zip(blocks, accs):
+            outs.append(rs.verify(*blk))
+            rs.commit(acc)
+            states.append(rs.state().copy())
+        runs.append((outs, states))
+    for outs, states in runs[1:]:
+        for a, b in zip(outs, runs[0][0]):
+            assert np.allclose(a, b, rtol=1e-10, atol=1e-10)
+        for a, b in zip(states, runs[0][1]):
+            assert np.allclose(a, b, rtol=1e-10, atol=1e-10)
