@@ -317,7 +317,11 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
   const uint64_t pol = policy_evict_first();
   // bulk copies (one thread): an item's checkpoint image and exponents into
   // the checkpoint tile / expS[slot], its first nb key rows into the key tile
+  // copy groups and product pairs issued / seen complete (thread 0's view),
+  // for the drain after a timed-out wait
+  uint32_t n_ck = 0, n_keys = 0, n_mma = 0, d_ck = 0, d_keys = 0, d_mma = 0;
   auto issue_ckpt = [&](int it_, int slot) {
+    ++n_ck;
     const size_t hbi = static_cast<size_t>(it_ / a.heads) * a.heads + it_ % a.heads;
     const uint8_t* img = a.ckpt + hbi * D * D * 4;
     mbar_expect_tx(&bars[0], 2u * NA * gS.atom + D * 4u);
@@ -329,6 +333,7 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
     bulk_load(expS + slot * 128, a.ckpt_exp + hbi * D, D * 4u, &bars[0], pol);
   };
   auto issue_keys = [&](int it_, int nbi, int slot) {
+    ++n_keys;
     nbi = min(max(nbi, 0), a.window - kRows);
     const size_t hbi = static_cast<size_t>(it_ / a.heads) * a.heads + it_ % a.heads;
     const uint8_t* img = a.buf_k + hbi * a.window * D * 4;
@@ -416,8 +421,8 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
                              a.buf_kexp + hb * kstride);
     }
     // ---- 2. the item's images
-    mbar_wait(&bars[0], it & 1u, abort_flag, a.status);
-    mbar_wait(&bars[1], it & 1u, abort_flag, a.status);
+    if (mbar_wait(&bars[0], it & 1u, abort_flag, a.status)) ++d_ck;
+    if (mbar_wait(&bars[1], it & 1u, abort_flag, a.status)) ++d_keys;
     cp_async_wait_all();
     fence_proxy_async();
     tc_fence_before();
@@ -437,14 +442,15 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
       tc_fence_after();
       ssm_issue<D>(tmem, tA, tB, &bars[2]);
       ssm_issue<D>(tmem + 64u, tK, tB, &bars[3]);
+      ++n_mma;
     }
     // ---- 3. P rows, then the coefficients from G
-    mbar_wait(&bars[2], mma_ph & 1u, abort_flag, a.status);
+    const bool p_done = mbar_wait(&bars[2], mma_ph & 1u, abort_flag, a.status);
     tc_fence_after();
     if (t == 0 && nx < items) issue_ckpt(nx, slot ^ 1);  // the checkpoint tile is free
     float P[kRows];
     if (row < D) ssm_tmem_row(taddr, kind, expS[slot * 128 + row], expB, P);
-    mbar_wait(&bars[3], mma_ph & 1u, abort_flag, a.status);
+    if (mbar_wait(&bars[3], mma_ph & 1u, abort_flag, a.status) && p_done) ++d_mma;
     ++mma_ph;
     tc_fence_after();
     if (t == 0 && nx < items) issue_keys(nx, nb_next, slot ^ 1);  // the key tile is free
@@ -527,6 +533,18 @@ __global__ void __launch_bounds__(kSsmThreads, 1) ssm_verify_kernel(const SsmArg
     }
     if (t < kRows) a.buf_L[brow + nb + t] = sL[nb + t];  // the block's log sums after the pointer
     __syncthreads();  // the shared buffers are reused by the next item
+  }
+  if (*abort_flag && t == 0) {
+    // a wait ran out (VSD_DEV_TIMEOUT is set): let this CTA's copies and
+    // products in flight land (each wait bounded) before the shared memory
+    // and TMEM are released
+    volatile int never = 0;
+    for (uint32_t p = d_ck; p < n_ck; ++p) mbar_wait(&bars[0], p & 1u, &never, nullptr);
+    for (uint32_t p = d_keys; p < n_keys; ++p) mbar_wait(&bars[1], p & 1u, &never, nullptr);
+    for (uint32_t p = d_mma; p < n_mma; ++p) {
+      mbar_wait(&bars[2], p & 1u, &never, nullptr);
+      mbar_wait(&bars[3], p & 1u, &never, nullptr);
+    }
   }
   tc_fence_before();
   __syncthreads();
