@@ -79,6 +79,26 @@ __device__ __forceinline__ void f16_pairs8(const float* v, float scale, uint32_t
   }
 }
 
+// Packed pairs of f32 operations (two IEEE results per instruction).
+__device__ __forceinline__ void fma2_bc(float a0, float a1, float b, float c, float& d0, float& d1) {
+  asm("{\n .reg .b64 x, y, z, r;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %4};\n mov.b64 z, {%5, %5};\n"
+      " fma.rn.f32x2 r, x, y, z;\n mov.b64 {%0, %1}, r;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void sub2(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+  asm("{\n .reg .b64 x, y, r;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n sub.rn.f32x2 r, x, y;\n"
+      " mov.b64 {%0, %1}, r;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n .reg .b64 x, y, r;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n add.rn.f32x2 r, x, y;\n"
+      " mov.b64 {%0, %1}, r;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
 // The maximum a row's softmax weights are taken against moves only when a
 // chunk exceeds it by more than this (log2 units): weights stay <= 2^8.
 constexpr float kRescaleLog2 = 8.0f;
@@ -498,20 +518,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tmem_st16_wait(o_tmem + d0, v);
           }
         }
-        float psum = 0.0f;
         // probabilities -> BF16 pairs P_hi, P_lo, one 16-byte chunk (8 keys) at a
-        // time: keys [col0, col0 + ncol) of row r live in atom col0 / 64
+        // time: keys [col0, col0 + ncol) of row r live in atom col0 / 64.  The
+        // exponent arguments, the lo parts and the row sums run as packed
+        // pairs (the softmax's instruction stream sets the chunk time).
+        float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
         for (int t = 0; t < 64; t += 8) {
           if (t < ncol) {
             uint32_t w[4], wl[4];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-              const float p0 = ex2(fmaf(s[t + e], sl, -m_use)), p1 = ex2(fmaf(s[t + e + 1], sl, -m_use));
+              float x0, x1, l0, l1;
+              fma2_bc(s[t + e], s[t + e + 1], sl, -m_use, x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
               w[e >> 1] = f32x2_to_bf16x2(p0, p1);
               const float h0 = __uint_as_float(w[e >> 1] << 16), h1 = __uint_as_float(w[e >> 1] & 0xFFFF0000u);
-              wl[e >> 1] = f32x2_to_bf16x2(p0 - h0, p1 - h1);
-              psum += p0 + p1;
+              sub2(p0, p1, h0, h1, l0, l1);
+              wl[e >> 1] = f32x2_to_bf16x2(l0, l1);
+              add2(ps0, ps1, p0, p1);
             }
             const int key = col0 + t;
             const uint32_t o = (key >> 6) * 16384 + sw128_off(r, (key & 63) >> 3);
@@ -523,7 +548,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive(&sfree[g & 1]);
         fence_proxy_async();
         mbar_arrive(pfull);
-        l = l * alpha + psum;
+        l = l * alpha + (ps0 + ps1);
       }
       g0 += x.n;
       if (!ok) break;
