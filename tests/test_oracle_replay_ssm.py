@@ -127,3 +127,28 @@ def test_flush_changes_no_result():
             assert np.allclose(a, b, rtol=1e-10, atol=1e-10)
         for a, b in zip(states, runs[0][1]):
             assert np.allclose(a, b, rtol=1e-10, atol=1e-10)
+
+
+
+def test_closed_form_of_the_buffered_state():
+    """The closed form the library's buffer relies on: with corrected values
+    u_t = beta_t (v_t - alpha_t S_{t-1} k_t) and L_t the sum of log alpha
+    since the checkpoint (floored at -200 per token, which stands for a zero
+    gate), S_t = e^{L_t} S_0 + sum_{s<=t} e^{L_t - L_s} u_s k_s^T -- checked
+    against the oracle's step-by-step recurrence, a zero gate included."""
+    rng = np.random.default_rng(33)
+    d_k, d_v, n = 6, 5, 40
+    S0 = rng.normal(size=(d_v, d_k))
+    ks = np.stack([_unit(x) for x in rng.normal(size=(n, d_k))])
+    vs = rng.normal(size=(n, d_v))
+    alphas = rng.uniform(0.5, 1.0, n)
+    alphas[7] = 0.0  # the state is forgotten at token 7
+    betas = rng.uniform(0.0, 1.0, n)
+    S = S0.copy()
+    us, L = [], []
+    for t in range(n):
+        us.append(betas[t] * (vs[t] - alphas[t] * (S @ ks[t])))
+        L.append((L[-1] if L else 0.0) + max(np.log(alphas[t]) if alphas[t] > 0 else -np.inf, -200.0))
+        S = gdn_update(S, ks[t], vs[t], alphas[t], betas[t])
+        closed = np.exp(L[t]) * S0 + sum(np.exp(L[t] - L[s]) * np.outer(us[s], ks[s]) for s in range(t + 1))
+        assert np.allclose(closed, S, rtol=1e-10, atol=1e-10), t
